@@ -1,0 +1,183 @@
+/*
+ * ffd.h -- C ABI of libffd.so: Faster Flash Decoding (FFD) sparse decode attention on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Method source: "Faster Than Flash: Exploiting Attention Sparsity for Efficient Long-Context
+ * Decoding" (technical summary pages), Methodology §1 "Content-aware scanning via low-bit
+ * quantization", §2 "Top-delta selection strategy", §3 "Fused kernel and system optimisation".
+ * The pages call FFD a drop-in replacement for a standard attention kernel (Significance §2),
+ * so the decode entry point has the shape of a paged flash-decode call.
+ *
+ * Conventions for every function:
+ *   - Pointers marked "device" are device memory owned by the caller; the library allocates no
+ *     memory and keeps no state between calls other than what the caller's workspace holds.
+ *   - Calls are asynchronous on the given stream (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream), except ffd_get_error, which synchronises that stream.
+ *   - Argument errors are detected on the host before anything is enqueued and returned as a
+ *     status. Launch failures return FFD_ERR_CUDA. Problems only the device can see (a block
+ *     table entry out of range, a key outside the fp16 range) set bits in a device error word
+ *     and are read with ffd_get_error; the kernels never trap.
+ *   - Supported shapes: head_dim = 128, page_size = 64, 1 <= num_q_heads/num_kv_heads <= 8.
+ *     Anything else returns FFD_ERR_UNSUPPORTED.
+ *
+ * Paged cache layout (P pages, Hkv KV heads, 64 tokens per page, d = 128 channels):
+ *   K, V       bf16 [P][Hkv][64][128]
+ *   thumb      u8   [P][Hkv][64][32]   2-bit code of channel c in byte c/4, bits 2(c%4)+{0,1}
+ *   t_scale    f16  [P][Hkv][64][4]    thumbnail scale of channel group g = c/32
+ *   t_zero     f16  [P][Hkv][64][4]    thumbnail zero (offset) of group g
+ *   resid      i8   [P][Hkv][64][128]  int8 residual code of channel c
+ *   r_scale    f16  [P][Hkv][64][4]    residual scale of group g
+ * Logical block b of sequence s (tokens 64b .. 64b+63) lives in page block_table[s][b].
+ */
+#ifndef FFD_H
+#define FFD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FFD_OK = 0,
+    FFD_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent shape */
+    FFD_ERR_UNSUPPORTED = 2, /* head_dim != 128, page_size != 64, GQA group size outside 1..8 */
+    FFD_ERR_WORKSPACE = 3,   /* workspace smaller than the matching *_workspace_size() */
+    FFD_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+    FFD_ERR_BOUNDS = 5,      /* device: a block_table / page_ids entry outside [0, num_pages) */
+    FFD_ERR_RANGE = 6,       /* device: a key outside the fp16 range (|k| >= 65504 or NaN) */
+} ffd_status;
+
+/* Bits of the device error word (first 4 bytes of a workspace, or the quantiser's word). */
+#define FFD_ERRBIT_BOUNDS 0x1
+#define FFD_ERRBIT_RANGE 0x2
+
+/* Static description of a paged key/value cache. */
+typedef struct {
+    int32_t num_pages;    /* P >= 1 */
+    int32_t num_kv_heads; /* Hkv >= 1 */
+    int32_t head_dim;     /* must be 128 */
+    int32_t page_size;    /* must be 64 */
+} ffd_cache_desc;
+
+/* One decode step: every sequence contributes one query token with num_q_heads heads. */
+typedef struct {
+    int32_t batch;              /* B >= 1 sequences */
+    int32_t num_q_heads;        /* Hq, a multiple of num_kv_heads */
+    int32_t num_kv_heads;       /* Hkv; G = Hq / Hkv query heads share a KV head (GQA) */
+    int32_t head_dim;           /* must be 128 */
+    int32_t page_size;          /* must be 64 */
+    int32_t num_pages;          /* P, bound for block_table entries */
+    int32_t max_blocks_per_seq; /* row stride of block_table; seq_lens[b] <= 64 * this */
+    int32_t sink_tokens;        /* S >= 0: tokens 0 .. S-1 are sink tokens */
+    int32_t local_tokens;       /* L >= 0: tokens n-L .. n-1 are local tokens */
+    float delta;                /* delta of the Top-delta rule; +INFINITY keeps every block */
+    float sm_scale;             /* score scale, normally 1/sqrt(head_dim) */
+    int32_t num_splits;         /* 0: library's choice; else KV splits per (sequence, KV head) */
+} ffd_decode_params;
+
+/* Human-readable name of a status. Never NULL. */
+const char *ffd_status_string(ffd_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t ffd_version(void);
+
+/*
+ * ffd_quantize_keys -- split bf16 keys into the 2-bit thumbnail and the int8 residual.
+ * Source: Methodology §1 (the K cache is partitioned into 2-bit quantized thumbnails used to
+ * estimate attention scores and 8-bit residuals that rebuild the keys close to fp16 precision).
+ * Format (the pages leave it open; fixed by this library), per token, KV head and group g of 32
+ * channels, all steps single-rounded IEEE fp32:
+ *   zero = f16(min x), scale = f16((max x - min x) / 3),
+ *   c2 = clamp(rint((x - zero) / scale), 0, 3)  (0 if scale == 0),
+ *   r = x - fma(c2, scale, zero), r_scale = f16(max |r| / 127),
+ *   c8 = clamp(rint(r / r_scale), -127, 127)     (0 if r_scale == 0);
+ * rint rounds half to even; a signed zero minimum or maximum counts as +0.
+ *
+ *   cache         shape of the cache (head_dim 128, page_size 64)
+ *   k_bf16        device, bf16 [P][Hkv][64][128], read only
+ *   thumb .. r_scale  device outputs in the layout above (written for the selected pages only)
+ *   page_ids      device int32 [num_page_ids] pages to quantise, or NULL for all P pages
+ *   num_page_ids  number of entries in page_ids (ignored when page_ids is NULL)
+ *   error_word    device int32, or NULL: FFD_ERRBIT_BOUNDS is OR-ed in for a page id outside
+ *                 [0, P) (that page is skipped), FFD_ERRBIT_RANGE for a key with |k| >= 65504 or
+ *                 NaN (its group is still written; its contents are then unspecified)
+ *   stream        cudaStream_t
+ * Returns FFD_OK, FFD_ERR_INVALID_ARG, FFD_ERR_UNSUPPORTED or FFD_ERR_CUDA.
+ */
+ffd_status ffd_quantize_keys(const ffd_cache_desc *cache, const void *k_bf16, uint8_t *thumb,
+                             void *t_scale, void *t_zero, int8_t *resid, void *r_scale,
+                             const int32_t *page_ids, int32_t num_page_ids, int32_t *error_word,
+                             void *stream);
+
+/*
+ * Bytes of device workspace that ffd_decode_attention needs for these parameters on the current
+ * device. Returns 0 for parameters that ffd_decode_attention would reject.
+ */
+size_t ffd_decode_workspace_size(const ffd_decode_params *params);
+
+/*
+ * ffd_decode_attention -- one FFD decode-attention step.
+ * Source: Methodology §2 (keep token j when s_ij >= m~_i - delta, m~_i a pseudo-max taken over
+ * the sink and local tokens only) and §3 (stage 1 pseudo-max estimation from sink and local
+ * tokens; stage 2 streams the 2-bit keys, computes provisional scores and filters blocks against
+ * the threshold; stage 3 loads the 8-bit residuals and V of the selected blocks and computes
+ * exact attention). Per sequence b (length n = seq_lens[b]) and query head i of KV head h:
+ *   K^_j = fma(c8, r_scale, fma(c2, scale, zero)) (thumbnail + residual), x^_j = thumbnail only,
+ *   s_ij = sm_scale * q_i . K^_j,  s^_ij = sm_scale * q_i . x^_j,
+ *   m~_i = max of s_ij over j < S and n-L <= j < n,
+ *   block c (tokens 64c .. 64c+63, j < n) is kept when it holds a sink or local token, or when
+ *   some head i of the group and token j of the block give s^_ij >= m~_i - delta,
+ *   out_i = softmax over the kept tokens of s_ij, applied to V (dropped tokens contribute 0).
+ * n = 0 gives out_i = 0 and m~_i = -inf. S = L = 0 gives m~ = -inf, so every block is kept.
+ *
+ *   q_bf16      device bf16 [B][Hq][128]
+ *   thumb .. r_scale, v_bf16   device cache in the layout above (from ffd_quantize_keys)
+ *   seq_lens    device int32 [B], 0 <= seq_lens[b] <= 64 * max_blocks_per_seq
+ *   block_table device int32 [B][max_blocks_per_seq]; only entries b < ceil(n/64) are read
+ *   out         device fp32 [B][Hq][128]
+ *   keep_mask   device u8 [B][Hkv][max_blocks_per_seq] or NULL: 1 = block kept, 0 = dropped;
+ *               entries at or past ceil(n/64) are set to 0
+ *   m_tilde     device fp32 [B][Hq] or NULL: the pseudo-max
+ *   workspace   device, >= ffd_decode_workspace_size(params) bytes, 256-byte aligned. Its
+ *               first 4 bytes are the device error word. Zero-fill it once before first use;
+ *               each call leaves it ready for the next one. Calls that share a workspace must
+ *               be ordered on one stream.
+ * Errors: host-side status as listed above; FFD_ERRBIT_BOUNDS in the workspace error word when
+ * a block_table entry lies outside [0, num_pages) (the block is treated as empty).
+ */
+ffd_status ffd_decode_attention(const ffd_decode_params *params, const void *q_bf16,
+                                const uint8_t *thumb, const void *t_scale, const void *t_zero,
+                                const int8_t *resid, const void *r_scale, const void *v_bf16,
+                                const int32_t *seq_lens, const int32_t *block_table, float *out,
+                                uint8_t *keep_mask, float *m_tilde, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace that ffd_dense_decode needs (same rules as above). */
+size_t ffd_dense_workspace_size(const ffd_decode_params *params);
+
+/*
+ * ffd_dense_decode -- dense bf16 flash-decode attention, the in-library comparison kernel:
+ * out_i = softmax_j(sm_scale * q_i . K_j) V over every token j < n, with the original bf16 keys.
+ * Source: the pages compare FFD against FlashAttention-2 decoding (Main results, kernel speedup
+ * and end-to-end throughput). sink_tokens, local_tokens and delta are ignored.
+ *   k_bf16, v_bf16  device bf16 [P][Hkv][64][128]; other arguments as in ffd_decode_attention.
+ */
+ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
+                            const void *k_bf16, const void *v_bf16, const int32_t *seq_lens,
+                            const int32_t *block_table, float *out, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
+ * ffd_get_error -- synchronise `stream`, read and clear the device error word at `error_word`
+ * (a workspace pointer, or the quantiser's error word), and return FFD_OK, FFD_ERR_BOUNDS or
+ * FFD_ERR_RANGE (bounds first when both bits are set), or FFD_ERR_CUDA if the read failed.
+ */
+ffd_status ffd_get_error(void *error_word, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FFD_H */

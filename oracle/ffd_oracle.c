@@ -113,6 +113,7 @@ uint16_t ffdo_f16_from_f32(float f) {
  *   r     = x - x^2;  r_scale = f16(max|r| / 127);
  *   c8    = clamp(rint(r / r_scale), -127, 127), 0 when the stored r_scale is 0;
  *   rint  = round half to even. Every operation is one IEEE fp32 operation, rounded once.
+ *   A signed-zero minimum or maximum counts as +0.
  * Returns 0, or 1 when an input lies outside the fp16 range (precondition |x| < 65504). */
 int ffdo_quantize_group(const float *x, uint8_t *c2, uint16_t *t_scale, uint16_t *t_zero,
                         int8_t *c8, uint16_t *r_scale) {
@@ -123,6 +124,10 @@ int ffdo_quantize_group(const float *x, uint8_t *c2, uint16_t *t_scale, uint16_t
         if (x[c] < mn) mn = x[c];
         if (x[c] > mx) mx = x[c];
     }
+    /* Reading: -0 and +0 compare equal, so which one is "the minimum" is not defined by the
+     * comparison; a zero extreme is taken as +0. */
+    if (mn == 0.0f) mn = 0.0f;
+    if (mx == 0.0f) mx = 0.0f;
     uint16_t zf16 = ffdo_f16_from_f32(mn);
     float range = mx - mn;
     float step = range / 3.0f;

@@ -486,3 +486,14 @@ def test_each_head_uses_its_own_threshold(delta):
     clear = ~(np.abs(mg) < 1e-9)
     assert np.array_equal(res.mask[0, 0, :47].astype(bool)[clear], mask[clear])
     assert 0 < mask.sum() < 47
+
+
+def test_signed_zero_extremes_count_as_plus_zero():
+    """Whichever zero comes first, a zero minimum gives zero = +0 (bits 0x0000)."""
+    for first in (-0.0, 0.0):
+        x = np.zeros(32, np.float32)
+        x[0] = first
+        x[1] = -first
+        x[2:] = 1.0
+        c2, ts, tz, c8, rs, _ = oracle.quantize_group(x)
+        assert tz == 0x0000 and ts == int(np.float32(1 / 3).astype(np.float16).view(np.uint16))
