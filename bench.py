@@ -1,0 +1,596 @@
+#!/usr/bin/env python3
+"""Benchmark of the FFD decode-attention step (stage 1 + fused stage 2/3 + merge) on GB300.
+
+Default workload: the Qwen2.5-7B-shaped decode step (batch 4, 28 query / 4 KV heads, 128K
+context, S=64, L=1024, delta=5), seeded synthetic inputs, N=1. Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+value = algorithmic HBM bytes of one step / device time of one step (GB/s): all 2-bit
+thumbnails (48 B per token and KV head) + int8 residual and bf16 V of the kept blocks (392 B per
+kept token and KV head) + q, output, seq_lens and block table. Inputs are resident in HBM and
+larger than L2, so no flush is needed between steps. N > 1 runs one rank per GPU, each on its own
+sequences (weak scaling, no collective on the data path).
+
+--impl reference times the CPU oracle (test infrastructure, fp64) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/step & achieved HBM GB/s vs 8 TB/s roofline, 32K–256K ctx"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129 * 1000 ** 2
+THUMB_B = 48          # bytes per token and KV head: 32 code bytes + 4 fp16 scales + 4 fp16 zeros
+REFINE_B = 136 + 256  # int8 residual + 4 fp16 residual scales + bf16 V
+DENSE_B = 512         # bf16 K + V
+LAUNCHES_PER_DECODE = 3  # stage 1, fused stage 2/3, merge
+PROFILE = os.path.join(ROOT, "profiles", "ffd_main_kernel_qwen2.5-7b_128k.txt")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def args_parse(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, help="workload id 0..4")
+    ap.add_argument("--delta", type=float, default=None)
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the peaked-attention variant and the CPU baseline")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------------------- #
+# Byte accounting (algorithmic, per step)                                                      #
+# ------------------------------------------------------------------------------------------- #
+
+def kept_tokens(seq_lens, keep_mask) -> int:
+    """Valid tokens inside kept blocks, summed over (sequence, KV head)."""
+    total = 0
+    B, Hkv, maxb = keep_mask.shape
+    for b in range(B):
+        n = int(seq_lens[b])
+        nb = (n + 63) // 64
+        if nb == 0:
+            continue
+        sizes = np.full(nb, 64, np.int64)
+        sizes[-1] = n - 64 * (nb - 1)
+        total += int((keep_mask[b, :, :nb].astype(np.int64) * sizes[None]).sum())
+    return total
+
+
+def step_bytes(w, seq_lens, max_blocks, kept) -> dict:
+    tok_heads = int(np.sum(seq_lens)) * w.num_kv_heads
+    q = w.batch * w.num_q_heads * 128 * 2
+    out = w.batch * w.num_q_heads * 128 * 4
+    meta = 4 * w.batch + 4 * w.batch * max_blocks
+    thumbs = THUMB_B * tok_heads
+    refine = REFINE_B * kept
+    return {"thumbs": thumbs, "refine": refine, "q": q, "out": out, "meta": meta,
+            "step": thumbs + refine + q + out + meta,
+            "main_kernel": thumbs + refine + q + 4 * w.batch * max_blocks,
+            "dense_step": DENSE_B * tok_heads + q + out + meta,
+            "token_heads": tok_heads}
+
+
+def unit_bytes(w, seq_lens, keep_mask, units) -> int:
+    """Algorithmic bytes of a subset of (sequence, KV head) units (CPU-baseline sample)."""
+    G = w.num_q_heads // w.num_kv_heads
+    total = 0
+    for (b, h) in units:
+        n = int(seq_lens[b])
+        nb = (n + 63) // 64
+        sizes = np.full(nb, 64, np.int64)
+        if nb:
+            sizes[-1] = n - 64 * (nb - 1)
+        kept = int((keep_mask[b, h, :nb].astype(np.int64) * sizes).sum())
+        total += THUMB_B * n + REFINE_B * kept + G * 128 * (2 + 4)
+    return total
+
+
+# ------------------------------------------------------------------------------------------- #
+# Multi-rank plumbing                                                                          #
+# ------------------------------------------------------------------------------------------- #
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max_sum(elapsed_ms: float, nbytes: float, backend_device="cpu"):
+    """Max of the per-rank times and sum of the per-rank bytes over the process group (a no-op
+    without one). Returns (max_ms, total_bytes)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_ms, nbytes
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=backend_device)
+    b = torch.tensor([nbytes], dtype=torch.float64, device=backend_device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank decodes its own sequences: rank 0 keeps the workload's seed."""
+    return base + 7919 * rank
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------------------------------------- #
+# Clocks                                                                                       #
+# ------------------------------------------------------------------------------------------- #
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark_on(self):
+        self.t_on = time.time()
+
+    def mark_off(self):
+        self.t_off = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9], parts[4]))
+            except ValueError:
+                continue
+        window = [r for r in rows if self.t_on and self.t_on <= r[0] <= (self.t_off or 1e30)]
+        which = "timed"
+        if len(window) < 3:
+            window, which = rows, "warmup+timed+after"
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in window for i, v in enumerate(r[3])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in window),
+                "sm_max_mhz": max(r[2] for r in window), "reasons": reasons,
+                "samples": len(window), "window": which}
+
+
+# ------------------------------------------------------------------------------------------- #
+# GPU arm                                                                                      #
+# ------------------------------------------------------------------------------------------- #
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0}, "fallback"
+
+
+def profile_traffic():
+    """DRAM bytes per launch of the main kernel from the committed ncu summary, if the kernel
+    source has not changed since the counters were taken (else None)."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None, None
+    fields = dict(line.split(":", 1) for line in text.splitlines() if ":" in line)
+    want = fields.get("source_sha256", "").strip()
+    src = os.path.join(ROOT, "sparse_quantized_attention_gb300", "csrc", "decode.cu")
+    have = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if want != have:
+        return None, "kernel changed since the ncu capture"
+    try:
+        return float(fields["dram_bytes_per_launch"].split()[0]), fields.get("workload", "").strip()
+    except (KeyError, ValueError):
+        return None, None
+
+
+def run_ours(a, rank, world, local):
+    import torch
+
+    import ffd_synth
+    import sparse_quantized_attention_gb300 as ffd
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = ffd_synth.WORKLOADS[a.workload]
+    delta = a.delta if a.delta is not None else w.deltas[0]
+    inp = ffd_synth.make_inputs(w, seed=rank_seed(w.seed, rank))
+    G = w.num_q_heads // w.num_kv_heads
+    sm = float(np.float32(1.0 / math.sqrt(128.0)))
+
+    def upload(i):
+        bf = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(  # noqa
+            torch.bfloat16).to(dev)
+        return {"q": bf(i.q_bits), "k": bf(i.k_bits), "v": bf(i.v_bits),
+                "seq_lens": torch.from_numpy(i.seq_lens).to(dev),
+                "block_table": torch.from_numpy(i.block_table).to(dev)}
+
+    d = upload(inp)
+    P, Hkv = d["k"].shape[0], d["k"].shape[1]
+    qc = ffd.alloc_quantized_cache(P, Hkv, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # a0: quantisation of the whole cache (precondition of the step, timed on its own)
+    ffd.ffd_quantize_keys(d["k"], qc)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    ffd.ffd_quantize_keys(d["k"], qc)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    quant_ms = e0.elapsed_time(e1)
+    quant_bytes = P * Hkv * 64 * (256 + 32 + 8 + 8 + 128 + 8)
+
+    params = ffd.make_params(w.batch, w.num_q_heads, w.num_kv_heads, P, inp.max_blocks,
+                             sink=w.sink, local=w.local, delta=delta, sm_scale=sm)
+    ws = ffd.alloc_workspace(params, device=dev)
+    out = torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.float32, device=dev)
+    mask = torch.zeros((w.batch, w.num_kv_heads, inp.max_blocks), dtype=torch.uint8, device=dev)
+
+    def step(keep=None):
+        ffd.ffd_decode_attention(params, d["q"], qc, d["v"], d["seq_lens"], d["block_table"],
+                                 out, ws, keep_mask=keep)
+
+    step(mask)
+    if ffd.ffd_get_error(ws) != 0:
+        raise RuntimeError("device error during the first decode step")
+    keep = mask.cpu().numpy()
+    kept = kept_tokens(inp.seq_lens, keep)
+    nb_total = int(sum((int(n) + 63) // 64 for n in inp.seq_lens)) * w.num_kv_heads
+    kept_blocks = int(keep.sum())
+    by = step_bytes(w, inp.seq_lens, inp.max_blocks, kept)
+
+    # timed region: W warm-up steps, then exactly K steps between barriers + syncs
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(a.warmup):
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(a.steps)]
+    for s_, e_ in ev:  # create the events before the timed region
+        s_.record(stream)
+        e_.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(local)
+    torch.cuda.synchronize(dev)
+    clocks.mark_on()
+    t0.record(stream)
+    for i in range(a.steps):
+        ffd.ffd_set_profile_events(*ev[i])
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark_off()
+    ffd.ffd_set_profile_events(None, None)
+    barrier(local)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    main_ms = [s_.elapsed_time(e_) for s_, e_ in ev]
+    if ffd.ffd_get_error(ws) != 0:
+        raise RuntimeError("device error during the timed steps")
+
+    max_ms, all_bytes = reduce_max_sum(total_ms, by["step"] * a.steps,
+                                       backend_device=dev if world > 1 else "cpu")
+    ms_per_step = max_ms / a.steps
+    value = all_bytes / a.steps / (ms_per_step * 1e-3) / 1e9
+
+    # e2e through the public API with pinned host buffers: q, seq_lens, block table in,
+    # output out, every step, inside the timed region
+    hq = torch.from_numpy(inp.q_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hsl = torch.from_numpy(inp.seq_lens).pin_memory()
+    hbt = torch.from_numpy(inp.block_table).pin_memory()
+    hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    h2d = hq.numel() * 2 + hsl.numel() * 4 + hbt.numel() * 4
+    d2h = hout.numel() * 4
+
+    def e2e_step():
+        d["q"].copy_(hq, non_blocking=True)
+        d["seq_lens"].copy_(hsl, non_blocking=True)
+        d["block_table"].copy_(hbt, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(a.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(local)
+    t0.record(stream)
+    for _ in range(a.steps):
+        e2e_step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms, e2e_bytes = reduce_max_sum(t0.elapsed_time(t1), by["step"] * a.steps,
+                                       backend_device=dev if world > 1 else "cpu")
+    e2e_value = e2e_bytes / a.steps / (e2e_ms / a.steps * 1e-3) / 1e9
+
+    # a5: the in-library dense bf16 flash-decode on the same inputs
+    wsd = ffd.alloc_workspace(params, dense=True, device=dev)
+    outd = torch.empty_like(out)
+    dense_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    dsteps = max(3, min(a.steps, 50))
+    for _ in range(3):
+        ffd.ffd_dense_decode(params, d["q"], d["k"], d["v"], d["seq_lens"], d["block_table"],
+                             outd, wsd)
+    torch.cuda.synchronize(dev)
+    dense_ev[0].record(stream)
+    for _ in range(dsteps):
+        ffd.ffd_dense_decode(params, d["q"], d["k"], d["v"], d["seq_lens"], d["block_table"],
+                             outd, wsd)
+    dense_ev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    dense_ms = dense_ev[0].elapsed_time(dense_ev[1]) / dsteps
+
+    peaks, peak_src = measured_peaks()
+    main_avg = sum(main_ms) / len(main_ms)
+    achieved = by["main_kernel"] / (main_avg * 1e-3) / 1e9
+    traffic, traffic_note = profile_traffic()
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_per_step, 5),
+        "us_per_step": round(ms_per_step * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "context": w.seq_len, "sink": w.sink,
+                   "local": w.local, "delta": delta, "page": 64, "head_dim": 128,
+                   "l2": f"inputs larger than L2 ({by['step'] / 1e6:.0f} MB read per step vs "
+                         f"{L2_BYTES / 1e6:.0f} MB L2), no flush",
+                   "parallelism": "single GPU" if world == 1 else
+                   f"replicas x{world} (own sequences per rank)"},
+        "roofline": {"bound": "hbm", "kernel": "ffd main (stage 2+3)",
+                     "achieved": round(achieved, 1), "peak": peaks.get("hbm_gbs"),
+                     "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "unit": "GB/s", "frac": round(achieved / peaks.get("hbm_gbs"), 4),
+                     "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "traffic": traffic, "traffic_note": traffic_note,
+                     "algorithmic_bytes_per_launch": by["main_kernel"],
+                     "kernel_us": round(main_avg * 1e3, 2),
+                     "kernel_share_of_step": round(main_avg / ms_per_step, 3)},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "us_per_step": round(e2e_ms / a.steps * 1e3, 2)},
+        "gpu_launches": LAUNCHES_PER_DECODE * a.steps,
+        "clocks": clock_info,
+        "ffd": {"needed_bytes_per_step": by["step"], "kept_blocks": kept_blocks,
+                "total_blocks": nb_total,
+                "sparsity": round(1 - kept_blocks / max(1, nb_total), 4),
+                "kept_token_fraction": round(kept / max(1, by["token_heads"]), 4),
+                "effective_kv_tokens_per_s": round(float(np.sum(inp.seq_lens)) /
+                                                   (ms_per_step * 1e-3), 1),
+                "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4)},
+        "rows": {"quantize_us": round(quant_ms * 1e3, 2),
+                 "quantize_gbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1),
+                 "dense_us": round(dense_ms * 1e3, 2),
+                 "dense_gbs": round(by["dense_step"] / (dense_ms * 1e-3) / 1e9, 1),
+                 "speedup_vs_dense": round(dense_ms / ms_per_step, 3),
+                 "main_kernel_us_p50": round(statistics.median(main_ms) * 1e3, 2)},
+    }
+
+    if not a.no_secondary and rank == 0 and world == 1:
+        result["secondary_peaked"] = peaked_variant(a, w, delta, dev, ffd, torch, upload,
+                                                    dense_ms)
+        result["cpu_baseline"] = cpu_baseline(w, inp, keep, delta, sm)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result
+
+
+def peaked_variant(a, w, delta, dev, ffd, torch, upload, dense_ms):
+    """Same shapes with the sink shift and needle magnitude stated in score units: attention is
+    concentrated, most blocks fall below m~ - delta and the stream is mostly thumbnails."""
+    import ffd_synth
+    inp = ffd_synth.make_inputs(w, signal_scale=ffd_synth.peaked_scale())
+    d = upload(inp)
+    P, Hkv = d["k"].shape[0], d["k"].shape[1]
+    qc = ffd.alloc_quantized_cache(P, Hkv, device=dev)
+    ffd.ffd_quantize_keys(d["k"], qc)
+    sm = float(np.float32(1.0 / math.sqrt(128.0)))
+    params = ffd.make_params(w.batch, w.num_q_heads, w.num_kv_heads, P, inp.max_blocks,
+                             sink=w.sink, local=w.local, delta=delta, sm_scale=sm)
+    ws = ffd.alloc_workspace(params, device=dev)
+    out = torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.float32, device=dev)
+    mask = torch.zeros((w.batch, w.num_kv_heads, inp.max_blocks), dtype=torch.uint8, device=dev)
+    ffd.ffd_decode_attention(params, d["q"], qc, d["v"], d["seq_lens"], d["block_table"], out,
+                             ws, keep_mask=mask)
+    keep = mask.cpu().numpy()
+    kept = kept_tokens(inp.seq_lens, keep)
+    by = step_bytes(w, inp.seq_lens, inp.max_blocks, kept)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(a.warmup):
+        ffd.ffd_decode_attention(params, d["q"], qc, d["v"], d["seq_lens"], d["block_table"],
+                                 out, ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(a.steps):
+        ffd.ffd_decode_attention(params, d["q"], qc, d["v"], d["seq_lens"], d["block_table"],
+                                 out, ws)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / a.steps
+    nb_total = int(sum((int(n) + 63) // 64 for n in inp.seq_lens)) * w.num_kv_heads
+    del d, qc
+    return {"signal_scale": round(ffd_synth.peaked_scale(), 4), "us_per_step": round(ms * 1e3, 2),
+            "needed_bytes_per_step": by["step"], "gbs": round(by["step"] / (ms * 1e-3) / 1e9, 1),
+            "sparsity": round(1 - int(keep.sum()) / nb_total, 4),
+            "speedup_vs_dense": round(dense_ms / ms, 3),
+            "effective_kv_tokens_per_s": round(float(np.sum(inp.seq_lens)) / (ms * 1e-3), 1)}
+
+
+def cpu_baseline(w, inp, keep, delta, sm):
+    """The CPU oracle as it stands, on the host cores, over a bounded sample of the same step's
+    (sequence, KV head) units. Quantisation (a precondition of the step) is not timed."""
+    import oracle
+    qk = oracle.quantize(inp.k_bits)
+    units = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
+    cores = oracle.default_threads()
+    # bound the sample to about 10-30 s of CPU work: ~3e-8 s per (token, head, query head)
+    G = w.num_q_heads // w.num_kv_heads
+    per_unit = [3e-8 * int(inp.seq_lens[b]) * G * 128 / 64 for (b, h) in units]
+    sample, cost = [], 0.0
+    for u, c in zip(units, per_unit):
+        if cost > 30.0 and sample:
+            break
+        sample.append(u)
+        cost += c
+    t = time.time()
+    oracle.decode(inp.q_bits, inp.seq_lens, inp.block_table, qk, inp.v_bits, sink=w.sink,
+                  local=w.local, delta=delta, sm_scale=sm, units=sample, threads=cores)
+    dt = time.time() - t
+    nbytes = unit_bytes(w, inp.seq_lens, keep, sample)
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": UNIT, "cores": min(cores, len(sample)),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"{len(sample)} of {len(units)} (sequence, KV head) units of one step "
+                      f"({nbytes / 1e6:.1f} MB algorithmic)"}
+
+
+# ------------------------------------------------------------------------------------------- #
+# Reference arm: the CPU oracle                                                                #
+# ------------------------------------------------------------------------------------------- #
+
+def run_reference(a):
+    import ffd_synth
+    import oracle
+    w = ffd_synth.WORKLOADS[a.workload]
+    delta = a.delta if a.delta is not None else w.deltas[0]
+    inp = ffd_synth.make_inputs(w)
+    sm = float(np.float32(1.0 / math.sqrt(128.0)))
+    qk = oracle.quantize(inp.k_bits)
+    cores = oracle.default_threads()
+    units = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
+    # each step decodes a bounded sample of the step's units, sized so that the whole run stays
+    # within a few minutes
+    per_step_units = max(1, min(len(units), cores))
+    steps_total = a.warmup + a.steps
+    budget_s = 150.0
+    probe = oracle.decode(inp.q_bits, inp.seq_lens, inp.block_table, qk, inp.v_bits,
+                          sink=w.sink, local=w.local, delta=delta, sm_scale=sm,
+                          units=units[:1], threads=1)
+    t = time.time()
+    oracle.decode(inp.q_bits, inp.seq_lens, inp.block_table, qk, inp.v_bits, sink=w.sink,
+                  local=w.local, delta=delta, sm_scale=sm, units=units[:per_step_units],
+                  threads=cores)
+    one = time.time() - t
+    while per_step_units > 1 and one * steps_total > budget_s:
+        per_step_units = max(1, per_step_units // 2)
+        one /= 2
+    full = oracle.decode(inp.q_bits, inp.seq_lens, inp.block_table, qk, inp.v_bits, sink=w.sink,
+                         local=w.local, delta=delta, sm_scale=sm, threads=cores)
+    del probe
+    times, nbytes_list = [], []
+    for s in range(steps_total):
+        sample = [units[(s * per_step_units + k) % len(units)] for k in range(per_step_units)]
+        t = time.time()
+        oracle.decode(inp.q_bits, inp.seq_lens, inp.block_table, qk, inp.v_bits, sink=w.sink,
+                      local=w.local, delta=delta, sm_scale=sm, units=sample, threads=cores)
+        dt = time.time() - t
+        if s >= a.warmup:
+            times.append(dt)
+            nbytes_list.append(unit_bytes(w, inp.seq_lens, full.mask, sample))
+    total_t = sum(times)
+    value = sum(nbytes_list) / total_t / 1e9
+    sample_desc = (f"{per_step_units} of {len(units)} (sequence, KV head) units per step, "
+                   f"rotating; fp64 oracle on {min(cores, per_step_units)} host threads")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": round(total_t / a.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+                       "num_kv_heads": w.num_kv_heads, "context": w.seq_len, "sink": w.sink,
+                       "local": w.local, "delta": delta},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT,
+                             "cores": min(cores, per_step_units), "kind": "oracle",
+                             "sample": sample_desc},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    a = args_parse(argv)
+    rank, world, local = dist_env()
+    if a.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(a)), flush=True)
+        return 0
+    if world != a.gpus:
+        log(f"warning: --gpus {a.gpus} but WORLD_SIZE={world}; using WORLD_SIZE")
+    result = run_ours(a, rank, world, local)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

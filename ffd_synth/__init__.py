@@ -6,7 +6,8 @@ decoding RULER / LongBench prompts at 16K-256K context, "Faster Than Flash", Mai
 need datasets and trained weights that are not used here.
 
 Recipe (per configuration; fp32 sampling, then one round-to-nearest-even cast to bf16):
-  * q ~ N(0, 1) [B, Hq, 128]; K, V ~ N(0, 1) [P, Hkv, 64, 128] in a paged layout (page = 64).
+  * q ~ N(0, 1) [B, Hq, 128] (torch generator); K, V ~ N(0, 1) [P, Hkv, 64, 128] in a paged
+    layout (page = 64), drawn from numpy PCG64 streams per chunk of 64 pages.
   * q_hat(b, h) = normalise(sum of the bf16 query rows of KV head h's GQA group), fp32.
   * Sink tokens j < S: K_j <- K_j + 3 * a * q_hat.
   * Needles: positions uniform without replacement in [S, n - L); K_j <- 4 * a * q_hat + eps,
@@ -20,6 +21,8 @@ Recipe (per configuration; fp32 sampling, then one round-to-nearest-even cast to
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -82,6 +85,25 @@ def _bf16_bits(x: torch.Tensor) -> np.ndarray:
     return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
+_CHUNK_PAGES = 64
+
+
+def _normal_pages(seed: int, stream: int, P: int, Hkv: int) -> torch.Tensor:
+    """N(0,1) fp32 [P, Hkv, 64, 128]; page chunk c draws from its own PCG64 stream
+    (seed, stream, c), so the values do not depend on how many threads draw them."""
+    out = np.empty((P, Hkv, PAGE, D), np.float32)
+    chunks = range(0, P, _CHUNK_PAGES)
+
+    def fill(p0):
+        rng = np.random.Generator(np.random.PCG64([seed, stream, p0 // _CHUNK_PAGES]))
+        p1 = min(P, p0 + _CHUNK_PAGES)
+        out[p0:p1] = rng.standard_normal((p1 - p0, Hkv, PAGE, D), dtype=np.float32)
+
+    with ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1))) as ex:
+        list(ex.map(fill, chunks))
+    return torch.from_numpy(out)
+
+
 def make_inputs(w: Workload, *, seed: int | None = None, signal_scale: float = 1.0,
                 seq_lens=None) -> Inputs:
     """Draw one step's inputs for workload ``w``. ``seq_lens`` overrides the drawn lengths."""
@@ -122,8 +144,9 @@ def make_inputs(w: Workload, *, seed: int | None = None, signal_scale: float = 1
     q = torch.randn((B, Hq, D), generator=g, dtype=torch.float32)
     q_bits = _bf16_bits(q)
     qf = q.to(torch.bfloat16).to(torch.float32)
-    k = torch.randn((P, Hkv, PAGE, D), generator=g, dtype=torch.float32)
-    v = torch.randn((P, Hkv, PAGE, D), generator=g, dtype=torch.float32)
+    base_seed = w.seed if seed is None else seed
+    k = _normal_pages(base_seed, 1, P, Hkv)
+    v = _normal_pages(base_seed, 2, P, Hkv)
 
     a = float(signal_scale)
     needle_pos = {}

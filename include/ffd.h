@@ -170,6 +170,17 @@ ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
                             size_t workspace_bytes, void *stream);
 
 /*
+ * ffd_set_profile_events -- optional instrumentation. While both events are non-NULL, every
+ * ffd_decode_attention / ffd_dense_decode call records `start` on its stream right before its
+ * main kernel (the fused stage-2/3 kernel, or the dense kernel) and `stop` right after it, so the
+ * caller can time that kernel alone with cudaEventElapsedTime. The events are cudaEvent_t values
+ * created and owned by the caller. Pass NULL, NULL to stop recording. Process-wide setting, not
+ * synchronised: set it from the thread that issues the calls. Returns FFD_OK, or
+ * FFD_ERR_INVALID_ARG when exactly one event is NULL.
+ */
+ffd_status ffd_set_profile_events(void *start, void *stop);
+
+/*
  * ffd_get_error -- synchronise `stream`, read and clear the device error word at `error_word`
  * (a workspace pointer, or the quantiser's error word), and return FFD_OK, FFD_ERR_BOUNDS or
  * FFD_ERR_RANGE (bounds first when both bits are set), or FFD_ERR_CUDA if the read failed.

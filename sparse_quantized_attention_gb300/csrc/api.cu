@@ -1,0 +1,241 @@
+// api.cu -- the C ABI of libffd.so (declared in include/ffd.h): argument checks, workspace
+// planning and kernel launches. No function here allocates device memory.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace ffd {
+cudaError_t launch_quantize(int P, int Hkv, const int32_t *page_ids, int num_pages_listed,
+                            const void *k, uint8_t *thumb, void *t_scale, void *t_zero,
+                            int8_t *resid, void *r_scale, int *err, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_dense(const DecodeArgs &a, cudaStream_t stream);
+}  // namespace ffd
+
+using namespace ffd;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kCtasPerSm = 4;  // target resident CTAs per SM for the split count
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int current_sm_count() {
+    static int cache[128];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (dev >= 0 && dev < 128 && cache[dev] > 0) return cache[dev];
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (dev >= 0 && dev < 128) cache[dev] = v;
+    return v;
+}
+
+ffd_status check_params(const ffd_decode_params *p) {
+    if (!p) return FFD_ERR_INVALID_ARG;
+    if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->num_pages < 1 ||
+        p->max_blocks_per_seq < 1 || p->sink_tokens < 0 || p->local_tokens < 0 ||
+        p->num_splits < 0)
+        return FFD_ERR_INVALID_ARG;
+    if (p->num_q_heads % p->num_kv_heads != 0) return FFD_ERR_INVALID_ARG;
+    if (isnan(p->delta) || p->delta == -INFINITY) return FFD_ERR_INVALID_ARG;
+    if (!isfinite(p->sm_scale)) return FFD_ERR_INVALID_ARG;
+    if (p->head_dim != kD || p->page_size != kPage) return FFD_ERR_UNSUPPORTED;
+    const int G = p->num_q_heads / p->num_kv_heads;
+    if (G < 1 || G > kMaxG) return FFD_ERR_UNSUPPORTED;
+    // grid.y = B * Hkv, grid.x = splits / forced slots
+    if ((int64_t)p->batch * p->num_kv_heads > 65535) return FFD_ERR_UNSUPPORTED;
+    return FFD_OK;
+}
+
+struct Plan {
+    int splits, bps, nf;
+    size_t m1_off, part_off, total;
+};
+
+ffd_status make_plan(const ffd_decode_params *p, bool dense, Plan *pl) {
+    ffd_status st = check_params(p);
+    if (st != FFD_OK) return st;
+    const int64_t units = (int64_t)p->batch * p->num_kv_heads;
+    const int G = p->num_q_heads / p->num_kv_heads;
+    int splits = p->num_splits;
+    if (splits == 0) {
+        const int sms = current_sm_count();
+        if (sms <= 0) return FFD_ERR_CUDA;
+        const int64_t target = (int64_t)sms * kCtasPerSm;
+        splits = (int)((target + units - 1) / units);
+    }
+    if (splits > p->max_blocks_per_seq) splits = p->max_blocks_per_seq;
+    if (splits < 1) splits = 1;
+    pl->bps = (p->max_blocks_per_seq + splits - 1) / splits;
+    pl->splits = (p->max_blocks_per_seq + pl->bps - 1) / pl->bps;
+    pl->nf = dense ? 0 : max_forced_blocks(p->sink_tokens, p->local_tokens, p->max_blocks_per_seq);
+    size_t off = kAlign;  // header: error word
+    pl->m1_off = off;
+    off = align_up(off + (size_t)units * pl->nf * kMaxG * sizeof(float));
+    pl->part_off = off;
+    off = align_up(off + (size_t)units * pl->splits * G * kPartStride * sizeof(float));
+    pl->total = off;
+    return FFD_OK;
+}
+
+cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+
+DecodeArgs make_args(const ffd_decode_params *p, const Plan &pl, void *ws) {
+    DecodeArgs a{};
+    a.prof_start = g_prof_start;
+    a.prof_stop = g_prof_stop;
+    a.B = p->batch;
+    a.Hq = p->num_q_heads;
+    a.Hkv = p->num_kv_heads;
+    a.G = p->num_q_heads / p->num_kv_heads;
+    a.P = p->num_pages;
+    a.max_blocks = p->max_blocks_per_seq;
+    a.S = p->sink_tokens;
+    a.L = p->local_tokens;
+    a.splits = pl.splits;
+    a.blk_per_split = pl.bps;
+    a.nf = pl.nf;
+    a.delta = p->delta;
+    a.sm_scale = p->sm_scale;
+    char *base = static_cast<char *>(ws);
+    a.err = reinterpret_cast<int *>(base);
+    a.ws_m1 = reinterpret_cast<float *>(base + pl.m1_off);
+    a.ws_part = reinterpret_cast<float *>(base + pl.part_off);
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ffd_status_string(ffd_status s) {
+    switch (s) {
+        case FFD_OK: return "FFD_OK";
+        case FFD_ERR_INVALID_ARG: return "FFD_ERR_INVALID_ARG";
+        case FFD_ERR_UNSUPPORTED: return "FFD_ERR_UNSUPPORTED";
+        case FFD_ERR_WORKSPACE: return "FFD_ERR_WORKSPACE";
+        case FFD_ERR_CUDA: return "FFD_ERR_CUDA";
+        case FFD_ERR_BOUNDS: return "FFD_ERR_BOUNDS";
+        case FFD_ERR_RANGE: return "FFD_ERR_RANGE";
+    }
+    return "FFD_ERR_UNKNOWN";
+}
+
+int32_t ffd_version(void) { return 100; }
+
+ffd_status ffd_quantize_keys(const ffd_cache_desc *cache, const void *k_bf16, uint8_t *thumb,
+                             void *t_scale, void *t_zero, int8_t *resid, void *r_scale,
+                             const int32_t *page_ids, int32_t num_page_ids, int32_t *error_word,
+                             void *stream) {
+    if (!cache || !k_bf16 || !thumb || !t_scale || !t_zero || !resid || !r_scale)
+        return FFD_ERR_INVALID_ARG;
+    if (cache->num_pages < 1 || cache->num_kv_heads < 1) return FFD_ERR_INVALID_ARG;
+    if (page_ids && num_page_ids < 0) return FFD_ERR_INVALID_ARG;
+    if (cache->head_dim != kD || cache->page_size != kPage) return FFD_ERR_UNSUPPORTED;
+    if (!aligned16(k_bf16) || !aligned16(thumb) || !aligned16(resid) ||
+        (reinterpret_cast<uintptr_t>(t_scale) & 7u) || (reinterpret_cast<uintptr_t>(t_zero) & 7u) ||
+        (reinterpret_cast<uintptr_t>(r_scale) & 7u))
+        return FFD_ERR_INVALID_ARG;
+    const int listed = page_ids ? num_page_ids : cache->num_pages;
+    if ((int64_t)listed * cache->num_kv_heads * kPage * 32 > INT32_MAX) return FFD_ERR_UNSUPPORTED;
+    cudaError_t e = launch_quantize(cache->num_pages, cache->num_kv_heads, page_ids, listed, k_bf16,
+                                    thumb, t_scale, t_zero, resid, r_scale, error_word,
+                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+}
+
+size_t ffd_decode_workspace_size(const ffd_decode_params *params) {
+    Plan pl;
+    return make_plan(params, false, &pl) == FFD_OK ? pl.total : 0;
+}
+
+size_t ffd_dense_workspace_size(const ffd_decode_params *params) {
+    Plan pl;
+    return make_plan(params, true, &pl) == FFD_OK ? pl.total : 0;
+}
+
+ffd_status ffd_decode_attention(const ffd_decode_params *params, const void *q_bf16,
+                                const uint8_t *thumb, const void *t_scale, const void *t_zero,
+                                const int8_t *resid, const void *r_scale, const void *v_bf16,
+                                const int32_t *seq_lens, const int32_t *block_table, float *out,
+                                uint8_t *keep_mask, float *m_tilde, void *workspace,
+                                size_t workspace_bytes, void *stream) {
+    if (!q_bf16 || !thumb || !t_scale || !t_zero || !resid || !r_scale || !v_bf16 || !seq_lens ||
+        !block_table || !out || !workspace)
+        return FFD_ERR_INVALID_ARG;
+    if (!aligned16(thumb) || !aligned16(resid) || !aligned16(v_bf16) || !aligned16(q_bf16) ||
+        (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+        return FFD_ERR_INVALID_ARG;
+    Plan pl;
+    ffd_status st = make_plan(params, false, &pl);
+    if (st != FFD_OK) return st;
+    if (workspace_bytes < pl.total) return FFD_ERR_WORKSPACE;
+    DecodeArgs a = make_args(params, pl, workspace);
+    a.q = static_cast<const __nv_bfloat16 *>(q_bf16);
+    a.thumb = thumb;
+    a.t_scale = static_cast<const __half *>(t_scale);
+    a.t_zero = static_cast<const __half *>(t_zero);
+    a.resid = resid;
+    a.r_scale = static_cast<const __half *>(r_scale);
+    a.v = static_cast<const __nv_bfloat16 *>(v_bf16);
+    a.seq_lens = seq_lens;
+    a.block_table = block_table;
+    a.out = out;
+    a.keep_mask = keep_mask;
+    a.m_tilde = m_tilde;
+    cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+}
+
+ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
+                            const void *k_bf16, const void *v_bf16, const int32_t *seq_lens,
+                            const int32_t *block_table, float *out, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    if (!q_bf16 || !k_bf16 || !v_bf16 || !seq_lens || !block_table || !out || !workspace)
+        return FFD_ERR_INVALID_ARG;
+    if (!aligned16(k_bf16) || !aligned16(v_bf16) || !aligned16(q_bf16) ||
+        (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+        return FFD_ERR_INVALID_ARG;
+    Plan pl;
+    ffd_status st = make_plan(params, true, &pl);
+    if (st != FFD_OK) return st;
+    if (workspace_bytes < pl.total) return FFD_ERR_WORKSPACE;
+    DecodeArgs a = make_args(params, pl, workspace);
+    a.q = static_cast<const __nv_bfloat16 *>(q_bf16);
+    a.k = static_cast<const __nv_bfloat16 *>(k_bf16);
+    a.v = static_cast<const __nv_bfloat16 *>(v_bf16);
+    a.seq_lens = seq_lens;
+    a.block_table = block_table;
+    a.out = out;
+    cudaError_t e = launch_dense(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+}
+
+ffd_status ffd_set_profile_events(void *start, void *stop) {
+    if ((start == nullptr) != (stop == nullptr)) return FFD_ERR_INVALID_ARG;
+    g_prof_start = static_cast<cudaEvent_t>(start);
+    g_prof_stop = static_cast<cudaEvent_t>(stop);
+    return FFD_OK;
+}
+
+ffd_status ffd_get_error(void *error_word, void *stream) {
+    if (!error_word) return FFD_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t h = 0;
+    if (cudaMemcpyAsync(&h, error_word, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return FFD_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FFD_ERR_CUDA;
+    if (h != 0) {
+        if (cudaMemsetAsync(error_word, 0, sizeof h, s) != cudaSuccess) return FFD_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return FFD_ERR_CUDA;
+    }
+    if (h & FFD_ERRBIT_BOUNDS) return FFD_ERR_BOUNDS;
+    if (h & FFD_ERRBIT_RANGE) return FFD_ERR_RANGE;
+    return FFD_OK;
+}
+
+}  // extern "C"

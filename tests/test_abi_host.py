@@ -1,0 +1,136 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every function that
+include/ffd.h declares, and rejects bad arguments on the host before it enqueues any work.
+
+Every call below fails validation, so no fake pointer ever reaches a kernel.
+"""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import sparse_quantized_attention_gb300 as ffd
+from sparse_quantized_attention_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ffd.h")
+FAKE = 0x10000  # 256-byte aligned, never dereferenced: every call here fails validation first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return ffd.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ffd_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("ffd_quantize_keys", "ffd_decode_attention", "ffd_dense_decode",
+                 "ffd_decode_workspace_size", "ffd_dense_workspace_size", "ffd_get_error",
+                 "ffd_status_string", "ffd_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(_build.LIB)
+    for name in declared_functions():
+        assert hasattr(raw, name), f"libffd.so does not export {name}"
+
+
+def test_status_strings(lib):
+    for code, name in ffd.ffd.STATUS_NAMES.items():
+        assert ffd.ffd_status_string(code) == name
+    assert ffd.ffd_version() >= 100
+
+
+def _params(**kw):
+    base = dict(batch=2, num_q_heads=8, num_kv_heads=2, num_pages=10, max_blocks_per_seq=5,
+                sink=64, local=128, delta=5.0, num_splits=2)
+    base.update(kw)
+    return ffd.make_params(base.pop("batch"), base.pop("num_q_heads"), base.pop("num_kv_heads"),
+                           base.pop("num_pages"), base.pop("max_blocks_per_seq"), **base)
+
+
+def _decode(lib, p, ws_bytes=1 << 30, **ptrs):
+    args = dict(q=FAKE, thumb=FAKE, ts=FAKE, tz=FAKE, resid=FAKE, rs=FAKE, v=FAKE, sl=FAKE,
+                bt=FAKE, out=FAKE, mask=None, mt=None, ws=FAKE)
+    args.update(ptrs)
+    return lib.ffd_decode_attention(ctypes.byref(p), *[args[k] for k in (
+        "q", "thumb", "ts", "tz", "resid", "rs", "v", "sl", "bt", "out", "mask", "mt", "ws")],
+        ws_bytes, None)
+
+
+def test_workspace_sizes(lib):
+    p = _params()
+    n = ffd.ffd_decode_workspace_size(p)
+    assert n > 0 and n % 256 == 0
+    assert ffd.ffd_dense_workspace_size(p) > 0
+    assert ffd.ffd_decode_workspace_size(_params(num_q_heads=7, num_kv_heads=2)) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_q_heads=7, num_kv_heads=2), 1),       # Hq not a multiple of Hkv
+    (dict(num_q_heads=18, num_kv_heads=2), 2),      # G = 9 unsupported
+    (dict(batch=0), 1),
+    (dict(delta=math.nan), 1),
+    (dict(delta=-math.inf), 1),
+    (dict(sink=-1), 1),
+    (dict(num_splits=-2), 1),
+    (dict(sm_scale=math.inf), 1),
+])
+def test_decode_rejects_bad_params(lib, kw, status):
+    assert _decode(lib, _params(**kw)) == status
+
+
+def test_decode_rejects_unsupported_shapes(lib):
+    p = _params()
+    p.head_dim = 64
+    assert _decode(lib, p) == 2
+    p = _params()
+    p.page_size = 16
+    assert _decode(lib, p) == 2
+
+
+def test_decode_rejects_null_and_misaligned_pointers(lib):
+    p = _params()
+    for key in ("q", "thumb", "ts", "tz", "resid", "rs", "v", "sl", "bt", "out", "ws"):
+        assert _decode(lib, p, **{key: None}) == 1, key
+    assert _decode(lib, p, thumb=FAKE + 4) == 1
+    assert _decode(lib, p, ws=FAKE + 16) == 1
+
+
+def test_decode_rejects_small_workspace(lib):
+    p = _params()
+    need = ffd.ffd_decode_workspace_size(p)
+    assert _decode(lib, p, ws_bytes=need - 1) == 3
+
+
+def test_dense_rejects_bad_arguments(lib):
+    p = _params()
+    need = ffd.ffd_dense_workspace_size(p)
+    call = lambda **kw: lib.ffd_dense_decode(  # noqa: E731
+        ctypes.byref(kw.get("p", p)), kw.get("q", FAKE), kw.get("k", FAKE), FAKE, FAKE, FAKE,
+        FAKE, FAKE, kw.get("ws_bytes", need), None)
+    assert call(q=None) == 1
+    assert call(k=FAKE + 2) == 1
+    assert call(ws_bytes=need - 256) == 3
+    assert call(p=_params(num_q_heads=18, num_kv_heads=2)) == 2
+
+
+def test_quantize_rejects_bad_arguments(lib):
+    good = ffd.CacheDesc(4, 2, 128, 64)
+    call = lambda d, k=FAKE, ids=None, nids=0: lib.ffd_quantize_keys(  # noqa: E731
+        ctypes.byref(d), k, FAKE, FAKE, FAKE, FAKE, FAKE, ids, nids, None, None)
+    assert call(good, k=None) == 1
+    assert call(ffd.CacheDesc(0, 2, 128, 64)) == 1
+    assert call(ffd.CacheDesc(4, 2, 96, 64)) == 2
+    assert call(ffd.CacheDesc(4, 2, 128, 32)) == 2
+    assert call(good, ids=FAKE, nids=-1) == 1
+    assert call(good, k=FAKE + 8) == 1

@@ -461,16 +461,19 @@ def test_pseudo_max_window_edges(where):
     assert abs(res.m_tilde[0, 0] - mt[0]) < 1e-12
 
 
-@pytest.mark.parametrize("delta", [0.0, 1.0, 2.0])
-def test_each_head_uses_its_own_threshold(delta):
+@pytest.mark.parametrize("target", [2.6, 2.8, 3.0])
+def test_each_head_uses_its_own_threshold(target):
     """Heads of one GQA group carry their own pseudo-max and threshold: with head 1's query
     scaled by 4 (exact in bf16) its scores and m~ are 4x head 0's, and the block mask is the
-    union of two different per-head masks, checked against the token-by-token definition."""
+    union of two different per-head masks, checked against the token-by-token definition.
+    delta is set so that head 0's threshold m~_0 - delta sits at ``target`` (background block
+    maxima are ~2-3 there), which makes the mask non-trivial whatever the random draw."""
     w, inp, qk = _setup(batch=1, hq=2, hkv=1, seq_lens=(3000,), sink=16, local=64, needles=0,
                         peaked=False)
     qb = torch.as_tensor(inp.q_bits.view(np.int16)).view(torch.bfloat16).clone()
     qb[0, 1] = qb[0, 0] * 4
     inp.q_bits[:] = qb.view(torch.int16).numpy().view(np.uint16)
+    delta = float(_decode(inp, qk, w, 5.0).m_tilde[0, 0]) - target
     res = _decode(inp, qk, w, delta)
     x2, kh = R.sequence_rows(qk, inp.block_table, 0, 0, 3000)
     q = R.bf16_bits_to_f64(inp.q_bits[0])
