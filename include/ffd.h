@@ -46,12 +46,15 @@ typedef enum {
     FFD_ERR_WORKSPACE = 3,   /* workspace smaller than the matching *_workspace_size() */
     FFD_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
     FFD_ERR_BOUNDS = 5,      /* device: a block_table / page_ids entry outside [0, num_pages) */
-    FFD_ERR_RANGE = 6,       /* device: a key outside the fp16 range (|k| >= 65504 or NaN) */
+    FFD_ERR_RANGE = 6,       /* device: a key outside the fp16 range (|k| >= 65504 or NaN), or a
+                                query with |q| >= 2^27 */
+    FFD_ERR_TIMEOUT = 7,     /* device: a pipeline wait exceeded its 2 s bound (results invalid) */
 } ffd_status;
 
 /* Bits of the device error word (first 4 bytes of a workspace, or the quantiser's word). */
 #define FFD_ERRBIT_BOUNDS 0x1
 #define FFD_ERRBIT_RANGE 0x2
+#define FFD_ERRBIT_TIMEOUT 0x4
 
 /* Static description of a paged key/value cache. */
 typedef struct {
@@ -74,7 +77,9 @@ typedef struct {
     int32_t local_tokens;       /* L >= 0: tokens n-L .. n-1 are local tokens */
     float delta;                /* delta of the Top-delta rule; +INFINITY keeps every block */
     float sm_scale;             /* score scale, normally 1/sqrt(head_dim) */
-    int32_t num_splits;         /* 0: library's choice; else KV splits per (sequence, KV head) */
+    int32_t num_splits;         /* 0: library's choice; else the number of KV partitions (CTAs of
+                                   the main kernel for ffd_decode_attention, splits per sequence
+                                   and KV head for ffd_dense_decode) */
 } ffd_decode_params;
 
 /* Human-readable name of a status. Never NULL. */
@@ -132,7 +137,7 @@ size_t ffd_decode_workspace_size(const ffd_decode_params *params);
  *   out_i = softmax over the kept tokens of s_ij, applied to V (dropped tokens contribute 0).
  * n = 0 gives out_i = 0 and m~_i = -inf. S = L = 0 gives m~ = -inf, so every block is kept.
  *
- *   q_bf16      device bf16 [B][Hq][128]
+ *   q_bf16      device bf16 [B][Hq][128], |q| < 2^27 (else FFD_ERRBIT_RANGE)
  *   thumb .. r_scale, v_bf16   device cache in the layout above (from ffd_quantize_keys)
  *   seq_lens    device int32 [B], 0 <= seq_lens[b] <= 64 * max_blocks_per_seq
  *   block_table device int32 [B][max_blocks_per_seq]; only entries b < ceil(n/64) are read
@@ -142,8 +147,9 @@ size_t ffd_decode_workspace_size(const ffd_decode_params *params);
  *   m_tilde     device fp32 [B][Hq] or NULL: the pseudo-max
  *   workspace   device, >= ffd_decode_workspace_size(params) bytes, 256-byte aligned. Its
  *               first 4 bytes are the device error word. Zero-fill it once before first use;
- *               each call leaves it ready for the next one. Calls that share a workspace must
- *               be ordered on one stream.
+ *               each call leaves it ready for the next one (zero-fill it again after a call that
+ *               reported FFD_ERR_TIMEOUT). Calls that share a workspace must be ordered on one
+ *               stream.
  * Errors: host-side status as listed above; FFD_ERRBIT_BOUNDS in the workspace error word when
  * a block_table entry lies outside [0, num_pages) (the block is treated as empty).
  */
@@ -183,7 +189,8 @@ ffd_status ffd_set_profile_events(void *start, void *stop);
 /*
  * ffd_get_error -- synchronise `stream`, read and clear the device error word at `error_word`
  * (a workspace pointer, or the quantiser's error word), and return FFD_OK, FFD_ERR_BOUNDS or
- * FFD_ERR_RANGE (bounds first when both bits are set), or FFD_ERR_CUDA if the read failed.
+ * FFD_ERR_RANGE or FFD_ERR_TIMEOUT (in that order of precedence when several bits are set), or
+ * FFD_ERR_CUDA if the read failed.
  */
 ffd_status ffd_get_error(void *error_word, void *stream);
 

@@ -8,7 +8,7 @@ namespace ffd {
 cudaError_t launch_quantize(int P, int Hkv, const int32_t *page_ids, int num_pages_listed,
                             const void *k, uint8_t *thumb, void *t_scale, void *t_zero,
                             int8_t *resid, void *r_scale, int *err, cudaStream_t stream);
-cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t stream);
 cudaError_t launch_dense(const DecodeArgs &a, cudaStream_t stream);
 }  // namespace ffd
 
@@ -52,11 +52,39 @@ ffd_status check_params(const ffd_decode_params *p) {
 }
 
 struct Plan {
-    int splits, bps, nf;
-    size_t m1_off, part_off, total;
+    int splits, bps, nf;  // dense: splits per unit and blocks per split; decode: nf slots
+    int ctas;             // decode: CTAs of the main kernel
+    size_t m1_off, part_off, cnt_off, total;
 };
 
-ffd_status make_plan(const ffd_decode_params *p, bool dense, Plan *pl) {
+// Workspace of ffd_decode_attention: [error word | stage-1 maxima | split records | tickets].
+// Records: one per (unit, CTA) pair that shares work, indexed unit + cta (< units + ctas).
+ffd_status make_decode_plan(const ffd_decode_params *p, Plan *pl) {
+    ffd_status st = check_params(p);
+    if (st != FFD_OK) return st;
+    const int64_t units = (int64_t)p->batch * p->num_kv_heads;
+    const int G = p->num_q_heads / p->num_kv_heads;
+    int ctas = p->num_splits;
+    if (ctas == 0) {
+        ctas = current_sm_count();
+        if (ctas <= 0) return FFD_ERR_CUDA;
+    }
+    pl->ctas = ctas;
+    pl->splits = pl->bps = 0;
+    pl->nf = max_forced_blocks(p->sink_tokens, p->local_tokens, p->max_blocks_per_seq);
+    size_t off = kAlign;
+    pl->m1_off = off;
+    off = align_up(off + (size_t)units * pl->nf * kMaxG * sizeof(float));
+    pl->part_off = off;
+    off = align_up(off + (size_t)(units + ctas) * G * kPartStride * sizeof(float));
+    pl->cnt_off = off;
+    off = align_up(off + (size_t)units * sizeof(int));
+    pl->total = off;
+    return FFD_OK;
+}
+
+// Workspace of ffd_dense_decode: [error word | split partials].
+ffd_status make_dense_plan(const ffd_decode_params *p, Plan *pl) {
     ffd_status st = check_params(p);
     if (st != FFD_OK) return st;
     const int64_t units = (int64_t)p->batch * p->num_kv_heads;
@@ -72,12 +100,13 @@ ffd_status make_plan(const ffd_decode_params *p, bool dense, Plan *pl) {
     if (splits < 1) splits = 1;
     pl->bps = (p->max_blocks_per_seq + splits - 1) / splits;
     pl->splits = (p->max_blocks_per_seq + pl->bps - 1) / pl->bps;
-    pl->nf = dense ? 0 : max_forced_blocks(p->sink_tokens, p->local_tokens, p->max_blocks_per_seq);
-    size_t off = kAlign;  // header: error word
+    pl->nf = 0;
+    pl->ctas = 0;
+    size_t off = kAlign;
     pl->m1_off = off;
-    off = align_up(off + (size_t)units * pl->nf * kMaxG * sizeof(float));
     pl->part_off = off;
     off = align_up(off + (size_t)units * pl->splits * G * kPartStride * sizeof(float));
+    pl->cnt_off = off;
     pl->total = off;
     return FFD_OK;
 }
@@ -105,6 +134,7 @@ DecodeArgs make_args(const ffd_decode_params *p, const Plan &pl, void *ws) {
     a.err = reinterpret_cast<int *>(base);
     a.ws_m1 = reinterpret_cast<float *>(base + pl.m1_off);
     a.ws_part = reinterpret_cast<float *>(base + pl.part_off);
+    a.ws_cnt = reinterpret_cast<int *>(base + pl.cnt_off);
     return a;
 }
 
@@ -121,6 +151,7 @@ const char *ffd_status_string(ffd_status s) {
         case FFD_ERR_CUDA: return "FFD_ERR_CUDA";
         case FFD_ERR_BOUNDS: return "FFD_ERR_BOUNDS";
         case FFD_ERR_RANGE: return "FFD_ERR_RANGE";
+        case FFD_ERR_TIMEOUT: return "FFD_ERR_TIMEOUT";
     }
     return "FFD_ERR_UNKNOWN";
 }
@@ -150,12 +181,12 @@ ffd_status ffd_quantize_keys(const ffd_cache_desc *cache, const void *k_bf16, ui
 
 size_t ffd_decode_workspace_size(const ffd_decode_params *params) {
     Plan pl;
-    return make_plan(params, false, &pl) == FFD_OK ? pl.total : 0;
+    return make_decode_plan(params, &pl) == FFD_OK ? pl.total : 0;
 }
 
 size_t ffd_dense_workspace_size(const ffd_decode_params *params) {
     Plan pl;
-    return make_plan(params, true, &pl) == FFD_OK ? pl.total : 0;
+    return make_dense_plan(params, &pl) == FFD_OK ? pl.total : 0;
 }
 
 ffd_status ffd_decode_attention(const ffd_decode_params *params, const void *q_bf16,
@@ -171,7 +202,7 @@ ffd_status ffd_decode_attention(const ffd_decode_params *params, const void *q_b
         (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
         return FFD_ERR_INVALID_ARG;
     Plan pl;
-    ffd_status st = make_plan(params, false, &pl);
+    ffd_status st = make_decode_plan(params, &pl);
     if (st != FFD_OK) return st;
     if (workspace_bytes < pl.total) return FFD_ERR_WORKSPACE;
     DecodeArgs a = make_args(params, pl, workspace);
@@ -187,7 +218,7 @@ ffd_status ffd_decode_attention(const ffd_decode_params *params, const void *q_b
     a.out = out;
     a.keep_mask = keep_mask;
     a.m_tilde = m_tilde;
-    cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_decode(a, pl.ctas, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
 }
 
@@ -201,7 +232,7 @@ ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
         (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
         return FFD_ERR_INVALID_ARG;
     Plan pl;
-    ffd_status st = make_plan(params, true, &pl);
+    ffd_status st = make_dense_plan(params, &pl);
     if (st != FFD_OK) return st;
     if (workspace_bytes < pl.total) return FFD_ERR_WORKSPACE;
     DecodeArgs a = make_args(params, pl, workspace);
@@ -235,6 +266,7 @@ ffd_status ffd_get_error(void *error_word, void *stream) {
     }
     if (h & FFD_ERRBIT_BOUNDS) return FFD_ERR_BOUNDS;
     if (h & FFD_ERRBIT_RANGE) return FFD_ERR_RANGE;
+    if (h & FFD_ERRBIT_TIMEOUT) return FFD_ERR_TIMEOUT;
     return FFD_OK;
 }
 

@@ -38,7 +38,8 @@ struct DecodeArgs {
     float *m_tilde;
     int *err;        // device error word
     float *ws_m1;    // [B*Hkv][nf][kMaxG] stage-1 block maxima
-    float *ws_part;  // [B*Hkv][splits][G][kPartStride]
+    float *ws_part;  // split records: [records][G][kPartStride]
+    int *ws_cnt;     // [B*Hkv] per-unit tickets of the in-kernel merge (kept at zero between calls)
     cudaEvent_t prof_start, prof_stop;  // optional: recorded around the main kernel
 };
 

@@ -1,30 +1,358 @@
-// decode.cu -- FFD decode attention: stage 1 (pseudo-max), fused stage 2 + 3 (Top-delta scan and
-// refinement over kept blocks, split-KV online softmax), and the log-sum-exp merge.
+// decode.cu -- FFD decode attention on GB300: stage 1 (pseudo-max) and the fused, persistent
+// stage-2/3 kernel (Top-delta scan of the 2-bit thumbnails, refinement of the kept blocks with the
+// int8 residual and V, online softmax, split merge).
 //
-// Source: "Faster Than Flash", Methodology §2 (Top-delta rule s_ij >= m~_i - delta, pseudo-max
-// from sink and local tokens) and §3 (three-stage fused kernel: pseudo-max estimation; stream the
-// 2-bit keys, compute provisional scores and filter blocks; load the 8-bit residuals and V of the
-// selected blocks and compute exact attention). The split-KV online softmax with a log-sum-exp
-// merge is the flash-decoding scheme the method's name refers to.
+// Source: "Faster Than Flash", Methodology §2 (keep token j when s_ij >= m~_i - delta; m~_i from
+// the sink and local tokens only) and §3 (stage 1 pseudo-max estimation; stage 2 streams the 2-bit
+// keys, computes provisional scores and filters blocks; stage 3 loads the 8-bit residuals and V of
+// the selected blocks and computes exact attention, reusing the scan results).
+//
+// Tensor-core operands (mma.sync m16n8k16, bf16 in, fp32 accumulate; 16 tokens x 8 heads):
+//   * A = keys of 16 tokens, B = the GQA group's queries (heads as N, padded to 8).
+//   * 2-bit codes enter as bf16 bit patterns (code << s) with s <= 6: exponent field 0, so the
+//     value is exactly code * 2^s * 2^-133. B holds q * 2^(kKq - s), so every product is exactly
+//     code * q * 2^(kKq-133) and one LOP3 turns two codes into an operand register.
+//   * int8 residual codes enter as (c8 + 128) with the same scaling; the +128 is removed in the
+//     epilogue with the per-group query sums.
+//   * PV: O^T(d x heads) += V^T(d x tokens) P^T(tokens x heads); V^T comes from the 128B-swizzled
+//     TMA tile by ldmatrix.trans, P^T from the score accumulators by movmatrix; P is split into
+//     bf16 hi + lo parts so that the product keeps ~2^-17 relative precision.
+// Channel order inside each 16-channel MMA step is permuted (the same permutation on A and B);
+// a dot product does not depend on it.
+#include <string.h>
+
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace ffd {
 
+constexpr int kSub = 8;              // blocks per sub-chunk (scan / refine pipeline unit)
+constexpr int kRing = 4;             // refine ring slots (residual + V of one kept block each)
+constexpr int kConsumerWarps = 8;    // warp = (grp, mt): m-tile mt of the blocks k with k%2 == grp
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kMainThreads = kConsumers + 32;  // + one producer (TMA) warp
+constexpr int kKq = 100;             // q enters the MMA scaled by 2^kKq (|q| < 2^27 required)
+constexpr float kUnscale = 8589934592.0f;      // 2^(133 - kKq)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kQMax = 134217728.0f;          // 2^27
+
+// ring slot: residual tile (64 x 128 B, swizzled), V tile (2 boxes of 64 x 128 B, swizzled),
+// residual scales (64 x 8 B)
+constexpr int kSlotV = 8192;
+constexpr int kSlotRScale = 8192 + 16384;
+constexpr int kSlotTx = 8192 + 16384 + 512;
+constexpr int kSlotBytes = 25600;
+constexpr int kThumbBlock = 3072;    // codes 2048 B + scales 512 B + zeros 512 B
+constexpr int kShatBuf = kSub * 4 * 32 * 16;       // provisional scores of one sub-chunk
+constexpr int kCbufWarp = kMaxG * kD + 2 * kMaxG;  // floats per warp for the combine
+
+constexpr int kOffRing = 0;
+constexpr int kOffThumb = kOffRing + kRing * kSlotBytes;
+constexpr int kOffShat = kOffThumb + 2 * kSub * kThumbBlock;
+constexpr int kOffCbuf = kOffShat + 2 * kShatBuf;
+constexpr int kOffUnit = kOffCbuf + kConsumerWarps * kCbufWarp * 4;
+constexpr int kOffMisc = kOffUnit + 2 * 4608;
+constexpr int kMiscBytes = 256;
+constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + slack to align the base to 1 KB
+
+struct Misc {
+    uint32_t votes[2][kConsumerWarps];
+    uint32_t final_mask[2];
+    uint32_t bad[2];
+    uint32_t merge_flag;
+    uint32_t aborted;
+    uint32_t pad[10];
+    uint64_t thumb_full[2];
+    uint64_t decision[2];
+    uint64_t ring_full[kRing];
+    uint64_t ring_empty[kRing];
+};
+static_assert(sizeof(Misc) <= kMiscBytes, "misc region");
+
+// Query operands of one (sequence, KV head) unit, laid out so that a lane loads its 16 B-fragment
+// registers with four conflict-free 128-bit loads. Two slots: the unit being scanned and the unit
+// being refined (they differ for at most one sub-chunk).
+struct UnitOps {
+    uint4 bt[4][32];   // thumbnail B fragments: [bt0[0..3], bt0[4..7], bt1[0..3], bt1[4..7]][lane]
+    uint4 br[4][32];   // residual B fragments, same arrangement
+    float4 qs[kMaxG];  // per-group query sums, [head].{group 0..3}
+    float thr[kMaxG];  // m~ - delta (+inf for heads >= G)
+    float mt[kMaxG];   // m~
+    int n;             // sequence length
+    int pad[15];
+};
+static_assert(sizeof(UnitOps) <= 4608, "unit operand slot");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+struct MainParams {
+    CUtensorMap tm_resid;
+    CUtensorMap tm_v;
+    DecodeArgs a;
+};
+
 // ------------------------------------------------------------------------------------------
-// Stage 1: one CTA per (forced-block slot, sequence x KV head). Exact scores
-// s = sm * q . K^ (K^ = thumbnail + residual) of the sink / local tokens of one block; writes the
-// per-head maximum of the block to ws_m1. 128 threads: token t = tid/2, channel half tid%2.
+// Work schedule: the blocks of all (sequence, KV head) units, concatenated unit by unit, are cut
+// into `ncta` contiguous ranges of equal length; each range is walked in sub-chunks of at most
+// kSub blocks that never cross a unit. Producer and consumers walk the same sequence.
 // ------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) stage1_kernel(DecodeArgs a) {
-    __shared__ float qs[kMaxG][kD + 4];
+__device__ __forceinline__ int len_of(const DecodeArgs &a, int b) {
+    const int n = a.seq_lens[b];
+    const int cap = a.max_blocks * kPage;
+    return n < 0 ? 0 : (n > cap ? cap : n);
+}
+
+__device__ __forceinline__ int blocks_of(const DecodeArgs &a, int b) {
+    return (len_of(a, b) + kPage - 1) / kPage;
+}
+
+struct Sub {
+    int b, h, j0, cnt;  // unit (b, h), first block, block count
+    int64_t x0;         // global index of the sub-chunk's first block
+    bool last;          // last sub-chunk of this CTA's segment of the unit
+};
+
+struct Sched {
+    int64_t x, x1, T;
+    int b, h, j, nbb;
+
+    __device__ void init(const DecodeArgs &a, int cta, int ncta) {
+        T = 0;
+        for (int bb = 0; bb < a.B; bb++) T += (int64_t)a.Hkv * blocks_of(a, bb);
+        x = T * cta / ncta;
+        x1 = T * (cta + 1) / ncta;
+        int64_t pre = 0;
+        b = h = j = nbb = 0;
+        for (; b < a.B; b++) {
+            const int nb = blocks_of(a, b);
+            const int64_t span = (int64_t)a.Hkv * nb;
+            if (x < pre + span) {
+                nbb = nb;
+                h = (int)((x - pre) / nb);
+                j = (int)((x - pre) % nb);
+                break;
+            }
+            pre += span;
+        }
+    }
+
+    __device__ bool next(const DecodeArgs &a, Sub &s) {
+        if (x >= x1) return false;
+        int cnt = kSub;
+        if (nbb - j < cnt) cnt = nbb - j;
+        if (x1 - x < cnt) cnt = (int)(x1 - x);
+        s.b = b;
+        s.h = h;
+        s.j0 = j;
+        s.cnt = cnt;
+        s.x0 = x;
+        s.last = (j + cnt == nbb) || (x + cnt == x1);
+        x += cnt;
+        j += cnt;
+        if (j == nbb) {
+            j = 0;
+            if (++h == a.Hkv) {
+                h = 0;
+                for (b++; b < a.B; b++) {
+                    nbb = blocks_of(a, b);
+                    if (nbb > 0) break;
+                }
+            }
+        }
+        return true;
+    }
+};
+
+// CTA whose range holds global block x (ranges are non-empty because ncta <= T).
+__device__ __forceinline__ int cta_of(int64_t x, int64_t T, int ncta) {
+    return (int)(((x + 1) * ncta - 1) / T);
+}
+
+// ------------------------------------------------------------------------------------------
+// Query operands. Thread (g = lane/4, tig = lane%4) holds the B fragments of head g and, for the
+// epilogue, the per-group query sums of heads 2*tig and 2*tig+1.
+// ------------------------------------------------------------------------------------------
+struct ThumbOps {
+    uint32_t bt0[8], bt1[8];  // chunk kc = channels 16kc .. 16kc+15, head g
+    float qs[2][4];           // sum of q over group gg for heads 2tig, 2tig+1
+};
+struct ResidOps {
+    uint32_t br0[8], br1[8];  // chunk 2gg + half, head g
+    float qs[2][4];
+};
+
+// Per-group query sums of heads 2tig, 2tig+1, from this thread's partial sums of head g over the
+// channels c = tig (mod 4): quad reduction, then fetch from the quads of heads 2tig and 2tig+1.
+__device__ __forceinline__ void group_sums(float (&part)[4], int tig, float (&qs)[2][4]) {
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) {
+        part[gg] += __shfl_xor_sync(0xffffffffu, part[gg], 1);
+        part[gg] += __shfl_xor_sync(0xffffffffu, part[gg], 2);
+    }
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) {
+        qs[0][gg] = __shfl_sync(0xffffffffu, part[gg], 8 * tig);
+        qs[1][gg] = __shfl_sync(0xffffffffu, part[gg], 8 * tig + 4);
+    }
+}
+
+__device__ __forceinline__ const __nv_bfloat16 *q_row(const DecodeArgs &a, int b, int h, int g) {
+    return a.q + ((size_t)b * a.Hq + h * a.G + (g < a.G ? g : 0)) * kD;
+}
+
+__device__ __forceinline__ void load_thumb_ops(const DecodeArgs &a, int b, int h, int lane,
+                                               ThumbOps &Q) {
+    const int g = lane >> 2, tig = lane & 3;
+    const bool hv = g < a.G;
+    const __nv_bfloat16 *qrow = q_row(a, b, h, g);
+    float big = 0.0f;
+    auto ld = [&](int c) {
+        const float v = hv ? __bfloat162float(qrow[c]) : 0.0f;
+        big = fmaxf(big, fabsf(v));
+        return v;
+    };
+    const float st = __int_as_float((127 + kKq - 2 * tig) << 23);  // 2^(kKq - 2 tig)
+    float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int kc = 0; kc < 8; kc++) {
+        const float x0 = ld(16 * kc + tig), x1 = ld(16 * kc + 8 + tig);
+        const float x2 = ld(16 * kc + 4 + tig), x3 = ld(16 * kc + 12 + tig);
+        Q.bt0[kc] = pack_bf16x2(x0 * st, x1 * st);
+        Q.bt1[kc] = pack_bf16x2(x2 * st, x3 * st);
+        part[kc >> 1] += (x0 + x1) + (x2 + x3);
+    }
+    group_sums(part, tig, Q.qs);
+    if (!(big < kQMax)) raise_error(a.err, FFD_ERRBIT_RANGE);
+}
+
+__device__ __forceinline__ void load_resid_ops(const DecodeArgs &a, int b, int h, int lane,
+                                               ResidOps &Q) {
+    const int g = lane >> 2, tig = lane & 3;
+    const bool hv = g < a.G;
+    const __nv_bfloat16 *qrow = q_row(a, b, h, g);
+    const float sr = __int_as_float((127 + kKq) << 23);  // 2^kKq
+    float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) {
+        const int base = 32 * gg + 8 * tig;
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) y[e] = hv ? __bfloat162float(qrow[base + e]) : 0.0f;
+        Q.br0[2 * gg] = pack_bf16x2(y[0] * sr, y[2] * sr);
+        Q.br1[2 * gg] = pack_bf16x2(y[1] * sr, y[3] * sr);
+        Q.br0[2 * gg + 1] = pack_bf16x2(y[4] * sr, y[6] * sr);
+        Q.br1[2 * gg + 1] = pack_bf16x2(y[5] * sr, y[7] * sr);
+        part[gg] = ((y[0] + y[1]) + (y[2] + y[3])) + ((y[4] + y[5]) + (y[6] + y[7]));
+    }
+    group_sums(part, tig, Q.qs);
+}
+
+// D[gg] = sum over group gg of q . code (scaled by 2^(kKq-133)) for rows (g, g+8) x heads.
+__device__ __forceinline__ void thumb_mma(float (&D)[4][4], const uint32_t (&w0)[8],
+                                          const uint32_t (&w1)[8], uint32_t m0,
+                                          const ThumbOps &Q) {
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) D[gg][0] = D[gg][1] = D[gg][2] = D[gg][3] = 0.0f;
+#pragma unroll
+    for (int kc = 0; kc < 8; kc++) {
+        const uint32_t a0 = w0[kc] & m0, a1 = w1[kc] & m0;
+        const uint32_t a2 = (w0[kc] >> 8) & m0, a3 = (w1[kc] >> 8) & m0;
+        mma_bf16(D[kc >> 1], a0, a1, a2, a3, Q.bt0[kc], Q.bt1[kc]);
+    }
+}
+
+// D[gg] = sum over group gg of q . (c8 + 128) (scaled by 2^(kKq-133)).
+// x0[gg] / x1[gg]: bytes 32gg + 8tig .. +7 of rows g / g+8.
+__device__ __forceinline__ void resid_mma(float (&D)[4][4], const uint2 (&x0)[4],
+                                          const uint2 (&x1)[4], const ResidOps &Q) {
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) D[gg][0] = D[gg][1] = D[gg][2] = D[gg][3] = 0.0f;
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) {
+#pragma unroll
+        for (int half = 0; half < 2; half++) {
+            const uint32_t v0 = half ? x0[gg].y : x0[gg].x;
+            const uint32_t v1 = half ? x1[gg].y : x1[gg].x;
+            const uint32_t a0 = (v0 & 0x00FF00FFu) ^ 0x00800080u;
+            const uint32_t a1 = (v1 & 0x00FF00FFu) ^ 0x00800080u;
+            const uint32_t a2 = ((v0 >> 8) & 0x00FF00FFu) ^ 0x00800080u;
+            const uint32_t a3 = ((v1 >> 8) & 0x00FF00FFu) ^ 0x00800080u;
+            mma_bf16(D[gg], a0, a1, a2, a3, Q.br0[2 * gg + half], Q.br1[2 * gg + half]);
+        }
+    }
+}
+
+__device__ __forceinline__ void unpack4h(uint2 v, float (&f)[4]) {
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+    f[0] = lo.x;
+    f[1] = lo.y;
+    f[2] = hi.x;
+    f[3] = hi.y;
+}
+
+// Provisional score s^ = sm * sum_g (scale_g q_g.c_g + zero_g sum(q_g)) of accumulator entry e.
+__device__ __forceinline__ float est_score(const float (&D)[4][4], int e, const float (&sf)[4],
+                                           const float (&zf)[4], const float (&qs)[4], float sm) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++)
+        acc = fmaf(sf[gg] * kUnscale, D[gg][e], fmaf(zf[gg], qs[gg], acc));
+    return acc * sm;
+}
+
+// Residual correction sm * sum_g r_scale_g q_g . c8_g of accumulator entry e.
+__device__ __forceinline__ float corr_score(const float (&D)[4][4], int e, const float (&sr)[4],
+                                            const float (&qs)[4], float sm) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++)
+        acc = fmaf(sr[gg], fmaf(kUnscale, D[gg][e], -128.0f * qs[gg]), acc);
+    return acc * sm;
+}
+
+// Pseudo-max of heads 2tig, 2tig+1 from the stage-1 block maxima (-inf when there are none).
+__device__ __forceinline__ void load_mtilde(const DecodeArgs &a, int u, int tig, float &m0,
+                                            float &m1) {
+    m0 = -INFINITY;
+    m1 = -INFINITY;
+    for (int s = 0; s < a.nf; s++) {
+        const float *p = a.ws_m1 + ((size_t)u * a.nf + s) * kMaxG;
+        m0 = fmaxf(m0, p[2 * tig]);
+        m1 = fmaxf(m1, p[2 * tig + 1]);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Stage 1: one CTA per (forced-block slot, unit); warp w takes 16 tokens. Exact scores of the sink
+// and local tokens; per-head maxima of the block go to ws_m1. Slot 0 of every unit also clears the
+// keep-mask tail and writes the output of an empty sequence.
+// ------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) stage1_kernel(const DecodeArgs a) {
+    grid_launch_dependents();
     __shared__ float red[4][kMaxG];
-    const int bh = blockIdx.y;
-    const int b = bh / a.Hkv, h = bh % a.Hkv;
+    const int u = blockIdx.y, b = u / a.Hkv, h = u % a.Hkv;
     const int slot = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = checked_seq_len(a, b);
+    const int g = lane >> 2, tig = lane & 3;
+    const int raw_n = a.seq_lens[b];
+    const int n = len_of(a, b);
+    if (slot == 0) {
+        if (tid == 0 && h == 0 && raw_n != n) raise_error(a.err, FFD_ERRBIT_BOUNDS);
+        const int nb = (n + kPage - 1) / kPage;
+        if (a.keep_mask)
+            for (int blk = nb + tid; blk < a.max_blocks; blk += blockDim.x)
+                a.keep_mask[(size_t)u * a.max_blocks + blk] = 0;
+        if (n == 0) {
+            for (int idx = tid; idx < a.G * kD; idx += blockDim.x)
+                a.out[((size_t)b * a.Hq + h * a.G) * kD + idx] = 0.0f;
+            if (a.m_tilde && tid < a.G) a.m_tilde[(size_t)b * a.Hq + h * a.G + tid] = -INFINITY;
+        }
+    }
+    if (a.nf == 0) return;
     const ForcedBlocks fb(n, a.S, a.L);
-    float *dst = a.ws_m1 + ((size_t)bh * a.nf + slot) * kMaxG;
+    float *dst = a.ws_m1 + ((size_t)u * a.nf + slot) * kMaxG;
     int page = -1;
     if (slot < fb.count) {
         page = a.block_table[(size_t)b * a.max_blocks + fb.block(slot)];
@@ -38,303 +366,631 @@ __global__ void __launch_bounds__(128) stage1_kernel(DecodeArgs a) {
         return;
     }
     const int blk = fb.block(slot);
-    for (int idx = tid; idx < a.G * kD; idx += blockDim.x) {
-        const int i = idx / kD, c = idx % kD;
-        qs[i][c] = __bfloat162float(a.q[((size_t)b * a.Hq + h * a.G + i) * kD + c]);
-    }
-    __syncthreads();
+    ThumbOps Q;
+    ResidOps QR;
+    load_thumb_ops(a, b, h, lane, Q);
+    load_resid_ops(a, b, h, lane, QR);
 
-    const int t = tid >> 1, hf = tid & 1;
-    const int j = blk * kPage + t;
-    const bool valid = j < n && (j < a.S || j >= n - a.L);
-    const size_t row = ((size_t)page * a.Hkv + h) * kPage + t;
-    float acc[kMaxG];
-#pragma unroll
-    for (int i = 0; i < kMaxG; i++) acc[i] = 0.0f;
-#pragma unroll
-    for (int gg = 0; gg < 2; gg++) {
-        const int g = 2 * hf + gg;
-        const float sf = __half2float(a.t_scale[row * kGroups + g]);
-        const float zf = __half2float(a.t_zero[row * kGroups + g]);
-        const float sr = __half2float(a.r_scale[row * kGroups + g]);
-        const uint2 cw = *reinterpret_cast<const uint2 *>(a.thumb + row * kThumbRow + g * 8);
-        const int4 *rp = reinterpret_cast<const int4 *>(a.resid + row * kD + g * kGroupSize);
-        int4 r8[2] = {rp[0], rp[1]};
-        const int8_t *r8b = reinterpret_cast<const int8_t *>(r8);
-#pragma unroll
-        for (int c = 0; c < kGroupSize; c++) {
-            const uint32_t word = c < 16 ? cw.x : cw.y;
-            const float code = (float)((word >> (2 * (c & 15))) & 3u);
-            const float x2 = __fmaf_rn(code, sf, zf);
-            const float kh = __fmaf_rn((float)r8b[c], sr, x2);
-#pragma unroll
-            for (int i = 0; i < kMaxG; i++)
-                if (i < a.G) acc[i] = fmaf(qs[i][g * kGroupSize + c], kh, acc[i]);
-        }
+    const size_t tile = (size_t)page * a.Hkv + h;
+    const int r0 = 16 * warp + g, r1 = r0 + 8;
+    uint32_t w0[8], w1[8];
+    {
+        const uint4 *c0 = reinterpret_cast<const uint4 *>(a.thumb + (tile * kPage + r0) * kThumbRow);
+        const uint4 *c1 = reinterpret_cast<const uint4 *>(a.thumb + (tile * kPage + r1) * kThumbRow);
+        const uint4 p0 = c0[0], p1 = c0[1], p2 = c1[0], p3 = c1[1];
+        w0[0] = p0.x; w0[1] = p0.y; w0[2] = p0.z; w0[3] = p0.w;
+        w0[4] = p1.x; w0[5] = p1.y; w0[6] = p1.z; w0[7] = p1.w;
+        w1[0] = p2.x; w1[1] = p2.y; w1[2] = p2.z; w1[3] = p2.w;
+        w1[4] = p3.x; w1[5] = p3.y; w1[6] = p3.z; w1[7] = p3.w;
     }
+    uint2 x0[4], x1[4];
 #pragma unroll
-    for (int i = 0; i < kMaxG; i++) {
-        acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 1);
-        float s = valid ? acc[i] * a.sm_scale : -INFINITY;
-        s = warp_max(s);
-        if (lane == 0) red[warp][i] = s;
+    for (int gg = 0; gg < 4; gg++) {
+        x0[gg] = *reinterpret_cast<const uint2 *>(a.resid + (tile * kPage + r0) * kD + 32 * gg + 8 * tig);
+        x1[gg] = *reinterpret_cast<const uint2 *>(a.resid + (tile * kPage + r1) * kD + 32 * gg + 8 * tig);
+    }
+    float sf0[4], sf1[4], zf0[4], zf1[4], sr0[4], sr1[4];
+    const uint2 *ts = reinterpret_cast<const uint2 *>(a.t_scale);
+    const uint2 *tz = reinterpret_cast<const uint2 *>(a.t_zero);
+    const uint2 *rs = reinterpret_cast<const uint2 *>(a.r_scale);
+    unpack4h(ts[tile * kPage + r0], sf0);
+    unpack4h(ts[tile * kPage + r1], sf1);
+    unpack4h(tz[tile * kPage + r0], zf0);
+    unpack4h(tz[tile * kPage + r1], zf1);
+    unpack4h(rs[tile * kPage + r0], sr0);
+    unpack4h(rs[tile * kPage + r1], sr1);
+
+    float D[4][4], Dr[4][4];
+    thumb_mma(D, w0, w1, 0x00030003u << (2 * tig), Q);
+    resid_mma(Dr, x0, x1, QR);
+    const float sm = a.sm_scale;
+    const float s00 = est_score(D, 0, sf0, zf0, Q.qs[0], sm) + corr_score(Dr, 0, sr0, Q.qs[0], sm);
+    const float s01 = est_score(D, 1, sf0, zf0, Q.qs[1], sm) + corr_score(Dr, 1, sr0, Q.qs[1], sm);
+    const float s10 = est_score(D, 2, sf1, zf1, Q.qs[0], sm) + corr_score(Dr, 2, sr1, Q.qs[0], sm);
+    const float s11 = est_score(D, 3, sf1, zf1, Q.qs[1], sm) + corr_score(Dr, 3, sr1, Q.qs[1], sm);
+    const int t0 = blk * kPage + r0, t1 = blk * kPage + r1;
+    const bool v0 = t0 < n && (t0 < a.S || t0 >= n - a.L);
+    const bool v1 = t1 < n && (t1 < a.S || t1 >= n - a.L);
+    float mx0 = fmaxf(v0 ? s00 : -INFINITY, v1 ? s10 : -INFINITY);
+    float mx1 = fmaxf(v0 ? s01 : -INFINITY, v1 ? s11 : -INFINITY);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    if (g == 0) {
+        red[warp][2 * tig] = mx0;
+        red[warp][2 * tig + 1] = mx1;
     }
     __syncthreads();
-    if (tid < a.G)
-        dst[tid] = fmaxf(fmaxf(red[0][tid], red[1][tid]), fmaxf(red[2][tid], red[3][tid]));
-    else if (tid < kMaxG)
-        dst[tid] = -INFINITY;
+    if (tid < kMaxG)
+        dst[tid] = tid < a.G ? fmaxf(fmaxf(red[0][tid], red[1][tid]), fmaxf(red[2][tid], red[3][tid]))
+                             : -INFINITY;
 }
 
 // ------------------------------------------------------------------------------------------
-// Stages 2 + 3, one CTA per (split, sequence x KV head); 128 threads.
-//   scan:   token t = tid/2 and channel half tid%2 compute the provisional score from the 2-bit
-//           thumbnail, group-factored: s^ = sm * sum_g (scale_g * (q_g . c_g) + zero_g * sum q_g).
-//   filter: the block is kept when any valid token of any head reaches m~ - delta, or when it is
-//           a sink / local block.
-//   refine: s = s^ + sm * sum_g r_scale_g * (q_g . c8_g) (the scan result is reused); online
-//           softmax per head; PV with thread = (channel pair, half of the heads).
+// Main kernel: persistent, one CTA per SM. Warp 8 is the TMA producer; warps 0-7 consume.
 // ------------------------------------------------------------------------------------------
-template <int G>
-__global__ void __launch_bounds__(128) main_kernel(DecodeArgs a) {
-    __shared__ float qs[G][kD + 4];
-    __shared__ float qsum[G][kGroups];
-    __shared__ float thr[G];
-    __shared__ float sp[kPage][G + 1];  // scores, then probabilities
-    __shared__ float m_run[G], l_run[G], alpha[G];
+struct Smem {
+    uint8_t *ring, *thumb, *shat;
+    float *cbuf;
+    UnitOps *unit;  // [2]
+    Misc *misc;
+};
 
-    const int bh = blockIdx.y;
-    const int split = blockIdx.x;
-    const int b = bh / a.Hkv, h = bh % a.Hkv;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = checked_seq_len(a, b);
+// Bounded wait: after kWaitTimeoutNs the CTA records FFD_ERRBIT_TIMEOUT, marks itself aborted and
+// stops waiting (its results are then garbage, but every thread still reaches every barrier).
+__device__ __forceinline__ void wait_bar(const DecodeArgs &a, Misc *m, uint64_t *bar,
+                                         uint32_t parity) {
+    if (*reinterpret_cast<volatile uint32_t *>(&m->aborted)) return;
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            raise_error(a.err, FFD_ERRBIT_TIMEOUT);
+            *reinterpret_cast<volatile uint32_t *>(&m->aborted) = 1;
+            return;
+        }
+    }
+}
+
+// Producer: thumbnails of sub-chunk t into buffer t&1.
+__device__ __forceinline__ void issue_thumbs(const DecodeArgs &a, const Smem &S, const Sub &s,
+                                             int t) {
+    Misc *m = S.misc;
+    const int buf = t & 1;
+    const int32_t *bt = a.block_table + (size_t)s.b * a.max_blocks + s.j0;
+    uint32_t bad = 0;
+    for (int k = 0; k < s.cnt; k++) {
+        const int page = bt[k];
+        if (page < 0 || page >= a.P) {
+            bad |= 1u << k;
+            raise_error(a.err, FFD_ERRBIT_BOUNDS);
+        }
+    }
+    m->bad[buf] = bad;
+    const int good = s.cnt - __popc(bad);
+    mbar_arrive_expect_tx(&m->thumb_full[buf], (uint32_t)(good * kThumbBlock));
+    uint8_t *dst = S.thumb + buf * (kSub * kThumbBlock);
+    for (int k = 0; k < s.cnt; k++) {
+        if (bad & (1u << k)) continue;
+        const size_t tile = (size_t)bt[k] * a.Hkv + s.h;
+        uint8_t *d = dst + k * kThumbBlock;
+        tma_load_1d(d, a.thumb + tile * kPage * kThumbRow, 2048, &m->thumb_full[buf]);
+        tma_load_1d(d + 2048, a.t_scale + tile * kPage * kGroups, 512, &m->thumb_full[buf]);
+        tma_load_1d(d + 2560, a.t_zero + tile * kPage * kGroups, 512, &m->thumb_full[buf]);
+    }
+}
+
+__device__ __forceinline__ void producer(const MainParams &prm, const Smem &S, int cta, int ncta) {
+    const DecodeArgs &a = prm.a;
+    Misc *m = S.misc;
+    prefetch_tensormap(&prm.tm_resid);
+    prefetch_tensormap(&prm.tm_v);
+    Sched sch;
+    sch.init(a, cta, ncta);
+    Sub q[3];
+    int fetched = 0;
+    while (fetched < 2 && sch.next(a, q[fetched])) fetched++;
+    for (int t = 0; t < fetched; t++) issue_thumbs(a, S, q[t], t);
+    int kb = 0;
+    for (int t = 0; t < fetched; t++) {
+        const Sub cur = q[t % 3];
+        wait_bar(a, m, &m->decision[t & 1], (t >> 1) & 1);
+        const uint32_t mask = *reinterpret_cast<volatile uint32_t *>(&m->final_mask[t & 1]);
+        if (sch.next(a, q[fetched % 3])) {
+            issue_thumbs(a, S, q[fetched % 3], fetched);
+            fetched++;
+        }
+        for (int k = 0; k < cur.cnt; k++) {
+            if (!(mask & (1u << k))) continue;
+            const int slot = kb % kRing, round = kb / kRing;
+            kb++;
+            if (round > 0) wait_bar(a, m, &m->ring_empty[slot], (round - 1) & 1);
+            const int page = a.block_table[(size_t)cur.b * a.max_blocks + cur.j0 + k];
+            const int row = (int)(((size_t)page * a.Hkv + cur.h) * kPage);
+            uint8_t *d = S.ring + slot * kSlotBytes;
+            uint64_t *bar = &m->ring_full[slot];
+            mbar_arrive_expect_tx(bar, kSlotTx);
+            tma_load_2d(d, &prm.tm_resid, 0, row, bar);
+            tma_load_2d(d + kSlotV, &prm.tm_v, 0, row, bar);
+            tma_load_2d(d + kSlotV + 8192, &prm.tm_v, 64, row, bar);
+            tma_load_1d(d + kSlotRScale, a.r_scale + (size_t)row * kGroups, 512, bar);
+        }
+    }
+    // leave no copy in flight: wait for the last fill of every ring slot
+    for (int s = 0; s < kRing && s < kb; s++) {
+        const int last = kb - 1 - ((kb - 1 - s) % kRing);
+        wait_bar(a, m, &m->ring_full[s], (last / kRing) & 1);
+    }
+}
+
+// Warp 0 computes the unit's query operands and thresholds into a unit slot; every consumer
+// warp then reads them from shared memory.
+__device__ __forceinline__ void setup_unit(const DecodeArgs &a, const Smem &S, const Sub &s,
+                                           int slot, int warp, int lane) {
+    if (warp == 0) {
+        UnitOps &U = S.unit[slot];
+        const int g = lane >> 2, tig = lane & 3;
+        ThumbOps T;
+        ResidOps Rr;
+        load_thumb_ops(a, s.b, s.h, lane, T);
+        load_resid_ops(a, s.b, s.h, lane, Rr);
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            U.bt[r][lane] = make_uint4(T.bt0[4 * r], T.bt0[4 * r + 1], T.bt0[4 * r + 2], T.bt0[4 * r + 3]);
+            U.bt[2 + r][lane] = make_uint4(T.bt1[4 * r], T.bt1[4 * r + 1], T.bt1[4 * r + 2], T.bt1[4 * r + 3]);
+            U.br[r][lane] = make_uint4(Rr.br0[4 * r], Rr.br0[4 * r + 1], Rr.br0[4 * r + 2], Rr.br0[4 * r + 3]);
+            U.br[2 + r][lane] = make_uint4(Rr.br1[4 * r], Rr.br1[4 * r + 1], Rr.br1[4 * r + 2], Rr.br1[4 * r + 3]);
+        }
+        if (g == 0) {
+            U.qs[2 * tig] = make_float4(T.qs[0][0], T.qs[0][1], T.qs[0][2], T.qs[0][3]);
+            U.qs[2 * tig + 1] = make_float4(T.qs[1][0], T.qs[1][1], T.qs[1][2], T.qs[1][3]);
+        }
+        if (lane < kMaxG) {
+            float m = -INFINITY;
+            const int u = s.b * a.Hkv + s.h;
+            for (int sl = 0; sl < a.nf; sl++)
+                m = fmaxf(m, a.ws_m1[((size_t)u * a.nf + sl) * kMaxG + lane]);
+            U.mt[lane] = m;
+            U.thr[lane] = lane < a.G ? m - a.delta : INFINITY;
+        }
+        if (lane == 0) U.n = len_of(a, s.b);
+    }
+    named_barrier_sync(1, kConsumers);
+}
+
+__device__ __forceinline__ void load_frags(const uint4 (&src)[4][32], int lane, uint32_t (&f0)[8],
+                                           uint32_t (&f1)[8]) {
+    const uint4 p0 = src[0][lane], p1 = src[1][lane], p2 = src[2][lane], p3 = src[3][lane];
+    f0[0] = p0.x; f0[1] = p0.y; f0[2] = p0.z; f0[3] = p0.w;
+    f0[4] = p1.x; f0[5] = p1.y; f0[6] = p1.z; f0[7] = p1.w;
+    f1[0] = p2.x; f1[1] = p2.y; f1[2] = p2.z; f1[3] = p2.w;
+    f1[4] = p3.x; f1[5] = p3.y; f1[6] = p3.z; f1[7] = p3.w;
+}
+
+// Scan of sub-chunk t: provisional scores of this warp's m-tiles, block votes, final mask.
+__device__ __forceinline__ uint32_t scan_sub(const DecodeArgs &a, const Smem &S, const Sub &s,
+                                             int t, int uslot, int warp, int lane) {
+    Misc *m = S.misc;
+    const UnitOps &U = S.unit[uslot];
+    const int g = lane >> 2, tig = lane & 3, grp = warp >> 2, mt = warp & 3;
+    const int buf = t & 1;
+    wait_bar(a, m, &m->thumb_full[buf], (t >> 1) & 1);
+    const uint32_t bad = m->bad[buf];
+    const uint32_t m0 = 0x00030003u << (2 * tig);
+    const float sm = a.sm_scale;
+    const float thr0 = U.thr[2 * tig], thr1 = U.thr[2 * tig + 1];
+    const int n = U.n;
+    uint32_t votes = 0;
+    const int r0 = 16 * mt + g, r1 = r0 + 8;
+    for (int k = grp; k < s.cnt; k += 2) {
+        ThumbOps Q;
+        load_frags(U.bt, lane, Q.bt0, Q.bt1);
+        {
+            const float4 q0 = U.qs[2 * tig], q1 = U.qs[2 * tig + 1];
+            Q.qs[0][0] = q0.x; Q.qs[0][1] = q0.y; Q.qs[0][2] = q0.z; Q.qs[0][3] = q0.w;
+            Q.qs[1][0] = q1.x; Q.qs[1][1] = q1.y; Q.qs[1][2] = q1.z; Q.qs[1][3] = q1.w;
+        }
+        const uint8_t *base = S.thumb + buf * (kSub * kThumbBlock) + k * kThumbBlock;
+        const uint4 *c0 = reinterpret_cast<const uint4 *>(base + r0 * kThumbRow);
+        const uint4 *c1 = reinterpret_cast<const uint4 *>(base + r1 * kThumbRow);
+        const uint4 p0 = c0[0], p1 = c0[1], p2 = c1[0], p3 = c1[1];
+        const uint32_t w0[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        const uint32_t w1[8] = {p2.x, p2.y, p2.z, p2.w, p3.x, p3.y, p3.z, p3.w};
+        float D[4][4];
+        thumb_mma(D, w0, w1, m0, Q);
+        float sf0[4], sf1[4], zf0[4], zf1[4];
+        const uint2 *ts = reinterpret_cast<const uint2 *>(base + 2048);
+        const uint2 *tz = reinterpret_cast<const uint2 *>(base + 2560);
+        unpack4h(ts[r0], sf0);
+        unpack4h(ts[r1], sf1);
+        unpack4h(tz[r0], zf0);
+        unpack4h(tz[r1], zf1);
+        float4 e;
+        e.x = est_score(D, 0, sf0, zf0, Q.qs[0], sm);
+        e.y = est_score(D, 1, sf0, zf0, Q.qs[1], sm);
+        e.z = est_score(D, 2, sf1, zf1, Q.qs[0], sm);
+        e.w = est_score(D, 3, sf1, zf1, Q.qs[1], sm);
+        const int blk = s.j0 + k;
+        const bool v0 = blk * kPage + r0 < n, v1 = blk * kPage + r1 < n;
+        const bool pass = (v0 && (e.x >= thr0 || e.y >= thr1)) ||
+                          (v1 && (e.z >= thr0 || e.w >= thr1));
+        if (__any_sync(0xffffffffu, pass)) votes |= 1u << k;
+        reinterpret_cast<float4 *>(S.shat + buf * kShatBuf)[((k * 4) + mt) * 32 + lane] = e;
+    }
+    if (lane == 0) m->votes[buf][warp] = votes;
+    named_barrier_sync(1, kConsumers);
+    uint32_t mask = 0;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; w++) mask |= m->votes[buf][w];
     const ForcedBlocks fb(n, a.S, a.L);
-    const int blk0 = split * a.blk_per_split;
-    const int blk_end = min(blk0 + a.blk_per_split, a.max_blocks);
-    const int blk1 = min(blk_end, fb.nb);
-
-    for (int idx = tid; idx < G * kD; idx += blockDim.x) {
-        const int i = idx / kD, c = idx % kD;
-        qs[i][c] = __bfloat162float(a.q[((size_t)b * a.Hq + h * G + i) * kD + c]);
+    for (int k = 0; k < s.cnt; k++)
+        if (fb.forced(s.j0 + k)) mask |= 1u << k;
+    mask &= ~bad;
+    mask &= (1u << s.cnt) - 1u;
+    if (warp == 0 && lane == 0) {
+        m->final_mask[buf] = mask;
+        if (a.keep_mask) {
+            uint8_t *km = a.keep_mask + ((size_t)s.b * a.Hkv + s.h) * a.max_blocks + s.j0;
+            for (int k = 0; k < s.cnt; k++) km[k] = (mask >> k) & 1u;
+        }
+        mbar_arrive(&m->decision[buf]);
     }
-    if (tid < G) {
-        float m = -INFINITY;
-        for (int s = 0; s < a.nf; s++) m = fmaxf(m, a.ws_m1[((size_t)bh * a.nf + s) * kMaxG + tid]);
-        thr[tid] = m - a.delta;  // -inf when delta = +inf or no sink/local token exists
-        m_run[tid] = -INFINITY;
-        l_run[tid] = 0.0f;
-        if (split == 0 && a.m_tilde) a.m_tilde[(size_t)b * a.Hq + h * G + tid] = m;
+    return mask;
+}
+
+// Refine-side state of the unit being refined: its query operands, and this warp's running
+// softmax state (max, sum, O^T accumulators) for heads 2tig, 2tig+1.
+struct RefineState {
+    float m0, m1, l0, l1;
+    float o[8][4];
+};
+
+__device__ __forceinline__ void reset_refine(RefineState &R) {
+    R.m0 = R.m1 = -INFINITY;
+    R.l0 = R.l1 = 0.0f;
+#pragma unroll
+    for (int md = 0; md < 8; md++) R.o[md][0] = R.o[md][1] = R.o[md][2] = R.o[md][3] = 0.0f;
+}
+
+// Stage 3 on this warp's m-tile of one kept block held in a ring slot.
+__device__ __forceinline__ void refine_tile(const DecodeArgs &a, const uint8_t *slot,
+                                            const UnitOps &U, const float4 est, int blk,
+                                            RefineState &R, int mt, int lane) {
+    const int g = lane >> 2, tig = lane & 3;
+    ResidOps Q;
+    load_frags(U.br, lane, Q.br0, Q.br1);
+    {
+        const float4 q0 = U.qs[2 * tig], q1 = U.qs[2 * tig + 1];
+        Q.qs[0][0] = q0.x; Q.qs[0][1] = q0.y; Q.qs[0][2] = q0.z; Q.qs[0][3] = q0.w;
+        Q.qs[1][0] = q1.x; Q.qs[1][1] = q1.y; Q.qs[1][2] = q1.z; Q.qs[1][3] = q1.w;
     }
-    if (a.keep_mask)
-        for (int blk = max(blk0, fb.nb) + tid; blk < blk_end; blk += blockDim.x)
-            a.keep_mask[(size_t)bh * a.max_blocks + blk] = 0;
-    __syncthreads();
-    if (tid < G * kGroups) {
-        const int i = tid / kGroups, g = tid % kGroups;
-        float s = 0.0f;
-        for (int c = 0; c < kGroupSize; c++) s += qs[i][g * kGroupSize + c];
-        qsum[i][g] = s;
+    const int n = U.n;
+    const int r0 = 16 * mt + g, r1 = r0 + 8;
+    uint2 x0[4], x1[4];
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) {
+        const int o = 32 * gg + 8 * tig;
+        x0[gg] = *reinterpret_cast<const uint2 *>(slot + r0 * 128 +
+                                                  ((((o >> 4) ^ (r0 & 7)) << 4) | (o & 15)));
+        x1[gg] = *reinterpret_cast<const uint2 *>(slot + r1 * 128 +
+                                                  ((((o >> 4) ^ (r1 & 7)) << 4) | (o & 15)));
     }
-    __syncthreads();
+    float Dr[4][4];
+    resid_mma(Dr, x0, x1, Q);
+    float sr0[4], sr1[4];
+    const uint2 *rs = reinterpret_cast<const uint2 *>(slot + kSlotRScale);
+    unpack4h(rs[r0], sr0);
+    unpack4h(rs[r1], sr1);
+    const float sm = a.sm_scale;
+    const bool v0 = blk * kPage + r0 < n, v1 = blk * kPage + r1 < n;
+    const float s00 = v0 ? est.x + corr_score(Dr, 0, sr0, Q.qs[0], sm) : -INFINITY;
+    const float s01 = v0 ? est.y + corr_score(Dr, 1, sr0, Q.qs[1], sm) : -INFINITY;
+    const float s10 = v1 ? est.z + corr_score(Dr, 2, sr1, Q.qs[0], sm) : -INFINITY;
+    const float s11 = v1 ? est.w + corr_score(Dr, 3, sr1, Q.qs[1], sm) : -INFINITY;
 
-    const int t = tid >> 1, hf = tid & 1;
-    const int dp = tid & 63, hh = tid >> 6;  // PV mapping: channel pair, head half
-    float o[4][2];
+    // online softmax, heads 2tig (0) and 2tig+1 (1)
+    float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
-    for (int k = 0; k < 4; k++) o[k][0] = o[k][1] = 0.0f;
+    for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(R.m0, mx0), mn1 = fmaxf(R.m1, mx1);
+    const float mu0 = mn0 == -INFINITY ? 0.0f : mn0, mu1 = mn1 == -INFINITY ? 0.0f : mn1;
+    const float al0 = exp2f((R.m0 - mu0) * kLog2e), al1 = exp2f((R.m1 - mu1) * kLog2e);
+    const float p00 = exp2f((s00 - mu0) * kLog2e), p01 = exp2f((s01 - mu1) * kLog2e);
+    const float p10 = exp2f((s10 - mu0) * kLog2e), p11 = exp2f((s11 - mu1) * kLog2e);
+    R.m0 = mn0;
+    R.m1 = mn1;
+    R.l0 = fmaf(R.l0, al0, p00 + p10);
+    R.l1 = fmaf(R.l1, al1, p01 + p11);
+    if (__any_sync(0xffffffffu, al0 != 1.0f || al1 != 1.0f)) {
+#pragma unroll
+        for (int md = 0; md < 8; md++) {
+            R.o[md][0] *= al0;
+            R.o[md][1] *= al1;
+            R.o[md][2] *= al0;
+            R.o[md][3] *= al1;
+        }
+    }
+    // P^T fragments, bf16 hi + lo
+    const uint32_t h0 = pack_bf16x2(p00, p01), h1 = pack_bf16x2(p10, p11);
+    const uint32_t l0 = pack_bf16x2(p00 - __uint_as_float(h0 << 16),
+                                    p01 - __uint_as_float(h0 & 0xffff0000u));
+    const uint32_t l1 = pack_bf16x2(p10 - __uint_as_float(h1 << 16),
+                                    p11 - __uint_as_float(h1 & 0xffff0000u));
+    const uint32_t bh0 = movmatrix_trans(h0), bh1 = movmatrix_trans(h1);
+    const uint32_t bl0 = movmatrix_trans(l0), bl1 = movmatrix_trans(l1);
+    // V^T fragments by ldmatrix.trans from the swizzled tile (16-byte chunk c of row r is stored
+    // at chunk c ^ (r % 8))
+    const int mi = lane >> 3, jr = lane & 7;
+    const int tok = 16 * mt + ((mi >> 1) << 3) + jr;
+    const uint32_t vrow = smem_u32(slot + kSlotV) + tok * 128;
+#pragma unroll
+    for (int md = 0; md < 8; md++) {
+        const int chunk = 2 * (md & 3) + (mi & 1);
+        const uint32_t addr = vrow + (md >> 2) * 8192 + ((chunk ^ jr) << 4);
+        uint32_t v0r, v1r, v2r, v3r;
+        ldmatrix_x4_trans(v0r, v1r, v2r, v3r, addr);
+        mma_bf16(R.o[md], v0r, v1r, v2r, v3r, bh0, bh1);
+        mma_bf16(R.o[md], v0r, v1r, v2r, v3r, bl0, bl1);
+    }
+}
 
-    for (int blk = blk0; blk < blk1; blk++) {
-        int page = a.block_table[(size_t)b * a.max_blocks + blk];
-        if (page < 0 || page >= a.P) {  // uniform across the CTA
-            if (tid == 0) {
-                raise_error(a.err, FFD_ERRBIT_BOUNDS);
-                if (a.keep_mask) a.keep_mask[(size_t)bh * a.max_blocks + blk] = 0;
-            }
-            continue;
-        }
-        const size_t row = ((size_t)page * a.Hkv + h) * kPage + t;
-        const int j = blk * kPage + t;
-        const bool valid = j < n;
-
-        // ---- stage 2: provisional scores from the thumbnail
-        float est[G];
+// Combine the 8 warps' softmax states into this CTA's record for the unit; the last CTA of the
+// unit (atomic ticket, no waiting) merges all records of the unit into the output.
+__device__ __forceinline__ void combine_unit(const DecodeArgs &a, const Smem &S, const Sub &s,
+                                             const RefineState &R, const UnitOps &U, int cta,
+                                             int ncta, int64_t T, int warp, int lane) {
+    const int g = lane >> 2, tig = lane & 3, tid = warp * 32 + lane;
+    float l0 = R.l0, l1 = R.l1;
 #pragma unroll
-        for (int i = 0; i < G; i++) est[i] = 0.0f;
+    for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    float *cb = S.cbuf + warp * kCbufWarp;
 #pragma unroll
-        for (int gg = 0; gg < 2; gg++) {
-            const int g = 2 * hf + gg;
-            const float sf = __half2float(a.t_scale[row * kGroups + g]);
-            const float zf = __half2float(a.t_zero[row * kGroups + g]);
-            const uint2 cw = *reinterpret_cast<const uint2 *>(a.thumb + row * kThumbRow + g * 8);
-            float acc[G];
+    for (int md = 0; md < 8; md++) {
+        const int d = 16 * md + g;
+        cb[(2 * tig) * kD + d] = R.o[md][0];
+        cb[(2 * tig + 1) * kD + d] = R.o[md][1];
+        cb[(2 * tig) * kD + d + 8] = R.o[md][2];
+        cb[(2 * tig + 1) * kD + d + 8] = R.o[md][3];
+    }
+    if (g == 0) {
+        cb[kMaxG * kD + 2 * tig] = R.m0;
+        cb[kMaxG * kD + 2 * tig + 1] = R.m1;
+        cb[kMaxG * kD + kMaxG + 2 * tig] = l0;
+        cb[kMaxG * kD + kMaxG + 2 * tig + 1] = l1;
+    }
+    named_barrier_sync(1, kConsumers);
+    const int u = s.b * a.Hkv + s.h;
+    float *rec = a.ws_part + (size_t)(u + cta) * a.G * kPartStride;
+    for (int idx = tid; idx < a.G * kD; idx += kConsumers) {
+        const int i = idx / kD, d = idx % kD;
+        float M = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < G; i++) acc[i] = 0.0f;
+        for (int w = 0; w < kConsumerWarps; w++)
+            M = fmaxf(M, S.cbuf[w * kCbufWarp + kMaxG * kD + i]);
+        float num = 0.0f, den = 0.0f;
+        if (M != -INFINITY) {
 #pragma unroll
-            for (int c = 0; c < kGroupSize; c++) {
-                const uint32_t word = c < 16 ? cw.x : cw.y;
-                const float code = (float)((word >> (2 * (c & 15))) & 3u);
-#pragma unroll
-                for (int i = 0; i < G; i++) acc[i] = fmaf(qs[i][g * kGroupSize + c], code, acc[i]);
-            }
-#pragma unroll
-            for (int i = 0; i < G; i++) est[i] = fmaf(sf, acc[i], fmaf(zf, qsum[i][g], est[i]));
-        }
-        bool pass = false;
-#pragma unroll
-        for (int i = 0; i < G; i++) {
-            est[i] += __shfl_xor_sync(0xffffffffu, est[i], 1);
-            pass |= valid && (est[i] * a.sm_scale >= thr[i]);
-        }
-        const bool keep = __syncthreads_or(pass) || fb.forced(blk);
-        if (a.keep_mask && tid == 0) a.keep_mask[(size_t)bh * a.max_blocks + blk] = keep ? 1 : 0;
-        if (!keep) continue;
-
-        // ---- stage 3: residual correction, exact scores
-        float corr[G];
-#pragma unroll
-        for (int i = 0; i < G; i++) corr[i] = 0.0f;
-#pragma unroll
-        for (int gg = 0; gg < 2; gg++) {
-            const int g = 2 * hf + gg;
-            const float sr = __half2float(a.r_scale[row * kGroups + g]);
-            const int4 *rp = reinterpret_cast<const int4 *>(a.resid + row * kD + g * kGroupSize);
-            int4 r8[2] = {rp[0], rp[1]};
-            const int8_t *r8b = reinterpret_cast<const int8_t *>(r8);
-            float acc[G];
-#pragma unroll
-            for (int i = 0; i < G; i++) acc[i] = 0.0f;
-#pragma unroll
-            for (int c = 0; c < kGroupSize; c++) {
-                const float c8 = (float)r8b[c];
-#pragma unroll
-                for (int i = 0; i < G; i++) acc[i] = fmaf(qs[i][g * kGroupSize + c], c8, acc[i]);
-            }
-#pragma unroll
-            for (int i = 0; i < G; i++) corr[i] = fmaf(sr, acc[i], corr[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < G; i++) {
-            corr[i] += __shfl_xor_sync(0xffffffffu, corr[i], 1);
-            const float s = valid ? (est[i] + corr[i]) * a.sm_scale : -INFINITY;
-            if (hf == 0) sp[t][i] = s;
-        }
-        __syncthreads();
-
-        // ---- online softmax bookkeeping: warp w handles heads w, w+4
-        for (int i = warp; i < G; i += 4) {
-            const float v0 = sp[lane][i], v1 = sp[lane + 32][i];
-            const float mb = warp_max(fmaxf(v0, v1));
-            const float m_old = m_run[i];
-            const float m_new = fmaxf(m_old, mb);
-            const float al = m_old == -INFINITY ? 0.0f : exp2f((m_old - m_new) * 1.4426950408889634f);
-            const float p0 = v0 == -INFINITY ? 0.0f : exp2f((v0 - m_new) * 1.4426950408889634f);
-            const float p1 = v1 == -INFINITY ? 0.0f : exp2f((v1 - m_new) * 1.4426950408889634f);
-            sp[lane][i] = p0;
-            sp[lane + 32][i] = p1;
-            const float ps = warp_sum(p0 + p1);
-            __syncwarp();
-            if (lane == 0) {
-                l_run[i] = l_run[i] * al + ps;
-                m_run[i] = m_new;
-                alpha[i] = al;
-            }
-        }
-        __syncthreads();
-
-        // ---- PV
-        const __nv_bfloat16 *vrow = a.v + ((size_t)page * a.Hkv + h) * kPage * kD + 2 * dp;
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int i = hh * 4 + k;
-            if (i < G) {
-                o[k][0] *= alpha[i];
-                o[k][1] *= alpha[i];
+            for (int w = 0; w < kConsumerWarps; w++) {
+                const float mw = S.cbuf[w * kCbufWarp + kMaxG * kD + i];
+                const float f = mw == -INFINITY ? 0.0f : exp2f((mw - M) * kLog2e);
+                num = fmaf(f, S.cbuf[w * kCbufWarp + i * kD + d], num);
+                den = fmaf(f, S.cbuf[w * kCbufWarp + kMaxG * kD + kMaxG + i], den);
             }
         }
-        for (int tt = 0; tt < kPage; tt++) {
-            const float2 vf = __bfloat1622float2(
-                *reinterpret_cast<const __nv_bfloat162 *>(vrow + (size_t)tt * kD));
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const int i = hh * 4 + k;
-                if (i < G) {
-                    const float p = sp[tt][i];
-                    o[k][0] = fmaf(p, vf.x, o[k][0]);
-                    o[k][1] = fmaf(p, vf.y, o[k][1]);
+        rec[i * kPartStride + d] = num;
+        if (d == 0) {
+            rec[i * kPartStride + kD] = M;
+            rec[i * kPartStride + kD + 1] = den;
+        }
+    }
+    __threadfence();
+    named_barrier_sync(1, kConsumers);
+    const int64_t first = s.x0 - s.j0;  // global index of the unit's block 0
+    const int nb = blocks_of(a, s.b);
+    const int cf = cta_of(first, T, ncta), cl = cta_of(first + nb - 1, T, ncta);
+    if (tid == 0) {
+        uint32_t last = 1;
+        if (cl > cf) {
+            int *cnt = a.ws_cnt + u;
+            const int old = atomicAdd(cnt, 1);
+            last = old == cl - cf;
+            if (last) *cnt = 0;  // ready for the next call
+        }
+        S.misc->merge_flag = last;
+    }
+    named_barrier_sync(1, kConsumers);
+    if (S.misc->merge_flag) {
+        __threadfence();
+        for (int idx = tid; idx < a.G * kD; idx += kConsumers) {
+            const int i = idx / kD, d = idx % kD;
+            float M = -INFINITY;
+            for (int c = cf; c <= cl; c++)
+                M = fmaxf(M, __ldcg(a.ws_part + ((size_t)(u + c) * a.G + i) * kPartStride + kD));
+            float num = 0.0f, den = 0.0f;
+            if (M != -INFINITY) {
+                for (int c = cf; c <= cl; c++) {
+                    const float *r = a.ws_part + ((size_t)(u + c) * a.G + i) * kPartStride;
+                    const float mc = __ldcg(r + kD);
+                    if (mc == -INFINITY) continue;
+                    const float f = exp2f((mc - M) * kLog2e);
+                    num = fmaf(f, __ldcg(r + d), num);
+                    den = fmaf(f, __ldcg(r + kD + 1), den);
                 }
             }
+            a.out[((size_t)s.b * a.Hq + s.h * a.G + i) * kD + d] = den > 0.0f ? num / den : 0.0f;
         }
-        __syncthreads();
+        if (a.m_tilde && tid < a.G) a.m_tilde[(size_t)s.b * a.Hq + s.h * a.G + tid] = U.mt[tid];
     }
+    named_barrier_sync(1, kConsumers);
+}
 
-    float *part = a.ws_part + ((size_t)bh * a.splits + split) * G * kPartStride;
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const int i = hh * 4 + k;
-        if (i < G) {
-            part[i * kPartStride + 2 * dp] = o[k][0];
-            part[i * kPartStride + 2 * dp + 1] = o[k][1];
+__device__ __forceinline__ void consumer(const MainParams &prm, const Smem &S, int cta, int ncta,
+                                         int warp, int lane) {
+    const DecodeArgs &a = prm.a;
+    Misc *m = S.misc;
+    const int grp = warp >> 2, mt = warp & 3;
+    Sched sch;
+    sch.init(a, cta, ncta);
+    Sub cur, nxt;
+    if (!sch.next(a, cur)) return;
+    grid_dependency_wait();  // stage-1 maxima are visible from here on
+    int scan_slot = 0, ref_slot = 0;
+    setup_unit(a, S, cur, scan_slot, warp, lane);
+    uint32_t mask_cur = scan_sub(a, S, cur, 0, scan_slot, warp, lane);
+    RefineState R;
+    reset_refine(R);
+    int t = 0, kb = 0;
+    while (true) {
+        const bool has_nxt = sch.next(a, nxt);
+        const bool new_unit = has_nxt && (nxt.b != cur.b || nxt.h != cur.h);
+        uint32_t mask_nxt = 0;
+        if (has_nxt) {
+            if (new_unit) {
+                scan_slot ^= 1;
+                setup_unit(a, S, nxt, scan_slot, warp, lane);
+            }
+            mask_nxt = scan_sub(a, S, nxt, t + 1, scan_slot, warp, lane);
         }
+        const float4 *shat = reinterpret_cast<const float4 *>(S.shat + (t & 1) * kShatBuf);
+        for (int k = 0; k < cur.cnt; k++) {
+            if (!(mask_cur & (1u << k))) continue;
+            const int slot = kb % kRing, round = kb / kRing;
+            kb++;
+            if ((k & 1) != grp) continue;
+            wait_bar(a, m, &m->ring_full[slot], round & 1);
+            refine_tile(a, S.ring + slot * kSlotBytes, S.unit[ref_slot],
+                        shat[(k * 4 + mt) * 32 + lane], cur.j0 + k, R, mt, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&m->ring_empty[slot]);
+        }
+        if (cur.last) {
+            combine_unit(a, S, cur, R, S.unit[ref_slot], cta, ncta, sch.T, warp, lane);
+            reset_refine(R);
+        }
+        if (!has_nxt) break;
+        if (new_unit) ref_slot = scan_slot;
+        cur = nxt;
+        mask_cur = mask_nxt;
+        t++;
     }
-    if (tid < G) {
-        part[tid * kPartStride + kD] = m_run[tid];
-        part[tid * kPartStride + kD + 1] = l_run[tid];
+}
+
+__global__ void __launch_bounds__(kMainThreads, 1)
+    main_kernel(const __grid_constant__ MainParams prm) {
+    const DecodeArgs &a = prm.a;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    Smem S;
+    S.ring = base + kOffRing;
+    S.thumb = base + kOffThumb;
+    S.shat = base + kOffShat;
+    S.cbuf = reinterpret_cast<float *>(base + kOffCbuf);
+    S.unit = reinterpret_cast<UnitOps *>(base + kOffUnit);
+    S.misc = reinterpret_cast<Misc *>(base + kOffMisc);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // every CTA range must hold at least one block: use at most T CTAs
+    int64_t T = 0;
+    for (int bb = 0; bb < a.B; bb++) T += (int64_t)a.Hkv * blocks_of(a, bb);
+    const int ncta = (int)(T < (int64_t)gridDim.x ? T : (int64_t)gridDim.x);
+    const int cta = blockIdx.x;
+    if (cta >= ncta) return;
+
+    if (threadIdx.x == 0) {
+        Misc *m = S.misc;
+        m->aborted = 0;
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&m->thumb_full[i], 1);
+            mbar_init(&m->decision[i], 1);
+        }
+        for (int i = 0; i < kRing; i++) {
+            mbar_init(&m->ring_full[i], 1);
+            mbar_init(&m->ring_empty[i], 4);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (warp == kConsumerWarps) {
+        if (lane == 0) producer(prm, S, cta, ncta);
+    } else {
+        consumer(prm, S, cta, ncta, warp, lane);
     }
 }
 
 // ------------------------------------------------------------------------------------------
-// Log-sum-exp merge of the split partials: out = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s.
-// One CTA per (sequence, query head); thread = channel. Shared by the dense kernel.
+// Host side
 // ------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) merge_kernel(DecodeArgs a) {
-    const int bq = blockIdx.x;
-    const int b = bq / a.Hq, qh = bq % a.Hq;
-    const int h = qh / a.G, i = qh % a.G;
-    const int bh = b * a.Hkv + h;
-    const int c = threadIdx.x;
-    const float *part = a.ws_part + (size_t)bh * a.splits * a.G * kPartStride + i * kPartStride;
-    const size_t split_stride = (size_t)a.G * kPartStride;
-    float M = -INFINITY;
-    for (int s = 0; s < a.splits; s++) M = fmaxf(M, part[s * split_stride + kD]);
-    float num = 0.0f, den = 0.0f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < a.splits; s++) {
-            const float m = part[s * split_stride + kD];
-            if (m == -INFINITY) continue;
-            const float w = exp2f((m - M) * 1.4426950408889634f);
-            den = fmaf(w, part[s * split_stride + kD + 1], den);
-            num = fmaf(w, part[s * split_stride + c], num);
-        }
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     }
-    a.out[(size_t)bq * kD + c] = den > 0.0f ? num / den : 0.0f;
+    return fn;
 }
 
-template <int G>
-static void launch_main(const DecodeArgs &a, cudaStream_t stream) {
-    main_kernel<G><<<dim3(a.splits, a.B * a.Hkv), 128, 0, stream>>>(a);
+// 2-D map over [rows][inner] elements with a box of 64 rows x box_inner elements, 128B swizzle.
+static bool make_map(CUtensorMap *map, CUtensorMapDataType type, void *ptr, uint64_t inner,
+                     uint64_t rows, uint64_t row_bytes, uint32_t box_inner) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, (cuuint32_t)kPage};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, type, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
-    if (a.nf > 0) stage1_kernel<<<dim3(a.nf, a.B * a.Hkv), 128, 0, stream>>>(a);
+cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t stream) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    MainParams prm;
+    memset(&prm, 0, sizeof prm);
+    prm.a = a;
+    const uint64_t rows = (uint64_t)a.P * a.Hkv * kPage;
+    if (!make_map(&prm.tm_resid, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<int8_t *>(a.resid),
+                  kD, rows, kD, kD) ||
+        !make_map(&prm.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<__nv_bfloat16 *>(a.v),
+                  kD, rows, kD * 2, 64))
+        return cudaErrorInvalidValue;
+
+    stage1_kernel<<<dim3(a.nf > 0 ? a.nf : 1, a.B * a.Hkv), 128, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     if (a.prof_start) cudaEventRecord(a.prof_start, stream);
-    switch (a.G) {
-        case 1: launch_main<1>(a, stream); break;
-        case 2: launch_main<2>(a, stream); break;
-        case 3: launch_main<3>(a, stream); break;
-        case 4: launch_main<4>(a, stream); break;
-        case 5: launch_main<5>(a, stream); break;
-        case 6: launch_main<6>(a, stream); break;
-        case 7: launch_main<7>(a, stream); break;
-        case 8: launch_main<8>(a, stream); break;
-        default: return cudaErrorInvalidValue;
-    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(main_ctas);
+    cfg.blockDim = dim3(kMainThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, main_kernel, prm);
+    if (e != cudaSuccess) return e;
     if (a.prof_stop) cudaEventRecord(a.prof_stop, stream);
-    merge_kernel<<<a.B * a.Hq, kD, 0, stream>>>(a);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_merge(const DecodeArgs &a, cudaStream_t stream) {
-    merge_kernel<<<a.B * a.Hq, kD, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -133,7 +133,30 @@ __global__ void __launch_bounds__(128) dense_kernel(DecodeArgs a) {
     }
 }
 
-cudaError_t launch_merge(const DecodeArgs &a, cudaStream_t stream);
+// Log-sum-exp merge of the split partials: out = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s.
+// One CTA per (sequence, query head); thread = channel.
+__global__ void __launch_bounds__(128) dense_merge_kernel(DecodeArgs a) {
+    const int bq = blockIdx.x;
+    const int b = bq / a.Hq, qh = bq % a.Hq;
+    const int h = qh / a.G, i = qh % a.G;
+    const int bh = b * a.Hkv + h;
+    const int c = threadIdx.x;
+    const float *part = a.ws_part + (size_t)bh * a.splits * a.G * kPartStride + i * kPartStride;
+    const size_t split_stride = (size_t)a.G * kPartStride;
+    float M = -INFINITY;
+    for (int s = 0; s < a.splits; s++) M = fmaxf(M, part[s * split_stride + kD]);
+    float num = 0.0f, den = 0.0f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < a.splits; s++) {
+            const float m = part[s * split_stride + kD];
+            if (m == -INFINITY) continue;
+            const float w = exp2f((m - M) * 1.4426950408889634f);
+            den = fmaf(w, part[s * split_stride + kD + 1], den);
+            num = fmaf(w, part[s * split_stride + c], num);
+        }
+    }
+    a.out[(size_t)bq * kD + c] = den > 0.0f ? num / den : 0.0f;
+}
 
 template <int G>
 static void launch_dense_g(const DecodeArgs &a, cudaStream_t stream) {
@@ -156,7 +179,8 @@ cudaError_t launch_dense(const DecodeArgs &a, cudaStream_t stream) {
     if (a.prof_stop) cudaEventRecord(a.prof_stop, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_merge(a, stream);
+    dense_merge_kernel<<<a.B * a.Hq, kD, 0, stream>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace ffd

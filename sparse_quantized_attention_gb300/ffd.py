@@ -22,7 +22,7 @@ _lib = None
 FFD_OK = 0
 STATUS_NAMES = {0: "FFD_OK", 1: "FFD_ERR_INVALID_ARG", 2: "FFD_ERR_UNSUPPORTED",
                 3: "FFD_ERR_WORKSPACE", 4: "FFD_ERR_CUDA", 5: "FFD_ERR_BOUNDS",
-                6: "FFD_ERR_RANGE"}
+                6: "FFD_ERR_RANGE", 7: "FFD_ERR_TIMEOUT"}
 HEAD_DIM = 128
 PAGE = 64
 
