@@ -176,6 +176,37 @@ ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
                             size_t workspace_bytes, void *stream);
 
 /*
+ * ffd_decode_attention_static -- ffd_decode_attention without a caller-supplied workspace.
+ * The paper has no counterpart: this entry point exists for callers that cannot allocate device
+ * memory for a workspace, such as a plain C host that links only this library and owns no device
+ * allocator, or a serving process that has committed all device memory to its KV-cache pool and
+ * must not allocate (or synchronise the device through cudaMalloc) inside its decode loop.
+ *
+ * It computes exactly what ffd_decode_attention computes, with the same arguments minus the
+ * workspace. Its scratch (stage-1 maxima, split records, merge tickets) is a static device array
+ * of 4 MiB inside libffd.so, held by every GPU that loads the library until the process exits.
+ * Nothing is allocated and no allocating routine is called.
+ *   - Limit: parameters whose ffd_decode_workspace_size() exceeds 4 MiB are rejected with
+ *     FFD_ERR_WORKSPACE before anything is enqueued (use ffd_decode_attention for those).
+ *   - Set-up: the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ *     capture. A failed look-up returns FFD_ERR_CUDA.
+ *   - Sharing: every call on a device uses the same array and it keeps the previous call's
+ *     contents; each call clears the parts that must start at zero (error word, merge tickets)
+ *     on its stream. Calls whose executions overlap on the GPU race with each other: order them
+ *     on one stream (or with events).
+ *   - error_word: device int32 or NULL. Device-detected errors (FFD_ERRBIT_*) are OR-ed into it;
+ *     read and clear it with ffd_get_error. With NULL they are not reported.
+ */
+ffd_status ffd_decode_attention_static(const ffd_decode_params *params, const void *q_bf16,
+                                       const uint8_t *thumb, const void *t_scale,
+                                       const void *t_zero, const int8_t *resid,
+                                       const void *r_scale, const void *v_bf16,
+                                       const int32_t *seq_lens, const int32_t *block_table,
+                                       float *out, uint8_t *keep_mask, float *m_tilde,
+                                       int32_t *error_word, void *stream);
+
+/*
  * ffd_set_profile_events -- optional instrumentation. While both events are non-NULL, every
  * ffd_decode_attention / ffd_dense_decode call records `start` on its stream right before its
  * main kernel (the fused stage-2/3 kernel, or the dense kernel) and `stop` right after it, so the

@@ -2,6 +2,8 @@
 // planning and kernel launches. No function here allocates device memory.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace ffd {
@@ -268,6 +270,91 @@ ffd_status ffd_get_error(void *error_word, void *stream) {
     if (h & FFD_ERRBIT_RANGE) return FFD_ERR_RANGE;
     if (h & FFD_ERRBIT_TIMEOUT) return FFD_ERR_TIMEOUT;
     return FFD_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Allocation-free decode: the same kernels, with their scratch in a fixed static device array.
+//
+// Some callers cannot hand the library a workspace: a plain C host that links only libffd.so and
+// owns no device allocator, or a serving process that has carved all device memory into its
+// KV-cache pool up front and may not allocate (cudaMalloc can also synchronise the device, which
+// a latency-critical decode loop must avoid). For them the scratch lives in the array below,
+// which every GPU that loads this library holds until the process exits.
+// ---------------------------------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void *g_static_ptr[kMaxDevices];
+
+// Device address of g_static_scratch on the current device (host code must not use the array's
+// name as an address). Looked up once per device, with that device current.
+ffd_status static_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FFD_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return FFD_ERR_CUDA;
+        g_static_ptr[dev] = p;
+    }
+    *out = g_static_ptr[dev];
+    return FFD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ffd_status ffd_decode_attention_static(const ffd_decode_params *params, const void *q_bf16,
+                                       const uint8_t *thumb, const void *t_scale,
+                                       const void *t_zero, const int8_t *resid,
+                                       const void *r_scale, const void *v_bf16,
+                                       const int32_t *seq_lens, const int32_t *block_table,
+                                       float *out, uint8_t *keep_mask, float *m_tilde,
+                                       int32_t *error_word, void *stream) {
+    if (!q_bf16 || !thumb || !t_scale || !t_zero || !resid || !r_scale || !v_bf16 || !seq_lens ||
+        !block_table || !out)
+        return FFD_ERR_INVALID_ARG;
+    if (!aligned16(thumb) || !aligned16(resid) || !aligned16(v_bf16) || !aligned16(q_bf16))
+        return FFD_ERR_INVALID_ARG;
+    Plan pl;
+    ffd_status st = make_decode_plan(params, &pl);
+    if (st != FFD_OK) return st;
+    if (pl.total > kStaticScratchBytes) return FFD_ERR_WORKSPACE;
+    void *ws = nullptr;
+    st = static_scratch(&ws);
+    if (st != FFD_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The array keeps the previous call's contents: the error word and the per-unit tickets of
+    // the in-kernel merge must start at zero.
+    const size_t units = (size_t)params->batch * params->num_kv_heads;
+    if (cudaMemsetAsync(ws, 0, kAlign, s) != cudaSuccess ||
+        cudaMemsetAsync(static_cast<char *>(ws) + pl.cnt_off, 0, units * sizeof(int), s) !=
+            cudaSuccess)
+        return FFD_ERR_CUDA;
+    DecodeArgs a = make_args(params, pl, ws);
+    if (error_word) a.err = reinterpret_cast<int *>(error_word);
+    a.q = static_cast<const __nv_bfloat16 *>(q_bf16);
+    a.thumb = thumb;
+    a.t_scale = static_cast<const __half *>(t_scale);
+    a.t_zero = static_cast<const __half *>(t_zero);
+    a.resid = resid;
+    a.r_scale = static_cast<const __half *>(r_scale);
+    a.v = static_cast<const __nv_bfloat16 *>(v_bf16);
+    a.seq_lens = seq_lens;
+    a.block_table = block_table;
+    a.out = out;
+    a.keep_mask = keep_mask;
+    a.m_tilde = m_tilde;
+    cudaError_t e = launch_decode(a, pl.ctas, s);
+    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -87,6 +87,9 @@ def lib() -> ctypes.CDLL:
             L.ffd_dense_decode.argtypes = [ctypes.POINTER(DecodeParams)] + [P] * 7 + \
                 [ctypes.c_size_t, P]
             L.ffd_dense_decode.restype = st
+            L.ffd_decode_attention_static.argtypes = [ctypes.POINTER(DecodeParams)] + \
+                [P] * 14
+            L.ffd_decode_attention_static.restype = st
             L.ffd_set_profile_events.argtypes = [P, P]
             L.ffd_set_profile_events.restype = st
             L.ffd_get_error.argtypes = [P, P]
@@ -177,6 +180,18 @@ def ffd_decode_attention(params: DecodeParams, q, cache: QuantizedCache, v, seq_
         ctypes.byref(params), _ptr(q), *map(_ptr, cache), _ptr(v), _ptr(seq_lens),
         _ptr(block_table), _ptr(out), _ptr(keep_mask), _ptr(m_tilde), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)), "ffd_decode_attention")
+
+
+def ffd_decode_attention_static(params: DecodeParams, q, cache: QuantizedCache, v, seq_lens,
+                                block_table, out, *, keep_mask=None, m_tilde=None,
+                                error_word=None, stream=None) -> None:
+    """ffd_decode_attention without a workspace, for callers that cannot allocate device memory:
+    the library's own 4 MiB static device scratch is used instead (calls that overlap on the GPU
+    race on it; the first call on a device should precede any stream capture)."""
+    _check(lib().ffd_decode_attention_static(
+        ctypes.byref(params), _ptr(q), *map(_ptr, cache), _ptr(v), _ptr(seq_lens),
+        _ptr(block_table), _ptr(out), _ptr(keep_mask), _ptr(m_tilde), _ptr(error_word),
+        _stream(stream)), "ffd_decode_attention_static")
 
 
 def ffd_dense_decode(params: DecodeParams, q, k, v, seq_lens, block_table, out, workspace, *,
