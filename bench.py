@@ -57,6 +57,9 @@ def args_parse(argv=None):
     ap.add_argument("--delta", type=float, default=None)
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the peaked-attention variant and the CPU baseline")
+    ap.add_argument("--peaked", action="store_true",
+                    help="measure the peaked-attention inputs (sink shift and needles in score "
+                         "units) as the primary workload")
     return ap.parse_args(argv)
 
 
@@ -263,7 +266,8 @@ def run_ours(a, rank, world, local):
 
     w = ffd_synth.WORKLOADS[a.workload]
     delta = a.delta if a.delta is not None else w.deltas[0]
-    inp = ffd_synth.make_inputs(w, seed=rank_seed(w.seed, rank))
+    inp = ffd_synth.make_inputs(w, seed=rank_seed(w.seed, rank),
+                                signal_scale=ffd_synth.peaked_scale() if a.peaked else 1.0)
     G = w.num_q_heads // w.num_kv_heads
     sm = float(np.float32(1.0 / math.sqrt(128.0)))
 
@@ -399,7 +403,8 @@ def run_ours(a, rank, world, local):
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_per_step, 5),
         "us_per_step": round(ms_per_step * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+        "config": {"workload": w.name + ("-peaked" if a.peaked else ""), "batch": w.batch,
+                   "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "context": w.seq_len, "sink": w.sink,
                    "local": w.local, "delta": delta, "page": 64, "head_dim": 128,
                    "l2": f"inputs larger than L2 ({by['step'] / 1e6:.0f} MB read per step vs "
@@ -435,7 +440,7 @@ def run_ours(a, rank, world, local):
                  "main_kernel_us_p50": round(statistics.median(main_ms) * 1e3, 2)},
     }
 
-    if not a.no_secondary and rank == 0 and world == 1:
+    if not a.no_secondary and not a.peaked and rank == 0 and world == 1:
         result["secondary_peaked"] = peaked_variant(a, w, delta, dev, ffd, torch, upload,
                                                     dense_ms)
         result["cpu_baseline"] = cpu_baseline(w, inp, keep, delta, sm)

@@ -56,11 +56,12 @@ ffd_status check_params(const ffd_decode_params *p) {
 struct Plan {
     int splits, bps, nf;  // dense: splits per unit and blocks per split; decode: nf slots
     int ctas;             // decode: CTAs of the main kernel
-    size_t m1_off, part_off, cnt_off, total;
+    size_t m1_off, s1_off, part_off, cnt_off, total;
 };
 
-// Workspace of ffd_decode_attention: [error word | stage-1 maxima | split records | tickets].
-// Records: one per (unit, CTA) pair that shares work, indexed unit + cta (< units + ctas).
+// Workspace of ffd_decode_attention: [error word | stage-1 maxima | stage-1 partials |
+// main-kernel split records | tickets]. Main records: one per (unit, CTA) pair that shares work,
+// indexed unit + cta (< units + ctas). Stage 1 has one slot per forced block (at least one).
 ffd_status make_decode_plan(const ffd_decode_params *p, Plan *pl) {
     ffd_status st = check_params(p);
     if (st != FFD_OK) return st;
@@ -73,14 +74,17 @@ ffd_status make_decode_plan(const ffd_decode_params *p, Plan *pl) {
     }
     pl->ctas = ctas;
     pl->splits = pl->bps = 0;
-    pl->nf = max_forced_blocks(p->sink_tokens, p->local_tokens, p->max_blocks_per_seq);
+    const int nf = max_forced_blocks(p->sink_tokens, p->local_tokens, p->max_blocks_per_seq);
+    pl->nf = nf > 0 ? nf : 1;
     size_t off = kAlign;
     pl->m1_off = off;
     off = align_up(off + (size_t)units * pl->nf * kMaxG * sizeof(float));
+    pl->s1_off = off;
+    off = align_up(off + (size_t)units * pl->nf * G * kPartStride * sizeof(float));
     pl->part_off = off;
     off = align_up(off + (size_t)(units + ctas) * G * kPartStride * sizeof(float));
     pl->cnt_off = off;
-    off = align_up(off + (size_t)units * sizeof(int));
+    off = align_up(off + 2 * (size_t)units * sizeof(int));
     pl->total = off;
     return FFD_OK;
 }
@@ -106,6 +110,7 @@ ffd_status make_dense_plan(const ffd_decode_params *p, Plan *pl) {
     pl->ctas = 0;
     size_t off = kAlign;
     pl->m1_off = off;
+    pl->s1_off = off;
     pl->part_off = off;
     off = align_up(off + (size_t)units * pl->splits * G * kPartStride * sizeof(float));
     pl->cnt_off = off;
@@ -135,6 +140,7 @@ DecodeArgs make_args(const ffd_decode_params *p, const Plan &pl, void *ws) {
     char *base = static_cast<char *>(ws);
     a.err = reinterpret_cast<int *>(base);
     a.ws_m1 = reinterpret_cast<float *>(base + pl.m1_off);
+    a.ws_s1 = reinterpret_cast<float *>(base + pl.s1_off);
     a.ws_part = reinterpret_cast<float *>(base + pl.part_off);
     a.ws_cnt = reinterpret_cast<int *>(base + pl.cnt_off);
     return a;
@@ -336,7 +342,7 @@ ffd_status ffd_decode_attention_static(const ffd_decode_params *params, const vo
     // the in-kernel merge must start at zero.
     const size_t units = (size_t)params->batch * params->num_kv_heads;
     if (cudaMemsetAsync(ws, 0, kAlign, s) != cudaSuccess ||
-        cudaMemsetAsync(static_cast<char *>(ws) + pl.cnt_off, 0, units * sizeof(int), s) !=
+        cudaMemsetAsync(static_cast<char *>(ws) + pl.cnt_off, 0, 2 * units * sizeof(int), s) !=
             cudaSuccess)
         return FFD_ERR_CUDA;
     DecodeArgs a = make_args(params, pl, ws);

@@ -37,9 +37,10 @@ struct DecodeArgs {
     uint8_t *keep_mask;
     float *m_tilde;
     int *err;        // device error word
-    float *ws_m1;    // [B*Hkv][nf][kMaxG] stage-1 block maxima
-    float *ws_part;  // split records: [records][G][kPartStride]
-    int *ws_cnt;     // [B*Hkv] per-unit tickets of the in-kernel merge (kept at zero between calls)
+    float *ws_m1;    // [B*Hkv][nf][kMaxG] stage-1 block maxima over the sink / local tokens
+    float *ws_s1;    // [B*Hkv][nf][G][kPartStride] stage-1 softmax partials of the forced blocks
+    float *ws_part;  // main-kernel split records: [B*Hkv + CTAs][G][kPartStride]
+    int *ws_cnt;     // [2][B*Hkv] merge tickets (main kernel, stage 1), zero between calls
     cudaEvent_t prof_start, prof_stop;  // optional: recorded around the main kernel
 };
 

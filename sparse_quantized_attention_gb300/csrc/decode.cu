@@ -54,7 +54,7 @@ constexpr int kOffShat = kOffThumb + 2 * kSub * kThumbBlock;
 constexpr int kOffCbuf = kOffShat + 2 * kShatBuf;
 constexpr int kOffUnit = kOffCbuf + kConsumerWarps * kCbufWarp * 4;
 constexpr int kOffMisc = kOffUnit + 2 * 4608;
-constexpr int kMiscBytes = 256;
+constexpr int kMiscBytes = 384;
 constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + slack to align the base to 1 KB
 
 struct Misc {
@@ -63,7 +63,8 @@ struct Misc {
     uint32_t bad[2];
     uint32_t merge_flag;
     uint32_t aborted;
-    uint32_t pad[10];
+    uint32_t pad[2];
+    int32_t pages[4][kSub];  // producer: block-table entries of sub-chunk t in pages[t % 4]
     uint64_t thumb_full[2];
     uint64_t decision[2];
     uint64_t ring_full[kRing];
@@ -460,9 +461,11 @@ __device__ __forceinline__ void issue_thumbs(const DecodeArgs &a, const Smem &S,
     Misc *m = S.misc;
     const int buf = t & 1;
     const int32_t *bt = a.block_table + (size_t)s.b * a.max_blocks + s.j0;
+    int32_t *pg = m->pages[t & 3];
     uint32_t bad = 0;
     for (int k = 0; k < s.cnt; k++) {
         const int page = bt[k];
+        pg[k] = page;
         if (page < 0 || page >= a.P) {
             bad |= 1u << k;
             raise_error(a.err, FFD_ERRBIT_BOUNDS);
@@ -474,7 +477,7 @@ __device__ __forceinline__ void issue_thumbs(const DecodeArgs &a, const Smem &S,
     uint8_t *dst = S.thumb + buf * (kSub * kThumbBlock);
     for (int k = 0; k < s.cnt; k++) {
         if (bad & (1u << k)) continue;
-        const size_t tile = (size_t)bt[k] * a.Hkv + s.h;
+        const size_t tile = (size_t)pg[k] * a.Hkv + s.h;
         uint8_t *d = dst + k * kThumbBlock;
         tma_load_1d(d, a.thumb + tile * kPage * kThumbRow, 2048, &m->thumb_full[buf]);
         tma_load_1d(d + 2048, a.t_scale + tile * kPage * kGroups, 512, &m->thumb_full[buf]);
@@ -482,33 +485,33 @@ __device__ __forceinline__ void issue_thumbs(const DecodeArgs &a, const Smem &S,
     }
 }
 
-__device__ __forceinline__ void producer(const MainParams &prm, const Smem &S, int cta, int ncta) {
+__device__ __forceinline__ void producer(const MainParams &prm, const Smem &S, int cta,
+                                         int ncta) {
     const DecodeArgs &a = prm.a;
     Misc *m = S.misc;
     prefetch_tensormap(&prm.tm_resid);
     prefetch_tensormap(&prm.tm_v);
     Sched sch;
     sch.init(a, cta, ncta);
-    Sub q[3];
-    int fetched = 0;
-    while (fetched < 2 && sch.next(a, q[fetched])) fetched++;
-    for (int t = 0; t < fetched; t++) issue_thumbs(a, S, q[t], t);
+    // descriptors of sub-chunks t (cur), t+1 (n1) and t+2 (n2)
+    Sub cur, n1, n2;
+    bool has_cur = sch.next(a, cur);
+    bool has_n1 = has_cur && sch.next(a, n1);
+    if (has_cur) issue_thumbs(a, S, cur, 0);
+    if (has_n1) issue_thumbs(a, S, n1, 1);
     int kb = 0;
-    for (int t = 0; t < fetched; t++) {
-        const Sub cur = q[t % 3];
+    for (int t = 0; has_cur; t++) {
         wait_bar(a, m, &m->decision[t & 1], (t >> 1) & 1);
         const uint32_t mask = *reinterpret_cast<volatile uint32_t *>(&m->final_mask[t & 1]);
-        if (sch.next(a, q[fetched % 3])) {
-            issue_thumbs(a, S, q[fetched % 3], fetched);
-            fetched++;
-        }
+        const bool has_n2 = has_n1 && sch.next(a, n2);
+        if (has_n2) issue_thumbs(a, S, n2, t + 2);  // buffer t & 1 is free after decision t
+        const int32_t *pg = m->pages[t & 3];
         for (int k = 0; k < cur.cnt; k++) {
             if (!(mask & (1u << k))) continue;
             const int slot = kb % kRing, round = kb / kRing;
             kb++;
             if (round > 0) wait_bar(a, m, &m->ring_empty[slot], (round - 1) & 1);
-            const int page = a.block_table[(size_t)cur.b * a.max_blocks + cur.j0 + k];
-            const int row = (int)(((size_t)page * a.Hkv + cur.h) * kPage);
+            const int row = (int)(((size_t)pg[k] * a.Hkv + cur.h) * kPage);
             uint8_t *d = S.ring + slot * kSlotBytes;
             uint64_t *bar = &m->ring_full[slot];
             mbar_arrive_expect_tx(bar, kSlotTx);
@@ -517,6 +520,10 @@ __device__ __forceinline__ void producer(const MainParams &prm, const Smem &S, i
             tma_load_2d(d + kSlotV + 8192, &prm.tm_v, 64, row, bar);
             tma_load_1d(d + kSlotRScale, a.r_scale + (size_t)row * kGroups, 512, bar);
         }
+        cur = n1;
+        n1 = n2;
+        has_cur = has_n1;
+        has_n1 = has_n2;
     }
     // leave no copy in flight: wait for the last fill of every ring slot
     for (int s = 0; s < kRing && s < kb; s++) {
