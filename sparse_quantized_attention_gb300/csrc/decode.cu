@@ -32,6 +32,7 @@ constexpr int kSub = 6;              // blocks per sub-chunk (scan / refine pipe
 constexpr int kRing = 6;             // refine ring slots (residual + V of one kept block each)
 constexpr int kPageSlots = 8;        // sub-chunks whose block-table entries are resolved ahead
 constexpr int kGroups3 = 3;          // consumer groups: group grp takes the blocks k with k%3==grp
+static_assert(kSub == 2 * kGroups3, "each consumer group refines two blocks of a sub-chunk");
 constexpr int kConsumerWarps = 12;   // warp c = 4 grp + mt works on m-tile mt (16 tokens)
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kMainThreads = kConsumers + 128;  // + the producer warpgroup (one TMA warp)
@@ -73,8 +74,7 @@ struct PageSlot {
 };
 
 struct Misc {
-    uint32_t votes[2][kConsumerWarps];
-    uint32_t final_mask[2];
+    uint32_t vote_mask[4];            // blocks of sub-chunk t voted kept, in vote_mask[t % 4]
     uint32_t bad[2];
     uint32_t merge_flag;
     uint32_t aborted;
@@ -696,7 +696,7 @@ __device__ __forceinline__ void drain_bar(const DecodeArgs &a, uint64_t *bar, ui
 // two phases ahead of the ring warp); lane k issues block k's copies.
 __device__ __forceinline__ void thumb_issuer(const DecodeArgs &a, const Smem &S, int lane) {
     Misc *m = S.misc;
-    uint32_t pend[2] = {0, 0};  // phases of thumb_full[0/1] armed by this warp
+    uint32_t pend0 = 0, pend1 = 0;  // phases of thumb_full[0/1] armed by this warp
     for (int t = 0;; t++) {
         const int buf = t & 1;
         if (t >= 2) wait_bar(a, m, &m->ring_seen[buf], ((t - 2) >> 1) & 1);
@@ -709,7 +709,8 @@ __device__ __forceinline__ void thumb_issuer(const DecodeArgs &a, const Smem &S,
             mbar_arrive_expect_tx(&m->thumb_full[buf],
                                   (uint32_t)((cnt - __popc(bad)) * kThumbBlock));
         }
-        pend[buf]++;
+        pend0 += buf == 0;
+        pend1 += buf == 1;
         __syncwarp();
         if (lane < cnt && !((bad >> lane) & 1u)) {
             const size_t row = (size_t)P.row[lane];
@@ -722,9 +723,10 @@ __device__ __forceinline__ void thumb_issuer(const DecodeArgs &a, const Smem &S,
         if (lane == 0) mbar_arrive(&m->pages_empty[t % kPageSlots]);
     }
     // leave no copy in flight
-    if (lane == 0)
-        for (int b = 0; b < 2; b++)
-            if (pend[b]) drain_bar(a, &m->thumb_full[b], (pend[b] - 1) & 1);
+    if (lane == 0) {
+        if (pend0) drain_bar(a, &m->thumb_full[0], (pend0 - 1) & 1);
+        if (pend1) drain_bar(a, &m->thumb_full[1], (pend1 - 1) & 1);
+    }
 }
 
 // Ring warp: residual tile, V tile and residual scales of every kept block of sub-chunk t, once
@@ -742,10 +744,15 @@ __device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S
         const int cnt = P.cnt;
         if (cnt == 0 || *reinterpret_cast<volatile uint32_t *>(&m->aborted)) break;
         wait_bar(a, m, &m->decision[t & 1], (t >> 1) & 1);
-        const uint32_t mask = *reinterpret_cast<volatile uint32_t *>(&m->final_mask[t & 1]) &
-                              ((1u << cnt) - 1u);
+        const uint32_t mask = *reinterpret_cast<volatile uint32_t *>(&m->vote_mask[t & 3]) &
+                              ~P.bad & ((1u << cnt) - 1u);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&m->ring_seen[t & 1]);
+        if (lane == 0) {
+            // every consumer has read the votes of sub-chunk t-2 (it voted on t since), and none
+            // votes on t+2 before this arrival releases its thumbnails
+            m->vote_mask[(t + 2) & 3] = 0;
+            mbar_arrive(&m->ring_seen[t & 1]);
+        }
         for (int k = 0; k < cnt; k++) {
             if (!(mask & (1u << k))) continue;
             const int slot = kb % kRing, round = kb / kRing;
@@ -847,9 +854,10 @@ __device__ __forceinline__ bool tile_passes(float4 e, bool v0, bool v1, float th
     return (v0 && (e.x >= thr0 || e.y >= thr1)) || (v1 && (e.z >= thr0 || e.w >= thr1));
 }
 
-// Scan of sub-chunk t: provisional scores of this warp's m-tiles, block votes, final mask. The
-// warp's blocks are k = grp and grp + 3, scanned side by side (two independent dependency
-// chains). The second tile is computed even past the sub-chunk's end (its shared-memory reads stay
+// Scan of sub-chunk t: provisional scores of this warp's m-tiles and its vote (an OR into
+// vote_mask, then one arrival on the decision barrier; no warp waits for the others here).
+// Returns the sub-chunk's never-loaded blocks. The warp's blocks are k = grp and grp + 3,
+// scanned side by side (two independent dependency chains). The second tile is computed even past the sub-chunk's end (its shared-memory reads stay
 // inside the buffer) and then ignored, so both chains stay in one basic block.
 __device__ __forceinline__ uint32_t scan_sub(const DecodeArgs &a, const Smem &S, const Sub &s,
                                              int t, int warp, int lane) {
@@ -886,22 +894,19 @@ __device__ __forceinline__ uint32_t scan_sub(const DecodeArgs &a, const Smem &S,
         shat[(kA * 4 + mt) * 32 + lane] = eA;
         if (kB < s.cnt) shat[(kB * 4 + mt) * 32 + lane] = eB;
     }
-    if (lane == 0) m->votes[buf][warp] = votes;
-    named_barrier_sync(1, kConsumers);
-    uint32_t mask = 0;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; w++) mask |= m->votes[buf][w];
-    mask &= ~bad;
-    mask &= (1u << s.cnt) - 1u;
-    if (warp == 0 && lane == 0) {
-        m->final_mask[buf] = mask;
-        if (a.keep_mask) {
-            uint8_t *km = a.keep_mask + ((size_t)s.b * a.Hkv + s.h) * a.max_blocks + s.j0;
-            for (int k = 0; k < s.cnt; k++) km[k] = (mask >> k) & 1u;
-        }
-        mbar_arrive(&m->decision[buf]);
+    if (lane == 0) {
+        if (votes) atomicOr(&m->vote_mask[t & 3], votes);
+        mbar_arrive(&m->decision[buf]);  // releases the vote; the decision completes at 12 votes
     }
-    return mask;
+    return bad;
+}
+
+// Kept blocks of sub-chunk t: every warp's vote, less the blocks that were never loaded.
+__device__ __forceinline__ uint32_t kept_mask(const DecodeArgs &a, Misc *m, const Sub &s, int t,
+                                              uint32_t bad) {
+    wait_bar(a, m, &m->decision[t & 1], (t >> 1) & 1);
+    return *reinterpret_cast<volatile uint32_t *>(&m->vote_mask[t & 3]) & ~bad &
+           ((1u << s.cnt) - 1u);
 }
 
 // Refine-side state of the unit being refined: its query operands, and this warp's running
@@ -1143,37 +1148,45 @@ __device__ __forceinline__ void consumer(const MainParams &prm, const Smem &S, i
     if (!sch.next(a, cur)) return;
     grid_dependency_wait();  // stage-1 results are visible from here on
     setup_unit(a, S, cur, warp, lane);
-    uint32_t mask_cur = scan_sub(a, S, cur, 0, warp, lane);
+    uint32_t bad_cur = scan_sub(a, S, cur, 0, warp, lane);
     RefineState R;
     reset_refine(R, *S.unit, lane);
     int t = 0, kb = 0;
     while (true) {
         const bool has_nxt = sch.next(a, nxt);
-        uint32_t mask_nxt = 0;
-        if (has_nxt && !cur.last) mask_nxt = scan_sub(a, S, nxt, t + 1, warp, lane);
+        uint32_t bad_nxt = 0;
+        if (has_nxt && !cur.last) bad_nxt = scan_sub(a, S, nxt, t + 1, warp, lane);
         const float4 *shat = reinterpret_cast<const float4 *>(S.shat + (t & 1) * kShatBuf);
-        for (int k = 0; k < cur.cnt; k++) {
-            if (!(mask_cur & (1u << k))) continue;
-            const int slot = kb % kRing, round = kb / kRing;
-            kb++;
-            if (k % kGroups3 != grp) continue;
-            wait_bar(a, m, &m->ring_full[slot], round & 1);
+        const uint32_t mask_cur = kept_mask(a, m, cur, t, bad_cur);
+        if (warp == 0 && a.keep_mask && lane < cur.cnt)
+            a.keep_mask[((size_t)cur.b * a.Hkv + cur.h) * a.max_blocks + cur.j0 + lane] =
+                (mask_cur >> lane) & 1u;
+        // this group's blocks k = grp and grp + 3; kept block number kb + (kept blocks before k)
+        // is the ring position the producer gave it
+#pragma unroll
+        for (int q = 0; q < 2; q++) {
+            const int k = grp + q * kGroups3;
+            if (k >= cur.cnt || !((mask_cur >> k) & 1u)) continue;
+            const int kbk = kb + __popc(mask_cur & ((1u << k) - 1u));
+            const int slot = kbk % kRing;
+            wait_bar(a, m, &m->ring_full[slot], (kbk / kRing) & 1);
             refine_tile(a, S.ring + slot * kSlotBytes, *S.unit, shat[(k * 4 + mt) * 32 + lane],
                         cur.j0 + k, R, mt, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&m->ring_empty[slot]);
         }
+        kb += __popc(mask_cur);
         if (cur.last) {
             combine_unit(a, S, cur, R, cta, ncta, sch.T, warp, lane);
             if (has_nxt) {  // a new unit only follows the last sub-chunk of the previous one
                 setup_unit(a, S, nxt, warp, lane);
-                mask_nxt = scan_sub(a, S, nxt, t + 1, warp, lane);
+                bad_nxt = scan_sub(a, S, nxt, t + 1, warp, lane);
                 reset_refine(R, *S.unit, lane);
             }
         }
         if (!has_nxt) break;
         cur = nxt;
-        mask_cur = mask_nxt;
+        bad_cur = bad_nxt;
         t++;
     }
 }
@@ -1201,9 +1214,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     if (threadIdx.x == 0) {
         Misc *m = S.misc;
         m->aborted = 0;
+        for (int i = 0; i < 4; i++) m->vote_mask[i] = 0;
         for (int i = 0; i < 2; i++) {
             mbar_init(&m->thumb_full[i], 1);
-            mbar_init(&m->decision[i], 1);
+            mbar_init(&m->decision[i], kConsumerWarps);
             mbar_init(&m->ring_seen[i], 1);
         }
         for (int i = 0; i < kRing; i++) {
