@@ -56,7 +56,7 @@ ffd_status check_params(const ffd_decode_params *p) {
 struct Plan {
     int splits, bps, nf;  // dense: splits per unit and blocks per split; decode: nf slots
     int ctas;             // decode: CTAs of the main kernel
-    size_t m1_off, s1_off, part_off, cnt_off, total;
+    size_t m1_off, part_off, cnt_off, total;
 };
 
 // Workspace of ffd_decode_attention: [error word | stage-1 maxima | stage-1 partials |
@@ -79,10 +79,8 @@ ffd_status make_decode_plan(const ffd_decode_params *p, Plan *pl) {
     size_t off = kAlign;
     pl->m1_off = off;
     off = align_up(off + (size_t)units * pl->nf * kMaxG * sizeof(float));
-    pl->s1_off = off;
-    off = align_up(off + (size_t)units * pl->nf * G * kPartStride * sizeof(float));
     pl->part_off = off;
-    off = align_up(off + (size_t)(units + ctas) * G * kPartStride * sizeof(float));
+    off = align_up(off + (size_t)(units + ctas) * 2 * G * kPartStride * sizeof(float));
     pl->cnt_off = off;
     off = align_up(off + 2 * (size_t)units * sizeof(int));
     pl->total = off;
@@ -110,7 +108,6 @@ ffd_status make_dense_plan(const ffd_decode_params *p, Plan *pl) {
     pl->ctas = 0;
     size_t off = kAlign;
     pl->m1_off = off;
-    pl->s1_off = off;
     pl->part_off = off;
     off = align_up(off + (size_t)units * pl->splits * G * kPartStride * sizeof(float));
     pl->cnt_off = off;
@@ -140,7 +137,6 @@ DecodeArgs make_args(const ffd_decode_params *p, const Plan &pl, void *ws) {
     char *base = static_cast<char *>(ws);
     a.err = reinterpret_cast<int *>(base);
     a.ws_m1 = reinterpret_cast<float *>(base + pl.m1_off);
-    a.ws_s1 = reinterpret_cast<float *>(base + pl.s1_off);
     a.ws_part = reinterpret_cast<float *>(base + pl.part_off);
     a.ws_cnt = reinterpret_cast<int *>(base + pl.cnt_off);
     return a;

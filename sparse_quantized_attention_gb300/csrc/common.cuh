@@ -38,9 +38,8 @@ struct DecodeArgs {
     float *m_tilde;
     int *err;        // device error word
     float *ws_m1;    // [B*Hkv][nf][kMaxG] stage-1 block maxima over the sink / local tokens
-    float *ws_s1;    // [B*Hkv][nf][G][kPartStride] stage-1 softmax partials of the forced blocks
-    float *ws_part;  // main-kernel split records: [B*Hkv + CTAs][G][kPartStride]
-    int *ws_cnt;     // [2][B*Hkv] merge tickets (main kernel, stage 1), zero between calls
+    float *ws_part;  // main-kernel split records: [B*Hkv + CTAs][2][G][kPartStride]
+    int *ws_cnt;     // [B*Hkv] merge tickets (plus a spare [B*Hkv]), zero between calls
     cudaEvent_t prof_start, prof_stop;  // optional: recorded around the main kernel
 };
 

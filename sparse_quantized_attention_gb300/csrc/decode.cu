@@ -1,11 +1,12 @@
-// decode.cu -- FFD decode attention on GB300: stage 1 (pseudo-max) and the fused, persistent
-// stage-2/3 kernel (Top-delta scan of the 2-bit thumbnails, refinement of the kept blocks with the
-// int8 residual and V, online softmax, split merge).
+// decode.cu -- FFD decode attention on GB300: stage 1 (pseudo-max of every (sequence, KV head)
+// unit) and the persistent, warp-specialised main kernel (Top-delta scan of the 2-bit thumbnails,
+// refinement of the kept blocks with the int8 residual and V, online softmax, split merge).
 //
 // Source: "Faster Than Flash", Methodology §2 (keep token j when s_ij >= m~_i - delta; m~_i from
 // the sink and local tokens only) and §3 (stage 1 pseudo-max estimation; stage 2 streams the 2-bit
 // keys, computes provisional scores and filters blocks; stage 3 loads the 8-bit residuals and V of
-// the selected blocks and computes exact attention, reusing the scan results).
+// the selected blocks and computes exact attention, reusing the scan results). The blocks that
+// hold a sink or local token are always kept.
 //
 // Tensor-core operands (mma.sync m16n8k16, bf16 in, fp32 accumulate; 16 tokens x 8 heads):
 //   * A = keys of 16 tokens, B = the GQA group's queries (heads as N, padded to 8).
@@ -28,18 +29,26 @@
 
 namespace ffd {
 
-constexpr int kSub = 6;              // blocks per sub-chunk (scan / refine pipeline unit)
-constexpr int kRing = 6;             // refine ring slots (residual + V of one kept block each)
+// ---- main kernel: roles ---------------------------------------------------------------------
+// Warpgroup 0: ring warp (0), page warp (1), thumbnail warp (2), one idle warp.
+// Warpgroup 1: scan warps 4-7; scan warp mt takes rows 16mt .. 16mt+15 of every block.
+// Warpgroups 2-3: refine groups 0 (warps 8-11) and 1 (warps 12-15); kept block number kb goes to
+// group kb & 1. In a group, warp mt computes the scores of rows 16mt .. 16mt+15 and the output
+// channels 32mt .. 32mt+31 (the probabilities are exchanged through shared memory).
+constexpr int kSub = 6;              // blocks per sub-chunk (scan decision unit)
+constexpr int kRing = 5;             // refine ring slots (residual + V of one kept block each)
+constexpr int kThumbBufs = 3;        // thumbnail buffers (sub-chunks in flight ahead of the ring)
+constexpr int kShatBufs = 2;         // provisional-score buffers (scan ahead of refinement)
+constexpr int kDepth = 8;            // ring of per-sub-chunk decision slots
 constexpr int kPageSlots = 8;        // sub-chunks whose block-table entries are resolved ahead
-constexpr int kGroups3 = 3;          // consumer groups: group grp takes the blocks k with k%3==grp
-static_assert(kSub == 2 * kGroups3, "each consumer group refines two blocks of a sub-chunk");
-constexpr int kConsumerWarps = 12;   // warp c = 4 grp + mt works on m-tile mt (16 tokens)
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kMainThreads = kConsumers + 128;  // + the producer warpgroup (one TMA warp)
-constexpr int kProducerRegs = 32;    // setmaxnreg budgets: 128 x 32 + 384 x 160 <= 512 x 128
-constexpr int kConsumerRegs = 160;
-static_assert(128 * kProducerRegs + kConsumers * kConsumerRegs <= kMainThreads * 128,
+constexpr int kMainThreads = 512;
+constexpr int kProducerRegs = 32;    // setmaxnreg shares: 128 x 32 + 128 x 128 + 256 x 176
+constexpr int kScanRegs = 128;       //   = 65536 = 512 threads x 128 at launch
+constexpr int kRefineRegs = 176;
+static_assert(128 * kProducerRegs + 128 * kScanRegs + 256 * kRefineRegs <= kMainThreads * 128,
               "register reallocation exceeds the launch allocation");
+static_assert(kScanRegs == 128, "the scan warpgroup keeps its launch allocation");
+static_assert(kDepth > kThumbBufs + 1 && kDepth > kShatBufs + kThumbBufs, "decision ring depth");
 constexpr int kKq = 100;             // q enters the MMA scaled by 2^kKq (|q| < 2^27 required)
 constexpr float kUnscale = 8589934592.0f;      // 2^(133 - kKq)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -53,46 +62,55 @@ constexpr int kSlotRScale = 8192 + 16384;
 constexpr int kSlotTx = 8192 + 16384 + 512;
 constexpr int kSlotBytes = 25600;
 constexpr int kThumbBlock = 3072;    // codes 2048 B + scales 512 B + zeros 512 B
+constexpr int kThumbBuf = kSub * kThumbBlock;
 constexpr int kShatBuf = kSub * 4 * 32 * 16;  // provisional scores of one sub-chunk
-constexpr int kCombineWarpBytes = kMaxG * kD * 4;  // one warp's O^T in the combine
+constexpr int kPxBuf = 4 * 32 * 16;           // P^T fragments of one block (4 k-steps)
+constexpr int kUnitBytes = 4352;
 
 constexpr int kOffRing = 0;
 constexpr int kOffThumb = kOffRing + kRing * kSlotBytes;
-constexpr int kOffShat = kOffThumb + 2 * kSub * kThumbBlock;  // also the combine buffer
-constexpr int kOffUnit = kOffShat + 2 * kShatBuf;
-constexpr int kOffMisc = kOffUnit + 4608;
-constexpr int kMiscBytes = 1536;
+constexpr int kOffShat = kOffThumb + kThumbBufs * kThumbBuf;
+constexpr int kOffPx = kOffShat + kShatBufs * kShatBuf;      // [group][2][kPxBuf]
+constexpr int kOffUnit = kOffPx + 2 * 2 * kPxBuf;            // [2] unit operand slots
+constexpr int kOffMisc = kOffUnit + 2 * kUnitBytes;
+constexpr int kMiscBytes = 2048;
 constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + slack to align the base to 1 KB
-static_assert(6 * kCombineWarpBytes <= 2 * kShatBuf, "combine buffer inside the score buffers");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(kSlotBytes % 1024 == 0 && kSlotV % 1024 == 0, "swizzled TMA tiles need 1 KB");
 
-// One sub-chunk as the page warp hands it to the TMA producer.
+// One sub-chunk as the page warp hands it to the copy warps.
 struct PageSlot {
     int32_t row[kSub];   // first token row of each block's tile: (page * Hkv + h) * 64
     uint32_t bad;        // entries outside [0, P), one bit per block (row 0, never loaded)
+    uint32_t forced;     // blocks holding a sink or local token (kept whatever the scan says)
     int32_t cnt;         // blocks; 0 marks the end of this CTA's schedule
-    int32_t pad[2];
+    int32_t pad;
 };
 
 struct Misc {
-    uint32_t vote_mask[4];            // blocks of sub-chunk t voted kept, in vote_mask[t % 4]
-    uint32_t bad[2];
-    uint32_t merge_flag;
+    uint32_t vote[kDepth];        // OR of the scan votes of sub-chunk t, in slot t % kDepth
+    uint32_t final_mask[kDepth];  // kept blocks of sub-chunk t, published by the ring warp
     uint32_t aborted;
-    float cm[kConsumerWarps][kMaxG];  // combine: per-warp softmax maxima
-    float cl[kConsumerWarps][kMaxG];  // combine: per-warp softmax sums
-    PageSlot ps[kPageSlots];          // sub-chunk t in ps[t % kPageSlots]
+    uint32_t merge_flag[2];
+    uint32_t over[2][2][4];       // refine [group][buffer][warp]: a score passed m + margin
+    float wmax[2][2][4][kMaxG];   // refine [group][buffer][warp][head]: block row maxima
+    float lsum[2][4][kMaxG];      // refine [group][warp][head]: softmax sums at a unit's end
+    PageSlot ps[kPageSlots];      // sub-chunk t in ps[t % kPageSlots]
     uint64_t pages_full[kPageSlots];
     uint64_t pages_empty[kPageSlots];
-    uint64_t thumb_full[2];
-    uint64_t decision[2];
-    uint64_t ring_seen[2];            // the ring warp has read the decision of sub-chunk t
+    uint64_t thumb_full[kThumbBufs];
+    uint64_t decision[kDepth];    // the 4 scan warps voted on sub-chunk t
+    uint64_t ring_seen[kDepth];   // the ring warp published the kept blocks of sub-chunk t
+    uint64_t shat_free[kShatBufs];
     uint64_t ring_full[kRing];
     uint64_t ring_empty[kRing];
+    uint64_t unit_ready[2];
+    uint64_t unit_free[2];
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc region");
 
-// Query operands of the (sequence, KV head) unit being processed, laid out so that a lane loads
-// its 16 B-fragment registers with four conflict-free 128-bit loads.
+// Query operands of one (sequence, KV head) unit, laid out so that a lane loads its 16
+// B-fragment registers with four conflict-free 128-bit loads.
 struct UnitOps {
     uint4 bt[4][32];   // thumbnail B fragments: [bt0[0..3], bt0[4..7], bt1[0..3], bt1[4..7]][lane]
     uint4 br[4][32];   // residual B fragments, same arrangement
@@ -100,10 +118,8 @@ struct UnitOps {
     float thr[kMaxG];  // m~ - delta (+inf for heads >= G)
     float mt[kMaxG];   // m~
     int n;             // sequence length
-    int pad[15];
 };
-static_assert(sizeof(UnitOps) <= 4608, "unit operand slot");
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(sizeof(UnitOps) <= kUnitBytes, "unit operand slot");
 
 struct MainParams {
     CUtensorMap tm_resid;
@@ -111,12 +127,16 @@ struct MainParams {
     DecodeArgs a;
 };
 
+struct Smem {
+    uint8_t *ring, *thumb, *shat, *px;
+    UnitOps *unit;
+    Misc *misc;
+};
+
 // ------------------------------------------------------------------------------------------
-// Work schedule. Stage 1 handles each unit's forced blocks (those holding a sink or a local
-// token); the main kernel takes the blocks between them, the unit's "middle" range, which is
-// contiguous. The middle blocks of all (sequence, KV head) units, concatenated unit by unit, are
-// cut into `ncta` contiguous ranges of equal length; each range is walked in sub-chunks of at
-// most kSub blocks that never cross a unit. Producer and consumers walk the same sequence.
+// Work schedule. The blocks of all (sequence, KV head) units, concatenated unit by unit, are cut
+// into `ncta` contiguous ranges of equal length; each range is walked in sub-chunks of at most
+// kSub blocks that never cross a unit. Every role of a CTA walks the same sequence.
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ int len_of(const DecodeArgs &a, int b) {
     const int n = a.seq_lens[b];
@@ -124,47 +144,41 @@ __device__ __forceinline__ int len_of(const DecodeArgs &a, int b) {
     return n < 0 ? 0 : (n > cap ? cap : n);
 }
 
-// First middle block and middle block count of sequence b.
-__device__ __forceinline__ int mid_range(const DecodeArgs &a, int b, int &lo) {
-    const ForcedBlocks fb(len_of(a, b), a.S, a.L);
-    lo = fb.ns;
-    return fb.local_first > fb.ns ? fb.local_first - fb.ns : 0;
+__device__ __forceinline__ int nblocks_of(const DecodeArgs &a, int b) {
+    return (len_of(a, b) + kPage - 1) / kPage;
 }
 
-__device__ __forceinline__ int64_t total_mid_blocks(const DecodeArgs &a) {
+__device__ __forceinline__ int64_t total_blocks(const DecodeArgs &a) {
     int64_t T = 0;
-    for (int bb = 0; bb < a.B; bb++) {
-        int lo;
-        T += (int64_t)a.Hkv * mid_range(a, bb, lo);
-    }
+    for (int bb = 0; bb < a.B; bb++) T += (int64_t)a.Hkv * nblocks_of(a, bb);
     return T;
 }
 
 struct Sub {
     int b, h, j0, cnt;  // unit (b, h), first block, block count
-    int jr;             // index of the first block within the unit's middle range
-    int nmid;           // middle blocks of the unit
+    int nblk;           // blocks of the unit
     int64_t x0;         // global index of the sub-chunk's first block
+    bool first;         // first sub-chunk of this CTA's segment of the unit
     bool last;          // last sub-chunk of this CTA's segment of the unit
 };
 
 struct Sched {
     int64_t x, x1, T;
-    int b, h, j, nbb, lob;  // j: index within the middle range [lob, lob + nbb)
+    int b, h, j, nbb;  // current unit (b, h), next block j of its nbb blocks
+    bool fresh;
 
     __device__ void init(const DecodeArgs &a, int cta, int ncta) {
-        T = total_mid_blocks(a);
+        T = total_blocks(a);
         x = T * cta / ncta;
         x1 = T * (cta + 1) / ncta;
         int64_t pre = 0;
-        b = h = j = nbb = lob = 0;
+        b = h = j = nbb = 0;
+        fresh = true;
         for (; b < a.B; b++) {
-            int lo;
-            const int nb = mid_range(a, b, lo);
+            const int nb = nblocks_of(a, b);
             const int64_t span = (int64_t)a.Hkv * nb;
             if (x < pre + span) {
                 nbb = nb;
-                lob = lo;
                 h = (int)((x - pre) / nb);
                 j = (int)((x - pre) % nb);
                 break;
@@ -180,20 +194,22 @@ struct Sched {
         if (x1 - x < cnt) cnt = (int)(x1 - x);
         s.b = b;
         s.h = h;
-        s.j0 = lob + j;
-        s.jr = j;
-        s.nmid = nbb;
+        s.j0 = j;
+        s.nblk = nbb;
         s.cnt = cnt;
         s.x0 = x;
+        s.first = fresh;
         s.last = (j + cnt == nbb) || (x + cnt == x1);
+        fresh = false;
         x += cnt;
         j += cnt;
         if (j == nbb) {
             j = 0;
+            fresh = true;
             if (++h == a.Hkv) {
                 h = 0;
                 for (b++; b < a.B; b++) {
-                    nbb = mid_range(a, b, lob);
+                    nbb = nblocks_of(a, b);
                     if (nbb > 0) break;
                 }
             }
@@ -350,471 +366,6 @@ __device__ __forceinline__ float corr_score(const float (&D)[4][4], int e, const
     return acc * sm;
 }
 
-// Pseudo-max of heads 2tig, 2tig+1 from the stage-1 block maxima (-inf when there are none).
-__device__ __forceinline__ void load_mtilde(const DecodeArgs &a, int u, int tig, float &m0,
-                                            float &m1) {
-    m0 = -INFINITY;
-    m1 = -INFINITY;
-    for (int s = 0; s < a.nf; s++) {
-        const float *p = a.ws_m1 + ((size_t)u * a.nf + s) * kMaxG;
-        m0 = fmaxf(m0, p[2 * tig]);
-        m1 = fmaxf(m1, p[2 * tig + 1]);
-    }
-}
-
-// ------------------------------------------------------------------------------------------
-// Split merge: out_i = sum_r e^(m_r - M) num_r / sum_r e^(m_r - M) den_r over a unit's records
-// (stage-1 slots of the forced blocks, and main-kernel records of CTAs cf..cl when it has a
-// middle range); records hold (num[128], m, den) per head.
-// ------------------------------------------------------------------------------------------
-__device__ __forceinline__ const float *s1_record(const DecodeArgs &a, int u, int slot, int i) {
-    return a.ws_s1 + (((size_t)u * a.nf + slot) * a.G + i) * kPartStride;
-}
-
-__device__ __forceinline__ const float *main_record(const DecodeArgs &a, int u, int c, int i) {
-    return a.ws_part + ((size_t)(u + c) * a.G + i) * kPartStride;
-}
-
-// Called after a __threadfence() that follows the atomic ticket showing this CTA came last.
-// Warp w of nwarps merges heads w, w + nwarps, ...: lane r owns record r's maximum, weight and
-// denominator; every lane accumulates 4 of the 128 channels over all records, whose loads do not
-// depend on each other.
-__device__ __forceinline__ void merge_unit(const DecodeArgs &a, int b, int h, bool with_main,
-                                           int cf, int cl, int warp, int nwarps, int lane) {
-    const int u = b * a.Hkv + h;
-    const int n1 = a.nf, nr = n1 + (with_main ? cl - cf + 1 : 0);
-    for (int i = warp; i < a.G; i += nwarps) {
-        auto rec = [&](int r) {
-            return r < n1 ? s1_record(a, u, r, i) : main_record(a, u, cf + r - n1, i);
-        };
-        float M = -INFINITY;
-        for (int r = lane; r < nr; r += 32) M = fmaxf(M, __ldcg(rec(r) + kD));
-        M = warp_max(M);
-        float num[4] = {0.0f, 0.0f, 0.0f, 0.0f}, den = 0.0f;
-        if (M != -INFINITY) {
-            for (int r0 = 0; r0 < nr; r0 += 32) {
-                const int r = r0 + lane;
-                float f = 0.0f;
-                if (r < nr) {
-                    const float *p = rec(r);
-                    const float mr = __ldcg(p + kD);
-                    if (mr != -INFINITY) {
-                        f = exp2f((mr - M) * kLog2e);
-                        den = fmaf(f, __ldcg(p + kD + 1), den);
-                    }
-                }
-                const int cnt = nr - r0 < 32 ? nr - r0 : 32;
-#pragma unroll 4
-                for (int j = 0; j < cnt; j++) {
-                    const float fj = __shfl_sync(0xffffffffu, f, j);
-                    const float *p = rec(r0 + j);
-#pragma unroll
-                    for (int k = 0; k < 4; k++) {
-                        const float x = __ldcg(p + lane + 32 * k);
-                        num[k] = fj > 0.0f ? fmaf(fj, x, num[k]) : num[k];
-                    }
-                }
-            }
-            den = warp_sum(den);
-        }
-        float *o = a.out + ((size_t)b * a.Hq + h * a.G + i) * kD;
-#pragma unroll
-        for (int k = 0; k < 4; k++) o[lane + 32 * k] = den > 0.0f ? num[k] / den : 0.0f;
-        if (a.m_tilde) {
-            float m = -INFINITY;
-            for (int sl = lane; sl < a.nf; sl += 32)
-                m = fmaxf(m, __ldcg(a.ws_m1 + ((size_t)u * a.nf + sl) * kMaxG + i));
-            m = warp_max(m);
-            if (lane == 0) a.m_tilde[(size_t)b * a.Hq + h * a.G + i] = m;
-        }
-    }
-}
-
-// ------------------------------------------------------------------------------------------
-// Stage 1: one CTA per (forced-block slot, unit); warp w takes 16 tokens of the block.
-//   * exact scores s = sm q . K^ (thumbnail + residual, on tensor cores);
-//   * per-head maximum over the block's sink / local tokens -> ws_m1 (the pseudo-max m~ is the
-//     maximum over the unit's slots);
-//   * softmax partial of the whole block (forced blocks are always kept) -> ws_s1, with PV on
-//     CUDA cores (V read straight from global memory; the CTA keeps 2 KB of shared memory, so it
-//     runs beside the persistent main kernel);
-//   * a unit without middle blocks is merged here by the last of its slot CTAs (atomic ticket).
-// Slot 0 of every unit also clears the keep-mask tail past the sequence.
-// ------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(128, 1) stage1_kernel(const DecodeArgs a) {
-    grid_launch_dependents();
-    __shared__ float red_m[4][kMaxG], red_x[4][kMaxG], red_l[4][kMaxG];
-    __shared__ float pbuf[kPage][kMaxG];
-    __shared__ uint32_t merge_flag;
-    const int u = blockIdx.y, b = u / a.Hkv, h = u % a.Hkv;
-    const int slot = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, tig = lane & 3;
-    const int raw_n = a.seq_lens[b];
-    const int n = len_of(a, b);
-    const int nb = (n + kPage - 1) / kPage;
-    if (slot == 0) {
-        if (tid == 0 && h == 0 && raw_n != n) raise_error(a.err, FFD_ERRBIT_BOUNDS);
-        if (a.keep_mask)
-            for (int blk = nb + tid; blk < a.max_blocks; blk += blockDim.x)
-                a.keep_mask[(size_t)u * a.max_blocks + blk] = 0;
-    }
-    const ForcedBlocks fb(n, a.S, a.L);
-    int page = -1;
-    const int blk = slot < fb.count ? fb.block(slot) : 0;
-    if (slot < fb.count) {
-        page = a.block_table[(size_t)b * a.max_blocks + blk];
-        if (page < 0 || page >= a.P) {
-            if (tid == 0) raise_error(a.err, FFD_ERRBIT_BOUNDS);
-            page = -1;
-        }
-        if (a.keep_mask && tid == 0) a.keep_mask[(size_t)u * a.max_blocks + blk] = page >= 0;
-    }
-    float *mdst = a.ws_m1 + ((size_t)u * a.nf + slot) * kMaxG;
-    float *rdst = a.ws_s1 + ((size_t)u * a.nf + slot) * a.G * kPartStride;
-    if (page < 0) {  // empty slot (uniform across the CTA)
-        if (tid < kMaxG) mdst[tid] = -INFINITY;
-        if (tid < a.G) {
-            rdst[tid * kPartStride + kD] = -INFINITY;
-            rdst[tid * kPartStride + kD + 1] = 0.0f;
-        }
-    } else {
-        ThumbOps Q;
-        ResidOps QR;
-        load_thumb_ops(a, b, h, lane, Q);
-        load_resid_ops(a, b, h, lane, QR);
-        const size_t tile = (size_t)page * a.Hkv + h;
-        const int r0 = 16 * warp + g, r1 = r0 + 8;
-        uint32_t w0[8], w1[8];
-        {
-            const uint4 *c0 = reinterpret_cast<const uint4 *>(a.thumb + (tile * kPage + r0) * kThumbRow);
-            const uint4 *c1 = reinterpret_cast<const uint4 *>(a.thumb + (tile * kPage + r1) * kThumbRow);
-            const uint4 p0 = c0[0], p1 = c0[1], p2 = c1[0], p3 = c1[1];
-            w0[0] = p0.x; w0[1] = p0.y; w0[2] = p0.z; w0[3] = p0.w;
-            w0[4] = p1.x; w0[5] = p1.y; w0[6] = p1.z; w0[7] = p1.w;
-            w1[0] = p2.x; w1[1] = p2.y; w1[2] = p2.z; w1[3] = p2.w;
-            w1[4] = p3.x; w1[5] = p3.y; w1[6] = p3.z; w1[7] = p3.w;
-        }
-        uint2 x0[4], x1[4];
-#pragma unroll
-        for (int gg = 0; gg < 4; gg++) {
-            x0[gg] = *reinterpret_cast<const uint2 *>(a.resid + (tile * kPage + r0) * kD + 32 * gg + 8 * tig);
-            x1[gg] = *reinterpret_cast<const uint2 *>(a.resid + (tile * kPage + r1) * kD + 32 * gg + 8 * tig);
-        }
-        float sf0[4], sf1[4], zf0[4], zf1[4], sr0[4], sr1[4];
-        const uint2 *ts = reinterpret_cast<const uint2 *>(a.t_scale);
-        const uint2 *tz = reinterpret_cast<const uint2 *>(a.t_zero);
-        const uint2 *rs = reinterpret_cast<const uint2 *>(a.r_scale);
-        unpack4h(ts[tile * kPage + r0], sf0);
-        unpack4h(ts[tile * kPage + r1], sf1);
-        unpack4h(tz[tile * kPage + r0], zf0);
-        unpack4h(tz[tile * kPage + r1], zf1);
-        unpack4h(rs[tile * kPage + r0], sr0);
-        unpack4h(rs[tile * kPage + r1], sr1);
-
-        float D[4][4], Dr[4][4];
-        thumb_mma(D, w0, w1, 0x00030003u << (2 * tig), Q);
-        resid_mma(Dr, x0, x1, QR);
-        const float sm = a.sm_scale;
-        const int t0 = blk * kPage + r0, t1 = blk * kPage + r1;
-        const bool in0 = t0 < n, in1 = t1 < n;
-        const float s00 = in0 ? est_score(D, 0, sf0, zf0, Q.qs[0], sm) + corr_score(Dr, 0, sr0, Q.qs[0], sm) : -INFINITY;
-        const float s01 = in0 ? est_score(D, 1, sf0, zf0, Q.qs[1], sm) + corr_score(Dr, 1, sr0, Q.qs[1], sm) : -INFINITY;
-        const float s10 = in1 ? est_score(D, 2, sf1, zf1, Q.qs[0], sm) + corr_score(Dr, 2, sr1, Q.qs[0], sm) : -INFINITY;
-        const float s11 = in1 ? est_score(D, 3, sf1, zf1, Q.qs[1], sm) + corr_score(Dr, 3, sr1, Q.qs[1], sm) : -INFINITY;
-        // pseudo-max candidates: sink and local tokens only
-        const bool v0 = in0 && (t0 < a.S || t0 >= n - a.L);
-        const bool v1 = in1 && (t1 < a.S || t1 >= n - a.L);
-        float mx0 = fmaxf(v0 ? s00 : -INFINITY, v1 ? s10 : -INFINITY);
-        float mx1 = fmaxf(v0 ? s01 : -INFINITY, v1 ? s11 : -INFINITY);
-        // block maximum over all its tokens (softmax reference of the partial)
-        float bx0 = fmaxf(s00, s10), bx1 = fmaxf(s01, s11);
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-            bx0 = fmaxf(bx0, __shfl_xor_sync(0xffffffffu, bx0, o));
-            bx1 = fmaxf(bx1, __shfl_xor_sync(0xffffffffu, bx1, o));
-        }
-        if (g == 0) {
-            red_m[warp][2 * tig] = mx0;
-            red_m[warp][2 * tig + 1] = mx1;
-            red_x[warp][2 * tig] = bx0;
-            red_x[warp][2 * tig + 1] = bx1;
-        }
-        __syncthreads();
-        const float M0 = fmaxf(fmaxf(red_x[0][2 * tig], red_x[1][2 * tig]),
-                               fmaxf(red_x[2][2 * tig], red_x[3][2 * tig]));
-        const float M1 = fmaxf(fmaxf(red_x[0][2 * tig + 1], red_x[1][2 * tig + 1]),
-                               fmaxf(red_x[2][2 * tig + 1], red_x[3][2 * tig + 1]));
-        const float p00 = in0 ? exp2f((s00 - M0) * kLog2e) : 0.0f;
-        const float p01 = in0 ? exp2f((s01 - M1) * kLog2e) : 0.0f;
-        const float p10 = in1 ? exp2f((s10 - M0) * kLog2e) : 0.0f;
-        const float p11 = in1 ? exp2f((s11 - M1) * kLog2e) : 0.0f;
-        pbuf[r0][2 * tig] = p00;
-        pbuf[r0][2 * tig + 1] = p01;
-        pbuf[r1][2 * tig] = p10;
-        pbuf[r1][2 * tig + 1] = p11;
-        float l0 = p00 + p10, l1 = p01 + p11;
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-        }
-        if (g == 0) {
-            red_l[warp][2 * tig] = l0;
-            red_l[warp][2 * tig + 1] = l1;
-        }
-        __syncthreads();
-        // PV: thread = channel d
-        float acc[kMaxG];
-#pragma unroll
-        for (int i = 0; i < kMaxG; i++) acc[i] = 0.0f;
-        const __nv_bfloat16 *vcol = a.v + tile * kPage * kD + tid;
-        for (int tt = 0; tt < kPage; tt++) {
-            const float vv = __bfloat162float(vcol[(size_t)tt * kD]);
-#pragma unroll
-            for (int i = 0; i < kMaxG; i++) acc[i] = fmaf(pbuf[tt][i], vv, acc[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < kMaxG; i++)
-            if (i < a.G) rdst[i * kPartStride + tid] = acc[i];
-        if (tid < kMaxG)
-            mdst[tid] = tid < a.G ? fmaxf(fmaxf(red_m[0][tid], red_m[1][tid]),
-                                          fmaxf(red_m[2][tid], red_m[3][tid]))
-                                  : -INFINITY;
-        if (tid < a.G) {
-            rdst[tid * kPartStride + kD] = fmaxf(fmaxf(red_x[0][tid], red_x[1][tid]),
-                                                 fmaxf(red_x[2][tid], red_x[3][tid]));
-            rdst[tid * kPartStride + kD + 1] =
-                (red_l[0][tid] + red_l[1][tid]) + (red_l[2][tid] + red_l[3][tid]);
-        }
-    }
-    // a unit with no middle blocks is merged by the last of its stage-1 CTAs
-    int lo;
-    if (mid_range(a, b, lo) > 0) return;  // uniform: the main kernel merges this unit
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        uint32_t last = 1;
-        if (a.nf > 1) {
-            int *cnt = a.ws_cnt + a.B * a.Hkv + u;
-            last = atomicAdd(cnt, 1) == a.nf - 1;
-            if (last) *cnt = 0;  // ready for the next call
-        }
-        merge_flag = last;
-    }
-    __syncthreads();
-    if (merge_flag) {
-        __threadfence();
-        merge_unit(a, b, h, false, 0, -1, warp, blockDim.x / 32, lane);
-    }
-}
-// ------------------------------------------------------------------------------------------
-// Main kernel: persistent, one CTA per SM. Warpgroup 0 issues the copies: the ring warp (0), the
-// page warp (1) and the thumbnail warp (2); warps 4-15 consume.
-// ------------------------------------------------------------------------------------------
-struct Smem {
-    uint8_t *ring, *thumb, *shat;
-    UnitOps *unit;
-    Misc *misc;
-};
-
-// Bounded wait: after kWaitTimeoutNs the CTA records FFD_ERRBIT_TIMEOUT, marks itself aborted and
-// stops waiting (its results are then garbage, but every thread still reaches every barrier).
-__device__ __forceinline__ void wait_bar(const DecodeArgs &a, Misc *m, uint64_t *bar,
-                                         uint32_t parity) {
-    if (*reinterpret_cast<volatile uint32_t *>(&m->aborted)) return;
-    if (mbar_try_wait(bar, parity)) return;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-            raise_error(a.err, FFD_ERRBIT_TIMEOUT);
-            *reinterpret_cast<volatile uint32_t *>(&m->aborted) = 1;
-            return;
-        }
-    }
-}
-
-// Page warp: walks the CTA's schedule ahead of the producer and resolves the block-table entries
-// of every sub-chunk (one lane per block) into the page ring, so that no global-load latency sits
-// on the TMA issue path; a slot with cnt == 0 ends the schedule. Entries outside [0, P) are
-// flagged (FFD_ERRBIT_BOUNDS) and their blocks are never loaded.
-__device__ __forceinline__ void pager(const DecodeArgs &a, const Smem &S, int cta, int ncta,
-                                      int lane) {
-    Misc *m = S.misc;
-    Sched sch;
-    sch.init(a, cta, ncta);
-    Sub s;
-    for (int t = 0;; t++) {
-        const bool more = sch.next(a, s);
-        const int ps = t % kPageSlots, round = t / kPageSlots;
-        if (round > 0) wait_bar(a, m, &m->pages_empty[ps], (round - 1) & 1);
-        PageSlot &P = m->ps[ps];
-        if (!more) {  // end marker
-            if (lane == 0) {
-                P.cnt = 0;
-                mbar_arrive(&m->pages_full[ps]);
-            }
-            return;
-        }
-        int page = 0;
-        if (lane < s.cnt) page = a.block_table[(size_t)s.b * a.max_blocks + s.j0 + lane];
-        const bool bad = lane < s.cnt && (page < 0 || page >= a.P);
-        const uint32_t badmask = __ballot_sync(0xffffffffu, bad);
-        // every row in the ring is in range (a bad entry reads as page 0 and is never loaded)
-        if (lane < s.cnt) P.row[lane] = ((bad ? 0 : page) * a.Hkv + s.h) * kPage;
-        if (lane == 0) {
-            P.bad = badmask;
-            P.cnt = s.cnt;
-            if (badmask) raise_error(a.err, FFD_ERRBIT_BOUNDS);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&m->pages_full[ps]);
-    }
-}
-
-__device__ __forceinline__ const PageSlot &page_slot(const DecodeArgs &a, Misc *m, int t) {
-    wait_bar(a, m, &m->pages_full[t % kPageSlots], (t / kPageSlots) & 1);
-    return m->ps[t % kPageSlots];
-}
-
-// Wait for a copy this CTA issued, ignoring the abort flag (still bounded in time): no CTA exits
-// with a copy into its shared memory in flight.
-__device__ __forceinline__ void drain_bar(const DecodeArgs &a, uint64_t *bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-            raise_error(a.err, FFD_ERRBIT_TIMEOUT);
-            return;
-        }
-    }
-}
-
-// Thumbnail warp: the 2-bit codes, scales and zeros of sub-chunk t go to buffer t&1 once the ring
-// warp has taken the decision of sub-chunk t-2 (so that buffer is free, and no decision can run
-// two phases ahead of the ring warp); lane k issues block k's copies.
-__device__ __forceinline__ void thumb_issuer(const DecodeArgs &a, const Smem &S, int lane) {
-    Misc *m = S.misc;
-    uint32_t pend0 = 0, pend1 = 0;  // phases of thumb_full[0/1] armed by this warp
-    for (int t = 0;; t++) {
-        const int buf = t & 1;
-        if (t >= 2) wait_bar(a, m, &m->ring_seen[buf], ((t - 2) >> 1) & 1);
-        const PageSlot &P = page_slot(a, m, t);
-        const int cnt = P.cnt;
-        if (cnt == 0 || *reinterpret_cast<volatile uint32_t *>(&m->aborted)) break;
-        const uint32_t bad = P.bad;
-        if (lane == 0) {
-            m->bad[buf] = bad;
-            mbar_arrive_expect_tx(&m->thumb_full[buf],
-                                  (uint32_t)((cnt - __popc(bad)) * kThumbBlock));
-        }
-        pend0 += buf == 0;
-        pend1 += buf == 1;
-        __syncwarp();
-        if (lane < cnt && !((bad >> lane) & 1u)) {
-            const size_t row = (size_t)P.row[lane];
-            uint8_t *d = S.thumb + buf * (kSub * kThumbBlock) + lane * kThumbBlock;
-            tma_load_1d(d, a.thumb + row * kThumbRow, 2048, &m->thumb_full[buf]);
-            tma_load_1d(d + 2048, a.t_scale + row * kGroups, 512, &m->thumb_full[buf]);
-            tma_load_1d(d + 2560, a.t_zero + row * kGroups, 512, &m->thumb_full[buf]);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&m->pages_empty[t % kPageSlots]);
-    }
-    // leave no copy in flight
-    if (lane == 0) {
-        if (pend0) drain_bar(a, &m->thumb_full[0], (pend0 - 1) & 1);
-        if (pend1) drain_bar(a, &m->thumb_full[1], (pend1 - 1) & 1);
-    }
-}
-
-// Ring warp: residual tile, V tile and residual scales of every kept block of sub-chunk t, once
-// the consumers have decided it; lanes 0-3 issue one block's four copies side by side.
-__device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S, int lane) {
-    const DecodeArgs &a = prm.a;
-    Misc *m = S.misc;
-    if (lane == 0) {
-        prefetch_tensormap(&prm.tm_resid);
-        prefetch_tensormap(&prm.tm_v);
-    }
-    int kb = 0;
-    for (int t = 0;; t++) {
-        const PageSlot &P = page_slot(a, m, t);
-        const int cnt = P.cnt;
-        if (cnt == 0 || *reinterpret_cast<volatile uint32_t *>(&m->aborted)) break;
-        wait_bar(a, m, &m->decision[t & 1], (t >> 1) & 1);
-        const uint32_t mask = *reinterpret_cast<volatile uint32_t *>(&m->vote_mask[t & 3]) &
-                              ~P.bad & ((1u << cnt) - 1u);
-        __syncwarp();
-        if (lane == 0) {
-            // every consumer has read the votes of sub-chunk t-2 (it voted on t since), and none
-            // votes on t+2 before this arrival releases its thumbnails
-            m->vote_mask[(t + 2) & 3] = 0;
-            mbar_arrive(&m->ring_seen[t & 1]);
-        }
-        for (int k = 0; k < cnt; k++) {
-            if (!(mask & (1u << k))) continue;
-            const int slot = kb % kRing, round = kb / kRing;
-            kb++;
-            if (round > 0) wait_bar(a, m, &m->ring_empty[slot], (round - 1) & 1);
-            const int row = P.row[k];
-            uint8_t *d = S.ring + slot * kSlotBytes;
-            uint64_t *bar = &m->ring_full[slot];
-            if (lane == 0) mbar_arrive_expect_tx(bar, kSlotTx);
-            __syncwarp();
-            if (lane == 0) tma_load_2d(d, &prm.tm_resid, 0, row, bar);
-            else if (lane == 1) tma_load_2d(d + kSlotV, &prm.tm_v, 0, row, bar);
-            else if (lane == 2) tma_load_2d(d + kSlotV + 8192, &prm.tm_v, 64, row, bar);
-            else if (lane == 3)
-                tma_load_1d(d + kSlotRScale, a.r_scale + (size_t)row * kGroups, 512, bar);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&m->pages_empty[t % kPageSlots]);
-    }
-    // leave no copy in flight: wait for the last fill of every ring slot
-    if (lane == 0)
-        for (int s = 0; s < kRing && s < kb; s++) {
-            const int last = kb - 1 - ((kb - 1 - s) % kRing);
-            drain_bar(a, &m->ring_full[s], (last / kRing) & 1);
-        }
-}
-
-// Consumer warp 0 computes the unit's query operands and thresholds into the unit slot; every
-// consumer warp then reads them from shared memory.
-__device__ __forceinline__ void setup_unit(const DecodeArgs &a, const Smem &S, const Sub &s,
-                                           int warp, int lane) {
-    if (warp == 0) {
-        UnitOps &U = *S.unit;
-        const int g = lane >> 2, tig = lane & 3;
-        ThumbOps T;
-        ResidOps Rr;
-        load_thumb_ops(a, s.b, s.h, lane, T);
-        load_resid_ops(a, s.b, s.h, lane, Rr);
-#pragma unroll
-        for (int r = 0; r < 2; r++) {
-            U.bt[r][lane] = make_uint4(T.bt0[4 * r], T.bt0[4 * r + 1], T.bt0[4 * r + 2], T.bt0[4 * r + 3]);
-            U.bt[2 + r][lane] = make_uint4(T.bt1[4 * r], T.bt1[4 * r + 1], T.bt1[4 * r + 2], T.bt1[4 * r + 3]);
-            U.br[r][lane] = make_uint4(Rr.br0[4 * r], Rr.br0[4 * r + 1], Rr.br0[4 * r + 2], Rr.br0[4 * r + 3]);
-            U.br[2 + r][lane] = make_uint4(Rr.br1[4 * r], Rr.br1[4 * r + 1], Rr.br1[4 * r + 2], Rr.br1[4 * r + 3]);
-        }
-        if (g == 0) {
-            U.qs[2 * tig] = make_float4(T.qs[0][0], T.qs[0][1], T.qs[0][2], T.qs[0][3]);
-            U.qs[2 * tig + 1] = make_float4(T.qs[1][0], T.qs[1][1], T.qs[1][2], T.qs[1][3]);
-        }
-        if (lane < kMaxG) {
-            float m = -INFINITY;
-            const int u = s.b * a.Hkv + s.h;
-            for (int sl = 0; sl < a.nf; sl++)
-                m = fmaxf(m, a.ws_m1[((size_t)u * a.nf + sl) * kMaxG + lane]);
-            U.mt[lane] = m;
-            U.thr[lane] = lane < a.G ? m - a.delta : INFINITY;
-        }
-        if (lane == 0) U.n = len_of(a, s.b);
-    }
-    named_barrier_sync(1, kConsumers);
-}
-
 __device__ __forceinline__ void load_frags(const uint4 (&src)[4][32], int lane, uint32_t (&f0)[8],
                                            uint32_t (&f1)[8]) {
     const uint4 p0 = src[0][lane], p1 = src[1][lane], p2 = src[2][lane], p3 = src[3][lane];
@@ -854,26 +405,415 @@ __device__ __forceinline__ bool tile_passes(float4 e, bool v0, bool v1, float th
     return (v0 && (e.x >= thr0 || e.y >= thr1)) || (v1 && (e.z >= thr0 || e.w >= thr1));
 }
 
-// Scan of sub-chunk t: provisional scores of this warp's m-tiles and its vote (an OR into
-// vote_mask, then one arrival on the decision barrier; no warp waits for the others here).
-// Returns the sub-chunk's never-loaded blocks. The warp's blocks are k = grp and grp + 3,
-// scanned side by side (two independent dependency chains). The second tile is computed even past the sub-chunk's end (its shared-memory reads stay
-// inside the buffer) and then ignored, so both chains stay in one basic block.
-__device__ __forceinline__ uint32_t scan_sub(const DecodeArgs &a, const Smem &S, const Sub &s,
-                                             int t, int warp, int lane) {
+
+// ------------------------------------------------------------------------------------------
+// Split merge: out_i = sum_r e^(m_r - M) num_r / sum_r e^(m_r - M) den_r over a unit's records.
+// Records of CTAs cf..cl, two per CTA (one per refine group), are contiguous from
+// ws_part[(u + cf) * 2]; a record holds (num[128], m, den) per head.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ float *unit_record(const DecodeArgs &a, int u, int c, int grp) {
+    return a.ws_part + ((size_t)(u + c) * 2 + grp) * a.G * kPartStride;
+}
+
+// Called after a __threadfence() that follows the atomic ticket showing this group came last.
+// Warp w of nwarps merges heads w, w + nwarps, ...: lane r owns record r's maximum, weight and
+// denominator; every lane accumulates 4 of the 128 channels, loading 8 records at a time.
+__device__ __forceinline__ void merge_unit(const DecodeArgs &a, int b, int h, int cf, int cl,
+                                           int warp, int nwarps, int lane) {
+    const int u = b * a.Hkv + h;
+    const int nr = 2 * (cl - cf + 1);
+    const float *base = unit_record(a, u, cf, 0);
+    const size_t rstride = (size_t)a.G * kPartStride;
+    for (int i = warp; i < a.G; i += nwarps) {
+        const float *hb = base + (size_t)i * kPartStride;
+        float M = -INFINITY;
+        for (int r = lane; r < nr; r += 32) M = fmaxf(M, __ldcg(hb + r * rstride + kD));
+        M = warp_max(M);
+        float num[4] = {0.0f, 0.0f, 0.0f, 0.0f}, den = 0.0f;
+        if (M != -INFINITY) {
+            for (int r0 = 0; r0 < nr; r0 += 32) {
+                const int r = r0 + lane;
+                float f = 0.0f;
+                if (r < nr) {
+                    const float mr = __ldcg(hb + r * rstride + kD);
+                    if (mr != -INFINITY) {
+                        f = exp2f((mr - M) * kLog2e);
+                        den = fmaf(f, __ldcg(hb + r * rstride + kD + 1), den);
+                    }
+                }
+                const int cnt = nr - r0 < 32 ? nr - r0 : 32;
+                for (int j0 = 0; j0 < cnt; j0 += 8) {
+                    float x[8][4];
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        const float *p = hb + (size_t)(r0 + (j0 + j < cnt ? j0 + j : 0)) * rstride;
+#pragma unroll
+                        for (int k = 0; k < 4; k++) x[j][k] = __ldcg(p + lane + 32 * k);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        const float fj = __shfl_sync(0xffffffffu, f, (j0 + j) & 31);
+                        if (j0 + j < cnt && fj > 0.0f) {
+#pragma unroll
+                            for (int k = 0; k < 4; k++) num[k] = fmaf(fj, x[j][k], num[k]);
+                        }
+                    }
+                }
+            }
+            den = warp_sum(den);
+        }
+        float *o = a.out + ((size_t)b * a.Hq + h * a.G + i) * kD;
+#pragma unroll
+        for (int k = 0; k < 4; k++) o[lane + 32 * k] = den > 0.0f ? num[k] / den : 0.0f;
+        if (a.m_tilde) {
+            float m = -INFINITY;
+            for (int sl = lane; sl < a.nf; sl += 32)
+                m = fmaxf(m, __ldcg(a.ws_m1 + ((size_t)u * a.nf + sl) * kMaxG + i));
+            m = warp_max(m);
+            if (lane == 0) a.m_tilde[(size_t)b * a.Hq + h * a.G + i] = m;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Stage 1 (pseudo-max): one CTA per (forced-block slot, unit); warp w takes 16 tokens of the
+// block. Exact scores s = sm q . K^ (thumbnail + residual, on tensor cores) of the block's sink
+// and local tokens; their per-head maximum goes to ws_m1 (the pseudo-max m~ of a unit is the
+// maximum over its slots). Slot 0 of every unit also clears the keep-mask tail past the sequence
+// and, for an empty sequence (which the main kernel never visits), writes the zero output and
+// m~ = -inf.
+// ------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(128, 1) stage1_kernel(const DecodeArgs a) {
+    grid_launch_dependents();
+    __shared__ float red_m[4][kMaxG];
+    const int u = blockIdx.y, b = u / a.Hkv, h = u % a.Hkv;
+    const int slot = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, tig = lane & 3;
+    const int raw_n = a.seq_lens[b];
+    const int n = len_of(a, b);
+    const int nb = (n + kPage - 1) / kPage;
+    if (slot == 0) {
+        if (tid == 0 && h == 0 && raw_n != n) raise_error(a.err, FFD_ERRBIT_BOUNDS);
+        if (a.keep_mask)
+            for (int blk = nb + tid; blk < a.max_blocks; blk += blockDim.x)
+                a.keep_mask[(size_t)u * a.max_blocks + blk] = 0;
+        if (n == 0) {
+            for (int idx = tid; idx < a.G * kD; idx += blockDim.x)
+                a.out[((size_t)b * a.Hq + h * a.G) * kD + idx] = 0.0f;
+            if (a.m_tilde && tid < a.G) a.m_tilde[(size_t)b * a.Hq + h * a.G + tid] = -INFINITY;
+        }
+    }
+    const ForcedBlocks fb(n, a.S, a.L);
+    float *mdst = a.ws_m1 + ((size_t)u * a.nf + slot) * kMaxG;
+    int page = -1;
+    const int blk = slot < fb.count ? fb.block(slot) : 0;
+    if (slot < fb.count) {
+        page = a.block_table[(size_t)b * a.max_blocks + blk];
+        if (page < 0 || page >= a.P) page = -1;  // flagged by the main kernel's page warp
+    }
+    if (page < 0) {  // empty slot (uniform across the CTA)
+        if (tid < kMaxG) mdst[tid] = -INFINITY;
+        return;
+    }
+    ThumbOps Q;
+    ResidOps QR;
+    load_thumb_ops(a, b, h, lane, Q);
+    load_resid_ops(a, b, h, lane, QR);
+    const size_t tile = (size_t)page * a.Hkv + h;
+    const int r0 = 16 * warp + g, r1 = r0 + 8;
+    uint32_t w0[8], w1[8];
+    {
+        const uint4 *c0 = reinterpret_cast<const uint4 *>(a.thumb + (tile * kPage + r0) * kThumbRow);
+        const uint4 *c1 = reinterpret_cast<const uint4 *>(a.thumb + (tile * kPage + r1) * kThumbRow);
+        const uint4 p0 = c0[0], p1 = c0[1], p2 = c1[0], p3 = c1[1];
+        w0[0] = p0.x; w0[1] = p0.y; w0[2] = p0.z; w0[3] = p0.w;
+        w0[4] = p1.x; w0[5] = p1.y; w0[6] = p1.z; w0[7] = p1.w;
+        w1[0] = p2.x; w1[1] = p2.y; w1[2] = p2.z; w1[3] = p2.w;
+        w1[4] = p3.x; w1[5] = p3.y; w1[6] = p3.z; w1[7] = p3.w;
+    }
+    uint2 x0[4], x1[4];
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) {
+        x0[gg] = *reinterpret_cast<const uint2 *>(a.resid + (tile * kPage + r0) * kD + 32 * gg + 8 * tig);
+        x1[gg] = *reinterpret_cast<const uint2 *>(a.resid + (tile * kPage + r1) * kD + 32 * gg + 8 * tig);
+    }
+    float sf0[4], sf1[4], zf0[4], zf1[4], sr0[4], sr1[4];
+    const uint2 *ts = reinterpret_cast<const uint2 *>(a.t_scale);
+    const uint2 *tz = reinterpret_cast<const uint2 *>(a.t_zero);
+    const uint2 *rs = reinterpret_cast<const uint2 *>(a.r_scale);
+    unpack4h(ts[tile * kPage + r0], sf0);
+    unpack4h(ts[tile * kPage + r1], sf1);
+    unpack4h(tz[tile * kPage + r0], zf0);
+    unpack4h(tz[tile * kPage + r1], zf1);
+    unpack4h(rs[tile * kPage + r0], sr0);
+    unpack4h(rs[tile * kPage + r1], sr1);
+    float D[4][4], Dr[4][4];
+    thumb_mma(D, w0, w1, 0x00030003u << (2 * tig), Q);
+    resid_mma(Dr, x0, x1, QR);
+    const float sm = a.sm_scale;
+    const int t0 = blk * kPage + r0, t1 = blk * kPage + r1;
+    // pseudo-max candidates: sink and local tokens inside the sequence
+    const bool v0 = t0 < n && (t0 < a.S || t0 >= n - a.L);
+    const bool v1 = t1 < n && (t1 < a.S || t1 >= n - a.L);
+    const float s00 = v0 ? est_score(D, 0, sf0, zf0, Q.qs[0], sm) + corr_score(Dr, 0, sr0, Q.qs[0], sm) : -INFINITY;
+    const float s01 = v0 ? est_score(D, 1, sf0, zf0, Q.qs[1], sm) + corr_score(Dr, 1, sr0, Q.qs[1], sm) : -INFINITY;
+    const float s10 = v1 ? est_score(D, 2, sf1, zf1, Q.qs[0], sm) + corr_score(Dr, 2, sr1, Q.qs[0], sm) : -INFINITY;
+    const float s11 = v1 ? est_score(D, 3, sf1, zf1, Q.qs[1], sm) + corr_score(Dr, 3, sr1, Q.qs[1], sm) : -INFINITY;
+    float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    if (g == 0) {
+        red_m[warp][2 * tig] = mx0;
+        red_m[warp][2 * tig + 1] = mx1;
+    }
+    __syncthreads();
+    if (tid < kMaxG)
+        mdst[tid] = tid < a.G ? fmaxf(fmaxf(red_m[0][tid], red_m[1][tid]),
+                                      fmaxf(red_m[2][tid], red_m[3][tid]))
+                              : -INFINITY;
+}
+
+
+// ------------------------------------------------------------------------------------------
+// Main kernel: waits and the copy warps.
+// ------------------------------------------------------------------------------------------
+// Bounded wait: after kWaitTimeoutNs the CTA records FFD_ERRBIT_TIMEOUT, marks itself aborted and
+// stops waiting (its results are then garbage, but every loop still ends).
+__device__ __forceinline__ void wait_bar(const DecodeArgs &a, Misc *m, uint64_t *bar,
+                                         uint32_t parity) {
+    if (*reinterpret_cast<volatile uint32_t *>(&m->aborted)) return;
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            raise_error(a.err, FFD_ERRBIT_TIMEOUT);
+            *reinterpret_cast<volatile uint32_t *>(&m->aborted) = 1;
+            return;
+        }
+    }
+}
+
+// Wait for a copy this CTA issued, ignoring the abort flag (still bounded in time): no CTA exits
+// with a copy into its shared memory in flight.
+__device__ __forceinline__ void drain_bar(const DecodeArgs &a, uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            raise_error(a.err, FFD_ERRBIT_TIMEOUT);
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ bool aborted(Misc *m) {
+    return *reinterpret_cast<volatile uint32_t *>(&m->aborted) != 0;
+}
+
+// Page warp: walks the CTA's schedule ahead of the copy warps and resolves the block-table entries
+// of every sub-chunk (one lane per block) into the page ring, so that no global-load latency sits
+// on a TMA issue path; a slot with cnt == 0 ends the schedule. Entries outside [0, P) are flagged
+// (FFD_ERRBIT_BOUNDS) and their blocks are never loaded.
+__device__ __forceinline__ void pager(const DecodeArgs &a, const Smem &S, int cta, int ncta,
+                                      int lane) {
     Misc *m = S.misc;
-    const UnitOps &U = *S.unit;
-    const int g = lane >> 2, tig = lane & 3, grp = warp >> 2, mt = warp & 3;
-    const int buf = t & 1;
-    wait_bar(a, m, &m->thumb_full[buf], (t >> 1) & 1);
-    const uint32_t bad = m->bad[buf];
-    uint32_t votes = 0;
-    const int kA = grp, kB = grp + kGroups3;
-    if (kA < s.cnt) {
-        const uint32_t m0 = 0x00030003u << (2 * tig);
-        const float sm = a.sm_scale;
-        const float thr0 = U.thr[2 * tig], thr1 = U.thr[2 * tig + 1];
-        const int n = U.n;
+    Sched sch;
+    sch.init(a, cta, ncta);
+    Sub s;
+    for (int t = 0;; t++) {
+        const bool more = sch.next(a, s);
+        const int ps = t % kPageSlots, round = t / kPageSlots;
+        if (round > 0) wait_bar(a, m, &m->pages_empty[ps], (round - 1) & 1);
+        PageSlot &P = m->ps[ps];
+        if (!more) {  // end marker
+            if (lane == 0) {
+                P.cnt = 0;
+                mbar_arrive(&m->pages_full[ps]);
+            }
+            return;
+        }
+        int page = 0;
+        if (lane < s.cnt) page = a.block_table[(size_t)s.b * a.max_blocks + s.j0 + lane];
+        const bool bad = lane < s.cnt && (page < 0 || page >= a.P);
+        const uint32_t badmask = __ballot_sync(0xffffffffu, bad);
+        const ForcedBlocks fb(len_of(a, s.b), a.S, a.L);
+        const uint32_t forced = __ballot_sync(0xffffffffu, lane < s.cnt && fb.forced(s.j0 + lane));
+        // every row in the ring is in range (a bad entry reads as page 0 and is never loaded)
+        if (lane < s.cnt) P.row[lane] = ((bad ? 0 : page) * a.Hkv + s.h) * kPage;
+        if (lane == 0) {
+            P.bad = badmask;
+            P.forced = forced;
+            P.cnt = s.cnt;
+            if (badmask) raise_error(a.err, FFD_ERRBIT_BOUNDS);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m->pages_full[ps]);
+    }
+}
+
+__device__ __forceinline__ const PageSlot &page_slot(const DecodeArgs &a, Misc *m, int t) {
+    wait_bar(a, m, &m->pages_full[t % kPageSlots], (t / kPageSlots) & 1);
+    return m->ps[t % kPageSlots];
+}
+
+// Thumbnail warp: the 2-bit codes, scales and zeros of sub-chunk t go to buffer t % kThumbBufs
+// once the ring warp has published sub-chunk t - kThumbBufs (so the scan warps are done with that
+// buffer, and no decision runs more than kThumbBufs sub-chunks ahead of the ring warp); lane k
+// issues block k's copies.
+__device__ __forceinline__ void thumb_issuer(const DecodeArgs &a, const Smem &S, int lane) {
+    Misc *m = S.misc;
+    int t = 0;
+    for (;; t++) {
+        const int buf = t % kThumbBufs;
+        if (t >= kThumbBufs) {
+            const int tp = t - kThumbBufs;
+            wait_bar(a, m, &m->ring_seen[tp % kDepth], (tp / kDepth) & 1);
+        }
+        const PageSlot &P = page_slot(a, m, t);
+        const int cnt = P.cnt;
+        if (cnt == 0 || aborted(m)) break;
+        const uint32_t bad = P.bad;
+        if (lane == 0)
+            mbar_arrive_expect_tx(&m->thumb_full[buf],
+                                  (uint32_t)((cnt - __popc(bad)) * kThumbBlock));
+        __syncwarp();
+        if (lane < cnt && !((bad >> lane) & 1u)) {
+            const size_t row = (size_t)P.row[lane];
+            uint8_t *d = S.thumb + buf * kThumbBuf + lane * kThumbBlock;
+            tma_load_1d(d, a.thumb + row * kThumbRow, 2048, &m->thumb_full[buf]);
+            tma_load_1d(d + 2048, a.t_scale + row * kGroups, 512, &m->thumb_full[buf]);
+            tma_load_1d(d + 2560, a.t_zero + row * kGroups, 512, &m->thumb_full[buf]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m->pages_empty[t % kPageSlots]);
+    }
+    // leave no copy in flight: wait for the last fill of every buffer (t fills were armed)
+    if (lane == 0)
+        for (int j = 0; j < kThumbBufs && j < t; j++)
+            drain_bar(a, &m->thumb_full[j], ((t - 1 - j) / kThumbBufs) & 1);
+}
+
+// Ring warp: publishes the kept blocks of sub-chunk t (scan votes, plus the forced blocks, less
+// the never-loaded ones), then issues the residual tile, V tile and residual scales of each kept
+// block into the next ring slot as it frees up; lanes 0-3 issue one block's four copies side by
+// side.
+__device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S, int lane) {
+    const DecodeArgs &a = prm.a;
+    Misc *m = S.misc;
+    if (lane == 0) {
+        prefetch_tensormap(&prm.tm_resid);
+        prefetch_tensormap(&prm.tm_v);
+    }
+    int kb = 0;
+    for (int t = 0;; t++) {
+        const PageSlot &P = page_slot(a, m, t);
+        const int cnt = P.cnt;
+        if (cnt == 0 || aborted(m)) break;
+        const int ds = t % kDepth;
+        wait_bar(a, m, &m->decision[ds], (t / kDepth) & 1);
+        const uint32_t mask = (*reinterpret_cast<volatile uint32_t *>(&m->vote[ds]) | P.forced) &
+                              ~P.bad & ((1u << cnt) - 1u);
+        __syncwarp();
+        if (lane == 0) {
+            m->final_mask[ds] = mask;
+            // the scan of sub-chunk t + kThumbBufs votes into this slot only after its
+            // thumbnails, which wait for this arrival; the slot's last reader was this warp
+            m->vote[(t + kThumbBufs) % kDepth] = 0;
+            mbar_arrive(&m->ring_seen[ds]);
+        }
+        for (int k = 0; k < cnt; k++) {
+            if (!(mask & (1u << k))) continue;
+            const int slot = kb % kRing, round = kb / kRing;
+            kb++;
+            if (round > 0) wait_bar(a, m, &m->ring_empty[slot], (round - 1) & 1);
+            const int row = P.row[k];
+            uint8_t *d = S.ring + slot * kSlotBytes;
+            uint64_t *bar = &m->ring_full[slot];
+            if (lane == 0) mbar_arrive_expect_tx(bar, kSlotTx);
+            __syncwarp();
+            if (lane == 0) tma_load_2d(d, &prm.tm_resid, 0, row, bar);
+            else if (lane == 1) tma_load_2d(d + kSlotV, &prm.tm_v, 0, row, bar);
+            else if (lane == 2) tma_load_2d(d + kSlotV + 8192, &prm.tm_v, 64, row, bar);
+            else if (lane == 3)
+                tma_load_1d(d + kSlotRScale, a.r_scale + (size_t)row * kGroups, 512, bar);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m->pages_empty[t % kPageSlots]);
+    }
+    // leave no copy in flight: wait for the last fill of every ring slot
+    if (lane == 0)
+        for (int s = 0; s < kRing && s < kb; s++) {
+            const int last = kb - 1 - ((kb - 1 - s) % kRing);
+            drain_bar(a, &m->ring_full[s], (last / kRing) & 1);
+        }
+}
+
+// ------------------------------------------------------------------------------------------
+// Scan warps (stage 2).
+// ------------------------------------------------------------------------------------------
+// Scan warp 0 computes the unit's query operands and thresholds into a unit slot.
+__device__ __forceinline__ void fill_unit(const DecodeArgs &a, UnitOps &U, int b, int h,
+                                          int lane) {
+    const int g = lane >> 2, tig = lane & 3;
+    ThumbOps T;
+    ResidOps Rr;
+    load_thumb_ops(a, b, h, lane, T);
+    load_resid_ops(a, b, h, lane, Rr);
+#pragma unroll
+    for (int r = 0; r < 2; r++) {
+        U.bt[r][lane] = make_uint4(T.bt0[4 * r], T.bt0[4 * r + 1], T.bt0[4 * r + 2], T.bt0[4 * r + 3]);
+        U.bt[2 + r][lane] = make_uint4(T.bt1[4 * r], T.bt1[4 * r + 1], T.bt1[4 * r + 2], T.bt1[4 * r + 3]);
+        U.br[r][lane] = make_uint4(Rr.br0[4 * r], Rr.br0[4 * r + 1], Rr.br0[4 * r + 2], Rr.br0[4 * r + 3]);
+        U.br[2 + r][lane] = make_uint4(Rr.br1[4 * r], Rr.br1[4 * r + 1], Rr.br1[4 * r + 2], Rr.br1[4 * r + 3]);
+    }
+    if (g == 0) {
+        U.qs[2 * tig] = make_float4(T.qs[0][0], T.qs[0][1], T.qs[0][2], T.qs[0][3]);
+        U.qs[2 * tig + 1] = make_float4(T.qs[1][0], T.qs[1][1], T.qs[1][2], T.qs[1][3]);
+    }
+    if (lane < kMaxG) {
+        float mx = -INFINITY;
+        const int u = b * a.Hkv + h;
+        for (int sl = 0; sl < a.nf; sl++)
+            mx = fmaxf(mx, a.ws_m1[((size_t)u * a.nf + sl) * kMaxG + lane]);
+        U.mt[lane] = mx;
+        U.thr[lane] = lane < a.G ? mx - a.delta : INFINITY;
+    }
+    if (lane == 0) U.n = len_of(a, b);
+}
+
+// Scan warp mt, every sub-chunk: provisional scores of rows 16mt .. 16mt+15 of each block into
+// the score buffer, and a vote for every block where one of those rows passes m~ - delta (an OR
+// into the sub-chunk's vote word, then one arrival on its decision barrier). Blocks k and k+3 are
+// scanned side by side (two independent dependency chains); a second tile past the sub-chunk's
+// end is computed from stale buffer contents (reads stay inside the buffer) and ignored.
+__device__ __forceinline__ void scanner(const DecodeArgs &a, const Smem &S, int cta, int ncta,
+                                        int mt, int lane) {
+    Misc *m = S.misc;
+    const int g = lane >> 2, tig = lane & 3;
+    const uint32_t m0 = 0x00030003u << (2 * tig);
+    const int r0 = 16 * mt + g, r1 = r0 + 8;
+    const float sm = a.sm_scale;
+    Sched sch;
+    sch.init(a, cta, ncta);
+    Sub s;
+    grid_dependency_wait();  // stage-1 maxima are visible from here on
+    int ui = -1;
+    for (int t = 0; sch.next(a, s); t++) {
+        if (s.first) {
+            ui++;
+            const int us = ui & 1;
+            if (ui >= 2) wait_bar(a, m, &m->unit_free[us], ((ui >> 1) - 1) & 1);
+            if (mt == 0) fill_unit(a, S.unit[us], s.b, s.h, lane);
+            named_barrier_sync(1, 128);
+            if (mt == 0 && lane == 0) mbar_arrive(&m->unit_ready[us]);
+        }
+        const UnitOps &U = S.unit[ui & 1];
+        const int tb = t % kThumbBufs, sb = t % kShatBufs;
+        wait_bar(a, m, &m->thumb_full[tb], (t / kThumbBufs) & 1);
+        if (t >= kShatBufs) wait_bar(a, m, &m->shat_free[sb], ((t / kShatBufs) - 1) & 1);
         ThumbOps Q;
         load_frags(U.bt, lane, Q.bt0, Q.bt1);
         {
@@ -881,55 +821,79 @@ __device__ __forceinline__ uint32_t scan_sub(const DecodeArgs &a, const Smem &S,
             Q.qs[0][0] = q0.x; Q.qs[0][1] = q0.y; Q.qs[0][2] = q0.z; Q.qs[0][3] = q0.w;
             Q.qs[1][0] = q1.x; Q.qs[1][1] = q1.y; Q.qs[1][2] = q1.z; Q.qs[1][3] = q1.w;
         }
-        const int r0 = 16 * mt + g, r1 = r0 + 8;
-        const uint8_t *tb = S.thumb + buf * (kSub * kThumbBlock);
-        float4 *shat = reinterpret_cast<float4 *>(S.shat + buf * kShatBuf);
-        const float4 eA = scan_tile(tb + kA * kThumbBlock, r0, r1, m0, Q, sm);
-        const float4 eB = scan_tile(tb + kB * kThumbBlock, r0, r1, m0, Q, sm);
-        const int tA = (s.j0 + kA) * kPage, tB = (s.j0 + kB) * kPage;
-        const bool pA = tile_passes(eA, tA + r0 < n, tA + r1 < n, thr0, thr1);
-        const bool pB = kB < s.cnt && tile_passes(eB, tB + r0 < n, tB + r1 < n, thr0, thr1);
-        if (__any_sync(0xffffffffu, pA)) votes |= 1u << kA;
-        if (__any_sync(0xffffffffu, pB)) votes |= 1u << kB;
-        shat[(kA * 4 + mt) * 32 + lane] = eA;
-        if (kB < s.cnt) shat[(kB * 4 + mt) * 32 + lane] = eB;
+        const float thr0 = U.thr[2 * tig], thr1 = U.thr[2 * tig + 1];
+        const int n = U.n;
+        const uint8_t *tbuf = S.thumb + tb * kThumbBuf;
+        float4 *shat = reinterpret_cast<float4 *>(S.shat + sb * kShatBuf);
+        uint32_t votes = 0;
+#pragma unroll 1
+        for (int kA = 0; kA < 3 && kA < s.cnt; kA++) {
+            const int kB = kA + 3;
+            const float4 eA = scan_tile(tbuf + kA * kThumbBlock, r0, r1, m0, Q, sm);
+            const float4 eB = scan_tile(tbuf + kB * kThumbBlock, r0, r1, m0, Q, sm);
+            const int tA = (s.j0 + kA) * kPage, tB = (s.j0 + kB) * kPage;
+            const bool pA = tile_passes(eA, tA + r0 < n, tA + r1 < n, thr0, thr1);
+            const bool pB = kB < s.cnt && tile_passes(eB, tB + r0 < n, tB + r1 < n, thr0, thr1);
+            if (__any_sync(0xffffffffu, pA)) votes |= 1u << kA;
+            if (__any_sync(0xffffffffu, pB)) votes |= 1u << kB;
+            shat[(kA * 4 + mt) * 32 + lane] = eA;
+            if (kB < s.cnt) shat[(kB * 4 + mt) * 32 + lane] = eB;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            if (votes) atomicOr(&m->vote[t % kDepth], votes);
+            mbar_arrive(&m->decision[t % kDepth]);  // releases the vote and the warp's scores
+        }
     }
-    if (lane == 0) {
-        if (votes) atomicOr(&m->vote_mask[t & 3], votes);
-        mbar_arrive(&m->decision[buf]);  // releases the vote; the decision completes at 12 votes
-    }
-    return bad;
 }
 
-// Kept blocks of sub-chunk t: every warp's vote, less the blocks that were never loaded.
-__device__ __forceinline__ uint32_t kept_mask(const DecodeArgs &a, Misc *m, const Sub &s, int t,
-                                              uint32_t bad) {
-    wait_bar(a, m, &m->decision[t & 1], (t >> 1) & 1);
-    return *reinterpret_cast<volatile uint32_t *>(&m->vote_mask[t & 3]) & ~bad &
-           ((1u << s.cnt) - 1u);
-}
-
-// Refine-side state of the unit being refined: its query operands, and this warp's running
-// softmax state (max, sum, O^T accumulators) for heads 2tig, 2tig+1.
+// ------------------------------------------------------------------------------------------
+// Refine groups (stage 3).
+// ------------------------------------------------------------------------------------------
+// Softmax state of one refine warp. The reference m (heads 2tig, 2tig+1) is the same in every
+// warp of a group; l holds this warp's rows only; o is O^T for channels 32mt + 16i + {g, g+8}
+// and heads {2tig, 2tig+1}: o[i] = {(g, 2tig), (g, 2tig+1), (g+8, 2tig), (g+8, 2tig+1)}.
 struct RefineState {
     float m0, m1, l0, l1;
-    float o[8][4];
+    float o[2][4];
 };
 
-// Fresh softmax state for a unit: the reference starts at its pseudo-max m~.
+// Fresh state for a unit: the reference starts at its pseudo-max m~.
 __device__ __forceinline__ void reset_refine(RefineState &R, const UnitOps &U, int lane) {
     R.m0 = U.mt[2 * (lane & 3)];
     R.m1 = U.mt[2 * (lane & 3) + 1];
     R.l0 = R.l1 = 0.0f;
 #pragma unroll
-    for (int md = 0; md < 8; md++) R.o[md][0] = R.o[md][1] = R.o[md][2] = R.o[md][3] = 0.0f;
+    for (int i = 0; i < 2; i++) R.o[i][0] = R.o[i][1] = R.o[i][2] = R.o[i][3] = 0.0f;
 }
 
-// Stage 3 on this warp's m-tile of one kept block held in a ring slot.
-__device__ __forceinline__ void refine_tile(const DecodeArgs &a, const uint8_t *slot,
-                                            const UnitOps &U, const float4 est, int blk,
-                                            RefineState &R, int mt, int lane) {
+__device__ __forceinline__ float safe_exp(float s, float m) {
+    return s == -INFINITY ? 0.0f : exp2f((s - m) * kLog2e);
+}
+
+// P^T fragments (bf16 hi and lo parts) of this warp's 16 rows for the PV k-step mt.
+__device__ __forceinline__ uint4 p_fragments(float p00, float p01, float p10, float p11) {
+    const uint32_t h0 = pack_bf16x2(p00, p01), h1 = pack_bf16x2(p10, p11);
+    const uint32_t l0 = pack_bf16x2(p00 - __uint_as_float(h0 << 16),
+                                    p01 - __uint_as_float(h0 & 0xffff0000u));
+    const uint32_t l1 = pack_bf16x2(p10 - __uint_as_float(h1 << 16),
+                                    p11 - __uint_as_float(h1 & 0xffff0000u));
+    return make_uint4(movmatrix_trans(h0), movmatrix_trans(h1), movmatrix_trans(l0),
+                      movmatrix_trans(l1));
+}
+
+// One kept block held in a ring slot, by the 4 warps of refine group grp (named barrier 2 + grp).
+// Warp mt: exact scores of rows 16mt .. 16mt+15 (provisional score from the scan + residual
+// correction), probabilities against the group's reference m (raised, with a rescale of the
+// state, only when a score passes m + kRescaleMargin in any warp), then O^T for channels
+// 32mt .. 32mt+31 over all 64 rows from the exchanged P^T fragments.
+__device__ __forceinline__ void refine_block(const DecodeArgs &a, const Smem &S, const uint8_t *slot,
+                                             const UnitOps &U, const float4 est, int blk,
+                                             RefineState &R, int grp, int mt, int pb, int lane) {
+    Misc *m = S.misc;
     const int g = lane >> 2, tig = lane & 3;
+    const uint32_t bar_id = 2 + grp;
+    // ---- scores of rows r0, r1 (heads 2tig, 2tig+1)
     ResidOps Q;
     load_frags(U.br, lane, Q.br0, Q.br1);
     {
@@ -961,20 +925,39 @@ __device__ __forceinline__ void refine_tile(const DecodeArgs &a, const uint8_t *
     const float s10 = v1 ? est.z + corr_score(Dr, 2, sr1, Q.qs[0], sm) : -INFINITY;
     const float s11 = v1 ? est.w + corr_score(Dr, 3, sr1, Q.qs[1], sm) : -INFINITY;
 
-    // online softmax, heads 2tig (0) and 2tig+1 (1). The running reference m starts at the
-    // pseudo-max m~ (an exact score of an always-kept token) and is raised only when a score
-    // exceeds it by more than kRescaleMargin: exp(s - m) then stays below e^kRescaleMargin and the
-    // common tile needs no max reduction and no rescaling of O.
+    // ---- probabilities against the group's reference
     const bool over = s00 > R.m0 + kRescaleMargin || s10 > R.m0 + kRescaleMargin ||
                       s01 > R.m1 + kRescaleMargin || s11 > R.m1 + kRescaleMargin;
-    if (__any_sync(0xffffffffu, over)) {
+    const uint32_t any_over = __any_sync(0xffffffffu, over);
+    uint4 *px = reinterpret_cast<uint4 *>(S.px + (grp * 2 + pb) * kPxBuf);
+    float p00 = safe_exp(s00, R.m0), p01 = safe_exp(s01, R.m1);
+    float p10 = safe_exp(s10, R.m0), p11 = safe_exp(s11, R.m1);
+    if (any_over) {  // this warp's row maxima, for the group's new reference
         float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
         }
-        const float mn0 = fmaxf(R.m0, mx0), mn1 = fmaxf(R.m1, mx1);
+        if (g == 0) {
+            m->wmax[grp][pb][mt][2 * tig] = mx0;
+            m->wmax[grp][pb][mt][2 * tig + 1] = mx1;
+        }
+    }
+    if (lane == 0) m->over[grp][pb][mt] = any_over;
+    px[mt * 32 + lane] = p_fragments(p00, p01, p10, p11);
+    named_barrier_sync(bar_id, 128);
+    const uint32_t group_over = m->over[grp][pb][0] | m->over[grp][pb][1] |
+                                m->over[grp][pb][2] | m->over[grp][pb][3];
+    if (group_over) {  // rare: raise the reference to the block maximum, rescale, redo P
+        float mn0 = R.m0, mn1 = R.m1;
+#pragma unroll
+        for (int w = 0; w < 4; w++) {
+            if (m->over[grp][pb][w]) {
+                mn0 = fmaxf(mn0, m->wmax[grp][pb][w][2 * tig]);
+                mn1 = fmaxf(mn1, m->wmax[grp][pb][w][2 * tig + 1]);
+            }
+        }
         const float al0 = R.m0 == -INFINITY ? 0.0f : exp2f((R.m0 - mn0) * kLog2e);
         const float al1 = R.m1 == -INFINITY ? 0.0f : exp2f((R.m1 - mn1) * kLog2e);
         R.m0 = mn0;
@@ -982,215 +965,159 @@ __device__ __forceinline__ void refine_tile(const DecodeArgs &a, const uint8_t *
         R.l0 *= al0;
         R.l1 *= al1;
 #pragma unroll
-        for (int md = 0; md < 8; md++) {
-            R.o[md][0] *= al0;
-            R.o[md][1] *= al1;
-            R.o[md][2] *= al0;
-            R.o[md][3] *= al1;
+        for (int i = 0; i < 2; i++) {
+            R.o[i][0] *= al0;
+            R.o[i][1] *= al1;
+            R.o[i][2] *= al0;
+            R.o[i][3] *= al1;
         }
+        p00 = safe_exp(s00, R.m0);
+        p01 = safe_exp(s01, R.m1);
+        p10 = safe_exp(s10, R.m0);
+        p11 = safe_exp(s11, R.m1);
+        px[mt * 32 + lane] = p_fragments(p00, p01, p10, p11);
+        named_barrier_sync(bar_id, 128);
     }
-    const float p00 = s00 == -INFINITY ? 0.0f : exp2f((s00 - R.m0) * kLog2e);
-    const float p01 = s01 == -INFINITY ? 0.0f : exp2f((s01 - R.m1) * kLog2e);
-    const float p10 = s10 == -INFINITY ? 0.0f : exp2f((s10 - R.m0) * kLog2e);
-    const float p11 = s11 == -INFINITY ? 0.0f : exp2f((s11 - R.m1) * kLog2e);
     R.l0 += p00 + p10;
     R.l1 += p01 + p11;
-    // P^T fragments, bf16 hi + lo
-    const uint32_t h0 = pack_bf16x2(p00, p01), h1 = pack_bf16x2(p10, p11);
-    const uint32_t l0 = pack_bf16x2(p00 - __uint_as_float(h0 << 16),
-                                    p01 - __uint_as_float(h0 & 0xffff0000u));
-    const uint32_t l1 = pack_bf16x2(p10 - __uint_as_float(h1 << 16),
-                                    p11 - __uint_as_float(h1 & 0xffff0000u));
-    const uint32_t bh0 = movmatrix_trans(h0), bh1 = movmatrix_trans(h1);
-    const uint32_t bl0 = movmatrix_trans(l0), bl1 = movmatrix_trans(l1);
-    // V^T fragments by ldmatrix.trans from the swizzled tile (16-byte chunk c of row r is stored
-    // at chunk c ^ (r % 8))
+
+    // ---- O^T(channels 32mt .. 32mt+31) += V^T P^T over the block's 64 rows. V^T fragments by
+    // ldmatrix.trans from the swizzled tile (16-byte chunk c of row r is stored at c ^ (r % 8)).
     const int mi = lane >> 3, jr = lane & 7;
-    const int tok = 16 * mt + ((mi >> 1) << 3) + jr;
-    const uint32_t vrow = smem_u32(slot + kSlotV) + tok * 128;
+    const uint32_t vbase = smem_u32(slot + kSlotV) + (mt >> 1) * 8192;
 #pragma unroll
-    for (int md = 0; md < 8; md++) {
-        const int chunk = 2 * (md & 3) + (mi & 1);
-        const uint32_t addr = vrow + (md >> 2) * 8192 + ((chunk ^ jr) << 4);
-        uint32_t v0r, v1r, v2r, v3r;
-        ldmatrix_x4_trans(v0r, v1r, v2r, v3r, addr);
-        mma_bf16(R.o[md], v0r, v1r, v2r, v3r, bh0, bh1);
-        mma_bf16(R.o[md], v0r, v1r, v2r, v3r, bl0, bl1);
+    for (int ks = 0; ks < 4; ks++) {
+        const uint4 bp = px[ks * 32 + lane];
+        const int tok = 16 * ks + ((mi >> 1) << 3) + jr;
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const int md = 2 * mt + i;  // channels 16md .. 16md+15
+            const int chunk = 2 * (md & 3) + (mi & 1);
+            uint32_t v0r, v1r, v2r, v3r;
+            ldmatrix_x4_trans(v0r, v1r, v2r, v3r, vbase + tok * 128 + ((chunk ^ jr) << 4));
+            mma_bf16(R.o[i], v0r, v1r, v2r, v3r, bp.x, bp.y);
+            mma_bf16(R.o[i], v0r, v1r, v2r, v3r, bp.z, bp.w);
+        }
     }
 }
 
-// Merge another warp's softmax state (reference maxima pm0/pm1, sums pl0/pl1, O^T in `src`)
-// into this warp's state.
-__device__ __forceinline__ void absorb(RefineState &R, float pm0, float pm1, float pl0, float pl1,
-                                       const float *src, int lane) {
-    const float M0 = fmaxf(R.m0, pm0), M1 = fmaxf(R.m1, pm1);
-    const float fa0 = R.m0 == -INFINITY ? 0.0f : exp2f((R.m0 - M0) * kLog2e);
-    const float fa1 = R.m1 == -INFINITY ? 0.0f : exp2f((R.m1 - M1) * kLog2e);
-    const float fb0 = pm0 == -INFINITY ? 0.0f : exp2f((pm0 - M0) * kLog2e);
-    const float fb1 = pm1 == -INFINITY ? 0.0f : exp2f((pm1 - M1) * kLog2e);
-#pragma unroll
-    for (int md = 0; md < 8; md++) {
-        R.o[md][0] = fmaf(R.o[md][0], fa0, fb0 * src[(md * 4 + 0) * 32 + lane]);
-        R.o[md][1] = fmaf(R.o[md][1], fa1, fb1 * src[(md * 4 + 1) * 32 + lane]);
-        R.o[md][2] = fmaf(R.o[md][2], fa0, fb0 * src[(md * 4 + 2) * 32 + lane]);
-        R.o[md][3] = fmaf(R.o[md][3], fa1, fb1 * src[(md * 4 + 3) * 32 + lane]);
-    }
-    R.l0 = fmaf(R.l0, fa0, fb0 * pl0);
-    R.l1 = fmaf(R.l1, fa1, fb1 * pl1);
-    R.m0 = M0;
-    R.m1 = M1;
-}
-
-// Combine the 12 consumer warps' softmax states into this CTA's record for the unit (three
-// pairwise rounds through the score buffers, which are free at a unit's end); the last CTA of the
-// unit (atomic ticket, no waiting) then merges all records of the unit into the output.
-__device__ __forceinline__ void combine_unit(const DecodeArgs &a, const Smem &S, const Sub &s,
-                                             RefineState &R, int cta, int ncta, int64_t T,
-                                             int warp, int lane) {
+// End of this CTA's segment of a unit, refine group grp: the group's softmax sums, its record
+// (each warp writes its channels), and the atomic ticket; the last group of the unit's CTAs
+// merges all records of the unit into the output (no waiting).
+__device__ __forceinline__ void unit_end(const DecodeArgs &a, const Smem &S, const Sub &s,
+                                         const RefineState &R, int cta, int ncta, int64_t T,
+                                         int grp, int mt, int lane) {
     Misc *m = S.misc;
-    const int g = lane >> 2, tig = lane & 3, tid = warp * 32 + lane;
+    const int g = lane >> 2, tig = lane & 3;
+    const uint32_t bar_id = 2 + grp;
+    float l0 = R.l0, l1 = R.l1;
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {  // this warp's sums over its 16-token rows
-        R.l0 += __shfl_xor_sync(0xffffffffu, R.l0, o);
-        R.l1 += __shfl_xor_sync(0xffffffffu, R.l1, o);
+    for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
-    float *buf = reinterpret_cast<float *>(S.shat);
-    constexpr int kWarpFloats = kCombineWarpBytes / 4;
-    named_barrier_sync(1, kConsumers);  // every warp is done reading its scores
-    // rounds: warps [half, 2 half) hand their state to warps [0, half)
-    const int halves[3] = {6, 3, 1};
-#pragma unroll
-    for (int r = 0; r < 3; r++) {
-        const int half = halves[r];
-        const int top = r == 0 ? 12 : (r == 1 ? 6 : 3);
-        if (warp >= half && warp < top) {
-            float *dst = buf + (warp - half) * kWarpFloats;
-#pragma unroll
-            for (int md = 0; md < 8; md++)
-#pragma unroll
-                for (int e = 0; e < 4; e++) dst[(md * 4 + e) * 32 + lane] = R.o[md][e];
-            if (g == 0) {
-                m->cm[warp][2 * tig] = R.m0;
-                m->cm[warp][2 * tig + 1] = R.m1;
-                m->cl[warp][2 * tig] = R.l0;
-                m->cl[warp][2 * tig + 1] = R.l1;
-            }
-        }
-        named_barrier_sync(1, kConsumers);
-        // round 2 hands 3 warps to 1: warps 1 and 2 both go to warp 0
-        for (int p = warp + half; p < top && warp < half; p += half) {
-            absorb(R, m->cm[p][2 * tig], m->cm[p][2 * tig + 1], m->cl[p][2 * tig],
-                   m->cl[p][2 * tig + 1], buf + (p - half) * kWarpFloats, lane);
-            if (r < 2) break;
-        }
-        named_barrier_sync(1, kConsumers);
+    if (g == 0) {
+        m->lsum[grp][mt][2 * tig] = l0;
+        m->lsum[grp][mt][2 * tig + 1] = l1;
     }
+    named_barrier_sync(bar_id, 128);
     const int u = s.b * a.Hkv + s.h;
-    if (warp == 0) {
-        float *rec = a.ws_part + (size_t)(u + cta) * a.G * kPartStride;
-        const int h0 = 2 * tig, h1 = 2 * tig + 1;
+    float *rec = unit_record(a, u, cta, grp);
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;
 #pragma unroll
-        for (int md = 0; md < 8; md++) {
-            const int d = 16 * md + g;
-            if (h0 < a.G) {
-                rec[h0 * kPartStride + d] = R.o[md][0];
-                rec[h0 * kPartStride + d + 8] = R.o[md][2];
-            }
-            if (h1 < a.G) {
-                rec[h1 * kPartStride + d] = R.o[md][1];
-                rec[h1 * kPartStride + d + 8] = R.o[md][3];
-            }
+    for (int i = 0; i < 2; i++) {
+        const int d = 32 * mt + 16 * i + g;
+        if (h0 < a.G) {
+            rec[h0 * kPartStride + d] = R.o[i][0];
+            rec[h0 * kPartStride + d + 8] = R.o[i][2];
         }
-        if (g == 0) {
-            if (h0 < a.G) {
-                rec[h0 * kPartStride + kD] = R.m0;
-                rec[h0 * kPartStride + kD + 1] = R.l0;
-            }
-            if (h1 < a.G) {
-                rec[h1 * kPartStride + kD] = R.m1;
-                rec[h1 * kPartStride + kD + 1] = R.l1;
-            }
+        if (h1 < a.G) {
+            rec[h1 * kPartStride + d] = R.o[i][1];
+            rec[h1 * kPartStride + d + 8] = R.o[i][3];
         }
+    }
+    if (mt == 0 && g == 0) {
+        const float L0 = (m->lsum[grp][0][h0] + m->lsum[grp][1][h0]) +
+                         (m->lsum[grp][2][h0] + m->lsum[grp][3][h0]);
+        const float L1 = (m->lsum[grp][0][h1] + m->lsum[grp][1][h1]) +
+                         (m->lsum[grp][2][h1] + m->lsum[grp][3][h1]);
+        if (h0 < a.G) {
+            rec[h0 * kPartStride + kD] = R.m0;
+            rec[h0 * kPartStride + kD + 1] = L0;
+        }
+        if (h1 < a.G) {
+            rec[h1 * kPartStride + kD] = R.m1;
+            rec[h1 * kPartStride + kD + 1] = L1;
+        }
+    }
+    __threadfence();
+    named_barrier_sync(bar_id, 128);
+    const int64_t first = s.x0 - s.j0;  // global index of the unit's first block
+    const int cf = cta_of(first, T, ncta), cl = cta_of(first + s.nblk - 1, T, ncta);
+    if (mt == 0 && lane == 0) {
+        int *cnt = a.ws_cnt + u;
+        const int old = atomicAdd(cnt, 1);
+        const uint32_t last = old == 2 * (cl - cf + 1) - 1;
+        if (last) *cnt = 0;  // ready for the next call
+        m->merge_flag[grp] = last;
+    }
+    named_barrier_sync(bar_id, 128);
+    if (m->merge_flag[grp]) {
         __threadfence();
+        merge_unit(a, s.b, s.h, cf, cl, mt, 4, lane);
     }
-    named_barrier_sync(1, kConsumers);
-    const int64_t first = s.x0 - s.jr;  // global index of the unit's first middle block
-    const int cf = cta_of(first, T, ncta), cl = cta_of(first + s.nmid - 1, T, ncta);
-    if (tid == 0) {
-        uint32_t last = 1;
-        if (cl > cf) {
-            int *cnt = a.ws_cnt + u;
-            const int old = atomicAdd(cnt, 1);
-            last = old == cl - cf;
-            if (last) *cnt = 0;  // ready for the next call
-        }
-        m->merge_flag = last;
-    }
-    named_barrier_sync(1, kConsumers);
-    if (m->merge_flag) {
-        __threadfence();
-        merge_unit(a, s.b, s.h, true, cf, cl, warp, kConsumerWarps, lane);
-    }
-    named_barrier_sync(1, kConsumers);
 }
 
-// Consumer warps (c = 0..11). Within a unit, sub-chunk t+1 is scanned before sub-chunk t is
-// refined, so the refine loads of t+1 can be issued while t is being refined. At a unit's end
-// the last sub-chunk is refined and combined first; the next unit's scan follows.
-__device__ __forceinline__ void consumer(const MainParams &prm, const Smem &S, int cta, int ncta,
-                                         int warp, int lane) {
-    const DecodeArgs &a = prm.a;
+// Refine warp mt of group grp: walks the schedule, takes the kept blocks with kb & 1 == grp.
+__device__ __forceinline__ void refiner(const DecodeArgs &a, const Smem &S, int cta, int ncta,
+                                        int grp, int mt, int lane) {
     Misc *m = S.misc;
-    const int grp = warp >> 2, mt = warp & 3;
     Sched sch;
     sch.init(a, cta, ncta);
-    Sub cur, nxt;
-    if (!sch.next(a, cur)) return;
-    grid_dependency_wait();  // stage-1 results are visible from here on
-    setup_unit(a, S, cur, warp, lane);
-    uint32_t bad_cur = scan_sub(a, S, cur, 0, warp, lane);
+    Sub s;
+    grid_dependency_wait();
     RefineState R;
-    reset_refine(R, *S.unit, lane);
-    int t = 0, kb = 0;
-    while (true) {
-        const bool has_nxt = sch.next(a, nxt);
-        uint32_t bad_nxt = 0;
-        if (has_nxt && !cur.last) bad_nxt = scan_sub(a, S, nxt, t + 1, warp, lane);
-        const float4 *shat = reinterpret_cast<const float4 *>(S.shat + (t & 1) * kShatBuf);
-        const uint32_t mask_cur = kept_mask(a, m, cur, t, bad_cur);
-        if (warp == 0 && a.keep_mask && lane < cur.cnt)
-            a.keep_mask[((size_t)cur.b * a.Hkv + cur.h) * a.max_blocks + cur.j0 + lane] =
-                (mask_cur >> lane) & 1u;
-        // this group's blocks k = grp and grp + 3; kept block number kb + (kept blocks before k)
-        // is the ring position the producer gave it
-#pragma unroll
-        for (int q = 0; q < 2; q++) {
-            const int k = grp + q * kGroups3;
-            if (k >= cur.cnt || !((mask_cur >> k) & 1u)) continue;
-            const int kbk = kb + __popc(mask_cur & ((1u << k) - 1u));
-            const int slot = kbk % kRing;
-            wait_bar(a, m, &m->ring_full[slot], (kbk / kRing) & 1);
-            refine_tile(a, S.ring + slot * kSlotBytes, *S.unit, shat[(k * 4 + mt) * 32 + lane],
-                        cur.j0 + k, R, mt, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&m->ring_empty[slot]);
+    int ui = -1, kb = 0, pb = 0;
+    for (int t = 0; sch.next(a, s); t++) {
+        if (s.first) {
+            ui++;
+            wait_bar(a, m, &m->unit_ready[ui & 1], (ui >> 1) & 1);
+            reset_refine(R, S.unit[ui & 1], lane);
         }
-        kb += __popc(mask_cur);
-        if (cur.last) {
-            combine_unit(a, S, cur, R, cta, ncta, sch.T, warp, lane);
-            if (has_nxt) {  // a new unit only follows the last sub-chunk of the previous one
-                setup_unit(a, S, nxt, warp, lane);
-                bad_nxt = scan_sub(a, S, nxt, t + 1, warp, lane);
-                reset_refine(R, *S.unit, lane);
+        const UnitOps &U = S.unit[ui & 1];
+        const int ds = t % kDepth;
+        wait_bar(a, m, &m->ring_seen[ds], (t / kDepth) & 1);
+        const uint32_t mask = *reinterpret_cast<volatile uint32_t *>(&m->final_mask[ds]);
+        if (grp == 0 && mt == 0 && a.keep_mask && lane < s.cnt)
+            a.keep_mask[((size_t)s.b * a.Hkv + s.h) * a.max_blocks + s.j0 + lane] =
+                (mask >> lane) & 1u;
+        const float4 *shat = reinterpret_cast<const float4 *>(S.shat + (t % kShatBufs) * kShatBuf);
+        for (int k = 0; k < s.cnt; k++) {
+            if (!((mask >> k) & 1u)) continue;
+            if ((kb & 1) == grp) {
+                const int slot = kb % kRing;
+                wait_bar(a, m, &m->ring_full[slot], (kb / kRing) & 1);
+                refine_block(a, S, S.ring + slot * kSlotBytes, U, shat[(k * 4 + mt) * 32 + lane],
+                             s.j0 + k, R, grp, mt, pb, lane);
+                pb ^= 1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&m->ring_empty[slot]);
             }
+            kb++;
         }
-        if (!has_nxt) break;
-        cur = nxt;
-        bad_cur = bad_nxt;
-        t++;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m->shat_free[t % kShatBufs]);
+        if (s.last) {
+            unit_end(a, S, s, R, cta, ncta, sch.T, grp, mt, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&m->unit_free[ui & 1]);
+        }
     }
 }
 
+// ------------------------------------------------------------------------------------------
+// Main kernel: persistent, one CTA per SM (at most one per block, so every range is non-empty).
+// ------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kMainThreads, 1)
     main_kernel(const __grid_constant__ MainParams prm) {
     const DecodeArgs &a = prm.a;
@@ -1201,12 +1128,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     S.ring = base + kOffRing;
     S.thumb = base + kOffThumb;
     S.shat = base + kOffShat;
+    S.px = base + kOffPx;
     S.unit = reinterpret_cast<UnitOps *>(base + kOffUnit);
     S.misc = reinterpret_cast<Misc *>(base + kOffMisc);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // every CTA range must hold at least one block: use at most T CTAs
-    const int64_t T = total_mid_blocks(a);
+    const int64_t T = total_blocks(a);
     const int ncta = (int)(T < (int64_t)gridDim.x ? T : (int64_t)gridDim.x);
     const int cta = blockIdx.x;
     if (cta >= ncta) return;
@@ -1214,31 +1141,38 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     if (threadIdx.x == 0) {
         Misc *m = S.misc;
         m->aborted = 0;
-        for (int i = 0; i < 4; i++) m->vote_mask[i] = 0;
-        for (int i = 0; i < 2; i++) {
-            mbar_init(&m->thumb_full[i], 1);
-            mbar_init(&m->decision[i], kConsumerWarps);
-            mbar_init(&m->ring_seen[i], 1);
-        }
-        for (int i = 0; i < kRing; i++) {
-            mbar_init(&m->ring_full[i], 1);
-            mbar_init(&m->ring_empty[i], 4);
+        for (int i = 0; i < kDepth; i++) {
+            m->vote[i] = 0;
+            mbar_init(&m->decision[i], 4);   // the scan warps
+            mbar_init(&m->ring_seen[i], 1);  // the ring warp
         }
         for (int i = 0; i < kPageSlots; i++) {
             mbar_init(&m->pages_full[i], 1);
             mbar_init(&m->pages_empty[i], 2);  // thumbnail warp and ring warp
         }
+        for (int i = 0; i < kThumbBufs; i++) mbar_init(&m->thumb_full[i], 1);
+        for (int i = 0; i < kShatBufs; i++) mbar_init(&m->shat_free[i], 8);  // refine warps
+        for (int i = 0; i < kRing; i++) {
+            mbar_init(&m->ring_full[i], 1);
+            mbar_init(&m->ring_empty[i], 4);  // the refine group that took the block
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&m->unit_ready[i], 1);  // scan warp 0
+            mbar_init(&m->unit_free[i], 8);   // refine warps
+        }
         fence_barrier_init();
     }
     __syncthreads();
-    if (warp < 4) {  // producer warpgroup: ring warp, page warp, thumbnail warp, one idle warp
+    if (warp < 4) {
         regs_decrease<kProducerRegs>();
         if (warp == 0) ring_issuer(prm, S, lane);
         else if (warp == 1) pager(a, S, cta, ncta, lane);
         else if (warp == 2) thumb_issuer(a, S, lane);
+    } else if (warp < 8) {
+        scanner(a, S, cta, ncta, warp - 4, lane);
     } else {
-        regs_increase<kConsumerRegs>();
-        consumer(prm, S, cta, ncta, warp - 4, lane);
+        regs_increase<kRefineRegs>();
+        refiner(a, S, cta, ncta, (warp - 8) >> 2, warp & 3, lane);
     }
 }
 
