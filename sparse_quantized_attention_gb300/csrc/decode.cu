@@ -92,6 +92,7 @@ struct Misc {
     uint32_t final_mask[kDepth];  // kept blocks of sub-chunk t, published by the ring warp
     uint32_t aborted;
     uint32_t merge_flag[2];
+    int32_t slot_kb[kRing];       // kept block whose copies were issued last into each ring slot
     uint32_t over[2][2][4];       // refine [group][buffer][warp]: a score passed m + margin
     float wmax[2][2][4][kMaxG];   // refine [group][buffer][warp][head]: block row maxima
     float lsum[2][4][kMaxG];      // refine [group][warp][head]: softmax sums at a unit's end
@@ -732,7 +733,10 @@ __device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S
             const int row = P.row[k];
             uint8_t *d = S.ring + slot * kSlotBytes;
             uint64_t *bar = &m->ring_full[slot];
-            if (lane == 0) mbar_arrive_expect_tx(bar, kSlotTx);
+            if (lane == 0) {
+                st_release_shared(&m->slot_kb[slot], kb - 1);  // kb was advanced above
+                mbar_arrive_expect_tx(bar, kSlotTx);
+            }
             __syncwarp();
             if (lane == 0) tma_load_2d(d, &prm.tm_resid, 0, row, bar);
             else if (lane == 1) tma_load_2d(d + kSlotV, &prm.tm_v, 0, row, bar);
@@ -1068,6 +1072,26 @@ __device__ __forceinline__ void unit_end(const DecodeArgs &a, const Smem &S, con
     }
 }
 
+// Wait until the copies of kept block kb have landed in its ring slot. The two refine groups share
+// the ring and may drift apart, so a parity wait alone could mistake the slot's previous fill (the
+// other group's block kb - kRing, maybe still in flight) for this one. The slot's tag names the
+// last block whose copies were issued; the ring warp sets it only after that previous fill was
+// consumed, so once the tag shows kb the parity wait is exact.
+__device__ __forceinline__ void wait_fill(const DecodeArgs &a, Misc *m, int slot, int kb) {
+    if (ld_acquire_shared(&m->slot_kb[slot]) != kb) {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_shared(&m->slot_kb[slot]) != kb) {
+            if (aborted(m)) return;
+            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                raise_error(a.err, FFD_ERRBIT_TIMEOUT);
+                *reinterpret_cast<volatile uint32_t *>(&m->aborted) = 1;
+                return;
+            }
+        }
+    }
+    wait_bar(a, m, &m->ring_full[slot], (kb / kRing) & 1);
+}
+
 // Refine warp mt of group grp: walks the schedule, takes the kept blocks with kb & 1 == grp.
 __device__ __forceinline__ void refiner(const DecodeArgs &a, const Smem &S, int cta, int ncta,
                                         int grp, int mt, int lane) {
@@ -1096,7 +1120,7 @@ __device__ __forceinline__ void refiner(const DecodeArgs &a, const Smem &S, int 
             if (!((mask >> k) & 1u)) continue;
             if ((kb & 1) == grp) {
                 const int slot = kb % kRing;
-                wait_bar(a, m, &m->ring_full[slot], (kb / kRing) & 1);
+                wait_fill(a, m, slot, kb);
                 refine_block(a, S, S.ring + slot * kSlotBytes, U, shat[(k * 4 + mt) * 32 + lane],
                              s.j0 + k, R, grp, mt, pb, lane);
                 pb ^= 1;
@@ -1153,6 +1177,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         for (int i = 0; i < kThumbBufs; i++) mbar_init(&m->thumb_full[i], 1);
         for (int i = 0; i < kShatBufs; i++) mbar_init(&m->shat_free[i], 8);  // refine warps
         for (int i = 0; i < kRing; i++) {
+            m->slot_kb[i] = -1;
             mbar_init(&m->ring_full[i], 1);
             mbar_init(&m->ring_empty[i], 4);  // the refine group that took the block
         }
