@@ -55,8 +55,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kQMax = 134217728.0f;          // 2^27
 constexpr float kRescaleMargin = 30.0f;        // lazy softmax rescaling, natural-log units
 
-// ring slot: residual tile (64 x 128 B, swizzled), V tile (2 boxes of 64 x 128 B, swizzled),
-// residual scales (64 x 8 B)
+// ring slot: residual tile (64 x 128 B, swizzled), V tile (channels 0-63 of the 64 rows, then
+// channels 64-127, each 64 x 128 B, swizzled; one 3-D copy), residual scales (64 x 8 B)
 constexpr int kSlotV = 8192;
 constexpr int kSlotRScale = 8192 + 16384;
 constexpr int kSlotTx = 8192 + 16384 + 512;
@@ -92,7 +92,6 @@ struct Misc {
     uint32_t final_mask[kDepth];  // kept blocks of sub-chunk t, published by the ring warp
     uint32_t aborted;
     uint32_t merge_flag[2];
-    int32_t slot_kb[kRing];       // kept block whose copies were issued last into each ring slot
     uint32_t over[2][2][4];       // refine [group][buffer][warp]: a score passed m + margin
     float wmax[2][2][4][kMaxG];   // refine [group][buffer][warp][head]: block row maxima
     float lsum[2][4][kMaxG];      // refine [group][warp][head]: softmax sums at a unit's end
@@ -103,7 +102,7 @@ struct Misc {
     uint64_t decision[kDepth];    // the 4 scan warps voted on sub-chunk t
     uint64_t ring_seen[kDepth];   // the ring warp published the kept blocks of sub-chunk t
     uint64_t shat_free[kShatBufs];
-    uint64_t ring_full[kRing];
+    uint64_t ring_full[2][kRing];  // [group of the block][slot]
     uint64_t ring_empty[kRing];
     uint64_t unit_ready[2];
     uint64_t unit_free[2];
@@ -732,26 +731,23 @@ __device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S
             if (round > 0) wait_bar(a, m, &m->ring_empty[slot], (round - 1) & 1);
             const int row = P.row[k];
             uint8_t *d = S.ring + slot * kSlotBytes;
-            uint64_t *bar = &m->ring_full[slot];
-            if (lane == 0) {
-                st_release_shared(&m->slot_kb[slot], kb - 1);  // kb was advanced above
-                mbar_arrive_expect_tx(bar, kSlotTx);
-            }
+            uint64_t *bar = &m->ring_full[(kb - 1) & 1][slot];  // kb was advanced above
+            if (lane == 0) mbar_arrive_expect_tx(bar, kSlotTx);
             __syncwarp();
             if (lane == 0) tma_load_2d(d, &prm.tm_resid, 0, row, bar);
-            else if (lane == 1) tma_load_2d(d + kSlotV, &prm.tm_v, 0, row, bar);
-            else if (lane == 2) tma_load_2d(d + kSlotV + 8192, &prm.tm_v, 64, row, bar);
-            else if (lane == 3)
+            else if (lane == 1) tma_load_3d(d + kSlotV, &prm.tm_v, 0, row, 0, bar);
+            else if (lane == 2)
                 tma_load_1d(d + kSlotRScale, a.r_scale + (size_t)row * kGroups, 512, bar);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&m->pages_empty[t % kPageSlots]);
     }
-    // leave no copy in flight: wait for the last fill of every ring slot
+    // leave no copy in flight: wait for the last fill of every ring slot (block kb - 1 - i went to
+    // slot (kb - 1 - i) % kRing, the ((kb - 1 - i) / (2 kRing))-th fill of its group's barrier)
     if (lane == 0)
-        for (int s = 0; s < kRing && s < kb; s++) {
-            const int last = kb - 1 - ((kb - 1 - s) % kRing);
-            drain_bar(a, &m->ring_full[s], (last / kRing) & 1);
+        for (int i = 0; i < kRing && i < kb; i++) {
+            const int last = kb - 1 - i;
+            drain_bar(a, &m->ring_full[last & 1][last % kRing], (last / (2 * kRing)) & 1);
         }
 }
 
@@ -804,6 +800,9 @@ __device__ __forceinline__ void scanner(const DecodeArgs &a, const Smem &S, int 
     sch.init(a, cta, ncta);
     Sub s;
     grid_dependency_wait();  // stage-1 maxima are visible from here on
+    ThumbOps Q;  // the unit's thumbnail B fragments, query sums and thresholds, in registers
+    float thr0 = 0.0f, thr1 = 0.0f;
+    int n = 0;
     int ui = -1;
     for (int t = 0; sch.next(a, s); t++) {
         if (s.first) {
@@ -813,20 +812,18 @@ __device__ __forceinline__ void scanner(const DecodeArgs &a, const Smem &S, int 
             if (mt == 0) fill_unit(a, S.unit[us], s.b, s.h, lane);
             named_barrier_sync(1, 128);
             if (mt == 0 && lane == 0) mbar_arrive(&m->unit_ready[us]);
-        }
-        const UnitOps &U = S.unit[ui & 1];
-        const int tb = t % kThumbBufs, sb = t % kShatBufs;
-        wait_bar(a, m, &m->thumb_full[tb], (t / kThumbBufs) & 1);
-        if (t >= kShatBufs) wait_bar(a, m, &m->shat_free[sb], ((t / kShatBufs) - 1) & 1);
-        ThumbOps Q;
-        load_frags(U.bt, lane, Q.bt0, Q.bt1);
-        {
+            const UnitOps &U = S.unit[us];
+            load_frags(U.bt, lane, Q.bt0, Q.bt1);
             const float4 q0 = U.qs[2 * tig], q1 = U.qs[2 * tig + 1];
             Q.qs[0][0] = q0.x; Q.qs[0][1] = q0.y; Q.qs[0][2] = q0.z; Q.qs[0][3] = q0.w;
             Q.qs[1][0] = q1.x; Q.qs[1][1] = q1.y; Q.qs[1][2] = q1.z; Q.qs[1][3] = q1.w;
+            thr0 = U.thr[2 * tig];
+            thr1 = U.thr[2 * tig + 1];
+            n = U.n;
         }
-        const float thr0 = U.thr[2 * tig], thr1 = U.thr[2 * tig + 1];
-        const int n = U.n;
+        const int tb = t % kThumbBufs, sb = t % kShatBufs;
+        wait_bar(a, m, &m->thumb_full[tb], (t / kThumbBufs) & 1);
+        if (t >= kShatBufs) wait_bar(a, m, &m->shat_free[sb], ((t / kShatBufs) - 1) & 1);
         const uint8_t *tbuf = S.thumb + tb * kThumbBuf;
         float4 *shat = reinterpret_cast<float4 *>(S.shat + sb * kShatBuf);
         uint32_t votes = 0;
@@ -892,20 +889,12 @@ __device__ __forceinline__ uint4 p_fragments(float p00, float p01, float p10, fl
 // state, only when a score passes m + kRescaleMargin in any warp), then O^T for channels
 // 32mt .. 32mt+31 over all 64 rows from the exchanged P^T fragments.
 __device__ __forceinline__ void refine_block(const DecodeArgs &a, const Smem &S, const uint8_t *slot,
-                                             const UnitOps &U, const float4 est, int blk,
+                                             const ResidOps &Q, int n, const float4 est, int blk,
                                              RefineState &R, int grp, int mt, int pb, int lane) {
     Misc *m = S.misc;
     const int g = lane >> 2, tig = lane & 3;
     const uint32_t bar_id = 2 + grp;
     // ---- scores of rows r0, r1 (heads 2tig, 2tig+1)
-    ResidOps Q;
-    load_frags(U.br, lane, Q.br0, Q.br1);
-    {
-        const float4 q0 = U.qs[2 * tig], q1 = U.qs[2 * tig + 1];
-        Q.qs[0][0] = q0.x; Q.qs[0][1] = q0.y; Q.qs[0][2] = q0.z; Q.qs[0][3] = q0.w;
-        Q.qs[1][0] = q1.x; Q.qs[1][1] = q1.y; Q.qs[1][2] = q1.z; Q.qs[1][3] = q1.w;
-    }
-    const int n = U.n;
     const int r0 = 16 * mt + g, r1 = r0 + 8;
     uint2 x0[4], x1[4];
 #pragma unroll
@@ -1072,24 +1061,13 @@ __device__ __forceinline__ void unit_end(const DecodeArgs &a, const Smem &S, con
     }
 }
 
-// Wait until the copies of kept block kb have landed in its ring slot. The two refine groups share
-// the ring and may drift apart, so a parity wait alone could mistake the slot's previous fill (the
-// other group's block kb - kRing, maybe still in flight) for this one. The slot's tag names the
-// last block whose copies were issued; the ring warp sets it only after that previous fill was
-// consumed, so once the tag shows kb the parity wait is exact.
+// Wait until the copies of kept block kb have landed in its ring slot. The two refine groups
+// share the ring (its size is odd, so consecutive occupants of a slot belong to different groups)
+// and may drift apart; each group therefore has its own fill barrier per slot, whose consecutive
+// phases are the group's own blocks kb, kb + 2 kRing, ..., consumed in order: the parity wait is
+// exact however far the other group lags.
 __device__ __forceinline__ void wait_fill(const DecodeArgs &a, Misc *m, int slot, int kb) {
-    if (ld_acquire_shared(&m->slot_kb[slot]) != kb) {
-        const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_shared(&m->slot_kb[slot]) != kb) {
-            if (aborted(m)) return;
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-                raise_error(a.err, FFD_ERRBIT_TIMEOUT);
-                *reinterpret_cast<volatile uint32_t *>(&m->aborted) = 1;
-                return;
-            }
-        }
-    }
-    wait_bar(a, m, &m->ring_full[slot], (kb / kRing) & 1);
+    wait_bar(a, m, &m->ring_full[kb & 1][slot], (kb / (2 * kRing)) & 1);
 }
 
 // Refine warp mt of group grp: walks the schedule, takes the kept blocks with kb & 1 == grp.
@@ -1101,14 +1079,22 @@ __device__ __forceinline__ void refiner(const DecodeArgs &a, const Smem &S, int 
     Sub s;
     grid_dependency_wait();
     RefineState R;
+    ResidOps Q;  // the unit's residual B fragments and query sums, kept in registers
+    int n = 0;
     int ui = -1, kb = 0, pb = 0;
     for (int t = 0; sch.next(a, s); t++) {
         if (s.first) {
             ui++;
             wait_bar(a, m, &m->unit_ready[ui & 1], (ui >> 1) & 1);
-            reset_refine(R, S.unit[ui & 1], lane);
+            const UnitOps &U = S.unit[ui & 1];
+            reset_refine(R, U, lane);
+            load_frags(U.br, lane, Q.br0, Q.br1);
+            const int tig = lane & 3;
+            const float4 q0 = U.qs[2 * tig], q1 = U.qs[2 * tig + 1];
+            Q.qs[0][0] = q0.x; Q.qs[0][1] = q0.y; Q.qs[0][2] = q0.z; Q.qs[0][3] = q0.w;
+            Q.qs[1][0] = q1.x; Q.qs[1][1] = q1.y; Q.qs[1][2] = q1.z; Q.qs[1][3] = q1.w;
+            n = U.n;
         }
-        const UnitOps &U = S.unit[ui & 1];
         const int ds = t % kDepth;
         wait_bar(a, m, &m->ring_seen[ds], (t / kDepth) & 1);
         const uint32_t mask = *reinterpret_cast<volatile uint32_t *>(&m->final_mask[ds]);
@@ -1121,7 +1107,7 @@ __device__ __forceinline__ void refiner(const DecodeArgs &a, const Smem &S, int 
             if ((kb & 1) == grp) {
                 const int slot = kb % kRing;
                 wait_fill(a, m, slot, kb);
-                refine_block(a, S, S.ring + slot * kSlotBytes, U, shat[(k * 4 + mt) * 32 + lane],
+                refine_block(a, S, S.ring + slot * kSlotBytes, Q, n, shat[(k * 4 + mt) * 32 + lane],
                              s.j0 + k, R, grp, mt, pb, lane);
                 pb ^= 1;
                 __syncwarp();
@@ -1177,8 +1163,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         for (int i = 0; i < kThumbBufs; i++) mbar_init(&m->thumb_full[i], 1);
         for (int i = 0; i < kShatBufs; i++) mbar_init(&m->shat_free[i], 8);  // refine warps
         for (int i = 0; i < kRing; i++) {
-            m->slot_kb[i] = -1;
-            mbar_init(&m->ring_full[i], 1);
+            mbar_init(&m->ring_full[0][i], 1);
+            mbar_init(&m->ring_full[1][i], 1);
             mbar_init(&m->ring_empty[i], 4);  // the refine group that took the block
         }
         for (int i = 0; i < 2; i++) {
@@ -1231,6 +1217,21 @@ static bool make_map(CUtensorMap *map, CUtensorMapDataType type, void *ptr, uint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// V as a 3-D tensor {64 channels, rows, 2 channel halves} (strides 256 B per row, 128 B per half)
+// with a box of {64, 64, 2}: one copy lands a block's 64 rows as two 64 x 128 B swizzled tiles,
+// channels 0-63 first.
+static bool make_v_map(CUtensorMap *map, void *ptr, uint64_t rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {64, rows, 2};
+    const cuuint64_t strides[2] = {kD * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kPage, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t stream) {
     static bool attr_done = false;
     if (!attr_done) {
@@ -1245,8 +1246,7 @@ cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t strea
     const uint64_t rows = (uint64_t)a.P * a.Hkv * kPage;
     if (!make_map(&prm.tm_resid, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<int8_t *>(a.resid),
                   kD, rows, kD, kD) ||
-        !make_map(&prm.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<__nv_bfloat16 *>(a.v),
-                  kD, rows, kD * 2, 64))
+        !make_v_map(&prm.tm_v, const_cast<__nv_bfloat16 *>(a.v), rows))
         return cudaErrorInvalidValue;
 
     stage1_kernel<<<dim3(a.nf > 0 ? a.nf : 1, a.B * a.Hkv), 128, 0, stream>>>(a);
