@@ -20,13 +20,23 @@
  *   - Supported shapes: head_dim = 128, page_size = 64, 1 <= num_q_heads/num_kv_heads <= 8.
  *     Anything else returns FFD_ERR_UNSUPPORTED.
  *
- * Paged cache layout (P pages, Hkv KV heads, 64 tokens per page, d = 128 channels):
- *   K, V       bf16 [P][Hkv][64][128]
- *   thumb      u8   [P][Hkv][64][32]   2-bit code of channel c in byte c/4, bits 2(c%4)+{0,1}
- *   t_scale    f16  [P][Hkv][64][4]    thumbnail scale of channel group g = c/32
- *   t_zero     f16  [P][Hkv][64][4]    thumbnail zero (offset) of group g
- *   resid      i8   [P][Hkv][64][128]  int8 residual code of channel c
- *   r_scale    f16  [P][Hkv][64][4]    residual scale of group g
+ * Paged cache layout (P pages, Hkv KV heads, 64 tokens per page, d = 128 channels, channel
+ * group g = c/32 of channel c, token r = 0..63 of a page):
+ *   K, V    bf16 [P][Hkv][64][128]
+ *   thumb   u8   [P][Hkv][FFD_THUMB_RECORD_BYTES]  one thumbnail record per (page, KV head):
+ *             bytes [0, 2048)     2-bit codes: token r at 32 r, channel c in byte c/4, bits
+ *                                 2(c%4)+{0,1}
+ *             bytes [2048, 2560)  f16 thumbnail scale of token r, group g at 2048 + 8 r + 2 g
+ *             bytes [2560, 3072)  f16 thumbnail zero (offset), at 2560 + 8 r + 2 g
+ *   resid   u8   [P][Hkv][FFD_RESID_RECORD_BYTES]  one residual record per (page, KV head):
+ *             bytes [0, 8192)     int8 residual codes: token r at 128 r; the 16-byte chunk j of
+ *                                 a token (channels 16j .. 16j+15, in order) is stored at chunk
+ *                                 position j ^ (r % 8), i.e. channel c at
+ *                                 128 r + 16 ((c / 16) ^ (r % 8)) + c % 16
+ *             bytes [8192, 8704)  f16 residual scale of token r, group g at 8192 + 8 r + 2 g
+ * Each record is what one stage of the method reads for a block, so a kernel moves it with one
+ * bulk copy; the chunk permutation of the residual codes is the order in which the decode kernel
+ * reads them from shared memory without bank conflicts.
  * Logical block b of sequence s (tokens 64b .. 64b+63) lives in page block_table[s][b].
  */
 #ifndef FFD_H
@@ -50,6 +60,9 @@ typedef enum {
                                 query with |q| >= 2^27 */
     FFD_ERR_TIMEOUT = 7,     /* device: a pipeline wait exceeded its 2 s bound (results invalid) */
 } ffd_status;
+
+#define FFD_THUMB_RECORD_BYTES 3072
+#define FFD_RESID_RECORD_BYTES 8704
 
 /* Bits of the device error word (first 4 bytes of a workspace, or the quantiser's word). */
 #define FFD_ERRBIT_BOUNDS 0x1
@@ -102,7 +115,8 @@ int32_t ffd_version(void);
  *
  *   cache         shape of the cache (head_dim 128, page_size 64)
  *   k_bf16        device, bf16 [P][Hkv][64][128], read only
- *   thumb .. r_scale  device outputs in the layout above (written for the selected pages only)
+ *   thumb, resid  device outputs, the records above (written for the selected pages only),
+ *                 16-byte aligned
  *   page_ids      device int32 [num_page_ids] pages to quantise, or NULL for all P pages
  *   num_page_ids  number of entries in page_ids (ignored when page_ids is NULL)
  *   error_word    device int32, or NULL: FFD_ERRBIT_BOUNDS is OR-ed in for a page id outside
@@ -112,9 +126,8 @@ int32_t ffd_version(void);
  * Returns FFD_OK, FFD_ERR_INVALID_ARG, FFD_ERR_UNSUPPORTED or FFD_ERR_CUDA.
  */
 ffd_status ffd_quantize_keys(const ffd_cache_desc *cache, const void *k_bf16, uint8_t *thumb,
-                             void *t_scale, void *t_zero, int8_t *resid, void *r_scale,
-                             const int32_t *page_ids, int32_t num_page_ids, int32_t *error_word,
-                             void *stream);
+                             uint8_t *resid, const int32_t *page_ids, int32_t num_page_ids,
+                             int32_t *error_word, void *stream);
 
 /*
  * Bytes of device workspace that ffd_decode_attention needs for these parameters on the current
@@ -138,7 +151,8 @@ size_t ffd_decode_workspace_size(const ffd_decode_params *params);
  * n = 0 gives out_i = 0 and m~_i = -inf. S = L = 0 gives m~ = -inf, so every block is kept.
  *
  *   q_bf16      device bf16 [B][Hq][128], |q| < 2^27 (else FFD_ERRBIT_RANGE)
- *   thumb .. r_scale, v_bf16   device cache in the layout above (from ffd_quantize_keys)
+ *   thumb, resid, v_bf16   device cache in the layout above (records from ffd_quantize_keys),
+ *               16-byte aligned
  *   seq_lens    device int32 [B], 0 <= seq_lens[b] <= 64 * max_blocks_per_seq
  *   block_table device int32 [B][max_blocks_per_seq]; only entries b < ceil(n/64) are read
  *   out         device fp32 [B][Hq][128]
@@ -154,8 +168,7 @@ size_t ffd_decode_workspace_size(const ffd_decode_params *params);
  * a block_table entry lies outside [0, num_pages) (the block is treated as empty).
  */
 ffd_status ffd_decode_attention(const ffd_decode_params *params, const void *q_bf16,
-                                const uint8_t *thumb, const void *t_scale, const void *t_zero,
-                                const int8_t *resid, const void *r_scale, const void *v_bf16,
+                                const uint8_t *thumb, const uint8_t *resid, const void *v_bf16,
                                 const int32_t *seq_lens, const int32_t *block_table, float *out,
                                 uint8_t *keep_mask, float *m_tilde, void *workspace,
                                 size_t workspace_bytes, void *stream);
@@ -199,12 +212,11 @@ ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
  *     read and clear it with ffd_get_error. With NULL they are not reported.
  */
 ffd_status ffd_decode_attention_static(const ffd_decode_params *params, const void *q_bf16,
-                                       const uint8_t *thumb, const void *t_scale,
-                                       const void *t_zero, const int8_t *resid,
-                                       const void *r_scale, const void *v_bf16,
-                                       const int32_t *seq_lens, const int32_t *block_table,
-                                       float *out, uint8_t *keep_mask, float *m_tilde,
-                                       int32_t *error_word, void *stream);
+                                       const uint8_t *thumb, const uint8_t *resid,
+                                       const void *v_bf16, const int32_t *seq_lens,
+                                       const int32_t *block_table, float *out,
+                                       uint8_t *keep_mask, float *m_tilde, int32_t *error_word,
+                                       void *stream);
 
 /*
  * ffd_set_profile_events -- optional instrumentation. While both events are non-NULL, every

@@ -8,8 +8,8 @@
 
 namespace ffd {
 cudaError_t launch_quantize(int P, int Hkv, const int32_t *page_ids, int num_pages_listed,
-                            const void *k, uint8_t *thumb, void *t_scale, void *t_zero,
-                            int8_t *resid, void *r_scale, int *err, cudaStream_t stream);
+                            const void *k, uint8_t *thumb, uint8_t *resid, int *err,
+                            cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t stream);
 cudaError_t launch_dense(const DecodeArgs &a, cudaStream_t stream);
 }  // namespace ffd
@@ -160,26 +160,20 @@ const char *ffd_status_string(ffd_status s) {
     return "FFD_ERR_UNKNOWN";
 }
 
-int32_t ffd_version(void) { return 100; }
+int32_t ffd_version(void) { return 200; }
 
 ffd_status ffd_quantize_keys(const ffd_cache_desc *cache, const void *k_bf16, uint8_t *thumb,
-                             void *t_scale, void *t_zero, int8_t *resid, void *r_scale,
-                             const int32_t *page_ids, int32_t num_page_ids, int32_t *error_word,
-                             void *stream) {
-    if (!cache || !k_bf16 || !thumb || !t_scale || !t_zero || !resid || !r_scale)
-        return FFD_ERR_INVALID_ARG;
+                             uint8_t *resid, const int32_t *page_ids, int32_t num_page_ids,
+                             int32_t *error_word, void *stream) {
+    if (!cache || !k_bf16 || !thumb || !resid) return FFD_ERR_INVALID_ARG;
     if (cache->num_pages < 1 || cache->num_kv_heads < 1) return FFD_ERR_INVALID_ARG;
     if (page_ids && num_page_ids < 0) return FFD_ERR_INVALID_ARG;
     if (cache->head_dim != kD || cache->page_size != kPage) return FFD_ERR_UNSUPPORTED;
-    if (!aligned16(k_bf16) || !aligned16(thumb) || !aligned16(resid) ||
-        (reinterpret_cast<uintptr_t>(t_scale) & 7u) || (reinterpret_cast<uintptr_t>(t_zero) & 7u) ||
-        (reinterpret_cast<uintptr_t>(r_scale) & 7u))
-        return FFD_ERR_INVALID_ARG;
+    if (!aligned16(k_bf16) || !aligned16(thumb) || !aligned16(resid)) return FFD_ERR_INVALID_ARG;
     const int listed = page_ids ? num_page_ids : cache->num_pages;
     if ((int64_t)listed * cache->num_kv_heads * kPage * 32 > INT32_MAX) return FFD_ERR_UNSUPPORTED;
     cudaError_t e = launch_quantize(cache->num_pages, cache->num_kv_heads, page_ids, listed, k_bf16,
-                                    thumb, t_scale, t_zero, resid, r_scale, error_word,
-                                    static_cast<cudaStream_t>(stream));
+                                    thumb, resid, error_word, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
 }
 
@@ -194,13 +188,11 @@ size_t ffd_dense_workspace_size(const ffd_decode_params *params) {
 }
 
 ffd_status ffd_decode_attention(const ffd_decode_params *params, const void *q_bf16,
-                                const uint8_t *thumb, const void *t_scale, const void *t_zero,
-                                const int8_t *resid, const void *r_scale, const void *v_bf16,
+                                const uint8_t *thumb, const uint8_t *resid, const void *v_bf16,
                                 const int32_t *seq_lens, const int32_t *block_table, float *out,
                                 uint8_t *keep_mask, float *m_tilde, void *workspace,
                                 size_t workspace_bytes, void *stream) {
-    if (!q_bf16 || !thumb || !t_scale || !t_zero || !resid || !r_scale || !v_bf16 || !seq_lens ||
-        !block_table || !out || !workspace)
+    if (!q_bf16 || !thumb || !resid || !v_bf16 || !seq_lens || !block_table || !out || !workspace)
         return FFD_ERR_INVALID_ARG;
     if (!aligned16(thumb) || !aligned16(resid) || !aligned16(v_bf16) || !aligned16(q_bf16) ||
         (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
@@ -212,10 +204,7 @@ ffd_status ffd_decode_attention(const ffd_decode_params *params, const void *q_b
     DecodeArgs a = make_args(params, pl, workspace);
     a.q = static_cast<const __nv_bfloat16 *>(q_bf16);
     a.thumb = thumb;
-    a.t_scale = static_cast<const __half *>(t_scale);
-    a.t_zero = static_cast<const __half *>(t_zero);
     a.resid = resid;
-    a.r_scale = static_cast<const __half *>(r_scale);
     a.v = static_cast<const __nv_bfloat16 *>(v_bf16);
     a.seq_lens = seq_lens;
     a.block_table = block_table;
@@ -315,14 +304,12 @@ ffd_status static_scratch(void **out) {
 extern "C" {
 
 ffd_status ffd_decode_attention_static(const ffd_decode_params *params, const void *q_bf16,
-                                       const uint8_t *thumb, const void *t_scale,
-                                       const void *t_zero, const int8_t *resid,
-                                       const void *r_scale, const void *v_bf16,
-                                       const int32_t *seq_lens, const int32_t *block_table,
-                                       float *out, uint8_t *keep_mask, float *m_tilde,
-                                       int32_t *error_word, void *stream) {
-    if (!q_bf16 || !thumb || !t_scale || !t_zero || !resid || !r_scale || !v_bf16 || !seq_lens ||
-        !block_table || !out)
+                                       const uint8_t *thumb, const uint8_t *resid,
+                                       const void *v_bf16, const int32_t *seq_lens,
+                                       const int32_t *block_table, float *out,
+                                       uint8_t *keep_mask, float *m_tilde, int32_t *error_word,
+                                       void *stream) {
+    if (!q_bf16 || !thumb || !resid || !v_bf16 || !seq_lens || !block_table || !out)
         return FFD_ERR_INVALID_ARG;
     if (!aligned16(thumb) || !aligned16(resid) || !aligned16(v_bf16) || !aligned16(q_bf16))
         return FFD_ERR_INVALID_ARG;
@@ -345,10 +332,7 @@ ffd_status ffd_decode_attention_static(const ffd_decode_params *params, const vo
     if (error_word) a.err = reinterpret_cast<int *>(error_word);
     a.q = static_cast<const __nv_bfloat16 *>(q_bf16);
     a.thumb = thumb;
-    a.t_scale = static_cast<const __half *>(t_scale);
-    a.t_zero = static_cast<const __half *>(t_zero);
     a.resid = resid;
-    a.r_scale = static_cast<const __half *>(r_scale);
     a.v = static_cast<const __nv_bfloat16 *>(v_bf16);
     a.seq_lens = seq_lens;
     a.block_table = block_table;

@@ -17,6 +17,19 @@ constexpr int kGroupSize = 32;   // channels per group
 constexpr int kThumbRow = kD / 4;  // bytes of 2-bit codes per token
 constexpr int kMaxG = 8;         // largest supported GQA group
 constexpr int kPartStride = 132; // floats per split partial: o[128], m, l, 2 pad
+// Cache records (layout in ffd.h): thumbnail = codes [64][32] | scale [64][4] f16 | zero [64][4]
+// f16; residual = codes [64][128] (16-byte chunk j of token r at j ^ (r % 8)) | scale [64][4] f16.
+constexpr int kThumbRec = FFD_THUMB_RECORD_BYTES;
+constexpr int kThumbScaleOff = 2048;
+constexpr int kThumbZeroOff = 2560;
+constexpr int kResidRec = FFD_RESID_RECORD_BYTES;
+constexpr int kResidScaleOff = 8192;
+static_assert(kThumbRec == 3072 && kResidRec == 8704, "record sizes");
+
+// Byte offset of residual channel c of token r inside its record.
+__host__ __device__ inline int resid_offset(int r, int c) {
+    return r * 128 + ((((c >> 4) ^ (r & 7)) << 4) | (c & 15));
+}
 
 // Everything a decode launch needs; passed by value to the kernels.
 struct DecodeArgs {
@@ -26,10 +39,8 @@ struct DecodeArgs {
     int nf;          // stage-1 slots per (sequence, KV head)
     float delta, sm_scale;
     const __nv_bfloat16 *q;
-    const uint8_t *thumb;
-    const __half *t_scale, *t_zero;
-    const int8_t *resid;
-    const __half *r_scale;
+    const uint8_t *thumb;    // thumbnail records, kThumbRec bytes per (page, KV head)
+    const uint8_t *resid;    // residual records, kResidRec bytes per (page, KV head)
     const __nv_bfloat16 *k;  // dense path only
     const __nv_bfloat16 *v;
     const int32_t *seq_lens, *block_table;

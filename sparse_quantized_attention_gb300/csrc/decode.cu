@@ -55,13 +55,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kQMax = 134217728.0f;          // 2^27
 constexpr float kRescaleMargin = 30.0f;        // lazy softmax rescaling, natural-log units
 
-// ring slot: residual tile (64 x 128 B, swizzled), V tile (channels 0-63 of the 64 rows, then
-// channels 64-127, each 64 x 128 B, swizzled; one 3-D copy), residual scales (64 x 8 B)
-constexpr int kSlotV = 8192;
-constexpr int kSlotRScale = 8192 + 16384;
-constexpr int kSlotTx = 8192 + 16384 + 512;
-constexpr int kSlotBytes = 25600;
-constexpr int kThumbBlock = 3072;    // codes 2048 B + scales 512 B + zeros 512 B
+// ring slot: the block's residual record (codes 64 x 128 B, already in the swizzled order, then
+// the scales 64 x 8 B; one bulk copy), V tile (channels 0-63 of the 64 rows, then channels 64-127,
+// each 64 x 128 B, swizzled; one 3-D copy)
+constexpr int kSlotRScale = kResidScaleOff;
+constexpr int kSlotV = 9216;
+constexpr int kSlotTx = kResidRec + 16384;
+constexpr int kSlotBytes = kSlotV + 16384;
+static_assert(kResidRec <= kSlotV, "residual record inside the slot");
+constexpr int kThumbBlock = kThumbRec;  // the block's thumbnail record: codes, scales, zeros
 constexpr int kThumbBuf = kSub * kThumbBlock;
 constexpr int kShatBuf = kSub * 4 * 32 * 16;  // provisional scores of one sub-chunk
 constexpr int kPxBuf = 4 * 32 * 16;           // P^T fragments of one block (4 k-steps)
@@ -122,7 +124,6 @@ struct UnitOps {
 static_assert(sizeof(UnitOps) <= kUnitBytes, "unit operand slot");
 
 struct MainParams {
-    CUtensorMap tm_resid;
     CUtensorMap tm_v;
     DecodeArgs a;
 };
@@ -387,8 +388,8 @@ __device__ __forceinline__ float4 scan_tile(const uint8_t *base, int r0, int r1,
     float D[4][4];
     thumb_mma(D, w0, w1, m0, Q);
     float sf0[4], sf1[4], zf0[4], zf1[4];
-    const uint2 *ts = reinterpret_cast<const uint2 *>(base + 2048);
-    const uint2 *tz = reinterpret_cast<const uint2 *>(base + 2560);
+    const uint2 *ts = reinterpret_cast<const uint2 *>(base + kThumbScaleOff);
+    const uint2 *tz = reinterpret_cast<const uint2 *>(base + kThumbZeroOff);
     unpack4h(ts[r0], sf0);
     unpack4h(ts[r1], sf1);
     unpack4h(tz[r0], zf0);
@@ -521,11 +522,13 @@ __global__ void __launch_bounds__(128, 1) stage1_kernel(const DecodeArgs a) {
     load_thumb_ops(a, b, h, lane, Q);
     load_resid_ops(a, b, h, lane, QR);
     const size_t tile = (size_t)page * a.Hkv + h;
+    const uint8_t *trec = a.thumb + tile * kThumbRec;
+    const uint8_t *rrec = a.resid + tile * kResidRec;
     const int r0 = 16 * warp + g, r1 = r0 + 8;
     uint32_t w0[8], w1[8];
     {
-        const uint4 *c0 = reinterpret_cast<const uint4 *>(a.thumb + (tile * kPage + r0) * kThumbRow);
-        const uint4 *c1 = reinterpret_cast<const uint4 *>(a.thumb + (tile * kPage + r1) * kThumbRow);
+        const uint4 *c0 = reinterpret_cast<const uint4 *>(trec + r0 * kThumbRow);
+        const uint4 *c1 = reinterpret_cast<const uint4 *>(trec + r1 * kThumbRow);
         const uint4 p0 = c0[0], p1 = c0[1], p2 = c1[0], p3 = c1[1];
         w0[0] = p0.x; w0[1] = p0.y; w0[2] = p0.z; w0[3] = p0.w;
         w0[4] = p1.x; w0[5] = p1.y; w0[6] = p1.z; w0[7] = p1.w;
@@ -535,19 +538,19 @@ __global__ void __launch_bounds__(128, 1) stage1_kernel(const DecodeArgs a) {
     uint2 x0[4], x1[4];
 #pragma unroll
     for (int gg = 0; gg < 4; gg++) {
-        x0[gg] = *reinterpret_cast<const uint2 *>(a.resid + (tile * kPage + r0) * kD + 32 * gg + 8 * tig);
-        x1[gg] = *reinterpret_cast<const uint2 *>(a.resid + (tile * kPage + r1) * kD + 32 * gg + 8 * tig);
+        x0[gg] = *reinterpret_cast<const uint2 *>(rrec + resid_offset(r0, 32 * gg + 8 * tig));
+        x1[gg] = *reinterpret_cast<const uint2 *>(rrec + resid_offset(r1, 32 * gg + 8 * tig));
     }
     float sf0[4], sf1[4], zf0[4], zf1[4], sr0[4], sr1[4];
-    const uint2 *ts = reinterpret_cast<const uint2 *>(a.t_scale);
-    const uint2 *tz = reinterpret_cast<const uint2 *>(a.t_zero);
-    const uint2 *rs = reinterpret_cast<const uint2 *>(a.r_scale);
-    unpack4h(ts[tile * kPage + r0], sf0);
-    unpack4h(ts[tile * kPage + r1], sf1);
-    unpack4h(tz[tile * kPage + r0], zf0);
-    unpack4h(tz[tile * kPage + r1], zf1);
-    unpack4h(rs[tile * kPage + r0], sr0);
-    unpack4h(rs[tile * kPage + r1], sr1);
+    const uint2 *ts = reinterpret_cast<const uint2 *>(trec + kThumbScaleOff);
+    const uint2 *tz = reinterpret_cast<const uint2 *>(trec + kThumbZeroOff);
+    const uint2 *rs = reinterpret_cast<const uint2 *>(rrec + kResidScaleOff);
+    unpack4h(ts[r0], sf0);
+    unpack4h(ts[r1], sf1);
+    unpack4h(tz[r0], zf0);
+    unpack4h(tz[r1], zf1);
+    unpack4h(rs[r0], sr0);
+    unpack4h(rs[r1], sr1);
     float D[4][4], Dr[4][4];
     thumb_mma(D, w0, w1, 0x00030003u << (2 * tig), Q);
     resid_mma(Dr, x0, x1, QR);
@@ -659,10 +662,10 @@ __device__ __forceinline__ const PageSlot &page_slot(const DecodeArgs &a, Misc *
     return m->ps[t % kPageSlots];
 }
 
-// Thumbnail warp: the 2-bit codes, scales and zeros of sub-chunk t go to buffer t % kThumbBufs
+// Thumbnail warp: the thumbnail records of sub-chunk t go to buffer t % kThumbBufs
 // once the ring warp has published sub-chunk t - kThumbBufs (so the scan warps are done with that
 // buffer, and no decision runs more than kThumbBufs sub-chunks ahead of the ring warp); lane k
-// issues block k's copies.
+// issues block k's copy.
 __device__ __forceinline__ void thumb_issuer(const DecodeArgs &a, const Smem &S, int lane) {
     Misc *m = S.misc;
     int t = 0;
@@ -681,11 +684,9 @@ __device__ __forceinline__ void thumb_issuer(const DecodeArgs &a, const Smem &S,
                                   (uint32_t)((cnt - __popc(bad)) * kThumbBlock));
         __syncwarp();
         if (lane < cnt && !((bad >> lane) & 1u)) {
-            const size_t row = (size_t)P.row[lane];
+            const size_t tile = (size_t)(P.row[lane] / kPage);
             uint8_t *d = S.thumb + buf * kThumbBuf + lane * kThumbBlock;
-            tma_load_1d(d, a.thumb + row * kThumbRow, 2048, &m->thumb_full[buf]);
-            tma_load_1d(d + 2048, a.t_scale + row * kGroups, 512, &m->thumb_full[buf]);
-            tma_load_1d(d + 2560, a.t_zero + row * kGroups, 512, &m->thumb_full[buf]);
+            tma_load_1d(d, a.thumb + tile * kThumbRec, kThumbRec, &m->thumb_full[buf]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&m->pages_empty[t % kPageSlots]);
@@ -697,16 +698,12 @@ __device__ __forceinline__ void thumb_issuer(const DecodeArgs &a, const Smem &S,
 }
 
 // Ring warp: publishes the kept blocks of sub-chunk t (scan votes, plus the forced blocks, less
-// the never-loaded ones), then issues the residual tile, V tile and residual scales of each kept
-// block into the next ring slot as it frees up; lanes 0-3 issue one block's four copies side by
-// side.
+// the never-loaded ones), then issues the residual record and the V tile of each kept block into
+// the next ring slot as it frees up; lanes 0 and 1 issue the two copies side by side.
 __device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S, int lane) {
     const DecodeArgs &a = prm.a;
     Misc *m = S.misc;
-    if (lane == 0) {
-        prefetch_tensormap(&prm.tm_resid);
-        prefetch_tensormap(&prm.tm_v);
-    }
+    if (lane == 0) prefetch_tensormap(&prm.tm_v);
     int kb = 0;
     for (int t = 0;; t++) {
         const PageSlot &P = page_slot(a, m, t);
@@ -734,10 +731,8 @@ __device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S
             uint64_t *bar = &m->ring_full[(kb - 1) & 1][slot];  // kb was advanced above
             if (lane == 0) mbar_arrive_expect_tx(bar, kSlotTx);
             __syncwarp();
-            if (lane == 0) tma_load_2d(d, &prm.tm_resid, 0, row, bar);
+            if (lane == 0) tma_load_1d(d, a.resid + (size_t)(row / kPage) * kResidRec, kResidRec, bar);
             else if (lane == 1) tma_load_3d(d + kSlotV, &prm.tm_v, 0, row, 0, bar);
-            else if (lane == 2)
-                tma_load_1d(d + kSlotRScale, a.r_scale + (size_t)row * kGroups, 512, bar);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&m->pages_empty[t % kPageSlots]);
@@ -900,10 +895,8 @@ __device__ __forceinline__ void refine_block(const DecodeArgs &a, const Smem &S,
 #pragma unroll
     for (int gg = 0; gg < 4; gg++) {
         const int o = 32 * gg + 8 * tig;
-        x0[gg] = *reinterpret_cast<const uint2 *>(slot + r0 * 128 +
-                                                  ((((o >> 4) ^ (r0 & 7)) << 4) | (o & 15)));
-        x1[gg] = *reinterpret_cast<const uint2 *>(slot + r1 * 128 +
-                                                  ((((o >> 4) ^ (r1 & 7)) << 4) | (o & 15)));
+        x0[gg] = *reinterpret_cast<const uint2 *>(slot + resid_offset(r0, o));
+        x1[gg] = *reinterpret_cast<const uint2 *>(slot + resid_offset(r1, o));
     }
     float Dr[4][4];
     resid_mma(Dr, x0, x1, Q);
@@ -1203,20 +1196,6 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D map over [rows][inner] elements with a box of 64 rows x box_inner elements, 128B swizzle.
-static bool make_map(CUtensorMap *map, CUtensorMapDataType type, void *ptr, uint64_t inner,
-                     uint64_t rows, uint64_t row_bytes, uint32_t box_inner) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {box_inner, (cuuint32_t)kPage};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, type, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // V as a 3-D tensor {64 channels, rows, 2 channel halves} (strides 256 B per row, 128 B per half)
 // with a box of {64, 64, 2}: one copy lands a block's 64 rows as two 64 x 128 B swizzled tiles,
 // channels 0-63 first.
@@ -1244,9 +1223,7 @@ cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t strea
     memset(&prm, 0, sizeof prm);
     prm.a = a;
     const uint64_t rows = (uint64_t)a.P * a.Hkv * kPage;
-    if (!make_map(&prm.tm_resid, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<int8_t *>(a.resid),
-                  kD, rows, kD, kD) ||
-        !make_v_map(&prm.tm_v, const_cast<__nv_bfloat16 *>(a.v), rows))
+    if (!make_v_map(&prm.tm_v, const_cast<__nv_bfloat16 *>(a.v), rows))
         return cudaErrorInvalidValue;
 
     stage1_kernel<<<dim3(a.nf > 0 ? a.nf : 1, a.B * a.Hkv), 128, 0, stream>>>(a);

@@ -2,7 +2,8 @@
 //
 // Source: "Faster Than Flash", Methodology §1 (content-aware scanning via low-bit quantization:
 // the K cache is kept as 2-bit thumbnails for score estimation plus 8-bit residuals that rebuild
-// the keys close to fp16 precision). The exact format is the one stated in include/ffd.h.
+// the keys close to fp16 precision). The exact format, and the record layout each (page, KV head)
+// tile is written in, are the ones stated in include/ffd.h.
 //
 // One warp quantises one token of one KV head: lane l holds channels 4l .. 4l+3, so a group of
 // 32 channels is 8 lanes and group reductions are 3 shuffles. Every arithmetic step is a single
@@ -25,8 +26,7 @@ __device__ __forceinline__ float group8_max(float v) {
 
 __global__ void __launch_bounds__(256) quantize_keys_kernel(
     int P, int Hkv, int num_rows, const int32_t *__restrict__ page_ids,
-    const __nv_bfloat16 *__restrict__ k, uint8_t *__restrict__ thumb, __half *__restrict__ t_scale,
-    __half *__restrict__ t_zero, int8_t *__restrict__ resid, __half *__restrict__ r_scale,
+    const __nv_bfloat16 *__restrict__ k, uint8_t *__restrict__ thumb, uint8_t *__restrict__ resid,
     int *err) {
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -43,7 +43,8 @@ __global__ void __launch_bounds__(256) quantize_keys_kernel(
             return;
         }
     }
-    const int64_t row = ((int64_t)page * Hkv + h) * kPage + slot;
+    const int64_t tile = (int64_t)page * Hkv + h;
+    const int64_t row = tile * kPage + slot;
 
     // 4 consecutive channels per lane (8 bytes of bf16)
     const uint2 raw = *reinterpret_cast<const uint2 *>(k + row * kD + 4 * lane);
@@ -99,27 +100,27 @@ __global__ void __launch_bounds__(256) quantize_keys_kernel(
         packed |= ((uint32_t)(int)q8 & 0xffu) << (8 * c);
     }
 
-    thumb[row * kThumbRow + lane] = (uint8_t)codes;
-    *reinterpret_cast<uint32_t *>(resid + row * kD + 4 * lane) = packed;
+    uint8_t *trec = thumb + tile * kThumbRec;
+    uint8_t *rrec = resid + tile * kResidRec;
+    trec[slot * kThumbRow + lane] = (uint8_t)codes;
+    *reinterpret_cast<uint32_t *>(rrec + resid_offset(slot, 4 * lane)) = packed;
     if ((lane & 7) == 0) {
         const int g = lane >> 3;
-        t_scale[row * kGroups + g] = sf16;
-        t_zero[row * kGroups + g] = zf16;
-        r_scale[row * kGroups + g] = sr16;
+        reinterpret_cast<__half *>(trec + kThumbScaleOff)[slot * kGroups + g] = sf16;
+        reinterpret_cast<__half *>(trec + kThumbZeroOff)[slot * kGroups + g] = zf16;
+        reinterpret_cast<__half *>(rrec + kResidScaleOff)[slot * kGroups + g] = sr16;
     }
 }
 
 cudaError_t launch_quantize(int P, int Hkv, const int32_t *page_ids, int num_pages_listed,
-                            const void *k, uint8_t *thumb, void *t_scale, void *t_zero,
-                            int8_t *resid, void *r_scale, int *err, cudaStream_t stream) {
+                            const void *k, uint8_t *thumb, uint8_t *resid, int *err,
+                            cudaStream_t stream) {
     const int64_t rows = (int64_t)num_pages_listed * Hkv * kPage;
     if (rows == 0) return cudaSuccess;
     const int threads = 256;
     const int64_t blocks = (rows * 32 + threads - 1) / threads;
     quantize_keys_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
-        P, Hkv, (int)rows, page_ids, static_cast<const __nv_bfloat16 *>(k), thumb,
-        static_cast<__half *>(t_scale), static_cast<__half *>(t_zero), resid,
-        static_cast<__half *>(r_scale), err);
+        P, Hkv, (int)rows, page_ids, static_cast<const __nv_bfloat16 *>(k), thumb, resid, err);
     return cudaGetLastError();
 }
 

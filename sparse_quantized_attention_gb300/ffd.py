@@ -74,21 +74,21 @@ def lib() -> ctypes.CDLL:
             L.ffd_status_string.restype = ctypes.c_char_p
             L.ffd_version.argtypes = []
             L.ffd_version.restype = ctypes.c_int32
-            L.ffd_quantize_keys.argtypes = [ctypes.POINTER(CacheDesc), P, P, P, P, P, P, P,
+            L.ffd_quantize_keys.argtypes = [ctypes.POINTER(CacheDesc), P, P, P, P,
                                             ctypes.c_int32, P, P]
             L.ffd_quantize_keys.restype = st
             L.ffd_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeParams)]
             L.ffd_decode_workspace_size.restype = ctypes.c_size_t
             L.ffd_dense_workspace_size.argtypes = [ctypes.POINTER(DecodeParams)]
             L.ffd_dense_workspace_size.restype = ctypes.c_size_t
-            L.ffd_decode_attention.argtypes = [ctypes.POINTER(DecodeParams)] + [P] * 13 + \
+            L.ffd_decode_attention.argtypes = [ctypes.POINTER(DecodeParams)] + [P] * 10 + \
                 [ctypes.c_size_t, P]
             L.ffd_decode_attention.restype = st
             L.ffd_dense_decode.argtypes = [ctypes.POINTER(DecodeParams)] + [P] * 7 + \
                 [ctypes.c_size_t, P]
             L.ffd_dense_decode.restype = st
             L.ffd_decode_attention_static.argtypes = [ctypes.POINTER(DecodeParams)] + \
-                [P] * 14
+                [P] * 11
             L.ffd_decode_attention_static.restype = st
             L.ffd_set_profile_events.argtypes = [P, P]
             L.ffd_set_profile_events.restype = st
@@ -119,24 +119,23 @@ def _check(status: int, where: str):
         raise FFDError(status, where)
 
 
+THUMB_RECORD_BYTES = 3072
+RESID_RECORD_BYTES = 8704
+
+
 class QuantizedCache(NamedTuple):
-    """The stored key format: thumb u8 [P,Hkv,64,32]; t_scale, t_zero f16 [P,Hkv,64,4];
-    resid i8 [P,Hkv,64,128]; r_scale f16 [P,Hkv,64,4]."""
+    """The stored key cache, one record pair per (page, KV head), byte layouts in include/ffd.h:
+    thumb u8 [P, Hkv, 3072] (2-bit codes, thumbnail scales, zeros); resid u8 [P, Hkv, 8704]
+    (int8 residual codes in the kernel's chunk order, residual scales)."""
     thumb: torch.Tensor
-    t_scale: torch.Tensor
-    t_zero: torch.Tensor
     resid: torch.Tensor
-    r_scale: torch.Tensor
 
 
 def alloc_quantized_cache(num_pages: int, num_kv_heads: int, device="cuda") -> QuantizedCache:
-    shp = (num_pages, num_kv_heads, PAGE)
+    shp = (num_pages, num_kv_heads)
     return QuantizedCache(
-        torch.empty(shp + (HEAD_DIM // 4,), dtype=torch.uint8, device=device),
-        torch.empty(shp + (4,), dtype=torch.float16, device=device),
-        torch.empty(shp + (4,), dtype=torch.float16, device=device),
-        torch.empty(shp + (HEAD_DIM,), dtype=torch.int8, device=device),
-        torch.empty(shp + (4,), dtype=torch.float16, device=device))
+        torch.empty(shp + (THUMB_RECORD_BYTES,), dtype=torch.uint8, device=device),
+        torch.empty(shp + (RESID_RECORD_BYTES,), dtype=torch.uint8, device=device))
 
 
 def ffd_status_string(status: int) -> str:

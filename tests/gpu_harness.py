@@ -48,12 +48,21 @@ def quantize(dev: dict) -> ffd.QuantizedCache:
 
 
 def cache_to_host(qc: ffd.QuantizedCache) -> oracle.QuantizedKeys:
+    """Unpack the library's (page, KV head) records into the method's arrays (record layout in
+    include/ffd.h; the residual codes' 16-byte chunk j of token r is stored at j ^ (r % 8))."""
+    th = qc.thumb.cpu().numpy()
+    rr = qc.resid.cpu().numpy()
+    P, Hkv = th.shape[:2]
+    rows = np.arange(64)[:, None]
+    chunks = np.arange(8)[None, :] ^ (rows % 8)
+    stored = rr[..., :8192].reshape(P, Hkv, 64, 8, 16)
     return oracle.QuantizedKeys(
-        thumb=qc.thumb.cpu().numpy(),
-        t_scale=qc.t_scale.cpu().view(torch.int16).numpy().view(np.uint16),
-        t_zero=qc.t_zero.cpu().view(torch.int16).numpy().view(np.uint16),
-        resid=qc.resid.cpu().numpy(),
-        r_scale=qc.r_scale.cpu().view(torch.int16).numpy().view(np.uint16))
+        thumb=np.ascontiguousarray(th[..., :2048]).reshape(P, Hkv, 64, 32),
+        t_scale=np.ascontiguousarray(th[..., 2048:2560]).view(np.uint16).reshape(P, Hkv, 64, 4),
+        t_zero=np.ascontiguousarray(th[..., 2560:3072]).view(np.uint16).reshape(P, Hkv, 64, 4),
+        resid=np.ascontiguousarray(stored[:, :, rows, chunks, :]).reshape(P, Hkv, 64, 128)
+        .view(np.int8),
+        r_scale=np.ascontiguousarray(rr[..., 8192:]).view(np.uint16).reshape(P, Hkv, 64, 4))
 
 
 def assert_cache_equal(gpu: oracle.QuantizedKeys, ref: oracle.QuantizedKeys):

@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings(lib):
     for code, name in ffd.ffd.STATUS_NAMES.items():
         assert ffd.ffd_status_string(code) == name
-    assert ffd.ffd_version() >= 100
+    assert ffd.ffd_version() >= 200
 
 
 def _params(**kw):
@@ -59,12 +59,11 @@ def _params(**kw):
 
 
 def _decode(lib, p, ws_bytes=1 << 30, **ptrs):
-    args = dict(q=FAKE, thumb=FAKE, ts=FAKE, tz=FAKE, resid=FAKE, rs=FAKE, v=FAKE, sl=FAKE,
-                bt=FAKE, out=FAKE, mask=None, mt=None, ws=FAKE)
+    args = dict(q=FAKE, thumb=FAKE, resid=FAKE, v=FAKE, sl=FAKE, bt=FAKE, out=FAKE, mask=None,
+                mt=None, ws=FAKE)
     args.update(ptrs)
     return lib.ffd_decode_attention(ctypes.byref(p), *[args[k] for k in (
-        "q", "thumb", "ts", "tz", "resid", "rs", "v", "sl", "bt", "out", "mask", "mt", "ws")],
-        ws_bytes, None)
+        "q", "thumb", "resid", "v", "sl", "bt", "out", "mask", "mt", "ws")], ws_bytes, None)
 
 
 def test_workspace_sizes(lib):
@@ -100,9 +99,10 @@ def test_decode_rejects_unsupported_shapes(lib):
 
 def test_decode_rejects_null_and_misaligned_pointers(lib):
     p = _params()
-    for key in ("q", "thumb", "ts", "tz", "resid", "rs", "v", "sl", "bt", "out", "ws"):
+    for key in ("q", "thumb", "resid", "v", "sl", "bt", "out", "ws"):
         assert _decode(lib, p, **{key: None}) == 1, key
     assert _decode(lib, p, thumb=FAKE + 4) == 1
+    assert _decode(lib, p, resid=FAKE + 8) == 1
     assert _decode(lib, p, ws=FAKE + 16) == 1
 
 
@@ -127,7 +127,7 @@ def test_dense_rejects_bad_arguments(lib):
 def test_quantize_rejects_bad_arguments(lib):
     good = ffd.CacheDesc(4, 2, 128, 64)
     call = lambda d, k=FAKE, ids=None, nids=0: lib.ffd_quantize_keys(  # noqa: E731
-        ctypes.byref(d), k, FAKE, FAKE, FAKE, FAKE, FAKE, ids, nids, None, None)
+        ctypes.byref(d), k, FAKE, FAKE, ids, nids, None, None)
     assert call(good, k=None) == 1
     assert call(ffd.CacheDesc(0, 2, 128, 64)) == 1
     assert call(ffd.CacheDesc(4, 2, 96, 64)) == 2
