@@ -54,6 +54,8 @@ constexpr float kUnscale = 8589934592.0f;      // 2^(133 - kKq)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kQMax = 134217728.0f;          // 2^27
 constexpr float kRescaleMargin = 30.0f;        // lazy softmax rescaling, natural-log units
+constexpr float kMarginLog2 = kRescaleMargin * kLog2e;
+constexpr float kNoReference = -1.0e30f;       // softmax reference of a unit whose m~ is -inf
 
 // ring slot: the block's residual record (codes 64 x 128 B, already in the swizzled order, then
 // the scales 64 x 8 B; one bulk copy), V tile (channels 0-63 of the 64 rows, then channels 64-127,
@@ -851,21 +853,23 @@ __device__ __forceinline__ void scanner(const DecodeArgs &a, const Smem &S, int 
 // and heads {2tig, 2tig+1}: o[i] = {(g, 2tig), (g, 2tig+1), (g+8, 2tig), (g+8, 2tig+1)}.
 struct RefineState {
     float m0, m1, l0, l1;
+    float nl0, nl1;  // -m * log2(e): p = 2^(s log2(e) - m log2(e)) is one FMA and one EX2
     float o[2][4];
 };
 
-// Fresh state for a unit: the reference starts at its pseudo-max m~.
+// Fresh state for a unit: the reference starts at its pseudo-max m~ (a large negative finite
+// value when m~ is -inf, so that the first finite score raises it through the rescale path).
 __device__ __forceinline__ void reset_refine(RefineState &R, const UnitOps &U, int lane) {
-    R.m0 = U.mt[2 * (lane & 3)];
-    R.m1 = U.mt[2 * (lane & 3) + 1];
+    const float m0 = U.mt[2 * (lane & 3)], m1 = U.mt[2 * (lane & 3) + 1];
+    R.m0 = m0 == -INFINITY ? kNoReference : m0;
+    R.m1 = m1 == -INFINITY ? kNoReference : m1;
+    R.nl0 = -R.m0 * kLog2e;
+    R.nl1 = -R.m1 * kLog2e;
     R.l0 = R.l1 = 0.0f;
 #pragma unroll
     for (int i = 0; i < 2; i++) R.o[i][0] = R.o[i][1] = R.o[i][2] = R.o[i][3] = 0.0f;
 }
 
-__device__ __forceinline__ float safe_exp(float s, float m) {
-    return s == -INFINITY ? 0.0f : exp2f((s - m) * kLog2e);
-}
 
 // P^T fragments (bf16 hi and lo parts) of this warp's 16 rows for the PV k-step mt.
 __device__ __forceinline__ uint4 p_fragments(float p00, float p01, float p10, float p11) {
@@ -911,13 +915,14 @@ __device__ __forceinline__ void refine_block(const DecodeArgs &a, const Smem &S,
     const float s10 = v1 ? est.z + corr_score(Dr, 2, sr1, Q.qs[0], sm) : -INFINITY;
     const float s11 = v1 ? est.w + corr_score(Dr, 3, sr1, Q.qs[1], sm) : -INFINITY;
 
-    // ---- probabilities against the group's reference
-    const bool over = s00 > R.m0 + kRescaleMargin || s10 > R.m0 + kRescaleMargin ||
-                      s01 > R.m1 + kRescaleMargin || s11 > R.m1 + kRescaleMargin;
+    // ---- probabilities against the group's reference: x = (s - m) log2(e), p = 2^x
+    float x00 = fmaf(s00, kLog2e, R.nl0), x01 = fmaf(s01, kLog2e, R.nl1);
+    float x10 = fmaf(s10, kLog2e, R.nl0), x11 = fmaf(s11, kLog2e, R.nl1);
+    const bool over = fmaxf(fmaxf(x00, x01), fmaxf(x10, x11)) > kMarginLog2;
     const uint32_t any_over = __any_sync(0xffffffffu, over);
     uint4 *px = reinterpret_cast<uint4 *>(S.px + (grp * 2 + pb) * kPxBuf);
-    float p00 = safe_exp(s00, R.m0), p01 = safe_exp(s01, R.m1);
-    float p10 = safe_exp(s10, R.m0), p11 = safe_exp(s11, R.m1);
+    float p00 = ex2_approx(x00), p01 = ex2_approx(x01);
+    float p10 = ex2_approx(x10), p11 = ex2_approx(x11);
     if (any_over) {  // this warp's row maxima, for the group's new reference
         float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
@@ -944,10 +949,12 @@ __device__ __forceinline__ void refine_block(const DecodeArgs &a, const Smem &S,
                 mn1 = fmaxf(mn1, m->wmax[grp][pb][w][2 * tig + 1]);
             }
         }
-        const float al0 = R.m0 == -INFINITY ? 0.0f : exp2f((R.m0 - mn0) * kLog2e);
-        const float al1 = R.m1 == -INFINITY ? 0.0f : exp2f((R.m1 - mn1) * kLog2e);
+        const float al0 = ex2_approx((R.m0 - mn0) * kLog2e);
+        const float al1 = ex2_approx((R.m1 - mn1) * kLog2e);
         R.m0 = mn0;
         R.m1 = mn1;
+        R.nl0 = -mn0 * kLog2e;
+        R.nl1 = -mn1 * kLog2e;
         R.l0 *= al0;
         R.l1 *= al1;
 #pragma unroll
@@ -957,10 +964,10 @@ __device__ __forceinline__ void refine_block(const DecodeArgs &a, const Smem &S,
             R.o[i][2] *= al0;
             R.o[i][3] *= al1;
         }
-        p00 = safe_exp(s00, R.m0);
-        p01 = safe_exp(s01, R.m1);
-        p10 = safe_exp(s10, R.m0);
-        p11 = safe_exp(s11, R.m1);
+        p00 = ex2_approx(fmaf(s00, kLog2e, R.nl0));
+        p01 = ex2_approx(fmaf(s01, kLog2e, R.nl1));
+        p10 = ex2_approx(fmaf(s10, kLog2e, R.nl0));
+        p11 = ex2_approx(fmaf(s11, kLog2e, R.nl1));
         px[mt * 32 + lane] = p_fragments(p00, p01, p10, p11);
         named_barrier_sync(bar_id, 128);
     }
