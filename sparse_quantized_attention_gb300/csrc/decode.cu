@@ -36,6 +36,7 @@ namespace ffd {
 // group kb & 1. In a group, warp mt computes the scores of rows 16mt .. 16mt+15 and the output
 // channels 32mt .. 32mt+31 (the probabilities are exchanged through shared memory).
 constexpr int kSub = 6;              // blocks per sub-chunk (scan decision unit)
+static_assert(kSub % 2 == 0, "the scan takes blocks k and k + kSub/2 side by side");
 constexpr int kRing = 5;             // refine ring slots (residual + V of one kept block each)
 constexpr int kThumbBufs = 3;        // thumbnail buffers (sub-chunks in flight ahead of the ring)
 constexpr int kShatBufs = 2;         // provisional-score buffers (scan ahead of refinement)
@@ -825,8 +826,8 @@ __device__ __forceinline__ void scanner(const DecodeArgs &a, const Smem &S, int 
         float4 *shat = reinterpret_cast<float4 *>(S.shat + sb * kShatBuf);
         uint32_t votes = 0;
 #pragma unroll 1
-        for (int kA = 0; kA < 3 && kA < s.cnt; kA++) {
-            const int kB = kA + 3;
+        for (int kA = 0; kA < kSub / 2 && kA < s.cnt; kA++) {
+            const int kB = kA + kSub / 2;
             const float4 eA = scan_tile(tbuf + kA * kThumbBlock, r0, r1, m0, Q, sm);
             const float4 eB = scan_tile(tbuf + kB * kThumbBlock, r0, r1, m0, Q, sm);
             const int tA = (s.j0 + kA) * kPage, tB = (s.j0 + kB) * kPage;
