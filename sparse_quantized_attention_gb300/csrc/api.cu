@@ -80,7 +80,7 @@ ffd_status make_decode_plan(const ffd_decode_params *p, Plan *pl) {
     pl->m1_off = off;
     off = align_up(off + (size_t)units * pl->nf * kMaxG * sizeof(float));
     pl->part_off = off;
-    off = align_up(off + (size_t)(units + ctas) * 2 * G * kPartStride * sizeof(float));
+    off = align_up(off + (size_t)(units + ctas) * kRefineGroups * G * kPartStride * sizeof(float));
     pl->cnt_off = off;
     off = align_up(off + 2 * (size_t)units * sizeof(int));
     pl->total = off;

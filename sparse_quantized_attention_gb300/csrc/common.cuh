@@ -17,6 +17,7 @@ constexpr int kGroupSize = 32;   // channels per group
 constexpr int kThumbRow = kD / 4;  // bytes of 2-bit codes per token
 constexpr int kMaxG = 8;         // largest supported GQA group
 constexpr int kPartStride = 132; // floats per split partial: o[128], m, l, 2 pad
+constexpr int kRefineGroups = 2; // decode refine groups = split records per (CTA, unit)
 // Cache records (layout in ffd.h): thumbnail = codes [64][32] | scale [64][4] f16 | zero [64][4]
 // f16; residual = codes [64][128] (16-byte chunk j of token r at j ^ (r % 8)) | scale [64][4] f16.
 constexpr int kThumbRec = FFD_THUMB_RECORD_BYTES;
@@ -49,7 +50,7 @@ struct DecodeArgs {
     float *m_tilde;
     int *err;        // device error word
     float *ws_m1;    // [B*Hkv][nf][kMaxG] stage-1 block maxima over the sink / local tokens
-    float *ws_part;  // main-kernel split records: [B*Hkv + CTAs][2][G][kPartStride]
+    float *ws_part;  // main-kernel split records: [B*Hkv + CTAs][kRefineGroups][G][kPartStride]
     int *ws_cnt;     // [B*Hkv] merge tickets (plus a spare [B*Hkv]), zero between calls
     cudaEvent_t prof_start, prof_stop;  // optional: recorded around the main kernel
 };

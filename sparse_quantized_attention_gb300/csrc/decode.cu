@@ -32,23 +32,34 @@ namespace ffd {
 // ---- main kernel: roles ---------------------------------------------------------------------
 // Warpgroup 0: ring warp (0), page warp (1), thumbnail warp (2), one idle warp.
 // Warpgroup 1: scan warps 4-7; scan warp mt takes rows 16mt .. 16mt+15 of every block.
-// Warpgroups 2-3: refine groups 0 (warps 8-11) and 1 (warps 12-15); kept block number kb goes to
-// group kb & 1. In a group, warp mt computes the scores of rows 16mt .. 16mt+15 and the output
-// channels 32mt .. 32mt+31 (the probabilities are exchanged through shared memory).
+// Warpgroups 2..: kRefineGroups refine groups (group grp = warps 8 + 4grp .. 11 + 4grp); kept
+// block number kb goes to group kb % kRefineGroups. In a group, warp mt computes the scores of
+// rows 16mt .. 16mt+15 and the output channels 32mt .. 32mt+31 (the probabilities are exchanged
+// through shared memory).
+constexpr int gcd_c(int x, int y) { return y == 0 ? x : gcd_c(y, x % y); }
 constexpr int kSub = 6;              // blocks per sub-chunk (scan decision unit)
 static_assert(kSub % 2 == 0, "the scan takes blocks k and k + kSub/2 side by side");
 constexpr int kRing = 5;             // refine ring slots (residual + V of one kept block each)
+// Kept block kb takes ring slot kb % kRing and refine group kb % kRefineGroups; the blocks that a
+// group's fill barrier of one slot sees are kb, kb + kFillPeriod, ... (the lcm of the two).
+constexpr int kFillPeriod = kRing / gcd_c(kRing, kRefineGroups) * kRefineGroups;
 constexpr int kThumbBufs = 3;        // thumbnail buffers (sub-chunks in flight ahead of the ring)
 constexpr int kShatBufs = 2;         // provisional-score buffers (scan ahead of refinement)
 constexpr int kDepth = 8;            // ring of per-sub-chunk decision slots
 constexpr int kPageSlots = 8;        // sub-chunks whose block-table entries are resolved ahead
-constexpr int kMainThreads = 512;
-constexpr int kProducerRegs = 32;    // setmaxnreg shares: 128 x 32 + 128 x 128 + 256 x 176
-constexpr int kScanRegs = 128;       //   = 65536 = 512 threads x 128 at launch
-constexpr int kRefineRegs = 176;
-static_assert(128 * kProducerRegs + 128 * kScanRegs + 256 * kRefineRegs <= kMainThreads * 128,
+constexpr int kMainThreads = 256 + 128 * kRefineGroups;
+constexpr int kLaunchRegs = (65536 / kMainThreads) & ~7;  // per thread at launch (one CTA/SM)
+// setmaxnreg shares of the producer, scan and refine warpgroups (multiples of 8); their sum must
+// fit the launch allocation, or an increase would wait forever
+constexpr int kProducerRegs = kRefineGroups == 2 ? 32 : 24;
+constexpr int kScanRegs = kRefineGroups == 2 ? 128 : 96;
+constexpr int kRefineRegs = kRefineGroups == 2 ? 176 : 120;
+static_assert(128 * kProducerRegs + 128 * kScanRegs + 128 * kRefineGroups * kRefineRegs <=
+                  kMainThreads * kLaunchRegs,
               "register reallocation exceeds the launch allocation");
-static_assert(kScanRegs == 128, "the scan warpgroup keeps its launch allocation");
+static_assert(kScanRegs <= kLaunchRegs && kProducerRegs <= kLaunchRegs &&
+                  kRefineRegs >= kLaunchRegs, "register shares");
+
 static_assert(kDepth > kThumbBufs + 1 && kDepth > kShatBufs + kThumbBufs, "decision ring depth");
 constexpr int kKq = 100;             // q enters the MMA scaled by 2^kKq (|q| < 2^27 required)
 constexpr float kUnscale = 8589934592.0f;      // 2^(133 - kKq)
@@ -76,9 +87,9 @@ constexpr int kOffRing = 0;
 constexpr int kOffThumb = kOffRing + kRing * kSlotBytes;
 constexpr int kOffShat = kOffThumb + kThumbBufs * kThumbBuf;
 constexpr int kOffPx = kOffShat + kShatBufs * kShatBuf;      // [group][2][kPxBuf]
-constexpr int kOffUnit = kOffPx + 2 * 2 * kPxBuf;            // [2] unit operand slots
+constexpr int kOffUnit = kOffPx + kRefineGroups * 2 * kPxBuf;  // [2] unit operand slots
 constexpr int kOffMisc = kOffUnit + 2 * kUnitBytes;
-constexpr int kMiscBytes = 2048;
+constexpr int kMiscBytes = 2560;
 constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + slack to align the base to 1 KB
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kSlotBytes % 1024 == 0 && kSlotV % 1024 == 0, "swizzled TMA tiles need 1 KB");
@@ -96,10 +107,10 @@ struct Misc {
     uint32_t vote[kDepth];        // OR of the scan votes of sub-chunk t, in slot t % kDepth
     uint32_t final_mask[kDepth];  // kept blocks of sub-chunk t, published by the ring warp
     uint32_t aborted;
-    uint32_t merge_flag[2];
-    uint32_t over[2][2][4];       // refine [group][buffer][warp]: a score passed m + margin
-    float wmax[2][2][4][kMaxG];   // refine [group][buffer][warp][head]: block row maxima
-    float lsum[2][4][kMaxG];      // refine [group][warp][head]: softmax sums at a unit's end
+    uint32_t merge_flag[kRefineGroups];
+    uint32_t over[kRefineGroups][2][4];      // [group][buffer][warp]: a score passed m + margin
+    float wmax[kRefineGroups][2][4][kMaxG];  // [group][buffer][warp][head]: block row maxima
+    float lsum[kRefineGroups][4][kMaxG];     // [group][warp][head]: softmax sums at unit end
     PageSlot ps[kPageSlots];      // sub-chunk t in ps[t % kPageSlots]
     uint64_t pages_full[kPageSlots];
     uint64_t pages_empty[kPageSlots];
@@ -107,7 +118,7 @@ struct Misc {
     uint64_t decision[kDepth];    // the 4 scan warps voted on sub-chunk t
     uint64_t ring_seen[kDepth];   // the ring warp published the kept blocks of sub-chunk t
     uint64_t shat_free[kShatBufs];
-    uint64_t ring_full[2][kRing];  // [group of the block][slot]
+    uint64_t ring_full[kRefineGroups][kRing];  // [group of the block][slot]
     uint64_t ring_empty[kRing];
     uint64_t unit_ready[2];
     uint64_t unit_free[2];
@@ -412,11 +423,11 @@ __device__ __forceinline__ bool tile_passes(float4 e, bool v0, bool v1, float th
 
 // ------------------------------------------------------------------------------------------
 // Split merge: out_i = sum_r e^(m_r - M) num_r / sum_r e^(m_r - M) den_r over a unit's records.
-// Records of CTAs cf..cl, two per CTA (one per refine group), are contiguous from
-// ws_part[(u + cf) * 2]; a record holds (num[128], m, den) per head.
+// Records of CTAs cf..cl, one per refine group, are contiguous from
+// ws_part[(u + cf) * kRefineGroups]; a record holds (num[128], m, den) per head.
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ float *unit_record(const DecodeArgs &a, int u, int c, int grp) {
-    return a.ws_part + ((size_t)(u + c) * 2 + grp) * a.G * kPartStride;
+    return a.ws_part + ((size_t)(u + c) * kRefineGroups + grp) * a.G * kPartStride;
 }
 
 // Called after a __threadfence() that follows the atomic ticket showing this group came last.
@@ -425,7 +436,7 @@ __device__ __forceinline__ float *unit_record(const DecodeArgs &a, int u, int c,
 __device__ __forceinline__ void merge_unit(const DecodeArgs &a, int b, int h, int cf, int cl,
                                            int warp, int nwarps, int lane) {
     const int u = b * a.Hkv + h;
-    const int nr = 2 * (cl - cf + 1);
+    const int nr = kRefineGroups * (cl - cf + 1);
     const float *base = unit_record(a, u, cf, 0);
     const size_t rstride = (size_t)a.G * kPartStride;
     for (int i = warp; i < a.G; i += nwarps) {
@@ -731,7 +742,7 @@ __device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S
             if (round > 0) wait_bar(a, m, &m->ring_empty[slot], (round - 1) & 1);
             const int row = P.row[k];
             uint8_t *d = S.ring + slot * kSlotBytes;
-            uint64_t *bar = &m->ring_full[(kb - 1) & 1][slot];  // kb was advanced above
+            uint64_t *bar = &m->ring_full[(kb - 1) % kRefineGroups][slot];  // kb advanced above
             if (lane == 0) mbar_arrive_expect_tx(bar, kSlotTx);
             __syncwarp();
             if (lane == 0) tma_load_1d(d, a.resid + (size_t)(row / kPage) * kResidRec, kResidRec, bar);
@@ -741,11 +752,12 @@ __device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S
         if (lane == 0) mbar_arrive(&m->pages_empty[t % kPageSlots]);
     }
     // leave no copy in flight: wait for the last fill of every ring slot (block kb - 1 - i went to
-    // slot (kb - 1 - i) % kRing, the ((kb - 1 - i) / (2 kRing))-th fill of its group's barrier)
+    // slot (kb - 1 - i) % kRing, the ((kb - 1 - i) / kFillPeriod)-th fill of its group's barrier)
     if (lane == 0)
         for (int i = 0; i < kRing && i < kb; i++) {
             const int last = kb - 1 - i;
-            drain_bar(a, &m->ring_full[last & 1][last % kRing], (last / (2 * kRing)) & 1);
+            drain_bar(a, &m->ring_full[last % kRefineGroups][last % kRing],
+                      (last / kFillPeriod) & 1);
         }
 }
 
@@ -1051,7 +1063,7 @@ __device__ __forceinline__ void unit_end(const DecodeArgs &a, const Smem &S, con
     if (mt == 0 && lane == 0) {
         int *cnt = a.ws_cnt + u;
         const int old = atomicAdd(cnt, 1);
-        const uint32_t last = old == 2 * (cl - cf + 1) - 1;
+        const uint32_t last = old == kRefineGroups * (cl - cf + 1) - 1;
         if (last) *cnt = 0;  // ready for the next call
         m->merge_flag[grp] = last;
     }
@@ -1062,16 +1074,16 @@ __device__ __forceinline__ void unit_end(const DecodeArgs &a, const Smem &S, con
     }
 }
 
-// Wait until the copies of kept block kb have landed in its ring slot. The two refine groups
-// share the ring (its size is odd, so consecutive occupants of a slot belong to different groups)
-// and may drift apart; each group therefore has its own fill barrier per slot, whose consecutive
-// phases are the group's own blocks kb, kb + 2 kRing, ..., consumed in order: the parity wait is
-// exact however far the other group lags.
+// Wait until the copies of kept block kb have landed in its ring slot. The refine groups share the
+// ring (consecutive occupants of a slot may belong to different groups) and may drift apart; each
+// group therefore has its own fill barrier per slot, whose consecutive phases are the group's own
+// blocks kb, kb + kFillPeriod, ..., consumed in order: the parity wait is exact however far the
+// other groups lag.
 __device__ __forceinline__ void wait_fill(const DecodeArgs &a, Misc *m, int slot, int kb) {
-    wait_bar(a, m, &m->ring_full[kb & 1][slot], (kb / (2 * kRing)) & 1);
+    wait_bar(a, m, &m->ring_full[kb % kRefineGroups][slot], (kb / kFillPeriod) & 1);
 }
 
-// Refine warp mt of group grp: walks the schedule, takes the kept blocks with kb & 1 == grp.
+// Refine warp mt of group grp: walks the schedule, takes the kept blocks kb % kRefineGroups == grp.
 __device__ __forceinline__ void refiner(const DecodeArgs &a, const Smem &S, int cta, int ncta,
                                         int grp, int mt, int lane) {
     Misc *m = S.misc;
@@ -1105,7 +1117,7 @@ __device__ __forceinline__ void refiner(const DecodeArgs &a, const Smem &S, int 
         const float4 *shat = reinterpret_cast<const float4 *>(S.shat + (t % kShatBufs) * kShatBuf);
         for (int k = 0; k < s.cnt; k++) {
             if (!((mask >> k) & 1u)) continue;
-            if ((kb & 1) == grp) {
+            if (kb % kRefineGroups == grp) {
                 const int slot = kb % kRing;
                 wait_fill(a, m, slot, kb);
                 refine_block(a, S, S.ring + slot * kSlotBytes, Q, n, shat[(k * 4 + mt) * 32 + lane],
@@ -1162,15 +1174,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             mbar_init(&m->pages_empty[i], 2);  // thumbnail warp and ring warp
         }
         for (int i = 0; i < kThumbBufs; i++) mbar_init(&m->thumb_full[i], 1);
-        for (int i = 0; i < kShatBufs; i++) mbar_init(&m->shat_free[i], 8);  // refine warps
+        for (int i = 0; i < kShatBufs; i++) mbar_init(&m->shat_free[i], 4 * kRefineGroups);
         for (int i = 0; i < kRing; i++) {
-            mbar_init(&m->ring_full[0][i], 1);
-            mbar_init(&m->ring_full[1][i], 1);
+            for (int g = 0; g < kRefineGroups; g++) mbar_init(&m->ring_full[g][i], 1);
             mbar_init(&m->ring_empty[i], 4);  // the refine group that took the block
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(&m->unit_ready[i], 1);  // scan warp 0
-            mbar_init(&m->unit_free[i], 8);   // refine warps
+            mbar_init(&m->unit_free[i], 4 * kRefineGroups);  // refine warps
         }
         fence_barrier_init();
     }
@@ -1181,6 +1192,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         else if (warp == 1) pager(a, S, cta, ncta, lane);
         else if (warp == 2) thumb_issuer(a, S, lane);
     } else if (warp < 8) {
+        if (kScanRegs < kLaunchRegs) regs_decrease<kScanRegs>();
         scanner(a, S, cta, ncta, warp - 4, lane);
     } else {
         regs_increase<kRefineRegs>();
