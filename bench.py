@@ -1,5 +1,5 @@
 #!/usr/bin/env python3
-"""Benchmark of the FFD decode-attention step (stage 1 + fused stage 2/3 + merge) on GB300.
+"""Benchmark of the FFD decode-attention step (one kernel: stages 1-3 and the split merge) on GB300.
 
 Default workload: the Qwen2.5-7B-shaped decode step (batch 4, 28 query / 4 KV heads, 128K
 context, S=64, L=1024, delta=5), seeded synthetic inputs, N=1. Prints ONE JSON line.
@@ -39,7 +39,7 @@ L2_BYTES = 129 * 1000 ** 2
 THUMB_B = 48          # bytes per token and KV head: 32 code bytes + 4 fp16 scales + 4 fp16 zeros
 REFINE_B = 136 + 256  # int8 residual + 4 fp16 residual scales + bf16 V
 DENSE_B = 512         # bf16 K + V
-LAUNCHES_PER_DECODE = 3  # stage 1, fused stage 2/3, merge
+LAUNCHES_PER_DECODE = 1  # one cooperative kernel: stage 1, stages 2/3, split merge
 PROFILE = os.path.join(ROOT, "profiles", "ffd_main_kernel_qwen2.5-7b_128k.txt")
 
 
@@ -91,7 +91,7 @@ def step_bytes(w, seq_lens, max_blocks, kept) -> dict:
     refine = REFINE_B * kept
     return {"thumbs": thumbs, "refine": refine, "q": q, "out": out, "meta": meta,
             "step": thumbs + refine + q + out + meta,
-            "main_kernel": thumbs + refine + q + 4 * w.batch * max_blocks,
+            "main_kernel": thumbs + refine + q + out + meta,  # the step is this one kernel
             "dense_step": DENSE_B * tok_heads + q + out + meta,
             "token_heads": tok_heads}
 
@@ -411,7 +411,7 @@ def run_ours(a, rank, world, local):
                          f"{L2_BYTES / 1e6:.0f} MB L2), no flush",
                    "parallelism": "single GPU" if world == 1 else
                    f"replicas x{world} (own sequences per rank)"},
-        "roofline": {"bound": "hbm", "kernel": "ffd main (stage 2+3)",
+        "roofline": {"bound": "hbm", "kernel": "ffd main (stages 1-3, merge)",
                      "achieved": round(achieved, 1), "peak": peaks.get("hbm_gbs"),
                      "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",

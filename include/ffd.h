@@ -91,7 +91,8 @@ typedef struct {
     float delta;                /* delta of the Top-delta rule; +INFINITY keeps every block */
     float sm_scale;             /* score scale, normally 1/sqrt(head_dim) */
     int32_t num_splits;         /* 0: library's choice; else the number of KV partitions (CTAs of
-                                   the main kernel for ffd_decode_attention, splits per sequence
+                                   the main kernel for ffd_decode_attention, at most one per SM:
+                                   larger values are clamped to the SM count; splits per sequence
                                    and KV head for ffd_dense_decode) */
 } ffd_decode_params;
 
@@ -164,6 +165,9 @@ size_t ffd_decode_workspace_size(const ffd_decode_params *params);
  *               each call leaves it ready for the next one (zero-fill it again after a call that
  *               reported FFD_ERR_TIMEOUT). Calls that share a workspace must be ordered on one
  *               stream.
+ * Launch: one cooperative kernel of at most one CTA per SM whose CTAs exchange the stage-1
+ * maxima, so all of them must be resident at once; a launch that cannot be (SMs held by other
+ * work under an SM limit) fails with FFD_ERR_CUDA and enqueues nothing.
  * Errors: host-side status as listed above; FFD_ERRBIT_BOUNDS in the workspace error word when
  * a block_table entry lies outside [0, num_pages) (the block is treated as empty).
  */
@@ -196,7 +200,7 @@ ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
  * must not allocate (or synchronise the device through cudaMalloc) inside its decode loop.
  *
  * It computes exactly what ffd_decode_attention computes, with the same arguments minus the
- * workspace. Its scratch (stage-1 maxima, split records, merge tickets) is a static device array
+ * workspace. Its scratch (stage-1 maxima, split records, counters) is a static device array
  * of 4 MiB inside libffd.so, held by every GPU that loads the library until the process exits.
  * Nothing is allocated and no allocating routine is called.
  *   - Limit: parameters whose ffd_decode_workspace_size() exceeds 4 MiB are rejected with
@@ -205,7 +209,8 @@ ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
  *     (cudaGetSymbolAddress) with that device current; make that first call before any stream
  *     capture. A failed look-up returns FFD_ERR_CUDA.
  *   - Sharing: every call on a device uses the same array and it keeps the previous call's
- *     contents; each call clears the parts that must start at zero (error word, merge tickets)
+ *     contents; each call clears the parts that must start at zero (error word, merge tickets,
+ *     slot counters)
  *     on its stream. Calls whose executions overlap on the GPU race with each other: order them
  *     on one stream (or with events).
  *   - error_word: device int32 or NULL. Device-detected errors (FFD_ERRBIT_*) are OR-ed into it;
@@ -221,7 +226,7 @@ ffd_status ffd_decode_attention_static(const ffd_decode_params *params, const vo
 /*
  * ffd_set_profile_events -- optional instrumentation. While both events are non-NULL, every
  * ffd_decode_attention / ffd_dense_decode call records `start` on its stream right before its
- * main kernel (the fused stage-2/3 kernel, or the dense kernel) and `stop` right after it, so the
+ * main kernel (the fused stage-1/2/3 kernel, or the dense kernel) and `stop` right after it, so the
  * caller can time that kernel alone with cudaEventElapsedTime. The events are cudaEvent_t values
  * created and owned by the caller. Pass NULL, NULL to stop recording. Process-wide setting, not
  * synchronised: set it from the thread that issues the calls. Returns FFD_OK, or

@@ -59,18 +59,24 @@ struct Plan {
     size_t m1_off, part_off, cnt_off, total;
 };
 
-// Workspace of ffd_decode_attention: [error word | stage-1 maxima | stage-1 partials |
-// main-kernel split records | tickets]. Main records: one per (unit, CTA) pair that shares work,
-// indexed unit + cta (< units + ctas). Stage 1 has one slot per forced block (at least one).
+// Workspace of ffd_decode_attention: [error word | stage-1 maxima | split records | merge
+// tickets, stage-1 slot counters]. Split records: one per (unit, CTA) pair that shares work and
+// refine group, indexed (unit + cta) * groups + group. Stage 1 has one slot per forced block (at
+// least one).
 ffd_status make_decode_plan(const ffd_decode_params *p, Plan *pl) {
     ffd_status st = check_params(p);
     if (st != FFD_OK) return st;
     const int64_t units = (int64_t)p->batch * p->num_kv_heads;
     const int G = p->num_q_heads / p->num_kv_heads;
+    // one CTA per SM, all resident at once (the main kernel is a cooperative launch); without a
+    // device to ask, an explicit count is taken as is (a size query then errs on the large side)
+    const int sms = current_sm_count();
     int ctas = p->num_splits;
     if (ctas == 0) {
-        ctas = current_sm_count();
-        if (ctas <= 0) return FFD_ERR_CUDA;
+        if (sms <= 0) return FFD_ERR_CUDA;
+        ctas = sms;
+    } else if (sms > 0 && ctas > sms) {
+        ctas = sms;
     }
     pl->ctas = ctas;
     pl->splits = pl->bps = 0;
@@ -82,7 +88,7 @@ ffd_status make_decode_plan(const ffd_decode_params *p, Plan *pl) {
     pl->part_off = off;
     off = align_up(off + (size_t)(units + ctas) * kRefineGroups * G * kPartStride * sizeof(float));
     pl->cnt_off = off;
-    off = align_up(off + 2 * (size_t)units * sizeof(int));
+    off = align_up(off + 3 * (size_t)units * sizeof(int));
     pl->total = off;
     return FFD_OK;
 }
@@ -325,7 +331,7 @@ ffd_status ffd_decode_attention_static(const ffd_decode_params *params, const vo
     // the in-kernel merge must start at zero.
     const size_t units = (size_t)params->batch * params->num_kv_heads;
     if (cudaMemsetAsync(ws, 0, kAlign, s) != cudaSuccess ||
-        cudaMemsetAsync(static_cast<char *>(ws) + pl.cnt_off, 0, 2 * units * sizeof(int), s) !=
+        cudaMemsetAsync(static_cast<char *>(ws) + pl.cnt_off, 0, 3 * units * sizeof(int), s) !=
             cudaSuccess)
         return FFD_ERR_CUDA;
     DecodeArgs a = make_args(params, pl, ws);

@@ -424,176 +424,190 @@ __device__ __forceinline__ bool tile_passes(float4 e, bool v0, bool v1, float th
 // ------------------------------------------------------------------------------------------
 // Split merge: out_i = sum_r e^(m_r - M) num_r / sum_r e^(m_r - M) den_r over a unit's records.
 // Records of CTAs cf..cl, one per refine group, are contiguous from
-// ws_part[(u + cf) * kRefineGroups]; a record holds (num[128], m, den) per head.
+// ws_part[(u + cf) * kRefineGroups]; a record holds (num[128], m, den) per head. Counters in
+// ws_cnt: [0, units) merge tickets, [units, 2 units) stage-1 slots, [2 units, 3 units) mergers
+// done.
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ float *unit_record(const DecodeArgs &a, int u, int c, int grp) {
     return a.ws_part + ((size_t)(u + c) * kRefineGroups + grp) * a.G * kPartStride;
 }
 
-// Called after a __threadfence() that follows the atomic ticket showing this group came last.
-// Warp w of nwarps merges heads w, w + nwarps, ...: lane r owns record r's maximum, weight and
-// denominator; every lane accumulates 4 of the 128 channels, loading 8 records at a time.
-__device__ __forceinline__ void merge_unit(const DecodeArgs &a, int b, int h, int cf, int cl,
-                                           int warp, int nwarps, int lane) {
+// Merge of head i of a unit by one refine group (128 threads, thread = output channel), after
+// every record of the unit is written. Records are loaded in independent batches: the maxima
+// (lane r loads record r), then 16 records at a time whose weights, denominators and channel
+// values are loaded together.
+__device__ __forceinline__ void merge_head(const DecodeArgs &a, int b, int h, int cf, int cl, int i,
+                                           int mt, int lane) {
     const int u = b * a.Hkv + h;
     const int nr = kRefineGroups * (cl - cf + 1);
-    const float *base = unit_record(a, u, cf, 0);
     const size_t rstride = (size_t)a.G * kPartStride;
-    for (int i = warp; i < a.G; i += nwarps) {
-        const float *hb = base + (size_t)i * kPartStride;
-        float M = -INFINITY;
-        for (int r = lane; r < nr; r += 32) M = fmaxf(M, __ldcg(hb + r * rstride + kD));
-        M = warp_max(M);
-        float num[4] = {0.0f, 0.0f, 0.0f, 0.0f}, den = 0.0f;
-        if (M != -INFINITY) {
-            for (int r0 = 0; r0 < nr; r0 += 32) {
-                const int r = r0 + lane;
-                float f = 0.0f;
-                if (r < nr) {
-                    const float mr = __ldcg(hb + r * rstride + kD);
-                    if (mr != -INFINITY) {
-                        f = exp2f((mr - M) * kLog2e);
-                        den = fmaf(f, __ldcg(hb + r * rstride + kD + 1), den);
-                    }
-                }
-                const int cnt = nr - r0 < 32 ? nr - r0 : 32;
-                for (int j0 = 0; j0 < cnt; j0 += 8) {
-                    float x[8][4];
+    const float *hb = unit_record(a, u, cf, 0) + (size_t)i * kPartStride;
+    const int ch = 32 * mt + lane;
+    float M = -INFINITY;
+    for (int r = lane; r < nr; r += 32) M = fmaxf(M, __ldcg(hb + r * rstride + kD));
+    M = warp_max(M);
+    float num = 0.0f, den = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll 1
+        for (int r0 = 0; r0 < nr; r0 += 16) {
+            const int cnt = nr - r0 < 16 ? nr - r0 : 16;
+            const float *own = hb + (size_t)(r0 + (lane < cnt ? lane : 0)) * rstride;
+            const float mr = lane < cnt ? __ldcg(own + kD) : -INFINITY;
+            const float dr = lane < cnt ? __ldcg(own + kD + 1) : 0.0f;
+            float x[16];
 #pragma unroll
-                    for (int j = 0; j < 8; j++) {
-                        const float *p = hb + (size_t)(r0 + (j0 + j < cnt ? j0 + j : 0)) * rstride;
+            for (int j = 0; j < 16; j++)
+                x[j] = __ldcg(hb + (size_t)(r0 + (j < cnt ? j : 0)) * rstride + ch);
+            const float f = mr == -INFINITY ? 0.0f : exp2f((mr - M) * kLog2e);
+            den = fmaf(f, dr, den);
 #pragma unroll
-                        for (int k = 0; k < 4; k++) x[j][k] = __ldcg(p + lane + 32 * k);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 8; j++) {
-                        const float fj = __shfl_sync(0xffffffffu, f, (j0 + j) & 31);
-                        if (j0 + j < cnt && fj > 0.0f) {
-#pragma unroll
-                            for (int k = 0; k < 4; k++) num[k] = fmaf(fj, x[j][k], num[k]);
-                        }
-                    }
-                }
+            for (int j = 0; j < 16; j++) {
+                const float fj = __shfl_sync(0xffffffffu, f, j);
+                if (j < cnt) num = fmaf(fj, x[j], num);
             }
-            den = warp_sum(den);
         }
-        float *o = a.out + ((size_t)b * a.Hq + h * a.G + i) * kD;
-#pragma unroll
-        for (int k = 0; k < 4; k++) o[lane + 32 * k] = den > 0.0f ? num[k] / den : 0.0f;
-        if (a.m_tilde) {
-            float m = -INFINITY;
-            for (int sl = lane; sl < a.nf; sl += 32)
-                m = fmaxf(m, __ldcg(a.ws_m1 + ((size_t)u * a.nf + sl) * kMaxG + i));
-            m = warp_max(m);
-            if (lane == 0) a.m_tilde[(size_t)b * a.Hq + h * a.G + i] = m;
-        }
+        den = warp_sum(den);
+    }
+    a.out[((size_t)b * a.Hq + h * a.G + i) * kD + ch] = den > 0.0f ? num / den : 0.0f;
+    if (a.m_tilde && mt == 0) {  // the reported pseudo-max, from the stage-1 slots
+        float mx = -INFINITY;
+        for (int sl = lane; sl < a.nf; sl += 32)
+            mx = fmaxf(mx, __ldcg(a.ws_m1 + ((size_t)u * a.nf + sl) * kMaxG + i));
+        mx = warp_max(mx);
+        if (lane == 0) a.m_tilde[(size_t)b * a.Hq + h * a.G + i] = mx;
     }
 }
 
 // ------------------------------------------------------------------------------------------
-// Stage 1 (pseudo-max): one CTA per (forced-block slot, unit); warp w takes 16 tokens of the
-// block. Exact scores s = sm q . K^ (thumbnail + residual, on tensor cores) of the block's sink
-// and local tokens; their per-head maximum goes to ws_m1 (the pseudo-max m~ of a unit is the
-// maximum over its slots). Slot 0 of every unit also clears the keep-mask tail past the sequence
-// and, for an empty sequence (which the main kernel never visits), writes the zero output and
-// m~ = -inf.
+// Stage 1 (pseudo-max), run by the refine groups at the start of the main kernel, before any
+// block reaches them. The (unit, forced-block slot) pairs are dealt round-robin to the
+// ncta * kRefineGroups groups of the grid; in a group, warp mt takes rows 16mt .. 16mt+15 of the
+// slot's block. Exact scores s = sm q . K^ (thumbnail + residual, on tensor cores) of the block's
+// sink and local tokens; their per-head maximum goes to ws_m1 (the pseudo-max m~ of a unit is the
+// maximum over its slots), then the unit's slot counter is raised. Scan warp 0 of every CTA that
+// walks the unit waits for all of its slots before it sets the thresholds. Slot 0 of every unit
+// also clears the keep-mask tail past the sequence and, for an empty sequence (which no CTA
+// walks, so its counter stays at zero), writes the zero output and m~ = -inf.
 // ------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(128, 1) stage1_kernel(const DecodeArgs a) {
-    grid_launch_dependents();
-    __shared__ float red_m[4][kMaxG];
-    const int u = blockIdx.y, b = u / a.Hkv, h = u % a.Hkv;
-    const int slot = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ __forceinline__ int *slot_counter(const DecodeArgs &a, int u) {
+    return a.ws_cnt + a.B * a.Hkv + u;
+}
+
+__device__ __forceinline__ int *done_counter(const DecodeArgs &a, int u) {
+    return a.ws_cnt + 2 * a.B * a.Hkv + u;
+}
+
+__device__ __forceinline__ void pseudo_max_slots(const DecodeArgs &a, Misc *m, int cta, int nctas,
+                                                 int grp, int mt, int lane) {
+    const int units = a.B * a.Hkv;
+    const int nz = units * a.nf;
+    const int workers = nctas * kRefineGroups;
+    const int tid = 32 * mt + lane;
     const int g = lane >> 2, tig = lane & 3;
-    const int raw_n = a.seq_lens[b];
-    const int n = len_of(a, b);
-    const int nb = (n + kPage - 1) / kPage;
-    if (slot == 0) {
-        if (tid == 0 && h == 0 && raw_n != n) raise_error(a.err, FFD_ERRBIT_BOUNDS);
-        if (a.keep_mask)
-            for (int blk = nb + tid; blk < a.max_blocks; blk += blockDim.x)
-                a.keep_mask[(size_t)u * a.max_blocks + blk] = 0;
-        if (n == 0) {
-            for (int idx = tid; idx < a.G * kD; idx += blockDim.x)
-                a.out[((size_t)b * a.Hq + h * a.G) * kD + idx] = 0.0f;
-            if (a.m_tilde && tid < a.G) a.m_tilde[(size_t)b * a.Hq + h * a.G + tid] = -INFINITY;
+    int it = 0;
+    for (int z = cta * kRefineGroups + grp; z < nz; z += workers, it++) {
+        const int u = z / a.nf, slot = z % a.nf;
+        const int b = u / a.Hkv, h = u % a.Hkv;
+        // the query operands do not depend on the page: their loads overlap the two dependent
+        // loads (sequence length, then block table) that locate the block
+        ThumbOps Q;
+        ResidOps QR;
+        load_thumb_ops(a, b, h, lane, Q);
+        load_resid_ops(a, b, h, lane, QR);
+        const int raw_n = a.seq_lens[b];
+        const int n = len_of(a, b);
+        const int nb = (n + kPage - 1) / kPage;
+        if (slot == 0) {
+            if (tid == 0 && h == 0 && raw_n != n) raise_error(a.err, FFD_ERRBIT_BOUNDS);
+            if (a.keep_mask)
+                for (int blk = nb + tid; blk < a.max_blocks; blk += 128)
+                    a.keep_mask[(size_t)u * a.max_blocks + blk] = 0;
+            if (n == 0) {
+                for (int idx = tid; idx < a.G * kD; idx += 128)
+                    a.out[((size_t)b * a.Hq + h * a.G) * kD + idx] = 0.0f;
+                if (a.m_tilde && tid < a.G)
+                    a.m_tilde[(size_t)b * a.Hq + h * a.G + tid] = -INFINITY;
+            }
         }
-    }
-    const ForcedBlocks fb(n, a.S, a.L);
-    float *mdst = a.ws_m1 + ((size_t)u * a.nf + slot) * kMaxG;
-    int page = -1;
-    const int blk = slot < fb.count ? fb.block(slot) : 0;
-    if (slot < fb.count) {
-        page = a.block_table[(size_t)b * a.max_blocks + blk];
-        if (page < 0 || page >= a.P) page = -1;  // flagged by the main kernel's page warp
-    }
-    if (page < 0) {  // empty slot (uniform across the CTA)
-        if (tid < kMaxG) mdst[tid] = -INFINITY;
-        return;
-    }
-    ThumbOps Q;
-    ResidOps QR;
-    load_thumb_ops(a, b, h, lane, Q);
-    load_resid_ops(a, b, h, lane, QR);
-    const size_t tile = (size_t)page * a.Hkv + h;
-    const uint8_t *trec = a.thumb + tile * kThumbRec;
-    const uint8_t *rrec = a.resid + tile * kResidRec;
-    const int r0 = 16 * warp + g, r1 = r0 + 8;
-    uint32_t w0[8], w1[8];
-    {
-        const uint4 *c0 = reinterpret_cast<const uint4 *>(trec + r0 * kThumbRow);
-        const uint4 *c1 = reinterpret_cast<const uint4 *>(trec + r1 * kThumbRow);
-        const uint4 p0 = c0[0], p1 = c0[1], p2 = c1[0], p3 = c1[1];
-        w0[0] = p0.x; w0[1] = p0.y; w0[2] = p0.z; w0[3] = p0.w;
-        w0[4] = p1.x; w0[5] = p1.y; w0[6] = p1.z; w0[7] = p1.w;
-        w1[0] = p2.x; w1[1] = p2.y; w1[2] = p2.z; w1[3] = p2.w;
-        w1[4] = p3.x; w1[5] = p3.y; w1[6] = p3.z; w1[7] = p3.w;
-    }
-    uint2 x0[4], x1[4];
+        if (n == 0) continue;  // uniform across the group; nobody waits for this unit
+        const ForcedBlocks fb(n, a.S, a.L);
+        float *mdst = a.ws_m1 + ((size_t)u * a.nf + slot) * kMaxG;
+        int page = -1;
+        const int blk = slot < fb.count ? fb.block(slot) : 0;
+        if (slot < fb.count) {
+            page = a.block_table[(size_t)b * a.max_blocks + blk];
+            if (page < 0 || page >= a.P) page = -1;  // flagged by the page warp
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+        if (page >= 0) {  // uniform across the group
+            const size_t tile = (size_t)page * a.Hkv + h;
+            const uint8_t *trec = a.thumb + tile * kThumbRec;
+            const uint8_t *rrec = a.resid + tile * kResidRec;
+            const int r0 = 16 * mt + g, r1 = r0 + 8;
+            uint32_t w0[8], w1[8];
+            {
+                const uint4 *c0 = reinterpret_cast<const uint4 *>(trec + r0 * kThumbRow);
+                const uint4 *c1 = reinterpret_cast<const uint4 *>(trec + r1 * kThumbRow);
+                const uint4 p0 = c0[0], p1 = c0[1], p2 = c1[0], p3 = c1[1];
+                w0[0] = p0.x; w0[1] = p0.y; w0[2] = p0.z; w0[3] = p0.w;
+                w0[4] = p1.x; w0[5] = p1.y; w0[6] = p1.z; w0[7] = p1.w;
+                w1[0] = p2.x; w1[1] = p2.y; w1[2] = p2.z; w1[3] = p2.w;
+                w1[4] = p3.x; w1[5] = p3.y; w1[6] = p3.z; w1[7] = p3.w;
+            }
+            uint2 x0[4], x1[4];
 #pragma unroll
-    for (int gg = 0; gg < 4; gg++) {
-        x0[gg] = *reinterpret_cast<const uint2 *>(rrec + resid_offset(r0, 32 * gg + 8 * tig));
-        x1[gg] = *reinterpret_cast<const uint2 *>(rrec + resid_offset(r1, 32 * gg + 8 * tig));
-    }
-    float sf0[4], sf1[4], zf0[4], zf1[4], sr0[4], sr1[4];
-    const uint2 *ts = reinterpret_cast<const uint2 *>(trec + kThumbScaleOff);
-    const uint2 *tz = reinterpret_cast<const uint2 *>(trec + kThumbZeroOff);
-    const uint2 *rs = reinterpret_cast<const uint2 *>(rrec + kResidScaleOff);
-    unpack4h(ts[r0], sf0);
-    unpack4h(ts[r1], sf1);
-    unpack4h(tz[r0], zf0);
-    unpack4h(tz[r1], zf1);
-    unpack4h(rs[r0], sr0);
-    unpack4h(rs[r1], sr1);
-    float D[4][4], Dr[4][4];
-    thumb_mma(D, w0, w1, 0x00030003u << (2 * tig), Q);
-    resid_mma(Dr, x0, x1, QR);
-    const float sm = a.sm_scale;
-    const int t0 = blk * kPage + r0, t1 = blk * kPage + r1;
-    // pseudo-max candidates: sink and local tokens inside the sequence
-    const bool v0 = t0 < n && (t0 < a.S || t0 >= n - a.L);
-    const bool v1 = t1 < n && (t1 < a.S || t1 >= n - a.L);
-    const float s00 = v0 ? est_score(D, 0, sf0, zf0, Q.qs[0], sm) + corr_score(Dr, 0, sr0, Q.qs[0], sm) : -INFINITY;
-    const float s01 = v0 ? est_score(D, 1, sf0, zf0, Q.qs[1], sm) + corr_score(Dr, 1, sr0, Q.qs[1], sm) : -INFINITY;
-    const float s10 = v1 ? est_score(D, 2, sf1, zf1, Q.qs[0], sm) + corr_score(Dr, 2, sr1, Q.qs[0], sm) : -INFINITY;
-    const float s11 = v1 ? est_score(D, 3, sf1, zf1, Q.qs[1], sm) + corr_score(Dr, 3, sr1, Q.qs[1], sm) : -INFINITY;
-    float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+            for (int gg = 0; gg < 4; gg++) {
+                x0[gg] = *reinterpret_cast<const uint2 *>(rrec + resid_offset(r0, 32 * gg + 8 * tig));
+                x1[gg] = *reinterpret_cast<const uint2 *>(rrec + resid_offset(r1, 32 * gg + 8 * tig));
+            }
+            float sf0[4], sf1[4], zf0[4], zf1[4], sr0[4], sr1[4];
+            const uint2 *ts = reinterpret_cast<const uint2 *>(trec + kThumbScaleOff);
+            const uint2 *tz = reinterpret_cast<const uint2 *>(trec + kThumbZeroOff);
+            const uint2 *rs = reinterpret_cast<const uint2 *>(rrec + kResidScaleOff);
+            unpack4h(ts[r0], sf0);
+            unpack4h(ts[r1], sf1);
+            unpack4h(tz[r0], zf0);
+            unpack4h(tz[r1], zf1);
+            unpack4h(rs[r0], sr0);
+            unpack4h(rs[r1], sr1);
+            float D[4][4], Dr[4][4];
+            thumb_mma(D, w0, w1, 0x00030003u << (2 * tig), Q);
+            resid_mma(Dr, x0, x1, QR);
+            const float sm = a.sm_scale;
+            const int t0 = blk * kPage + r0, t1 = blk * kPage + r1;
+            // pseudo-max candidates: sink and local tokens inside the sequence
+            const bool v0 = t0 < n && (t0 < a.S || t0 >= n - a.L);
+            const bool v1 = t1 < n && (t1 < a.S || t1 >= n - a.L);
+            const float s00 = v0 ? est_score(D, 0, sf0, zf0, Q.qs[0], sm) + corr_score(Dr, 0, sr0, Q.qs[0], sm) : -INFINITY;
+            const float s01 = v0 ? est_score(D, 1, sf0, zf0, Q.qs[1], sm) + corr_score(Dr, 1, sr0, Q.qs[1], sm) : -INFINITY;
+            const float s10 = v1 ? est_score(D, 2, sf1, zf1, Q.qs[0], sm) + corr_score(Dr, 2, sr1, Q.qs[0], sm) : -INFINITY;
+            const float s11 = v1 ? est_score(D, 3, sf1, zf1, Q.qs[1], sm) + corr_score(Dr, 3, sr1, Q.qs[1], sm) : -INFINITY;
+            mx0 = fmaxf(s00, s10);
+            mx1 = fmaxf(s01, s11);
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+        }
+        float (&red)[4][kMaxG] = m->wmax[grp][it & 1];
+        if (g == 0) {
+            red[mt][2 * tig] = mx0;
+            red[mt][2 * tig + 1] = mx1;
+        }
+        named_barrier_sync(2 + grp, 128);
+        if (tid < kMaxG) {
+            mdst[tid] = tid < a.G ? fmaxf(fmaxf(red[0][tid], red[1][tid]),
+                                          fmaxf(red[2][tid], red[3][tid]))
+                                  : -INFINITY;
+            __threadfence();
+        }
+        named_barrier_sync(2 + grp, 128);
+        if (tid == 0) atomicAdd(slot_counter(a, u), 1);
     }
-    if (g == 0) {
-        red_m[warp][2 * tig] = mx0;
-        red_m[warp][2 * tig + 1] = mx1;
-    }
-    __syncthreads();
-    if (tid < kMaxG)
-        mdst[tid] = tid < a.G ? fmaxf(fmaxf(red_m[0][tid], red_m[1][tid]),
-                                      fmaxf(red_m[2][tid], red_m[3][tid]))
-                              : -INFINITY;
+    // the reduction buffers are the refine warps' block-maxima buffers
+    named_barrier_sync(2 + grp, 128);
 }
-
 
 // ------------------------------------------------------------------------------------------
 // Main kernel: waits and the copy warps.
@@ -628,6 +642,22 @@ __device__ __forceinline__ void drain_bar(const DecodeArgs &a, uint64_t *bar, ui
 
 __device__ __forceinline__ bool aborted(Misc *m) {
     return *reinterpret_cast<volatile uint32_t *>(&m->aborted) != 0;
+}
+
+// Bounded wait until the global counter *c reaches target (written by other CTAs, which the
+// cooperative launch keeps resident).
+__device__ __forceinline__ void wait_count(const DecodeArgs &a, Misc *m, const int *c, int target) {
+    if (ld_acquire_gpu(c) >= target) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(c) < target) {
+        if (aborted(m)) return;
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            raise_error(a.err, FFD_ERRBIT_TIMEOUT);
+            *reinterpret_cast<volatile uint32_t *>(&m->aborted) = 1;
+            return;
+        }
+        __nanosleep(32);
+    }
 }
 
 // Page warp: walks the CTA's schedule ahead of the copy warps and resolves the block-table entries
@@ -765,7 +795,7 @@ __device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S
 // Scan warps (stage 2).
 // ------------------------------------------------------------------------------------------
 // Scan warp 0 computes the unit's query operands and thresholds into a unit slot.
-__device__ __forceinline__ void fill_unit(const DecodeArgs &a, UnitOps &U, int b, int h,
+__device__ __forceinline__ void fill_unit(const DecodeArgs &a, Misc *m, UnitOps &U, int b, int h,
                                           int lane) {
     const int g = lane >> 2, tig = lane & 3;
     ThumbOps T;
@@ -786,8 +816,9 @@ __device__ __forceinline__ void fill_unit(const DecodeArgs &a, UnitOps &U, int b
     if (lane < kMaxG) {
         float mx = -INFINITY;
         const int u = b * a.Hkv + h;
+        wait_count(a, m, slot_counter(a, u), a.nf);  // every stage-1 slot of the unit is in
         for (int sl = 0; sl < a.nf; sl++)
-            mx = fmaxf(mx, a.ws_m1[((size_t)u * a.nf + sl) * kMaxG + lane]);
+            mx = fmaxf(mx, __ldcg(a.ws_m1 + ((size_t)u * a.nf + sl) * kMaxG + lane));
         U.mt[lane] = mx;
         U.thr[lane] = lane < a.G ? mx - a.delta : INFINITY;
     }
@@ -809,7 +840,6 @@ __device__ __forceinline__ void scanner(const DecodeArgs &a, const Smem &S, int 
     Sched sch;
     sch.init(a, cta, ncta);
     Sub s;
-    grid_dependency_wait();  // stage-1 maxima are visible from here on
     ThumbOps Q;  // the unit's thumbnail B fragments, query sums and thresholds, in registers
     float thr0 = 0.0f, thr1 = 0.0f;
     int n = 0;
@@ -819,7 +849,7 @@ __device__ __forceinline__ void scanner(const DecodeArgs &a, const Smem &S, int 
             ui++;
             const int us = ui & 1;
             if (ui >= 2) wait_bar(a, m, &m->unit_free[us], ((ui >> 1) - 1) & 1);
-            if (mt == 0) fill_unit(a, S.unit[us], s.b, s.h, lane);
+            if (mt == 0) fill_unit(a, m, S.unit[us], s.b, s.h, lane);
             named_barrier_sync(1, 128);
             if (mt == 0 && lane == 0) mbar_arrive(&m->unit_ready[us]);
             const UnitOps &U = S.unit[us];
@@ -1008,8 +1038,9 @@ __device__ __forceinline__ void refine_block(const DecodeArgs &a, const Smem &S,
 }
 
 // End of this CTA's segment of a unit, refine group grp: the group's softmax sums, its record
-// (each warp writes its channels), and the atomic ticket; the last group of the unit's CTAs
-// merges all records of the unit into the output (no waiting).
+// (each warp writes its channels), and the atomic ticket. The last min(G, groups of the unit)
+// groups to take a ticket wait for the remaining ones (only groups that are already finishing
+// the unit, or earlier units) and split the merge by head.
 __device__ __forceinline__ void unit_end(const DecodeArgs &a, const Smem &S, const Sub &s,
                                          const RefineState &R, int cta, int ncta, int64_t T,
                                          int grp, int mt, int lane) {
@@ -1060,17 +1091,28 @@ __device__ __forceinline__ void unit_end(const DecodeArgs &a, const Smem &S, con
     named_barrier_sync(bar_id, 128);
     const int64_t first = s.x0 - s.j0;  // global index of the unit's first block
     const int cf = cta_of(first, T, ncta), cl = cta_of(first + s.nblk - 1, T, ncta);
+    const int target = kRefineGroups * (cl - cf + 1);
+    // the last nm groups to finish merge the unit, head i by merger i % nm
+    const int nm = a.G < target ? a.G : target;
     if (mt == 0 && lane == 0) {
-        int *cnt = a.ws_cnt + u;
-        const int old = atomicAdd(cnt, 1);
-        const uint32_t last = old == kRefineGroups * (cl - cf + 1) - 1;
-        if (last) *cnt = 0;  // ready for the next call
-        m->merge_flag[grp] = last;
+        const int old = atomicAdd(a.ws_cnt + u, 1);
+        m->merge_flag[grp] = old >= target - nm ? (uint32_t)(old - (target - nm) + 1) : 0u;
     }
     named_barrier_sync(bar_id, 128);
-    if (m->merge_flag[grp]) {
-        __threadfence();
-        merge_unit(a, s.b, s.h, cf, cl, mt, 4, lane);
+    const int rank = (int)m->merge_flag[grp] - 1;
+    if (rank < 0) return;
+    // wait for the others (the last ones of the unit, already past their final block)
+    if (mt == 0 && lane == 0) wait_count(a, m, a.ws_cnt + u, target);
+    named_barrier_sync(bar_id, 128);
+    __threadfence();
+    for (int i = rank; i < a.G; i += nm) merge_head(a, s.b, s.h, cf, cl, i, mt, lane);
+    if (mt == 0 && lane == 0) {
+        // every merger has seen the full ticket: the last one clears the counters for the next call
+        if (atomicAdd(done_counter(a, u), 1) == nm - 1) {
+            a.ws_cnt[u] = 0;
+            *slot_counter(a, u) = 0;
+            *done_counter(a, u) = 0;
+        }
     }
 }
 
@@ -1090,7 +1132,6 @@ __device__ __forceinline__ void refiner(const DecodeArgs &a, const Smem &S, int 
     Sched sch;
     sch.init(a, cta, ncta);
     Sub s;
-    grid_dependency_wait();
     RefineState R;
     ResidOps Q;  // the unit's residual B fragments and query sums, kept in registers
     int n = 0;
@@ -1156,10 +1197,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     S.misc = reinterpret_cast<Misc *>(base + kOffMisc);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // CTAs 0 .. ncta-1 walk the blocks; every CTA of the grid takes part in stage 1 (which also
+    // writes the results of empty sequences, so it runs when no CTA walks anything)
     const int64_t T = total_blocks(a);
     const int ncta = (int)(T < (int64_t)gridDim.x ? T : (int64_t)gridDim.x);
     const int cta = blockIdx.x;
-    if (cta >= ncta) return;
+    const bool walker = cta < ncta;
 
     if (threadIdx.x == 0) {
         Misc *m = S.misc;
@@ -1188,15 +1231,17 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     __syncthreads();
     if (warp < 4) {
         regs_decrease<kProducerRegs>();
+        if (!walker) return;
         if (warp == 0) ring_issuer(prm, S, lane);
         else if (warp == 1) pager(a, S, cta, ncta, lane);
         else if (warp == 2) thumb_issuer(a, S, lane);
     } else if (warp < 8) {
         if (kScanRegs < kLaunchRegs) regs_decrease<kScanRegs>();
-        scanner(a, S, cta, ncta, warp - 4, lane);
+        if (walker) scanner(a, S, cta, ncta, warp - 4, lane);
     } else {
         regs_increase<kRefineRegs>();
-        refiner(a, S, cta, ncta, (warp - 8) >> 2, warp & 3, lane);
+        pseudo_max_slots(a, S.misc, cta, gridDim.x, (warp - 8) >> 2, warp & 3, lane);
+        if (walker) refiner(a, S, cta, ncta, (warp - 8) >> 2, warp & 3, lane);
     }
 }
 
@@ -1246,21 +1291,19 @@ cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t strea
     if (!make_v_map(&prm.tm_v, const_cast<__nv_bfloat16 *>(a.v), rows))
         return cudaErrorInvalidValue;
 
-    stage1_kernel<<<dim3(a.nf > 0 ? a.nf : 1, a.B * a.Hkv), 128, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     if (a.prof_start) cudaEventRecord(a.prof_start, stream);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(main_ctas);
     cfg.blockDim = dim3(kMainThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
+    // scan warps wait for stage-1 slots computed by other CTAs: all CTAs must be resident
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, main_kernel, prm);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, main_kernel, prm);
     if (e != cudaSuccess) return e;
     if (a.prof_stop) cudaEventRecord(a.prof_stop, stream);
     return cudaGetLastError();

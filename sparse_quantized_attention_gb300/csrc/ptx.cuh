@@ -1,5 +1,5 @@
 // ptx.cuh -- inline-PTX helpers for sm_103a: mbarriers, TMA (bulk and tensor copies), warp-level
-// tensor-core MMA, ldmatrix / movmatrix, named barriers and programmatic dependent launch.
+// tensor-core MMA, ldmatrix / movmatrix, named barriers and register reallocation.
 #pragma once
 
 #include <cuda.h>
@@ -47,6 +47,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+// Acquire load at GPU scope (pairs with a __threadfence() before the writer's atomic).
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // Nanosecond wall clock of the GPU.
@@ -133,7 +140,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
-// ---- barriers, launch control ---------------------------------------------------------------
+// ---- barriers, register shares --------------------------------------------------------------
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -148,16 +155,6 @@ __device__ __forceinline__ void regs_increase() {
 template <int kRegs>
 __device__ __forceinline__ void regs_decrease() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-
-// Programmatic dependent launch: wait until the preceding kernel's results are visible.
-__device__ __forceinline__ void grid_dependency_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-// Allow the dependent kernel to start launching.
-__device__ __forceinline__ void grid_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace ffd
