@@ -27,7 +27,8 @@
  * bit-defined; everything in attention is fp64. Build with -ffp-contract=off: every fused
  * multiply-add below is written as fma()/fmaf() on purpose and no other may be formed.
  *
- * Memory layout of the cache (shared with the CUDA library only through this written spec):
+ * The oracle's own layout of the quantised cache (plain arrays; the tests unpack the library's
+ * per-tile records, whose layout include/ffd.h states, into it):
  *   k, v      bf16 bits   [P][Hkv][64][128]
  *   thumb     u8          [P][Hkv][64][32]   channel c -> byte c/4, bits 2*(c%4)..2*(c%4)+1
  *   t_scale   f16 bits    [P][Hkv][64][4]    one per group of 32 channels
