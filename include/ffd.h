@@ -90,10 +90,10 @@ typedef struct {
     int32_t local_tokens;       /* L >= 0: tokens n-L .. n-1 are local tokens */
     float delta;                /* delta of the Top-delta rule; +INFINITY keeps every block */
     float sm_scale;             /* score scale, normally 1/sqrt(head_dim) */
-    int32_t num_splits;         /* 0: library's choice; else the number of KV partitions (CTAs of
-                                   the main kernel for ffd_decode_attention, at most one per SM:
-                                   larger values are clamped to the SM count; splits per sequence
-                                   and KV head for ffd_dense_decode) */
+    int32_t num_splits;         /* 0: library's choice (one per SM); else the number of KV
+                                   partitions, i.e. the CTAs of the persistent kernel of
+                                   ffd_decode_attention or ffd_dense_decode, at most one per SM:
+                                   larger values are clamped to the SM count */
 } ffd_decode_params;
 
 /* Human-readable name of a status. Never NULL. */
@@ -185,7 +185,8 @@ size_t ffd_dense_workspace_size(const ffd_decode_params *params);
  * out_i = softmax_j(sm_scale * q_i . K_j) V over every token j < n, with the original bf16 keys.
  * Source: the pages compare FFD against FlashAttention-2 decoding (Main results, kernel speedup
  * and end-to-end throughput). sink_tokens, local_tokens and delta are ignored.
- *   k_bf16, v_bf16  device bf16 [P][Hkv][64][128]; other arguments as in ffd_decode_attention.
+ *   k_bf16, v_bf16  device bf16 [P][Hkv][64][128]; other arguments as in ffd_decode_attention
+ *   (the workspace rules and the cooperative launch included).
  */
 ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
                             const void *k_bf16, const void *v_bf16, const int32_t *seq_lens,

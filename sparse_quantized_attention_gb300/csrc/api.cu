@@ -11,7 +11,7 @@ cudaError_t launch_quantize(int P, int Hkv, const int32_t *page_ids, int num_pag
                             const void *k, uint8_t *thumb, uint8_t *resid, int *err,
                             cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t stream);
-cudaError_t launch_dense(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_dense(const DecodeArgs &a, int ctas, cudaStream_t stream);
 }  // namespace ffd
 
 using namespace ffd;
@@ -19,7 +19,6 @@ using namespace ffd;
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kCtasPerSm = 4;  // target resident CTAs per SM for the split count
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -54,8 +53,8 @@ ffd_status check_params(const ffd_decode_params *p) {
 }
 
 struct Plan {
-    int splits, bps, nf;  // dense: splits per unit and blocks per split; decode: nf slots
-    int ctas;             // decode: CTAs of the main kernel
+    int nf;    // stage-1 slots per unit (FFD step)
+    int ctas;  // CTAs of the persistent kernel
     size_t m1_off, part_off, cnt_off, total;
 };
 
@@ -79,7 +78,6 @@ ffd_status make_decode_plan(const ffd_decode_params *p, Plan *pl) {
         ctas = sms;
     }
     pl->ctas = ctas;
-    pl->splits = pl->bps = 0;
     const int nf = max_forced_blocks(p->sink_tokens, p->local_tokens, p->max_blocks_per_seq);
     pl->nf = nf > 0 ? nf : 1;
     size_t off = kAlign;
@@ -93,30 +91,29 @@ ffd_status make_decode_plan(const ffd_decode_params *p, Plan *pl) {
     return FFD_OK;
 }
 
-// Workspace of ffd_dense_decode: [error word | split partials].
+// Workspace of ffd_dense_decode: [error word | split records | counters], the FFD step's layout
+// without the stage-1 parts (the dense kernel uses the same schedule, records and merge).
 ffd_status make_dense_plan(const ffd_decode_params *p, Plan *pl) {
     ffd_status st = check_params(p);
     if (st != FFD_OK) return st;
     const int64_t units = (int64_t)p->batch * p->num_kv_heads;
     const int G = p->num_q_heads / p->num_kv_heads;
-    int splits = p->num_splits;
-    if (splits == 0) {
-        const int sms = current_sm_count();
+    const int sms = current_sm_count();
+    int ctas = p->num_splits;
+    if (ctas == 0) {
         if (sms <= 0) return FFD_ERR_CUDA;
-        const int64_t target = (int64_t)sms * kCtasPerSm;
-        splits = (int)((target + units - 1) / units);
+        ctas = sms;
+    } else if (sms > 0 && ctas > sms) {
+        ctas = sms;
     }
-    if (splits > p->max_blocks_per_seq) splits = p->max_blocks_per_seq;
-    if (splits < 1) splits = 1;
-    pl->bps = (p->max_blocks_per_seq + splits - 1) / splits;
-    pl->splits = (p->max_blocks_per_seq + pl->bps - 1) / pl->bps;
+    pl->ctas = ctas;
     pl->nf = 0;
-    pl->ctas = 0;
     size_t off = kAlign;
     pl->m1_off = off;
     pl->part_off = off;
-    off = align_up(off + (size_t)units * pl->splits * G * kPartStride * sizeof(float));
+    off = align_up(off + (size_t)(units + ctas) * kRefineGroups * G * kPartStride * sizeof(float));
     pl->cnt_off = off;
+    off = align_up(off + 3 * (size_t)units * sizeof(int));
     pl->total = off;
     return FFD_OK;
 }
@@ -135,8 +132,6 @@ DecodeArgs make_args(const ffd_decode_params *p, const Plan &pl, void *ws) {
     a.max_blocks = p->max_blocks_per_seq;
     a.S = p->sink_tokens;
     a.L = p->local_tokens;
-    a.splits = pl.splits;
-    a.blk_per_split = pl.bps;
     a.nf = pl.nf;
     a.delta = p->delta;
     a.sm_scale = p->sm_scale;
@@ -241,7 +236,7 @@ ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
     a.seq_lens = seq_lens;
     a.block_table = block_table;
     a.out = out;
-    cudaError_t e = launch_dense(a, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_dense(a, pl.ctas, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
 }
 

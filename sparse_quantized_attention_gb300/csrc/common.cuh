@@ -35,8 +35,6 @@ __host__ __device__ inline int resid_offset(int r, int c) {
 // Everything a decode launch needs; passed by value to the kernels.
 struct DecodeArgs {
     int B, Hq, Hkv, G, P, max_blocks, S, L;
-    int splits;      // KV splits per (sequence, KV head)
-    int blk_per_split;
     int nf;          // stage-1 slots per (sequence, KV head)
     float delta, sm_scale;
     const __nv_bfloat16 *q;

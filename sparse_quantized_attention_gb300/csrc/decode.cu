@@ -869,34 +869,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 // ------------------------------------------------------------------------------------------
 // Host side
 // ------------------------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// V as a 3-D tensor {64 channels, rows, 2 channel halves} (strides 256 B per row, 128 B per half)
-// with a box of {64, 64, 2}: one copy lands a block's 64 rows as two 64 x 128 B swizzled tiles,
-// channels 0-63 first.
-static bool make_v_map(CUtensorMap *map, void *ptr, uint64_t rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[3] = {64, rows, 2};
-    const cuuint64_t strides[2] = {kD * 2, 128};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kPage, 2};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t stream) {
     static bool attr_done = false;
     if (!attr_done) {
@@ -909,7 +881,7 @@ cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t strea
     memset(&prm, 0, sizeof prm);
     prm.a = a;
     const uint64_t rows = (uint64_t)a.P * a.Hkv * kPage;
-    if (!make_v_map(&prm.tm_v, const_cast<__nv_bfloat16 *>(a.v), rows))
+    if (!make_tile_map(&prm.tm_v, const_cast<__nv_bfloat16 *>(a.v), rows))
         return cudaErrorInvalidValue;
 
     if (a.prof_start) cudaEventRecord(a.prof_start, stream);

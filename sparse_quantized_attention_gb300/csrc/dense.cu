@@ -2,184 +2,279 @@
 //
 // Source: the pages compare FFD with FlashAttention-2 decoding ("Faster Than Flash", Main results:
 // kernel speedup and end-to-end throughput). This kernel computes plain softmax attention over
-// every cached token with the original bf16 keys, split over the KV sequence with the same
-// partial format and log-sum-exp merge as the FFD path.
-#include "common.cuh"
+// every cached token with the original bf16 keys. It is the FFD step without stages 1 and 2: a
+// persistent CTA per SM walks an equal share of all blocks (splitkv.cuh schedule), a copy warp
+// streams each block's K and V tiles (two 3-D TMA copies, 32 KB) into a 6-slot ring, and two
+// groups of four warps take alternate blocks: scores q.K on the tensor cores, then the same
+// online-softmax and P.V update, records and by-head merge as the FFD path.
+#include "splitkv.cuh"
 
 namespace ffd {
+namespace {
 
-template <int G>
-__global__ void __launch_bounds__(128) dense_kernel(DecodeArgs a) {
-    __shared__ float qs[G][kD + 4];
-    __shared__ float sp[kPage][G + 1];
-    __shared__ float m_run[G], l_run[G], alpha[G];
+constexpr int kDRing = 6;          // ring slots: K tile, then V tile, of one block
+constexpr int kDPageSlots = 8;     // sub-chunks whose block-table entries are resolved ahead
+constexpr int kDThreads = 128 + 128 * kRefineGroups;  // copy warpgroup + refine groups
+constexpr int kDFillPeriod = kDRing / gcd_c(kDRing, kRefineGroups) * kRefineGroups;
+constexpr int kDSlotK = 0;
+constexpr int kDSlotV = 16384;
+constexpr int kDSlotBytes = 32768;
+constexpr int kDOffPx = kDRing * kDSlotBytes;                   // [group][2][kPxBuf]
+constexpr int kDOffMisc = kDOffPx + kRefineGroups * 2 * kPxBuf;
+constexpr int kDMiscBytes = 2048;
+constexpr int kDSmemBytes = kDOffMisc + kDMiscBytes + 1024;     // + slack to align to 1 KB
+static_assert(kDSmemBytes <= 232448, "shared memory per CTA");
 
-    const int bh = blockIdx.y;
-    const int split = blockIdx.x;
-    const int b = bh / a.Hkv, h = bh % a.Hkv;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = checked_seq_len(a, b);
-    const int nb = (n + kPage - 1) / kPage;
-    const int blk0 = split * a.blk_per_split;
-    const int blk1 = min(min(blk0 + a.blk_per_split, a.max_blocks), nb);
+// One sub-chunk's tiles as the page warp hands them to the copy warp.
+struct DensePages {
+    int32_t row[kSub];  // first row of each block's tile: (page * Hkv + h) * 64
+    uint32_t bad;       // entries outside [0, P), one bit per block (never loaded)
+    int32_t cnt;        // blocks; 0 ends this CTA's schedule
+};
 
-    for (int idx = tid; idx < G * kD; idx += blockDim.x) {
-        const int i = idx / kD, c = idx % kD;
-        qs[i][c] = __bfloat162float(a.q[((size_t)b * a.Hq + h * G + i) * kD + c]);
+struct DenseMisc {
+    uint32_t aborted;
+    uint32_t merge_flag[kRefineGroups];
+    uint32_t slot_bad[kDRing];               // the block in ring slot s was not loaded
+    uint32_t over[kRefineGroups][2][4];      // as in the FFD kernel (softmax_pv)
+    float wmax[kRefineGroups][2][4][kMaxG];
+    float lsum[kRefineGroups][4][kMaxG];
+    DensePages ps[kDPageSlots];
+    uint64_t pages_full[kDPageSlots];
+    uint64_t pages_empty[kDPageSlots];
+    uint64_t full[kRefineGroups][kDRing];    // [group of the block][slot]
+    uint64_t empty[kDRing];
+};
+static_assert(sizeof(DenseMisc) <= kDMiscBytes, "control block");
+
+struct DenseParams {
+    CUtensorMap tm_k, tm_v;
+    DecodeArgs a;
+};
+
+// Page warp: resolves the block-table entries of every sub-chunk of the CTA's schedule (one lane
+// per block) into the page ring; entries outside [0, P) raise FFD_ERRBIT_BOUNDS and are skipped.
+__device__ __forceinline__ void dense_pager(const DecodeArgs &a, DenseMisc *m, int cta, int ncta,
+                                            int lane) {
+    Sched sch;
+    sch.init(a, cta, ncta);
+    Sub s;
+    for (int t = 0;; t++) {
+        const bool more = sch.next(a, s);
+        const int ps = t % kDPageSlots;
+        if (t >= kDPageSlots) wait_bar(a, m, &m->pages_empty[ps], ((t / kDPageSlots) - 1) & 1);
+        if (aborted(m)) return;
+        DensePages &P = m->ps[ps];
+        bool bad = false;
+        if (more && lane < s.cnt) {
+            const int page = a.block_table[(size_t)s.b * a.max_blocks + s.j0 + lane];
+            bad = page < 0 || page >= a.P;
+            if (bad) raise_error(a.err, FFD_ERRBIT_BOUNDS);
+            P.row[lane] = bad ? 0 : (page * a.Hkv + s.h) * kPage;
+        }
+        const uint32_t badm = __ballot_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            P.bad = badm;
+            P.cnt = more ? s.cnt : 0;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m->pages_full[ps]);
+        if (!more) return;
     }
-    if (tid < G) {
-        m_run[tid] = -INFINITY;
-        l_run[tid] = 0.0f;
+}
+
+// Copy warp: block kb goes to ring slot kb % kDRing as soon as the slot is free; lanes 0 and 1
+// issue the K and V copies side by side. Each refine group has its own fill barrier per slot
+// (consecutive phases = its blocks kb, kb + kDFillPeriod, ...).
+__device__ __forceinline__ void dense_ring(const DenseParams &prm, DenseMisc *m, uint8_t *ring,
+                                           int lane) {
+    const DecodeArgs &a = prm.a;
+    if (lane == 0) {
+        prefetch_tensormap(&prm.tm_k);
+        prefetch_tensormap(&prm.tm_v);
+    }
+    int kb = 0;
+    for (int t = 0;; t++) {
+        const int ps = t % kDPageSlots;
+        wait_bar(a, m, &m->pages_full[ps], (t / kDPageSlots) & 1);
+        const DensePages &P = m->ps[ps];
+        const int cnt = P.cnt;
+        if (cnt == 0 || aborted(m)) break;
+        for (int k = 0; k < cnt; k++, kb++) {
+            const int slot = kb % kDRing, round = kb / kDRing;
+            if (round > 0) wait_bar(a, m, &m->empty[slot], (round - 1) & 1);
+            uint64_t *bar = &m->full[kb % kRefineGroups][slot];
+            const bool bad = (P.bad >> k) & 1u;
+            uint8_t *d = ring + slot * kDSlotBytes;
+            if (lane == 0) {
+                m->slot_bad[slot] = bad;
+                if (bad) mbar_arrive(bar);
+                else mbar_arrive_expect_tx(bar, kDSlotBytes);
+            }
+            __syncwarp();
+            if (!bad) {
+                if (lane == 0) tma_load_3d(d + kDSlotK, &prm.tm_k, 0, P.row[k], 0, bar);
+                else if (lane == 1) tma_load_3d(d + kDSlotV, &prm.tm_v, 0, P.row[k], 0, bar);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m->pages_empty[ps]);
+    }
+    // leave no copy in flight: wait for the last fill of every ring slot
+    if (lane == 0)
+        for (int i = 0; i < kDRing && i < kb; i++) {
+            const int last = kb - 1 - i;
+            drain_bar(a, &m->full[last % kRefineGroups][last % kDRing], (last / kDFillPeriod) & 1);
+        }
+}
+
+// Refine warp mt of group grp: blocks kb % kRefineGroups == grp of the CTA's schedule. Scores of
+// rows r0 = 16mt + g, r1 = r0 + 8 for heads 2tig, 2tig+1: K rows by ldmatrix from the swizzled
+// tile (A operand), q of head g as bf16 pairs (B operand, exact), fp32 accumulation over the 8
+// k-steps of 16 channels.
+__device__ __forceinline__ void dense_refiner(const DecodeArgs &a, DenseMisc *m, uint8_t *ring,
+                                              uint8_t *px, int cta, int ncta, int grp, int mt,
+                                              int lane) {
+    const int g = lane >> 2, tig = lane & 3;
+    const int mi = lane >> 3, jr = lane & 7;
+    const int tok = 16 * mt + ((mi & 1) << 3) + jr;  // the row this lane addresses for ldmatrix
+    Sched sch;
+    sch.init(a, cta, ncta);
+    Sub s;
+    RefineState R;
+    uint32_t qb0[8], qb1[8];
+    int n = 0, kb = 0, pb = 0;
+    while (sch.next(a, s)) {
+        if (s.first) {
+            const bool hv = g < a.G;
+            const uint32_t *qw = reinterpret_cast<const uint32_t *>(
+                a.q + ((size_t)s.b * a.Hq + s.h * a.G + (hv ? g : 0)) * kD);
+#pragma unroll
+            for (int kc = 0; kc < 8; kc++) {
+                qb0[kc] = hv ? qw[8 * kc + tig] : 0u;      // channels 16kc + 2tig, +1
+                qb1[kc] = hv ? qw[8 * kc + 4 + tig] : 0u;  // channels 16kc + 8 + 2tig, +1
+            }
+            R.m0 = R.m1 = kNoReference;  // the first block raises it through the rescale path
+            R.nl0 = R.nl1 = -kNoReference * kLog2e;
+            R.l0 = R.l1 = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 2; i++) R.o[i][0] = R.o[i][1] = R.o[i][2] = R.o[i][3] = 0.0f;
+            n = len_of(a, s.b);
+        }
+        for (int k = 0; k < s.cnt; k++, kb++) {
+            if (kb % kRefineGroups != grp) continue;
+            const int slot = kb % kDRing;
+            wait_bar(a, m, &m->full[grp][slot], (kb / kDFillPeriod) & 1);
+            const uint8_t *d = ring + slot * kDSlotBytes;
+            if (!*reinterpret_cast<volatile uint32_t *>(&m->slot_bad[slot])) {  // group-uniform
+                const uint32_t kbase = smem_u32(d + kDSlotK);
+                float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int kc = 0; kc < 8; kc++) {
+                    const int c = 2 * kc + (mi >> 1);  // 16-byte chunk of the 256-byte row
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4(a0, a1, a2, a3,
+                                kbase + (c >> 3) * 8192 + tok * 128 + (((c & 7) ^ jr) << 4));
+                    mma_bf16(D, a0, a1, a2, a3, qb0[kc], qb1[kc]);
+                }
+                const float sm = a.sm_scale;
+                const int t0 = (s.j0 + k) * kPage + 16 * mt + g;
+                const bool v0 = t0 < n, v1 = t0 + 8 < n;
+                softmax_pv(m, px + (grp * 2 + pb) * kPxBuf, d + kDSlotV, v0 ? D[0] * sm : -INFINITY,
+                           v0 ? D[1] * sm : -INFINITY, v1 ? D[2] * sm : -INFINITY,
+                           v1 ? D[3] * sm : -INFINITY, R, grp, mt, pb, lane);
+                pb ^= 1;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&m->empty[slot]);
+        }
+        if (s.last) {
+            const int u = s.b * a.Hkv + s.h;
+            write_record(a, m, R, unit_record(a, u, cta, grp), grp, mt, lane);
+            finish_unit(a, m, s, cta, ncta, sch.T, grp, mt, lane);
+        }
+    }
+}
+
+// Persistent, one CTA per SM; CTAs 0 .. ncta-1 walk the blocks. Warp 2 of every CTA writes the
+// zero output of empty sequences (no CTA walks them) and flags lengths past the block table.
+__global__ void __launch_bounds__(kDThreads, 1) dense_kernel(const __grid_constant__ DenseParams prm) {
+    const DecodeArgs &a = prm.a;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *ring = base;
+    uint8_t *px = base + kDOffPx;
+    DenseMisc *m = reinterpret_cast<DenseMisc *>(base + kDOffMisc);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t T = total_blocks(a);
+    const int ncta = (int)(T < (int64_t)gridDim.x ? T : (int64_t)gridDim.x);
+    const int cta = blockIdx.x;
+    const bool walker = cta < ncta;
+    if (threadIdx.x == 0) {
+        m->aborted = 0;
+        for (int i = 0; i < kDPageSlots; i++) {
+            mbar_init(&m->pages_full[i], 1);
+            mbar_init(&m->pages_empty[i], 1);  // the copy warp
+        }
+        for (int i = 0; i < kDRing; i++) {
+            for (int g = 0; g < kRefineGroups; g++) mbar_init(&m->full[g][i], 1);
+            mbar_init(&m->empty[i], 4);  // the refine group that took the block
+        }
+        fence_barrier_init();
     }
     __syncthreads();
-
-    const int t = tid >> 1, hf = tid & 1;
-    const int dp = tid & 63, hh = tid >> 6;
-    float o[4][2];
-#pragma unroll
-    for (int k = 0; k < 4; k++) o[k][0] = o[k][1] = 0.0f;
-
-    for (int blk = blk0; blk < blk1; blk++) {
-        const int page = a.block_table[(size_t)b * a.max_blocks + blk];
-        if (page < 0 || page >= a.P) {
-            if (tid == 0) raise_error(a.err, FFD_ERRBIT_BOUNDS);
-            continue;
+    if (warp == 0) {
+        if (walker) dense_ring(prm, m, ring, lane);
+    } else if (warp == 1) {
+        if (walker) dense_pager(a, m, cta, ncta, lane);
+    } else if (warp == 2) {
+        for (int u = cta; u < a.B * a.Hkv; u += gridDim.x) {
+            const int b = u / a.Hkv, h = u % a.Hkv;
+            const int raw_n = a.seq_lens[b];
+            const int n = len_of(a, b);
+            if (lane == 0 && h == 0 && raw_n != n) raise_error(a.err, FFD_ERRBIT_BOUNDS);
+            if (n == 0)
+                for (int idx = lane; idx < a.G * kD; idx += 32)
+                    a.out[((size_t)b * a.Hq + h * a.G) * kD + idx] = 0.0f;
         }
-        const size_t tile = (size_t)page * a.Hkv + h;
-        const int j = blk * kPage + t;
-        const bool valid = j < n;
-        const uint4 *kp = reinterpret_cast<const uint4 *>(a.k + (tile * kPage + t) * kD + hf * 64);
-        float acc[G];
-#pragma unroll
-        for (int i = 0; i < G; i++) acc[i] = 0.0f;
-#pragma unroll
-        for (int w = 0; w < 8; w++) {
-            const uint4 raw = kp[w];
-            const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const float k0 = __uint_as_float(wd[e] << 16);
-                const float k1 = __uint_as_float(wd[e] & 0xffff0000u);
-                const int c = hf * 64 + w * 8 + e * 2;
-#pragma unroll
-                for (int i = 0; i < G; i++) {
-                    acc[i] = fmaf(qs[i][c], k0, acc[i]);
-                    acc[i] = fmaf(qs[i][c + 1], k1, acc[i]);
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < G; i++) {
-            acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 1);
-            if (hf == 0) sp[t][i] = valid ? acc[i] * a.sm_scale : -INFINITY;
-        }
-        __syncthreads();
-        for (int i = warp; i < G; i += 4) {
-            const float v0 = sp[lane][i], v1 = sp[lane + 32][i];
-            const float mb = warp_max(fmaxf(v0, v1));
-            const float m_old = m_run[i];
-            const float m_new = fmaxf(m_old, mb);
-            const float al = m_old == -INFINITY ? 0.0f : exp2f((m_old - m_new) * 1.4426950408889634f);
-            const float p0 = v0 == -INFINITY ? 0.0f : exp2f((v0 - m_new) * 1.4426950408889634f);
-            const float p1 = v1 == -INFINITY ? 0.0f : exp2f((v1 - m_new) * 1.4426950408889634f);
-            sp[lane][i] = p0;
-            sp[lane + 32][i] = p1;
-            const float ps = warp_sum(p0 + p1);
-            __syncwarp();
-            if (lane == 0) {
-                l_run[i] = l_run[i] * al + ps;
-                m_run[i] = m_new;
-                alpha[i] = al;
-            }
-        }
-        __syncthreads();
-        const __nv_bfloat16 *vrow = a.v + tile * kPage * kD + 2 * dp;
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int i = hh * 4 + k;
-            if (i < G) {
-                o[k][0] *= alpha[i];
-                o[k][1] *= alpha[i];
-            }
-        }
-        for (int tt = 0; tt < kPage; tt++) {
-            const float2 vf = __bfloat1622float2(
-                *reinterpret_cast<const __nv_bfloat162 *>(vrow + (size_t)tt * kD));
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const int i = hh * 4 + k;
-                if (i < G) {
-                    const float p = sp[tt][i];
-                    o[k][0] = fmaf(p, vf.x, o[k][0]);
-                    o[k][1] = fmaf(p, vf.y, o[k][1]);
-                }
-            }
-        }
-        __syncthreads();
-    }
-
-    float *part = a.ws_part + ((size_t)bh * a.splits + split) * G * kPartStride;
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const int i = hh * 4 + k;
-        if (i < G) {
-            part[i * kPartStride + 2 * dp] = o[k][0];
-            part[i * kPartStride + 2 * dp + 1] = o[k][1];
-        }
-    }
-    if (tid < G) {
-        part[tid * kPartStride + kD] = m_run[tid];
-        part[tid * kPartStride + kD + 1] = l_run[tid];
+    } else if (warp >= 4 && walker) {
+        dense_refiner(a, m, ring, px, cta, ncta, (warp - 4) >> 2, warp & 3, lane);
     }
 }
 
-// Log-sum-exp merge of the split partials: out = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s.
-// One CTA per (sequence, query head); thread = channel.
-__global__ void __launch_bounds__(128) dense_merge_kernel(DecodeArgs a) {
-    const int bq = blockIdx.x;
-    const int b = bq / a.Hq, qh = bq % a.Hq;
-    const int h = qh / a.G, i = qh % a.G;
-    const int bh = b * a.Hkv + h;
-    const int c = threadIdx.x;
-    const float *part = a.ws_part + (size_t)bh * a.splits * a.G * kPartStride + i * kPartStride;
-    const size_t split_stride = (size_t)a.G * kPartStride;
-    float M = -INFINITY;
-    for (int s = 0; s < a.splits; s++) M = fmaxf(M, part[s * split_stride + kD]);
-    float num = 0.0f, den = 0.0f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < a.splits; s++) {
-            const float m = part[s * split_stride + kD];
-            if (m == -INFINITY) continue;
-            const float w = exp2f((m - M) * 1.4426950408889634f);
-            den = fmaf(w, part[s * split_stride + kD + 1], den);
-            num = fmaf(w, part[s * split_stride + c], num);
-        }
+}  // namespace
+
+cudaError_t launch_dense(const DecodeArgs &a, int ctas, cudaStream_t stream) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
     }
-    a.out[(size_t)bq * kD + c] = den > 0.0f ? num / den : 0.0f;
-}
-
-template <int G>
-static void launch_dense_g(const DecodeArgs &a, cudaStream_t stream) {
-    dense_kernel<G><<<dim3(a.splits, a.B * a.Hkv), 128, 0, stream>>>(a);
-}
-
-cudaError_t launch_dense(const DecodeArgs &a, cudaStream_t stream) {
+    DenseParams prm;
+    memset(&prm, 0, sizeof prm);
+    prm.a = a;
+    const uint64_t rows = (uint64_t)a.P * a.Hkv * kPage;
+    if (!make_tile_map(&prm.tm_k, const_cast<__nv_bfloat16 *>(a.k), rows) ||
+        !make_tile_map(&prm.tm_v, const_cast<__nv_bfloat16 *>(a.v), rows))
+        return cudaErrorInvalidValue;
     if (a.prof_start) cudaEventRecord(a.prof_start, stream);
-    switch (a.G) {
-        case 1: launch_dense_g<1>(a, stream); break;
-        case 2: launch_dense_g<2>(a, stream); break;
-        case 3: launch_dense_g<3>(a, stream); break;
-        case 4: launch_dense_g<4>(a, stream); break;
-        case 5: launch_dense_g<5>(a, stream); break;
-        case 6: launch_dense_g<6>(a, stream); break;
-        case 7: launch_dense_g<7>(a, stream); break;
-        case 8: launch_dense_g<8>(a, stream); break;
-        default: return cudaErrorInvalidValue;
-    }
-    if (a.prof_stop) cudaEventRecord(a.prof_stop, stream);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(kDThreads);
+    cfg.dynamicSmemBytes = kDSmemBytes;
+    cfg.stream = stream;
+    // the last groups of a unit wait for the unit's other CTAs: all CTAs must be resident
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, dense_kernel, prm);
     if (e != cudaSuccess) return e;
-    dense_merge_kernel<<<a.B * a.Hq, kD, 0, stream>>>(a);
+    if (a.prof_stop) cudaEventRecord(a.prof_stop, stream);
     return cudaGetLastError();
 }
 

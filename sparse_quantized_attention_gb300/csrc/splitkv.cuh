@@ -6,6 +6,8 @@
 // computation over every block.
 #pragma once
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -426,6 +428,37 @@ __device__ __forceinline__ void finish_unit(const DecodeArgs &a, M *m, const Sub
             *done_counter(a, u) = 0;
         }
     }
+}
+
+// ------------------------------------------------------------------------------------------
+// Host: TMA tensor map of a bf16 [rows][128] tile array (V, or K on the dense path).
+// ------------------------------------------------------------------------------------------
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// The array as a 3-D tensor {64 channels, rows, 2 channel halves} (strides 256 B per row, 128 B
+// per half) with a box of {64, 64, 2}: one copy lands a block's 64 rows as two 64 x 128 B tiles
+// with the 128-byte swizzle (16-byte chunk c of row r at c ^ (r % 8)), channels 0-63 first.
+inline bool make_tile_map(CUtensorMap *map, void *ptr, uint64_t rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {64, rows, 2};
+    const cuuint64_t strides[2] = {kD * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kPage, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace ffd
