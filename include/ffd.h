@@ -131,6 +131,38 @@ ffd_status ffd_quantize_keys(const ffd_cache_desc *cache, const void *k_bf16, ui
                              int32_t *error_word, void *stream);
 
 /*
+ * ffd_append_kv -- append one new token per sequence to the paged cache: quantise its key into
+ * the thumbnail and residual records and store its value (and, optionally, the raw key).
+ * Source: Methodology §1 (the K cache is kept as 2-bit thumbnails plus 8-bit residuals); in a
+ * decode loop every generated token is added to that cache before the next attention step, so
+ * this is the incremental form of ffd_quantize_keys. The token's codes and scales are bit for
+ * bit those ffd_quantize_keys writes for the same key.
+ *
+ *   cache        shape of the cache (head_dim 128, page_size 64)
+ *   batch        B >= 1 sequences
+ *   max_blocks_per_seq  row stride of block_table (>= 1)
+ *   k_new_bf16   device bf16 [B][Hkv][128], the new keys, 16-byte aligned
+ *   v_new_bf16   device bf16 [B][Hkv][128], the new values, 16-byte aligned
+ *   positions    device int32 [B]: token index p of the new token of sequence b (normally its
+ *                length before the append); it is stored in row p % 64 of page
+ *                block_table[b][p / 64]. A negative entry appends nothing for that sequence.
+ *   block_table  device int32 [B][max_blocks_per_seq]
+ *   thumb, resid device records (layout above): the token's row is rewritten, nothing else
+ *   v_bf16       device bf16 [P][Hkv][64][128]: the token's row receives the new value
+ *   k_bf16       device bf16 [P][Hkv][64][128] or NULL: the token's row receives the raw key
+ *   error_word   device int32, or NULL: FFD_ERRBIT_BOUNDS for p >= 64 * max_blocks_per_seq or a
+ *                page outside [0, P) (that sequence is skipped), FFD_ERRBIT_RANGE for a key
+ *                outside the fp16 range (written as by ffd_quantize_keys)
+ *   stream       cudaStream_t
+ * Two sequences that name the same (page, row) race; the caller's block table must not do that.
+ * Returns FFD_OK, FFD_ERR_INVALID_ARG, FFD_ERR_UNSUPPORTED or FFD_ERR_CUDA.
+ */
+ffd_status ffd_append_kv(const ffd_cache_desc *cache, int32_t batch, int32_t max_blocks_per_seq,
+                         const void *k_new_bf16, const void *v_new_bf16, const int32_t *positions,
+                         const int32_t *block_table, uint8_t *thumb, uint8_t *resid,
+                         void *v_bf16, void *k_bf16, int32_t *error_word, void *stream);
+
+/*
  * Bytes of device workspace that ffd_decode_attention needs for these parameters on the current
  * device. Returns 0 for parameters that ffd_decode_attention would reject.
  */

@@ -4,14 +4,14 @@ The compute path is libffd.so (hand-written CUDA, C ABI in include/ffd.h); this 
 ctypes binding. See ``ffd`` for the entry points.
 """
 from .ffd import (CacheDesc, DecodeParams, FFDError, QuantizedCache, alloc_quantized_cache,
-                  alloc_workspace, ffd_decode_attention, ffd_decode_attention_static,
+                  alloc_workspace, ffd_append_kv, ffd_decode_attention, ffd_decode_attention_static,
                   ffd_decode_workspace_size,
                   ffd_dense_decode, ffd_dense_workspace_size, ffd_get_error, ffd_quantize_keys,
                   ffd_set_profile_events, ffd_status_string, ffd_version, lib, library_path,
                   make_params)
 
 __all__ = ["CacheDesc", "DecodeParams", "FFDError", "QuantizedCache", "alloc_quantized_cache",
-           "alloc_workspace", "ffd_decode_attention", "ffd_decode_attention_static",
+           "alloc_workspace", "ffd_append_kv", "ffd_decode_attention", "ffd_decode_attention_static",
            "ffd_decode_workspace_size",
            "ffd_dense_decode", "ffd_dense_workspace_size", "ffd_get_error",
            "ffd_quantize_keys", "ffd_set_profile_events", "ffd_status_string", "ffd_version",

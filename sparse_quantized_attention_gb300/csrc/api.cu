@@ -10,6 +10,10 @@ namespace ffd {
 cudaError_t launch_quantize(int P, int Hkv, const int32_t *page_ids, int num_pages_listed,
                             const void *k, uint8_t *thumb, uint8_t *resid, int *err,
                             cudaStream_t stream);
+cudaError_t launch_append(int B, int Hkv, int P, int max_blocks, const int32_t *positions,
+                          const int32_t *block_table, const void *k_new, const void *v_new,
+                          uint8_t *thumb, uint8_t *resid, void *v_cache, void *k_cache, int *err,
+                          cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t stream);
 cudaError_t launch_dense(const DecodeArgs &a, int ctas, cudaStream_t stream);
 }  // namespace ffd
@@ -161,7 +165,7 @@ const char *ffd_status_string(ffd_status s) {
     return "FFD_ERR_UNKNOWN";
 }
 
-int32_t ffd_version(void) { return 200; }
+int32_t ffd_version(void) { return 201; }
 
 ffd_status ffd_quantize_keys(const ffd_cache_desc *cache, const void *k_bf16, uint8_t *thumb,
                              uint8_t *resid, const int32_t *page_ids, int32_t num_page_ids,
@@ -175,6 +179,28 @@ ffd_status ffd_quantize_keys(const ffd_cache_desc *cache, const void *k_bf16, ui
     if ((int64_t)listed * cache->num_kv_heads * kPage * 32 > INT32_MAX) return FFD_ERR_UNSUPPORTED;
     cudaError_t e = launch_quantize(cache->num_pages, cache->num_kv_heads, page_ids, listed, k_bf16,
                                     thumb, resid, error_word, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+}
+
+ffd_status ffd_append_kv(const ffd_cache_desc *cache, int32_t batch, int32_t max_blocks_per_seq,
+                         const void *k_new_bf16, const void *v_new_bf16, const int32_t *positions,
+                         const int32_t *block_table, uint8_t *thumb, uint8_t *resid,
+                         void *v_bf16, void *k_bf16, int32_t *error_word, void *stream) {
+    if (!cache || !k_new_bf16 || !v_new_bf16 || !positions || !block_table || !thumb || !resid ||
+        !v_bf16)
+        return FFD_ERR_INVALID_ARG;
+    if (cache->num_pages < 1 || cache->num_kv_heads < 1 || batch < 1 || max_blocks_per_seq < 1)
+        return FFD_ERR_INVALID_ARG;
+    if (cache->head_dim != kD || cache->page_size != kPage) return FFD_ERR_UNSUPPORTED;
+    if (!aligned16(k_new_bf16) || !aligned16(v_new_bf16) || !aligned16(thumb) ||
+        !aligned16(resid) || !aligned16(v_bf16) || (k_bf16 && !aligned16(k_bf16)))
+        return FFD_ERR_INVALID_ARG;
+    if ((int64_t)batch * cache->num_kv_heads * 4 > INT32_MAX ||
+        (int64_t)max_blocks_per_seq * kPage > INT32_MAX)
+        return FFD_ERR_UNSUPPORTED;
+    cudaError_t e = launch_append(batch, cache->num_kv_heads, cache->num_pages, max_blocks_per_seq,
+                                  positions, block_table, k_new_bf16, v_new_bf16, thumb, resid,
+                                  v_bf16, k_bf16, error_word, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
 }
 

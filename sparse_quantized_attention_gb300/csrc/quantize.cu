@@ -5,122 +5,268 @@
 // the keys close to fp16 precision). The exact format, and the record layout each (page, KV head)
 // tile is written in, are the ones stated in include/ffd.h.
 //
-// One warp quantises one token of one KV head: lane l holds channels 4l .. 4l+3, so a group of
-// 32 channels is 8 lanes and group reductions are 3 shuffles. Every arithmetic step is a single
-// IEEE fp32 operation with an explicit rounding intrinsic, so the outputs are bit-defined.
+// One CTA of 256 threads quantises one (page, KV head) tile: thread t owns token t / 4 and
+// channel group t % 4, so the 32 channels that share a scale live in one thread and no group
+// reduction crosses lanes. The thread loads its 64 bytes of keys with four 16-byte loads and
+// writes its codes, its two 16-byte residual chunks and its three scales with vector stores; a
+// warp covers 8 whole tokens, so every store of the tile's records is a full 32-byte sector.
+//
+// Every arithmetic step is a single IEEE fp32 operation with an explicit rounding intrinsic, so
+// the outputs are bit-defined. The per-channel code needs round-half-even of the correctly
+// rounded quotient (x - zero) / scale (and r / r_scale). Instead of one IEEE division per
+// channel the kernel forms the quotient from a correctly rounded reciprocal, with the clamp
+// folded into a saturating multiply, and rounds it with one fused multiply-add. Where that fast
+// quotient lies within a few ulps of a rounding boundary k + 1/2 (ties are frequent: keys, zeros
+// and scales sit on the bf16 / fp16 grids), the side of the boundary is decided exactly from the
+// sign of x - zero - (k + 1/2) scale (boundary_step below).
 #include "common.cuh"
 
 namespace ffd {
 
-__device__ __forceinline__ float group8_min(float v) {
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+namespace {
+
+// 1.5 * 2^23: adding it to |t| < 2^22 rounds t to an integer half-to-even (the sum's ulp is 1),
+// and the integer is then the sum's low mantissa bits (two's complement for t < 0).
+constexpr float kMagic = 12582912.0f;
+// kMagic - 127, the base of the residual codes' sums (its low byte is 0x81 = -127 mod 256)
+constexpr float kMagicB = 12582785.0f;
+// Half-widths of the windows around k + 1/2 in which the fast quotient is not trusted. Stage A
+// evaluates a / scale as 3 sat(a * rcp(3 scale)): absolute error below 4e-7 on [0, 3]. Stage B
+// evaluates r / r_scale as 254 sat(r * rcp(254 r_scale) + 1/2) - 127: error below 1.6e-5 on
+// [-127, 127].
+constexpr float kNearA = 1.0e-5f;
+constexpr float kNearB = 4.0e-5f;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Exact rounding near a boundary. With t the fast quotient of a / b and c = rint(t), the only
+// rounding boundary within reach is k = c + 1/2 sign(t - c); k * b is exact in fp32 (k has at
+// most 9 significant bits, b is an fp16 value), so e = a - k b, formed by one fused multiply-add,
+// has the exact sign of a / b - k. Because a and b lie on the fp32 and fp16 grids, the IEEE
+// quotient rounds onto k only when a / b == k exactly (e == 0, a tie: half to even); otherwise
+// it lies on the same side of k as a / b. Returns the step (-1, 0, +1) to add to c.
+__device__ __forceinline__ float boundary_step(float a, float b, float c, float d, bool c_odd) {
+    const float dir = copysignf(1.0f, d);
+    const float e = __fmaf_rn(-__fadd_rn(c, 0.5f * dir), b, a);
+    if (e == 0.0f) return c_odd ? dir : 0.0f;
+    return (e > 0.0f) == (d > 0.0f) ? dir : 0.0f;
 }
 
-__device__ __forceinline__ float group8_max(float v) {
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+// 2-bit code of a = x - zero: clamp(rint(a / scale), 0, 3), from r3 = rcp(3 scale) (0 when
+// scale is 0).
+__device__ __forceinline__ float code2_of(float a, float scale, float r3) {
+    const float tp = __saturatef(__fmul_rn(a, r3));
+    float code = __fsub_rn(__fmaf_rn(tp, 3.0f, kMagic), kMagic);
+    const float d = __fmaf_rn(tp, 3.0f, -code);
+    if (fabsf(d) > 0.5f - kNearA)
+        code = __fadd_rn(code, boundary_step(a, scale, code, d, ((int)code & 1) != 0));
+    return code;
 }
 
-__global__ void __launch_bounds__(256) quantize_keys_kernel(
-    int P, int Hkv, int num_rows, const int32_t *__restrict__ page_ids,
-    const __nv_bfloat16 *__restrict__ k, uint8_t *__restrict__ thumb, uint8_t *__restrict__ resid,
-    int *err) {
-    const int lane = threadIdx.x & 31;
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (warp >= num_rows) return;  // warp-uniform
-    // warp -> (tile, slot); tile -> (page, head)
-    const int slot = warp % kPage;
-    const int tile_local = warp / kPage;
-    int page = tile_local / Hkv;
-    const int h = tile_local % Hkv;
+// int8 code of r: clamp(rint(r / r_scale), -127, 127) in the low byte (two's complement), from
+// r254 = rcp(254 r_scale) (0 when r_scale is 0).
+__device__ __forceinline__ uint32_t code8_of(float r, float rscale, float r254) {
+    const float tp = __saturatef(__fmaf_rn(r, r254, 0.5f));
+    float cm = __fmaf_rn(tp, 254.0f, kMagicB);  // kMagicB + (code + 127)
+    const float d = __fmaf_rn(tp, 254.0f, -__fsub_rn(cm, kMagicB));
+    if (fabsf(d) > 0.5f - kNearB) {
+        const float code = __fsub_rn(cm, kMagic);  // exact
+        cm = __fadd_rn(cm, boundary_step(r, rscale, code, d, (__float_as_uint(cm) & 1u) != 0));
+    }
+    return __float_as_uint(cm);
+}
+
+// The quantised form of one group of 32 channels of one token.
+struct GroupCodes {
+    uint32_t codes[2];   // 2-bit codes, channel c of the group at bit 2c of the 64-bit pair
+    uint32_t packed[8];  // int8 residual codes, channel c in byte c % 4 of word c / 4
+    __half scale, zero, rscale;
+    bool bad;            // a key outside the fp16 range, or NaN
+};
+
+__device__ __forceinline__ void load_words(const __nv_bfloat16 *src, uint32_t (&u)[16]) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const uint4 w = __ldg(p + i);
+        u[4 * i] = w.x;
+        u[4 * i + 1] = w.y;
+        u[4 * i + 2] = w.z;
+        u[4 * i + 3] = w.w;
+    }
+}
+
+// Group scale and zero (and the range check) from the 32 keys in u (word m: channels 2m in the
+// low half, 2m+1 in the high half).
+__device__ __forceinline__ void group_params(const uint32_t (&u)[16], GroupCodes &o) {
+    // the NaN-propagating forms let the range check see a NaN key
+    __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162 *>(&u[0]);
+    __nv_bfloat162 mx2 = mn2;
+#pragma unroll
+    for (int m = 1; m < 16; m++) {
+        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&u[m]);
+        mn2 = __hmin2_nan(mn2, v);
+        mx2 = __hmax2_nan(mx2, v);
+    }
+    float mn = __bfloat162float(__hmin_nan(mn2.x, mn2.y));
+    float mx = __bfloat162float(__hmax_nan(mx2.x, mx2.y));
+    o.bad = !(fabsf(mn) < 65504.0f) || !(fabsf(mx) < 65504.0f);
+    if (mn == 0.0f) mn = 0.0f;  // a signed-zero extreme counts as +0
+    if (mx == 0.0f) mx = 0.0f;
+    o.zero = __float2half_rn(mn);
+    o.scale = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+}
+
+// Quantise the group held in u (word m: channels 2m in the low half, 2m+1 in the high half).
+__device__ __forceinline__ void quantize_group(const uint32_t (&u)[16], GroupCodes &o) {
+    group_params(u, o);
+    const float zf = __half2float(o.zero);
+    const float sf = __half2float(o.scale);
+    const float r3 = sf == 0.0f ? 0.0f : __frcp_rn(__fmul_rn(sf, 3.0f));  // 3 sf is exact
+
+    // stage A: 2-bit codes and the residual r = x - x^2. The codes are summed as code * 4^c in
+    // fp32 (exact: each sum stays below 2^24), 12 + 4 channels per 32-bit word.
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float r[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 32; c++) {
+        const float x = (c & 1) ? bf16_hi(u[c >> 1]) : bf16_lo(u[c >> 1]);
+        const float code = code2_of(__fsub_rn(x, zf), sf, r3);
+        const int part = (c >> 4) * 2 + ((c & 15) >= 12);
+        const float weight = (float)(1u << (2 * ((c & 15) % 12)));
+        acc[part] = __fmaf_rn(code, weight, acc[part]);
+        r[c] = __fsub_rn(x, __fmaf_rn(code, sf, zf));
+        amax = fmaxf(amax, fabsf(r[c]));
+    }
+    o.codes[0] = __float2uint_rn(acc[0]) | (__float2uint_rn(acc[1]) << 24);
+    o.codes[1] = __float2uint_rn(acc[2]) | (__float2uint_rn(acc[3]) << 24);
+
+    o.rscale = __float2half_rn(__fdiv_rn(amax, 127.0f));
+    const float sr = __half2float(o.rscale);
+    const float r254 = sr == 0.0f ? 0.0f : __frcp_rn(__fmul_rn(sr, 254.0f));  // exact product
+
+    // stage B: symmetric int8 residual codes, four channels per word
+#pragma unroll
+    for (int w = 0; w < 8; w++) {
+        uint32_t b[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) b[e] = code8_of(r[4 * w + e], sr, r254);
+        o.packed[w] = __byte_perm(__byte_perm(b[0], b[1], 0x0040),
+                                  __byte_perm(b[2], b[3], 0x0040), 0x5410);
+    }
+}
+
+// Write group g of token `row` into the tile's thumbnail and residual records.
+__device__ __forceinline__ void store_group(const GroupCodes &o, uint8_t *trec, uint8_t *rrec,
+                                            int row, int g) {
+    *reinterpret_cast<uint2 *>(trec + row * kThumbRow + 8 * g) = make_uint2(o.codes[0], o.codes[1]);
+    // residual chunk j = 2g + s (channels 16 j .. 16 j + 15) is stored at chunk j ^ (row % 8)
+#pragma unroll
+    for (int s = 0; s < 2; s++) {
+        const int j = 2 * g + s;
+        *reinterpret_cast<uint4 *>(rrec + row * kD + 16 * (j ^ (row & 7))) = make_uint4(
+            o.packed[4 * s], o.packed[4 * s + 1], o.packed[4 * s + 2], o.packed[4 * s + 3]);
+    }
+    reinterpret_cast<__half *>(trec + kThumbScaleOff)[row * kGroups + g] = o.scale;
+    reinterpret_cast<__half *>(trec + kThumbZeroOff)[row * kGroups + g] = o.zero;
+    reinterpret_cast<__half *>(rrec + kResidScaleOff)[row * kGroups + g] = o.rscale;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(256, 4) quantize_keys_kernel(
+    int P, int Hkv, const int32_t *__restrict__ page_ids, const __nv_bfloat16 *__restrict__ k,
+    uint8_t *__restrict__ thumb, uint8_t *__restrict__ resid, int *err) {
+    int page = blockIdx.x / Hkv;
+    const int h = blockIdx.x - page * Hkv;
     if (page_ids) {
         page = page_ids[page];
         if (page < 0 || page >= P) {
-            if (lane == 0 && slot == 0 && h == 0) raise_error(err, FFD_ERRBIT_BOUNDS);
-            return;
+            if (threadIdx.x == 0 && h == 0) raise_error(err, FFD_ERRBIT_BOUNDS);
+            return;  // CTA-uniform
         }
     }
     const int64_t tile = (int64_t)page * Hkv + h;
-    const int64_t row = tile * kPage + slot;
+    const int row = threadIdx.x >> 2;
+    const int g = threadIdx.x & 3;
+    uint32_t u[16];
+    load_words(k + (tile * kPage + row) * kD + 32 * g, u);
+    GroupCodes o;
+    quantize_group(u, o);
+    if (o.bad) raise_error(err, FFD_ERRBIT_RANGE);
+    store_group(o, thumb + tile * kThumbRec, resid + tile * kResidRec, row, g);
+}
 
-    // 4 consecutive channels per lane (8 bytes of bf16)
-    const uint2 raw = *reinterpret_cast<const uint2 *>(k + row * kD + 4 * lane);
-    float x[4];
-    x[0] = __uint_as_float(raw.x << 16);
-    x[1] = __uint_as_float(raw.x & 0xffff0000u);
-    x[2] = __uint_as_float(raw.y << 16);
-    x[3] = __uint_as_float(raw.y & 0xffff0000u);
-
-    bool bad = false;
-#pragma unroll
-    for (int c = 0; c < 4; c++) bad |= !(fabsf(x[c]) < 65504.0f);
-    if (bad) raise_error(err, FFD_ERRBIT_RANGE);
-
-    float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
-    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-    mn = group8_min(mn);
-    mx = group8_max(mx);
-    if (mn == 0.0f) mn = 0.0f;  // a signed-zero extreme counts as +0
-    if (mx == 0.0f) mx = 0.0f;
-
-    const __half zf16 = __float2half_rn(mn);
-    const __half sf16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
-    const float zf = __half2float(zf16);
-    const float sf = __half2float(sf16);
-
-    uint32_t codes = 0;
-    float r[4];
-    float amax = 0.0f;
-#pragma unroll
-    for (int c = 0; c < 4; c++) {
-        float code = 0.0f;
-        if (sf != 0.0f) {
-            code = rintf(__fdiv_rn(__fsub_rn(x[c], zf), sf));
-            code = fminf(fmaxf(code, 0.0f), 3.0f);
-        }
-        codes |= (uint32_t)code << (2 * c);
-        const float xh = __fmaf_rn(code, sf, zf);
-        r[c] = __fsub_rn(x[c], xh);
-        amax = fmaxf(amax, fabsf(r[c]));
+// Append: four threads per (sequence, KV head), one channel group each. The new token of
+// sequence b goes to row p % 64 of page block_table[b][p / 64], p = positions[b].
+__global__ void __launch_bounds__(128) append_kv_kernel(
+    int B, int Hkv, int P, int max_blocks, const int32_t *__restrict__ positions,
+    const int32_t *__restrict__ block_table, const __nv_bfloat16 *__restrict__ k_new,
+    const __nv_bfloat16 *__restrict__ v_new, uint8_t *__restrict__ thumb,
+    uint8_t *__restrict__ resid, __nv_bfloat16 *__restrict__ v_cache,
+    __nv_bfloat16 *__restrict__ k_cache, int *err) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    const int th = t >> 2;  // (sequence, KV head) index b * Hkv + h
+    const int g = t & 3;
+    if (th >= B * Hkv) return;
+    const int b = th / Hkv;
+    const int h = th - b * Hkv;
+    const int pos = positions[b];
+    if (pos < 0) return;  // no token for this sequence in this step
+    if (pos >= max_blocks * kPage) {
+        if (g == 0 && h == 0) raise_error(err, FFD_ERRBIT_BOUNDS);
+        return;
     }
-    amax = group8_max(amax);
-    const __half sr16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
-    const float sr = __half2float(sr16);
-    uint32_t packed = 0;
+    const int page = block_table[(int64_t)b * max_blocks + pos / kPage];
+    if (page < 0 || page >= P) {
+        if (g == 0 && h == 0) raise_error(err, FFD_ERRBIT_BOUNDS);
+        return;
+    }
+    const int row = pos % kPage;
+    const int64_t tile = (int64_t)page * Hkv + h;
+    const int64_t src = (int64_t)th * kD;
+    const int64_t dst = (tile * kPage + row) * kD;
+    uint32_t u[16];
+    load_words(k_new + src + 32 * g, u);
+    GroupCodes o;
+    quantize_group(u, o);
+    if (o.bad) raise_error(err, FFD_ERRBIT_RANGE);
+    store_group(o, thumb + tile * kThumbRec, resid + tile * kResidRec, row, g);
+    const uint4 *vs = reinterpret_cast<const uint4 *>(v_new + src + 32 * g);
+    uint4 *vd = reinterpret_cast<uint4 *>(v_cache + dst + 32 * g);
 #pragma unroll
-    for (int c = 0; c < 4; c++) {
-        float q8 = 0.0f;
-        if (sr != 0.0f) {
-            q8 = rintf(__fdiv_rn(r[c], sr));
-            q8 = fminf(fmaxf(q8, -127.0f), 127.0f);
-        }
-        packed |= ((uint32_t)(int)q8 & 0xffu) << (8 * c);
+    for (int i = 0; i < 4; i++) vd[i] = __ldg(vs + i);
+    if (k_cache) {
+        uint4 *kd = reinterpret_cast<uint4 *>(k_cache + dst + 32 * g);
+#pragma unroll
+        for (int i = 0; i < 4; i++) kd[i] = make_uint4(u[4 * i], u[4 * i + 1], u[4 * i + 2],
+                                                       u[4 * i + 3]);
     }
+}
 
-    uint8_t *trec = thumb + tile * kThumbRec;
-    uint8_t *rrec = resid + tile * kResidRec;
-    trec[slot * kThumbRow + lane] = (uint8_t)codes;
-    *reinterpret_cast<uint32_t *>(rrec + resid_offset(slot, 4 * lane)) = packed;
-    if ((lane & 7) == 0) {
-        const int g = lane >> 3;
-        reinterpret_cast<__half *>(trec + kThumbScaleOff)[slot * kGroups + g] = sf16;
-        reinterpret_cast<__half *>(trec + kThumbZeroOff)[slot * kGroups + g] = zf16;
-        reinterpret_cast<__half *>(rrec + kResidScaleOff)[slot * kGroups + g] = sr16;
-    }
+cudaError_t launch_append(int B, int Hkv, int P, int max_blocks, const int32_t *positions,
+                          const int32_t *block_table, const void *k_new, const void *v_new,
+                          uint8_t *thumb, uint8_t *resid, void *v_cache, void *k_cache, int *err,
+                          cudaStream_t stream) {
+    const int64_t threads = (int64_t)B * Hkv * 4;
+    const unsigned blocks = (unsigned)((threads + 127) / 128);
+    append_kv_kernel<<<blocks, 128, 0, stream>>>(
+        B, Hkv, P, max_blocks, positions, block_table, static_cast<const __nv_bfloat16 *>(k_new),
+        static_cast<const __nv_bfloat16 *>(v_new), thumb, resid,
+        static_cast<__nv_bfloat16 *>(v_cache), static_cast<__nv_bfloat16 *>(k_cache), err);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(int P, int Hkv, const int32_t *page_ids, int num_pages_listed,
                             const void *k, uint8_t *thumb, uint8_t *resid, int *err,
                             cudaStream_t stream) {
-    const int64_t rows = (int64_t)num_pages_listed * Hkv * kPage;
-    if (rows == 0) return cudaSuccess;
-    const int threads = 256;
-    const int64_t blocks = (rows * 32 + threads - 1) / threads;
-    quantize_keys_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
-        P, Hkv, (int)rows, page_ids, static_cast<const __nv_bfloat16 *>(k), thumb, resid, err);
+    const int64_t tiles = (int64_t)num_pages_listed * Hkv;
+    if (tiles == 0) return cudaSuccess;
+    if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+    quantize_keys_kernel<<<(unsigned)tiles, 256, 0, stream>>>(
+        P, Hkv, page_ids, static_cast<const __nv_bfloat16 *>(k), thumb, resid, err);
     return cudaGetLastError();
 }
 

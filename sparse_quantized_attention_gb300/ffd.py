@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
             L.ffd_quantize_keys.argtypes = [ctypes.POINTER(CacheDesc), P, P, P, P,
                                             ctypes.c_int32, P, P]
             L.ffd_quantize_keys.restype = st
+            L.ffd_append_kv.argtypes = [ctypes.POINTER(CacheDesc), ctypes.c_int32,
+                                        ctypes.c_int32] + [P] * 10
+            L.ffd_append_kv.restype = st
             L.ffd_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeParams)]
             L.ffd_decode_workspace_size.restype = ctypes.c_size_t
             L.ffd_dense_workspace_size.argtypes = [ctypes.POINTER(DecodeParams)]
@@ -154,6 +157,18 @@ def ffd_quantize_keys(k: torch.Tensor, cache: QuantizedCache, *, page_ids=None,
     _check(lib().ffd_quantize_keys(ctypes.byref(desc), _ptr(k), *map(_ptr, cache),
                                    _ptr(page_ids), n_ids, _ptr(error_word), _stream(stream)),
            "ffd_quantize_keys")
+
+
+def ffd_append_kv(k_new, v_new, positions, block_table, cache: QuantizedCache, v_cache, *,
+                  k_cache=None, error_word=None, stream=None) -> None:
+    """Append one token per sequence: k_new, v_new bf16 [B,Hkv,128] go to row p % 64 of page
+    block_table[b, p // 64], p = positions[b] (negative: nothing for that sequence)."""
+    P, Hkv = v_cache.shape[0], v_cache.shape[1]
+    desc = CacheDesc(P, Hkv, v_cache.shape[3], v_cache.shape[2])
+    _check(lib().ffd_append_kv(ctypes.byref(desc), k_new.shape[0], block_table.shape[1],
+                               _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(block_table),
+                               *map(_ptr, cache), _ptr(v_cache), _ptr(k_cache),
+                               _ptr(error_word), _stream(stream)), "ffd_append_kv")
 
 
 def ffd_decode_workspace_size(params: DecodeParams) -> int:

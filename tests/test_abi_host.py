@@ -32,7 +32,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for want in ("ffd_quantize_keys", "ffd_decode_attention", "ffd_dense_decode",
+    for want in ("ffd_quantize_keys", "ffd_append_kv", "ffd_decode_attention", "ffd_dense_decode",
                  "ffd_decode_workspace_size", "ffd_dense_workspace_size", "ffd_get_error",
                  "ffd_status_string", "ffd_version"):
         assert want in names
@@ -134,3 +134,23 @@ def test_quantize_rejects_bad_arguments(lib):
     assert call(ffd.CacheDesc(4, 2, 128, 32)) == 2
     assert call(good, ids=FAKE, nids=-1) == 1
     assert call(good, k=FAKE + 8) == 1
+
+
+def test_append_rejects_bad_arguments(lib):
+    good = ffd.CacheDesc(4, 2, 128, 64)
+
+    def call(d=good, batch=2, mb=3, **kw):
+        a = dict(kn=FAKE, vn=FAKE, pos=FAKE, bt=FAKE, th=FAKE, rs=FAKE, v=FAKE, k=None)
+        a.update(kw)
+        return lib.ffd_append_kv(ctypes.byref(d), batch, mb, *[a[x] for x in (
+            "kn", "vn", "pos", "bt", "th", "rs", "v", "k")], None, None)
+
+    for key in ("kn", "vn", "pos", "bt", "th", "rs", "v"):
+        assert call(**{key: None}) == 1, key
+    assert call(batch=0) == 1
+    assert call(mb=0) == 1
+    assert call(d=ffd.CacheDesc(0, 2, 128, 64)) == 1
+    assert call(d=ffd.CacheDesc(4, 2, 64, 64)) == 2
+    assert call(d=ffd.CacheDesc(4, 2, 128, 16)) == 2
+    assert call(kn=FAKE + 2) == 1
+    assert call(k=FAKE + 4) == 1
