@@ -233,7 +233,7 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0}, "fallback"
 
 
-MAIN_KERNEL_SOURCES = ("decode.cu", "splitkv.cuh", "common.cuh", "ptx.cuh")
+MAIN_KERNEL_SOURCES = ("decode.cu", "scan.cuh", "splitkv.cuh", "common.cuh", "ptx.cuh")
 
 
 def main_kernel_sha256():
@@ -541,12 +541,70 @@ def peaked_variant(a, w, delta, dev, ffd, torch, upload, dense_ms):
     torch.cuda.synchronize(dev)
     ms = e0.elapsed_time(e1) / a.steps
     nb_total = int(sum((int(n) + 63) // 64 for n in inp.seq_lens)) * w.num_kv_heads
+
+    def timed(fn, reps=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps * 1e3
+
+    # the delta sweep: sparsity and step time of the Top-delta rule
+    sweep = []
+    for dl in (2.0, 5.0, 7.0, 10.0, math.inf):
+        pd = ffd.make_params(w.batch, w.num_q_heads, w.num_kv_heads, P, inp.max_blocks,
+                             sink=w.sink, local=w.local, delta=dl, sm_scale=sm)
+        mk = torch.zeros_like(mask)
+        ffd.ffd_decode_attention(pd, d["q"], qc, d["v"], d["seq_lens"], d["block_table"], out,
+                                 ws, keep_mask=mk)
+        us = timed(lambda: ffd.ffd_decode_attention(pd, d["q"], qc, d["v"], d["seq_lens"],
+                                                    d["block_table"], out, ws))
+        sweep.append({"delta": dl if math.isfinite(dl) else "inf", "us": round(us, 2),
+                      "sparsity": round(1 - int(mk.sum()) / nb_total, 4)})
+    # the comparison selectors on the same thumbnails: Top-k at the budget Top-delta used (its
+    # mean kept non-forced blocks per unit), Top-p at p = 0.9 and 0.99; select + attention
+    sws = ffd.alloc_select_workspace(params, device=dev)
+    smask = torch.zeros_like(mask)
+    forced_total = sum(forced_count(int(n), w.sink, w.local) for n in inp.seq_lens) * w.num_kv_heads
+    k_budget = max(0, round((int(keep.sum()) - forced_total) / (w.batch * w.num_kv_heads)))
+    selectors = {}
+    for name, sel, budget in (("top_k", ffd.SELECT_TOPK, float(k_budget)),
+                              ("top_p_0.9", ffd.SELECT_TOPP, 0.9),
+                              ("top_p_0.99", ffd.SELECT_TOPP, 0.99)):
+        def select():
+            ffd.ffd_select_blocks(params, sel, budget, d["q"], qc, d["seq_lens"],
+                                  d["block_table"], smask, sws)
+
+        def attend():
+            ffd.ffd_decode_attention_masked(params, d["q"], qc, d["v"], d["seq_lens"],
+                                            d["block_table"], smask, out, ws)
+        select()
+        t_sel = timed(select)
+        t_att = timed(attend)
+        selectors[name] = {"budget": budget, "select_us": round(t_sel, 2),
+                           "attention_us": round(t_att, 2),
+                           "step_us": round(t_sel + t_att, 2),
+                           "sparsity": round(1 - int(smask.sum()) / nb_total, 4)}
+    if ffd.ffd_get_error(ws) != 0 or ffd.ffd_get_error(sws) != 0:
+        raise RuntimeError("device error in the selector comparison")
     del d, qc
     return {"signal_scale": round(ffd_synth.peaked_scale(), 4), "us_per_step": round(ms * 1e3, 2),
+            "delta_sweep": sweep, "selectors": selectors,
             "needed_bytes_per_step": by["step"], "gbs": round(by["step"] / (ms * 1e-3) / 1e9, 1),
             "sparsity": round(1 - int(keep.sum()) / nb_total, 4),
             "speedup_vs_dense": round(dense_ms / ms, 3),
             "effective_kv_tokens_per_s": round(float(np.sum(inp.seq_lens)) / (ms * 1e-3), 1)}
+
+
+def forced_count(n, sink, local):
+    """Blocks of a length-n sequence that hold a sink or local token."""
+    nb = (n + 63) // 64
+    return sum(1 for c in range(nb)
+               if any(j < sink or j >= n - local for j in range(64 * c, min(n, 64 * c + 64))))
 
 
 def cpu_baseline(w, inp, keep, delta, sm):

@@ -225,6 +225,64 @@ ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
                             const int32_t *block_table, float *out, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/* Comparison selectors of ffd_select_blocks. */
+#define FFD_SELECT_TOPK 1
+#define FFD_SELECT_TOPP 2
+
+/*
+ * Bytes of device workspace that ffd_select_blocks needs for these parameters (0 for parameters
+ * it would reject, including max_blocks_per_seq > 16384).
+ */
+size_t ffd_select_workspace_size(const ffd_decode_params *params);
+
+/*
+ * ffd_select_blocks -- choose blocks by one of the comparison rules the method is measured
+ * against: fixed-budget Top-k or distribution-adaptive Top-p on the same thumbnail scores.
+ * Source: Problem statement (the selection dilemma: Top-k does not adapt to attention entropy;
+ * Top-p needs a global softmax and a sort). The pages give no detailed definition; this library's:
+ *   s^_ij = sm_scale * q_i . x^2_j (thumbnail only, as in stage 2 of ffd_decode_attention);
+ *   Top-k (selector FFD_SELECT_TOPK, budget = k, a non-negative integer): importance of block c =
+ *     max over the group's heads i and its tokens j < n of s^_ij; the k non-forced blocks of
+ *     largest importance are kept (ties: lower block index first);
+ *   Top-p (FFD_SELECT_TOPP, budget = p in (0, 1]): per head i, P_ij = softmax over all j < n of
+ *     s^_ij and block mass m_ic = sum of P_ij over the block; blocks ranked by mass (descending,
+ *     ties: lower index first) are kept while the masses ranked before them sum to less than p
+ *     (the shortest prefix reaching p); the union over the group's heads is kept.
+ * Both keep the blocks holding a sink or local token, like ffd_decode_attention.
+ *   params      as for ffd_decode_attention (delta is ignored)
+ *   q_bf16, thumb, seq_lens, block_table   as for ffd_decode_attention
+ *   keep_mask   device u8 [B][Hkv][max_blocks_per_seq] output: 1 = kept; entries at or past
+ *               ceil(n/64) are set to 0
+ *   workspace   device, >= ffd_select_workspace_size(params) bytes, 256-byte aligned; its first
+ *               4 bytes are the device error word (zero it before first use)
+ * Two kernel launches (a pass over every thumbnail, then one CTA per (sequence, KV head) that
+ * sorts its blocks). Errors: as ffd_decode_attention; FFD_ERR_INVALID_ARG for a bad selector or
+ * budget; FFD_ERRBIT_BOUNDS for a block-table entry outside [0, P) (that block scores -inf).
+ */
+ffd_status ffd_select_blocks(const ffd_decode_params *params, int32_t selector, float budget,
+                             const void *q_bf16, const uint8_t *thumb, const int32_t *seq_lens,
+                             const int32_t *block_table, uint8_t *keep_mask, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/*
+ * ffd_decode_attention_masked -- stage 3 of the decode step over a caller-given block mask (for
+ * instance one from ffd_select_blocks): out_i = softmax over the tokens j < n of the given blocks
+ * of s_ij = sm_scale * q_i . K^_j, applied to V (the exact scores of ffd_decode_attention).
+ * Source: Methodology §3 (stage 3: exact attention over the selected blocks).
+ *   keep_in     device u8 [B][Hkv][max_blocks_per_seq]: nonzero = attend to the block. The mask
+ *               alone decides: sink and local blocks are not added.
+ *   keep_mask   device u8 [B][Hkv][max_blocks_per_seq] or NULL: the mask used (keep_in less the
+ *               blocks whose block-table entry is out of range)
+ *   other arguments, workspace rules and errors as ffd_decode_attention (delta is ignored;
+ *   m_tilde still reports the pseudo-max of the sink and local tokens).
+ */
+ffd_status ffd_decode_attention_masked(const ffd_decode_params *params, const void *q_bf16,
+                                       const uint8_t *thumb, const uint8_t *resid,
+                                       const void *v_bf16, const int32_t *seq_lens,
+                                       const int32_t *block_table, const uint8_t *keep_in,
+                                       float *out, uint8_t *keep_mask, float *m_tilde,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
 /*
  * ffd_decode_attention_static -- ffd_decode_attention without a caller-supplied workspace.
  * The paper has no counterpart: this entry point exists for callers that cannot allocate device

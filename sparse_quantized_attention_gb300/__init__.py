@@ -8,11 +8,14 @@ from .ffd import (CacheDesc, DecodeParams, FFDError, QuantizedCache, alloc_quant
                   ffd_decode_workspace_size,
                   ffd_dense_decode, ffd_dense_workspace_size, ffd_get_error, ffd_quantize_keys,
                   ffd_set_profile_events, ffd_status_string, ffd_version, lib, library_path,
-                  make_params)
+                  make_params, SELECT_TOPK, SELECT_TOPP, alloc_select_workspace,
+                  ffd_select_workspace_size, ffd_select_blocks, ffd_decode_attention_masked)
 
 __all__ = ["CacheDesc", "DecodeParams", "FFDError", "QuantizedCache", "alloc_quantized_cache",
            "alloc_workspace", "ffd_append_kv", "ffd_decode_attention", "ffd_decode_attention_static",
            "ffd_decode_workspace_size",
            "ffd_dense_decode", "ffd_dense_workspace_size", "ffd_get_error",
            "ffd_quantize_keys", "ffd_set_profile_events", "ffd_status_string", "ffd_version",
-           "lib", "library_path", "make_params"]
+           "lib", "library_path", "make_params", "SELECT_TOPK", "SELECT_TOPP",
+           "alloc_select_workspace", "ffd_select_workspace_size", "ffd_select_blocks",
+           "ffd_decode_attention_masked"]

@@ -16,6 +16,10 @@ cudaError_t launch_append(int B, int Hkv, int P, int max_blocks, const int32_t *
                           cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t stream);
 cudaError_t launch_dense(const DecodeArgs &a, int ctas, cudaStream_t stream);
+cudaError_t launch_select(const DecodeArgs &a, int selector, float budget, float *imp, float2 *ml,
+                          cudaStream_t stream);
+size_t select_smem_bytes(int max_blocks);
+int select_max_blocks();
 }  // namespace ffd
 
 using namespace ffd;
@@ -165,7 +169,7 @@ const char *ffd_status_string(ffd_status s) {
     return "FFD_ERR_UNKNOWN";
 }
 
-int32_t ffd_version(void) { return 201; }
+int32_t ffd_version(void) { return 202; }
 
 ffd_status ffd_quantize_keys(const ffd_cache_desc *cache, const void *k_bf16, uint8_t *thumb,
                              uint8_t *resid, const int32_t *page_ids, int32_t num_page_ids,
@@ -263,6 +267,104 @@ ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
     a.block_table = block_table;
     a.out = out;
     cudaError_t e = launch_dense(a, pl.ctas, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+}
+
+// Workspace of ffd_select_blocks: [error word | importance [units][max_blocks] f32 |
+// per-head (max, sum) [units][max_blocks][G] float2].
+struct SelectPlan {
+    size_t imp_off, ml_off, total;
+};
+
+ffd_status make_select_plan(const ffd_decode_params *p, SelectPlan *pl) {
+    ffd_status st = check_params(p);
+    if (st != FFD_OK) return st;
+    if (p->max_blocks_per_seq > select_max_blocks()) return FFD_ERR_UNSUPPORTED;
+    const size_t units = (size_t)p->batch * p->num_kv_heads;
+    const size_t G = (size_t)(p->num_q_heads / p->num_kv_heads);
+    pl->imp_off = kAlign;
+    pl->ml_off = align_up(pl->imp_off + units * p->max_blocks_per_seq * sizeof(float));
+    pl->total = align_up(pl->ml_off + units * p->max_blocks_per_seq * G * 2 * sizeof(float));
+    return FFD_OK;
+}
+
+size_t ffd_select_workspace_size(const ffd_decode_params *params) {
+    SelectPlan pl;
+    return make_select_plan(params, &pl) == FFD_OK ? pl.total : 0;
+}
+
+ffd_status ffd_select_blocks(const ffd_decode_params *params, int32_t selector, float budget,
+                             const void *q_bf16, const uint8_t *thumb, const int32_t *seq_lens,
+                             const int32_t *block_table, uint8_t *keep_mask, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    if (!q_bf16 || !thumb || !seq_lens || !block_table || !keep_mask || !workspace)
+        return FFD_ERR_INVALID_ARG;
+    if (!aligned16(thumb) || !aligned16(q_bf16) ||
+        (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+        return FFD_ERR_INVALID_ARG;
+    if (selector == FFD_SELECT_TOPK) {
+        if (!(budget >= 0.0f) || budget != floorf(budget) || budget > 2147483647.0f)
+            return FFD_ERR_INVALID_ARG;
+    } else if (selector == FFD_SELECT_TOPP) {
+        if (!(budget > 0.0f && budget <= 1.0f)) return FFD_ERR_INVALID_ARG;
+    } else {
+        return FFD_ERR_INVALID_ARG;
+    }
+    SelectPlan pl;
+    ffd_status st = make_select_plan(params, &pl);
+    if (st != FFD_OK) return st;
+    if (workspace_bytes < pl.total) return FFD_ERR_WORKSPACE;
+    DecodeArgs a{};
+    a.B = params->batch;
+    a.Hq = params->num_q_heads;
+    a.Hkv = params->num_kv_heads;
+    a.G = params->num_q_heads / params->num_kv_heads;
+    a.P = params->num_pages;
+    a.max_blocks = params->max_blocks_per_seq;
+    a.S = params->sink_tokens;
+    a.L = params->local_tokens;
+    a.sm_scale = params->sm_scale;
+    a.q = static_cast<const __nv_bfloat16 *>(q_bf16);
+    a.thumb = thumb;
+    a.seq_lens = seq_lens;
+    a.block_table = block_table;
+    a.keep_mask = keep_mask;
+    char *base = static_cast<char *>(workspace);
+    a.err = reinterpret_cast<int *>(base);
+    cudaError_t e = launch_select(a, selector, budget, reinterpret_cast<float *>(base + pl.imp_off),
+                                  reinterpret_cast<float2 *>(base + pl.ml_off),
+                                  static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+}
+
+ffd_status ffd_decode_attention_masked(const ffd_decode_params *params, const void *q_bf16,
+                                       const uint8_t *thumb, const uint8_t *resid,
+                                       const void *v_bf16, const int32_t *seq_lens,
+                                       const int32_t *block_table, const uint8_t *keep_in,
+                                       float *out, uint8_t *keep_mask, float *m_tilde,
+                                       void *workspace, size_t workspace_bytes, void *stream) {
+    if (!keep_in) return FFD_ERR_INVALID_ARG;
+    if (!q_bf16 || !thumb || !resid || !v_bf16 || !seq_lens || !block_table || !out || !workspace)
+        return FFD_ERR_INVALID_ARG;
+    if (!aligned16(thumb) || !aligned16(resid) || !aligned16(v_bf16) || !aligned16(q_bf16) ||
+        (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+        return FFD_ERR_INVALID_ARG;
+    Plan pl;
+    ffd_status st = make_decode_plan(params, &pl);
+    if (st != FFD_OK) return st;
+    if (workspace_bytes < pl.total) return FFD_ERR_WORKSPACE;
+    DecodeArgs a = make_args(params, pl, workspace);
+    a.q = static_cast<const __nv_bfloat16 *>(q_bf16);
+    a.thumb = thumb;
+    a.resid = resid;
+    a.v = static_cast<const __nv_bfloat16 *>(v_bf16);
+    a.seq_lens = seq_lens;
+    a.block_table = block_table;
+    a.out = out;
+    a.keep_mask = keep_mask;
+    a.keep_in = keep_in;
+    a.m_tilde = m_tilde;
+    cudaError_t e = launch_decode(a, pl.ctas, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
 }
 

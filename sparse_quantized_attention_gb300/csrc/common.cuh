@@ -45,6 +45,7 @@ struct DecodeArgs {
     const int32_t *seq_lens, *block_table;
     float *out;
     uint8_t *keep_mask;
+    const uint8_t *keep_in;  // optional [B][Hkv][max_blocks] given block mask (replaces Top-delta)
     float *m_tilde;
     int *err;        // device error word
     float *ws_m1;    // [B*Hkv][nf][kMaxG] stage-1 block maxima over the sink / local tokens

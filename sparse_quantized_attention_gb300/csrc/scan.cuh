@@ -1,0 +1,137 @@
+// scan.cuh -- the stage-2 provisional scores on the tensor cores, shared by the FFD decode kernel
+// and the comparison selectors: query operands of a (sequence, KV head) unit, and the scores
+// s^ = sm * q . x^2 of 16 x 8 (token, head) tiles of a thumbnail record.
+//
+// Source: "Faster Than Flash", Methodology §1 (2-bit thumbnails as a fast proxy for importance)
+// and §3 (stage 2 streams the 2-bit keys and computes provisional scores).
+//
+// Tensor-core operands (mma.sync m16n8k16, bf16 in, fp32 accumulate; 16 tokens x 8 heads):
+// A = codes of 16 tokens, B = the GQA group's queries (heads as N, padded to 8). 2-bit codes enter
+// as bf16 bit patterns (code << s) with s <= 6: exponent field 0, so the value is exactly
+// code * 2^s * 2^-133. B holds q * 2^(kKq - s), so every product is exactly code * q * 2^(kKq-133)
+// and one LOP3 turns two codes into an operand register. Channel order inside each 16-channel
+// MMA step is permuted (the same permutation on A and B); a dot product does not depend on it.
+#pragma once
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace ffd {
+
+constexpr int kKq = 100;             // q enters the MMA scaled by 2^kKq (|q| < 2^27 required)
+constexpr float kUnscale = 8589934592.0f;      // 2^(133 - kKq)
+constexpr float kQMax = 134217728.0f;          // 2^27
+
+// ------------------------------------------------------------------------------------------
+// Query operands. Thread (g = lane/4, tig = lane%4) holds the B fragments of head g and, for the
+// epilogue, the per-group query sums of heads 2*tig and 2*tig+1.
+// ------------------------------------------------------------------------------------------
+struct ThumbOps {
+    uint32_t bt0[8], bt1[8];  // chunk kc = channels 16kc .. 16kc+15, head g
+    float qs[2][4];           // sum of q over group gg for heads 2tig, 2tig+1
+};
+
+// Per-group query sums of heads 2tig, 2tig+1, from this thread's partial sums of head g over the
+// channels c = tig (mod 4): quad reduction, then fetch from the quads of heads 2tig and 2tig+1.
+__device__ __forceinline__ void group_sums(float (&part)[4], int tig, float (&qs)[2][4]) {
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) {
+        part[gg] += __shfl_xor_sync(0xffffffffu, part[gg], 1);
+        part[gg] += __shfl_xor_sync(0xffffffffu, part[gg], 2);
+    }
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) {
+        qs[0][gg] = __shfl_sync(0xffffffffu, part[gg], 8 * tig);
+        qs[1][gg] = __shfl_sync(0xffffffffu, part[gg], 8 * tig + 4);
+    }
+}
+
+__device__ __forceinline__ const __nv_bfloat16 *q_row(const DecodeArgs &a, int b, int h, int g) {
+    return a.q + ((size_t)b * a.Hq + h * a.G + (g < a.G ? g : 0)) * kD;
+}
+
+__device__ __forceinline__ void load_thumb_ops(const DecodeArgs &a, int b, int h, int lane,
+                                               ThumbOps &Q) {
+    const int g = lane >> 2, tig = lane & 3;
+    const bool hv = g < a.G;
+    const __nv_bfloat16 *qrow = q_row(a, b, h, g);
+    float big = 0.0f;
+    auto ld = [&](int c) {
+        const float v = hv ? __bfloat162float(qrow[c]) : 0.0f;
+        big = fmaxf(big, fabsf(v));
+        return v;
+    };
+    const float st = __int_as_float((127 + kKq - 2 * tig) << 23);  // 2^(kKq - 2 tig)
+    float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int kc = 0; kc < 8; kc++) {
+        const float x0 = ld(16 * kc + tig), x1 = ld(16 * kc + 8 + tig);
+        const float x2 = ld(16 * kc + 4 + tig), x3 = ld(16 * kc + 12 + tig);
+        Q.bt0[kc] = pack_bf16x2(x0 * st, x1 * st);
+        Q.bt1[kc] = pack_bf16x2(x2 * st, x3 * st);
+        part[kc >> 1] += (x0 + x1) + (x2 + x3);
+    }
+    group_sums(part, tig, Q.qs);
+    if (!(big < kQMax)) raise_error(a.err, FFD_ERRBIT_RANGE);
+}
+
+// D[gg] = sum over group gg of q . code (scaled by 2^(kKq-133)) for rows (g, g+8) x heads.
+__device__ __forceinline__ void thumb_mma(float (&D)[4][4], const uint32_t (&w0)[8],
+                                          const uint32_t (&w1)[8], uint32_t m0,
+                                          const ThumbOps &Q) {
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) D[gg][0] = D[gg][1] = D[gg][2] = D[gg][3] = 0.0f;
+#pragma unroll
+    for (int kc = 0; kc < 8; kc++) {
+        const uint32_t a0 = w0[kc] & m0, a1 = w1[kc] & m0;
+        const uint32_t a2 = (w0[kc] >> 8) & m0, a3 = (w1[kc] >> 8) & m0;
+        mma_bf16(D[kc >> 1], a0, a1, a2, a3, Q.bt0[kc], Q.bt1[kc]);
+    }
+}
+
+__device__ __forceinline__ void unpack4h(uint2 v, float (&f)[4]) {
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+    f[0] = lo.x;
+    f[1] = lo.y;
+    f[2] = hi.x;
+    f[3] = hi.y;
+}
+
+// Provisional score s^ = sm * sum_g (scale_g q_g.c_g + zero_g sum(q_g)) of accumulator entry e.
+__device__ __forceinline__ float est_score(const float (&D)[4][4], int e, const float (&sf)[4],
+                                           const float (&zf)[4], const float (&qs)[4], float sm) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++)
+        acc = fmaf(sf[gg] * kUnscale, D[gg][e], fmaf(zf[gg], qs[gg], acc));
+    return acc * sm;
+}
+
+// Provisional scores of one m-tile (rows r0 = 16 mt + g and r1 = r0 + 8 of a thumbnail block in
+// shared memory), for heads 2tig, 2tig+1: {(r0,h0), (r0,h1), (r1,h0), (r1,h1)}.
+__device__ __forceinline__ float4 scan_tile(const uint8_t *base, int r0, int r1, uint32_t m0,
+                                            const ThumbOps &Q, float sm) {
+    const uint4 *c0 = reinterpret_cast<const uint4 *>(base + r0 * kThumbRow);
+    const uint4 *c1 = reinterpret_cast<const uint4 *>(base + r1 * kThumbRow);
+    const uint4 p0 = c0[0], p1 = c0[1], p2 = c1[0], p3 = c1[1];
+    const uint32_t w0[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    const uint32_t w1[8] = {p2.x, p2.y, p2.z, p2.w, p3.x, p3.y, p3.z, p3.w};
+    float D[4][4];
+    thumb_mma(D, w0, w1, m0, Q);
+    float sf0[4], sf1[4], zf0[4], zf1[4];
+    const uint2 *ts = reinterpret_cast<const uint2 *>(base + kThumbScaleOff);
+    const uint2 *tz = reinterpret_cast<const uint2 *>(base + kThumbZeroOff);
+    unpack4h(ts[r0], sf0);
+    unpack4h(ts[r1], sf1);
+    unpack4h(tz[r0], zf0);
+    unpack4h(tz[r1], zf1);
+    float4 e;
+    e.x = est_score(D, 0, sf0, zf0, Q.qs[0], sm);
+    e.y = est_score(D, 1, sf0, zf0, Q.qs[1], sm);
+    e.z = est_score(D, 2, sf1, zf1, Q.qs[0], sm);
+    e.w = est_score(D, 3, sf1, zf1, Q.qs[1], sm);
+    return e;
+}
+
+}  // namespace ffd

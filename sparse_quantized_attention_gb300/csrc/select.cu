@@ -1,0 +1,280 @@
+// select.cu -- the comparison block selectors Top-k and Top-p on the FFD thumbnails.
+//
+// Source: "Faster Than Flash", Problem statement (the selection dilemma: a fixed-budget Top-k does
+// not adapt to the attention entropy, a distribution-adaptive Top-p needs a global softmax and a
+// sort, which breaks a streaming pipeline). Both rank the same 64-token blocks as Top-delta, on
+// the same provisional scores s^_ij = sm * q_i . x^2_j (Methodology §3, stage 2), and keep the same
+// always-kept sink and local blocks (Methodology §2). Definitions (the pages give none in detail):
+//   Top-k: importance of block c = max over the group's heads i and its tokens j < n of s^_ij;
+//          keep the k non-forced blocks of largest importance (ties: lower block index first).
+//   Top-p: per head i, P_ij = softmax over all j < n of s^_ij, block mass m_ic = sum of P_ij over
+//          the block; rank blocks by mass (descending, ties: lower index first) and keep a block
+//          when the masses ranked before it sum to less than p; union over the heads.
+//
+// Two passes, as the rules require (the whole sequence must be scored before anything is chosen):
+//   block_stats_kernel  streams every thumbnail record once and writes, per block, its importance
+//                       and, per head, the block's (max s^, sum of e^(s^ - max)) pair;
+//   select_kernel       one CTA per (sequence, KV head): a bitonic sort of the blocks in shared
+//                       memory (and, for Top-p, the global softmax normalisation and a prefix sum
+//                       per head), then the keep mask.
+// The chosen mask then goes to the decode kernel as a given mask (ffd_decode_attention_masked).
+#include "common.cuh"
+#include "ptx.cuh"
+#include "scan.cuh"
+
+namespace ffd {
+
+namespace {
+
+constexpr int kStatBlocks = 8;     // blocks per CTA of the statistics pass
+constexpr int kSelThreads = 1024;  // threads of the selection CTA
+constexpr int kSelMaxBlocks = 16384;
+constexpr float kLog2e = 1.4426950408889634f;  // 1 / ln 2
+
+__device__ __forceinline__ int stat_len(const DecodeArgs &a, int b) {
+    int n = a.seq_lens[b];
+    const int cap = a.max_blocks * kPage;
+    if (n < 0 || n > cap) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) raise_error(a.err, FFD_ERRBIT_BOUNDS);
+        n = n < 0 ? 0 : cap;
+    }
+    return n;
+}
+
+// Pass 1. CTA (x, u) takes blocks kStatBlocks x .. of unit u; warp mt scores rows 16mt .. 16mt+15
+// of each block for every head of the group (scan_tile), straight from the record in global
+// memory. Block importance -> imp[u][c]; per head (max, sum e^(s^ - max)) -> ml[u][c][G].
+__global__ void __launch_bounds__(128) block_stats_kernel(DecodeArgs a, float *imp, float2 *ml) {
+    const int u = blockIdx.y;
+    const int b = u / a.Hkv, h = u - b * a.Hkv;
+    const int n = stat_len(a, b);
+    const int nb = (n + kPage - 1) / kPage;
+    const int c0 = blockIdx.x * kStatBlocks;
+    if (c0 >= nb) return;  // CTA-uniform
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;
+    const int r0 = 16 * warp + g, r1 = r0 + 8;
+    const uint32_t m0 = 0x00030003u << (2 * tig);
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;
+    ThumbOps Q;
+    load_thumb_ops(a, b, h, lane, Q);
+    __shared__ float s_imp[4];
+    __shared__ float2 s_ml[4][kMaxG];
+    for (int c = c0; c < c0 + kStatBlocks && c < nb; c++) {
+        const int page = a.block_table[(size_t)b * a.max_blocks + c];
+        const bool bad = page < 0 || page >= a.P;  // block-uniform
+        if (bad && threadIdx.x == 0) raise_error(a.err, FFD_ERRBIT_BOUNDS);
+        float4 e = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (!bad) e = scan_tile(a.thumb + ((size_t)page * a.Hkv + h) * kThumbRec, r0, r1, m0, Q,
+                                a.sm_scale);
+        const bool v0 = c * kPage + r0 < n, v1 = c * kPage + r1 < n;
+        const bool w0 = h0 < a.G, w1 = h1 < a.G;
+        const float x00 = v0 && w0 ? e.x : -INFINITY, x01 = v0 && w1 ? e.y : -INFINITY;
+        const float x10 = v1 && w0 ? e.z : -INFINITY, x11 = v1 && w1 ? e.w : -INFINITY;
+        // importance: max over the warp's rows and every head
+        const float wm = warp_max(fmaxf(fmaxf(x00, x01), fmaxf(x10, x11)));
+        // per head: max over the warp's 16 rows (lanes with the same tig), then the sum
+        float mh0 = fmaxf(x00, x10), mh1 = fmaxf(x01, x11);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            mh0 = fmaxf(mh0, __shfl_xor_sync(0xffffffffu, mh0, o));
+            mh1 = fmaxf(mh1, __shfl_xor_sync(0xffffffffu, mh1, o));
+        }
+        const float b0 = mh0 == -INFINITY ? 0.0f : mh0, b1 = mh1 == -INFINITY ? 0.0f : mh1;
+        float l0 = ex2_approx((x00 - b0) * kLog2e) + ex2_approx((x10 - b0) * kLog2e);
+        float l1 = ex2_approx((x01 - b1) * kLog2e) + ex2_approx((x11 - b1) * kLog2e);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+        }
+        if (lane == 0) s_imp[warp] = wm;
+        if (g == 0) {
+            s_ml[warp][h0] = make_float2(mh0, l0);
+            s_ml[warp][h1] = make_float2(mh1, l1);
+        }
+        __syncthreads();
+        const size_t slot = (size_t)u * a.max_blocks + c;
+        if (threadIdx.x == 0)
+            imp[slot] = fmaxf(fmaxf(s_imp[0], s_imp[1]), fmaxf(s_imp[2], s_imp[3]));
+        if (threadIdx.x < a.G) {
+            const int hh = threadIdx.x;
+            float M = -INFINITY;
+            for (int w = 0; w < 4; w++) M = fmaxf(M, s_ml[w][hh].x);
+            float L = 0.0f;
+            if (M != -INFINITY)
+                for (int w = 0; w < 4; w++)
+                    if (s_ml[w][hh].x != -INFINITY)
+                        L += s_ml[w][hh].y * ex2_approx((s_ml[w][hh].x - M) * kLog2e);
+            ml[slot * a.G + hh] = make_float2(M, L);
+        }
+        __syncthreads();
+    }
+}
+
+// Float -> unsigned key whose unsigned order is the float's order (NaN never occurs here).
+__device__ __forceinline__ uint32_t ordered(float f) {
+    const uint32_t x = __float_as_uint(f);
+    return (x & 0x80000000u) ? ~x : (x | 0x80000000u);
+}
+
+// Ascending bitonic sort of key[0 .. N), N a power of two, by the whole CTA.
+__device__ void bitonic_sort(uint64_t *key, int N) {
+    for (int k = 2; k <= N; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < N; i += blockDim.x) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const uint64_t x = key[i], y = key[ixj];
+                    if ((x > y) == ((i & k) == 0)) {
+                        key[i] = y;
+                        key[ixj] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+__device__ __forceinline__ float block_max_reduce(float v, float *red) {
+    v = warp_max(v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = -INFINITY;
+    for (int w = 0; w < kSelThreads / 32; w++) r = fmaxf(r, red[w]);
+    __syncthreads();
+    return r;
+}
+
+__device__ __forceinline__ float block_sum_reduce(float v, float *red) {
+    v = warp_sum(v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = 0.0f;
+    for (int w = 0; w < kSelThreads / 32; w++) r += red[w];
+    __syncthreads();
+    return r;
+}
+
+// Pass 2: one CTA of kSelThreads per unit. Shared memory: keys [N] u64, mass [N] f32, keep [N] u8,
+// N = the block count rounded up to a power of two.
+__global__ void __launch_bounds__(kSelThreads) select_kernel(DecodeArgs a, int selector, float budget,
+                                                             int N, const float *imp,
+                                                             const float2 *ml) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint64_t *key = reinterpret_cast<uint64_t *>(smem);
+    float *mass = reinterpret_cast<float *>(key + N);
+    uint8_t *keep = reinterpret_cast<uint8_t *>(mass + N);
+    __shared__ float red[kSelThreads / 32];
+    __shared__ float wsum[kSelThreads / 32];
+    const int u = blockIdx.x;
+    const int b = u / a.Hkv;
+    int n = a.seq_lens[b];
+    const int cap = a.max_blocks * kPage;
+    n = n < 0 ? 0 : (n > cap ? cap : n);
+    const int nb = (n + kPage - 1) / kPage;
+    const ForcedBlocks fb(n, a.S, a.L);
+    const size_t row = (size_t)u * a.max_blocks;
+    for (int c = threadIdx.x; c < N; c += blockDim.x) keep[c] = c < nb && fb.forced(c);
+    __syncthreads();
+
+    if (selector == FFD_SELECT_TOPK) {
+        for (int c = threadIdx.x; c < N; c += blockDim.x) {
+            const float v = c < nb ? imp[row + c] : -INFINITY;
+            const bool eligible = c < nb && !fb.forced(c) && v != -INFINITY;
+            key[c] = eligible ? ((uint64_t)(~ordered(v)) << 32) | (uint32_t)c : ~0ull;
+        }
+        __syncthreads();
+        bitonic_sort(key, N);
+        const int k = (int)budget;
+        for (int t = threadIdx.x; t < k && t < N; t += blockDim.x)
+            if (key[t] != ~0ull) keep[(uint32_t)key[t]] = 1;
+        __syncthreads();
+    } else {
+        const int per = (N + kSelThreads - 1) / kSelThreads;  // sorted positions per thread
+        for (int hh = 0; hh < a.G; hh++) {
+            // global softmax normalisation over the blocks: M = max, L = sum e^(m - M) l
+            float lm = -INFINITY;
+            for (int c = threadIdx.x; c < nb; c += blockDim.x)
+                if (ml[(row + c) * a.G + hh].y > 0.0f) lm = fmaxf(lm, ml[(row + c) * a.G + hh].x);
+            const float M = block_max_reduce(lm, red);
+            float ls = 0.0f;
+            for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+                const float2 v = ml[(row + c) * a.G + hh];
+                const float w = v.y > 0.0f ? v.y * ex2_approx((v.x - M) * kLog2e) : 0.0f;
+                mass[c] = w;
+                ls += w;
+            }
+            const float Ltot = block_sum_reduce(ls, red);
+            const float inv = Ltot > 0.0f ? 1.0f / Ltot : 0.0f;
+            for (int c = threadIdx.x; c < N; c += blockDim.x) {
+                const float m = c < nb ? mass[c] * inv : 0.0f;
+                key[c] = c < nb ? ((uint64_t)(~ordered(m)) << 32) | (uint32_t)c : ~0ull;
+            }
+            __syncthreads();
+            bitonic_sort(key, N);
+            // exclusive prefix sum of the masses in sorted order: thread t owns positions
+            // per*t .. per*t + per - 1
+            float run = 0.0f;
+            const int t0 = threadIdx.x * per;
+            for (int t = t0; t < t0 + per && t < N; t++)
+                if (key[t] != ~0ull) run += mass[(uint32_t)key[t]] * inv;
+            // block-wide exclusive scan of the per-thread sums
+            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+            float incl = run;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) wsum[warp] = incl;
+            __syncthreads();
+            float before = 0.0f;
+            for (int w = 0; w < warp; w++) before += wsum[w];
+            before += incl - run;
+            for (int t = t0; t < t0 + per && t < N; t++) {
+                if (key[t] == ~0ull) break;
+                const uint32_t c = (uint32_t)key[t];
+                if (before < budget) keep[c] = 1;
+                before += mass[c] * inv;
+            }
+            __syncthreads();
+        }
+    }
+    for (int c = threadIdx.x; c < a.max_blocks; c += blockDim.x)
+        a.keep_mask[row + c] = c < nb ? keep[c] : 0;
+}
+
+}  // namespace
+
+size_t select_smem_bytes(int max_blocks) {
+    int N = 1;
+    while (N < max_blocks) N <<= 1;
+    return (size_t)N * (8 + 4 + 1);
+}
+
+int select_max_blocks() { return kSelMaxBlocks; }
+
+cudaError_t launch_select(const DecodeArgs &a, int selector, float budget, float *imp, float2 *ml,
+                          cudaStream_t stream) {
+    const int units = a.B * a.Hkv;
+    dim3 g1((a.max_blocks + kStatBlocks - 1) / kStatBlocks, units);
+    block_stats_kernel<<<g1, 128, 0, stream>>>(a, imp, ml);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    int N = 1;
+    while (N < a.max_blocks) N <<= 1;
+    const size_t smem = select_smem_bytes(a.max_blocks);
+    static size_t attr_bytes = 0;
+    if (smem > 48 * 1024 && smem > attr_bytes) {
+        e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_bytes = smem;
+    }
+    select_kernel<<<units, kSelThreads, smem, stream>>>(a, selector, budget, N, imp, ml);
+    return cudaGetLastError();
+}
+
+}  // namespace ffd

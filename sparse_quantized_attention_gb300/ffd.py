@@ -93,6 +93,14 @@ def lib() -> ctypes.CDLL:
             L.ffd_decode_attention_static.argtypes = [ctypes.POINTER(DecodeParams)] + \
                 [P] * 11
             L.ffd_decode_attention_static.restype = st
+            L.ffd_select_workspace_size.argtypes = [ctypes.POINTER(DecodeParams)]
+            L.ffd_select_workspace_size.restype = ctypes.c_size_t
+            L.ffd_select_blocks.argtypes = [ctypes.POINTER(DecodeParams), ctypes.c_int32,
+                                            ctypes.c_float] + [P] * 6 + [ctypes.c_size_t, P]
+            L.ffd_select_blocks.restype = st
+            L.ffd_decode_attention_masked.argtypes = [ctypes.POINTER(DecodeParams)] + \
+                [P] * 11 + [ctypes.c_size_t, P]
+            L.ffd_decode_attention_masked.restype = st
             L.ffd_set_profile_events.argtypes = [P, P]
             L.ffd_set_profile_events.restype = st
             L.ffd_get_error.argtypes = [P, P]
@@ -206,6 +214,41 @@ def ffd_decode_attention_static(params: DecodeParams, q, cache: QuantizedCache, 
         ctypes.byref(params), _ptr(q), *map(_ptr, cache), _ptr(v), _ptr(seq_lens),
         _ptr(block_table), _ptr(out), _ptr(keep_mask), _ptr(m_tilde), _ptr(error_word),
         _stream(stream)), "ffd_decode_attention_static")
+
+
+SELECT_TOPK = 1
+SELECT_TOPP = 2
+
+
+def ffd_select_workspace_size(params: DecodeParams) -> int:
+    return int(lib().ffd_select_workspace_size(ctypes.byref(params)))
+
+
+def alloc_select_workspace(params: DecodeParams, device="cuda") -> torch.Tensor:
+    n = ffd_select_workspace_size(params)
+    if n == 0:
+        raise FFDError(1, "select workspace size")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def ffd_select_blocks(params: DecodeParams, selector: int, budget: float, q, cache: QuantizedCache,
+                      seq_lens, block_table, keep_mask, workspace, *, stream=None) -> None:
+    """Top-k (selector 1, budget = k) or Top-p (selector 2, budget = p) block mask."""
+    _check(lib().ffd_select_blocks(
+        ctypes.byref(params), selector, budget, _ptr(q), _ptr(cache.thumb), _ptr(seq_lens),
+        _ptr(block_table), _ptr(keep_mask), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "ffd_select_blocks")
+
+
+def ffd_decode_attention_masked(params: DecodeParams, q, cache: QuantizedCache, v, seq_lens,
+                                block_table, keep_in, out, workspace, *, keep_mask=None,
+                                m_tilde=None, stream=None) -> None:
+    """Exact attention over the blocks a given mask selects (the decode workspace)."""
+    _check(lib().ffd_decode_attention_masked(
+        ctypes.byref(params), _ptr(q), *map(_ptr, cache), _ptr(v), _ptr(seq_lens),
+        _ptr(block_table), _ptr(keep_in), _ptr(out), _ptr(keep_mask), _ptr(m_tilde),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "ffd_decode_attention_masked")
 
 
 def ffd_dense_decode(params: DecodeParams, q, k, v, seq_lens, block_table, out, workspace, *,

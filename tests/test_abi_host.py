@@ -154,3 +154,39 @@ def test_append_rejects_bad_arguments(lib):
     assert call(d=ffd.CacheDesc(4, 2, 128, 16)) == 2
     assert call(kn=FAKE + 2) == 1
     assert call(k=FAKE + 4) == 1
+
+
+def test_select_and_masked_reject_bad_arguments(lib):
+    p = _params()
+    need = ffd.ffd_select_workspace_size(p)
+    assert need > 0 and need % 256 == 0
+    assert ffd.ffd_select_workspace_size(_params(max_blocks_per_seq=20000)) == 0
+
+    def sel(selector=1, budget=3.0, ws_bytes=need, **kw):
+        a = dict(q=FAKE, th=FAKE, sl=FAKE, bt=FAKE, km=FAKE, ws=FAKE)
+        a.update(kw)
+        return lib.ffd_select_blocks(ctypes.byref(kw.pop("p", p)), selector, budget,
+                                     *[a[x] for x in ("q", "th", "sl", "bt", "km", "ws")],
+                                     ws_bytes, None)
+
+    for key in ("q", "th", "sl", "bt", "km", "ws"):
+        assert sel(**{key: None}) == 1, key
+    assert sel(selector=0) == 1 and sel(selector=3) == 1
+    assert sel(budget=-1.0) == 1 and sel(budget=2.5) == 1
+    assert sel(selector=2, budget=0.0) == 1 and sel(selector=2, budget=1.5) == 1
+    assert sel(selector=2, budget=math.nan) == 1
+    assert sel(ws_bytes=need - 1) == 3
+    assert sel(ws=FAKE + 16) == 1
+
+    dneed = ffd.ffd_decode_workspace_size(p)
+
+    def masked(**kw):
+        a = dict(q=FAKE, th=FAKE, rs=FAKE, v=FAKE, sl=FAKE, bt=FAKE, ki=FAKE, out=FAKE, km=None,
+                 mt=None, ws=FAKE)
+        a.update(kw)
+        return lib.ffd_decode_attention_masked(ctypes.byref(p), *[a[x] for x in (
+            "q", "th", "rs", "v", "sl", "bt", "ki", "out", "km", "mt", "ws")], dneed, None)
+
+    for key in ("q", "th", "rs", "v", "sl", "bt", "ki", "out", "ws"):
+        assert masked(**{key: None}) == 1, key
+    assert masked(v=FAKE + 2) == 1
