@@ -14,9 +14,9 @@
 // Two passes, as the rules require (the whole sequence must be scored before anything is chosen):
 //   block_stats_kernel  streams every thumbnail record once and writes, per block, its importance
 //                       and, per head, the block's (max s^, sum of e^(s^ - max)) pair;
-//   select_kernel       one CTA per (sequence, KV head): a bitonic sort of the blocks in shared
-//                       memory (and, for Top-p, the global softmax normalisation and a prefix sum
-//                       per head), then the keep mask.
+//   select_kernel       one CTA per (sequence, KV head), and for Top-p per query head too: a
+//                       bitonic sort of the blocks in shared memory (for Top-p after the global
+//                       softmax normalisation, followed by a prefix sum), then the kept bytes.
 // The chosen mask then goes to the decode kernel as a given mask (ffd_decode_attention_masked).
 #include "common.cuh"
 #include "ptx.cuh"
@@ -41,32 +41,76 @@ __device__ __forceinline__ int stat_len(const DecodeArgs &a, int b) {
     return n;
 }
 
-// Pass 1. CTA (x, u) takes blocks kStatBlocks x .. of unit u; warp mt scores rows 16mt .. 16mt+15
-// of each block for every head of the group (scan_tile), straight from the record in global
-// memory. Block importance -> imp[u][c]; per head (max, sum e^(s^ - max)) -> ml[u][c][G].
+// Pass 1. CTA (x, u) takes blocks kStatBlocks x .. of unit u: it writes their initial keep-mask
+// bytes (1 for a sink or local block, 0 otherwise, 0 past the sequence), brings their thumbnail
+// records into shared memory with one bulk copy each (all issued at once), and then warp mt scores
+// rows 16mt .. 16mt+15 of each block for every head of the group (scan_tile). Block importance ->
+// imp[u][c]; per head (max, sum e^(s^ - max)) -> ml[u][c][G].
 __global__ void __launch_bounds__(128) block_stats_kernel(DecodeArgs a, float *imp, float2 *ml) {
+    __shared__ __align__(128) uint8_t recs[kStatBlocks][kThumbRec];
+    __shared__ __align__(8) uint64_t full;
+    __shared__ int pages[kStatBlocks];
+    __shared__ float s_imp[4];
+    __shared__ float2 s_ml[4][kMaxG];
     const int u = blockIdx.y;
     const int b = u / a.Hkv, h = u - b * a.Hkv;
     const int n = stat_len(a, b);
     const int nb = (n + kPage - 1) / kPage;
     const int c0 = blockIdx.x * kStatBlocks;
+    const size_t row = (size_t)u * a.max_blocks;
+    if (threadIdx.x < kStatBlocks && c0 + threadIdx.x < a.max_blocks) {
+        const int c = c0 + threadIdx.x;
+        const ForcedBlocks fb(n, a.S, a.L);
+        a.keep_mask[row + c] = c < nb && fb.forced(c);
+    }
     if (c0 >= nb) return;  // CTA-uniform
+    const int cnt = nb - c0 < kStatBlocks ? nb - c0 : kStatBlocks;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0) {
+        int page = -1;
+        if (lane < cnt) {
+            page = a.block_table[(size_t)b * a.max_blocks + c0 + lane];
+            if (page < 0 || page >= a.P) {
+                raise_error(a.err, FFD_ERRBIT_BOUNDS);
+                page = -1;
+            }
+        }
+        const uint32_t good = __ballot_sync(0xffffffffu, page >= 0);
+        if (lane < kStatBlocks) pages[lane] = page;
+        if (lane == 0) {
+            mbar_init(&full, 1);
+            fence_barrier_init();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&full, (uint32_t)__popc(good) * kThumbRec);
+        __syncwarp();
+        if (page >= 0)
+            tma_load_1d(recs[lane], a.thumb + ((size_t)page * a.Hkv + h) * kThumbRec, kThumbRec,
+                        &full);
+    }
     const int g = lane >> 2, tig = lane & 3;
     const int r0 = 16 * warp + g, r1 = r0 + 8;
     const uint32_t m0 = 0x00030003u << (2 * tig);
     const int h0 = 2 * tig, h1 = 2 * tig + 1;
     ThumbOps Q;
-    load_thumb_ops(a, b, h, lane, Q);
-    __shared__ float s_imp[4];
-    __shared__ float2 s_ml[4][kMaxG];
-    for (int c = c0; c < c0 + kStatBlocks && c < nb; c++) {
-        const int page = a.block_table[(size_t)b * a.max_blocks + c];
-        const bool bad = page < 0 || page >= a.P;  // block-uniform
-        if (bad && threadIdx.x == 0) raise_error(a.err, FFD_ERRBIT_BOUNDS);
+    load_thumb_ops(a, b, h, lane, Q);  // overlaps the copies
+    __syncthreads();                   // barrier initialised, pages published
+    // bounded wait for the copies (they were issued by this CTA)
+    const uint64_t t0 = globaltimer_ns();
+    bool ok = true;
+    while (!mbar_try_wait(&full, 0)) {
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            if (threadIdx.x == 0) raise_error(a.err, FFD_ERRBIT_TIMEOUT);
+            ok = false;
+            break;
+        }
+    }
+    if (!ok) return;
+    for (int k = 0; k < cnt; k++) {
+        const int c = c0 + k;
+        const bool bad = pages[k] < 0;  // block-uniform
         float4 e = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        if (!bad) e = scan_tile(a.thumb + ((size_t)page * a.Hkv + h) * kThumbRec, r0, r1, m0, Q,
-                                a.sm_scale);
+        if (!bad) e = scan_tile(recs[k], r0, r1, m0, Q, a.sm_scale);
         const bool v0 = c * kPage + r0 < n, v1 = c * kPage + r1 < n;
         const bool w0 = h0 < a.G, w1 = h1 < a.G;
         const float x00 = v0 && w0 ? e.x : -INFINITY, x01 = v0 && w1 ? e.y : -INFINITY;
@@ -94,7 +138,7 @@ __global__ void __launch_bounds__(128) block_stats_kernel(DecodeArgs a, float *i
             s_ml[warp][h1] = make_float2(mh1, l1);
         }
         __syncthreads();
-        const size_t slot = (size_t)u * a.max_blocks + c;
+        const size_t slot = row + c;
         if (threadIdx.x == 0)
             imp[slot] = fmaxf(fmaxf(s_imp[0], s_imp[1]), fmaxf(s_imp[2], s_imp[3]));
         if (threadIdx.x < a.G) {
@@ -157,18 +201,19 @@ __device__ __forceinline__ float block_sum_reduce(float v, float *red) {
     return r;
 }
 
-// Pass 2: one CTA of kSelThreads per unit. Shared memory: keys [N] u64, mass [N] f32, keep [N] u8,
-// N = the block count rounded up to a power of two.
+// Pass 2: CTA (u, i) of kSelThreads threads: unit u, and for Top-p its head i (Top-k has one CTA
+// per unit). It only raises keep-mask bytes to 1 (pass 1 wrote the initial mask), so the heads of
+// a unit OR their choices without further synchronisation. Shared memory: keys [N] u64, mass [N]
+// f32, N = the block count rounded up to a power of two.
 __global__ void __launch_bounds__(kSelThreads) select_kernel(DecodeArgs a, int selector, float budget,
                                                              int N, const float *imp,
                                                              const float2 *ml) {
     extern __shared__ __align__(16) unsigned char smem[];
     uint64_t *key = reinterpret_cast<uint64_t *>(smem);
     float *mass = reinterpret_cast<float *>(key + N);
-    uint8_t *keep = reinterpret_cast<uint8_t *>(mass + N);
     __shared__ float red[kSelThreads / 32];
     __shared__ float wsum[kSelThreads / 32];
-    const int u = blockIdx.x;
+    const int u = blockIdx.x, hh = blockIdx.y;
     const int b = u / a.Hkv;
     int n = a.seq_lens[b];
     const int cap = a.max_blocks * kPage;
@@ -176,8 +221,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DecodeArgs a, int s
     const int nb = (n + kPage - 1) / kPage;
     const ForcedBlocks fb(n, a.S, a.L);
     const size_t row = (size_t)u * a.max_blocks;
-    for (int c = threadIdx.x; c < N; c += blockDim.x) keep[c] = c < nb && fb.forced(c);
-    __syncthreads();
+    uint8_t *keep = a.keep_mask + row;
 
     if (selector == FFD_SELECT_TOPK) {
         for (int c = threadIdx.x; c < N; c += blockDim.x) {
@@ -190,60 +234,53 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DecodeArgs a, int s
         const int k = (int)budget;
         for (int t = threadIdx.x; t < k && t < N; t += blockDim.x)
             if (key[t] != ~0ull) keep[(uint32_t)key[t]] = 1;
-        __syncthreads();
-    } else {
-        const int per = (N + kSelThreads - 1) / kSelThreads;  // sorted positions per thread
-        for (int hh = 0; hh < a.G; hh++) {
-            // global softmax normalisation over the blocks: M = max, L = sum e^(m - M) l
-            float lm = -INFINITY;
-            for (int c = threadIdx.x; c < nb; c += blockDim.x)
-                if (ml[(row + c) * a.G + hh].y > 0.0f) lm = fmaxf(lm, ml[(row + c) * a.G + hh].x);
-            const float M = block_max_reduce(lm, red);
-            float ls = 0.0f;
-            for (int c = threadIdx.x; c < nb; c += blockDim.x) {
-                const float2 v = ml[(row + c) * a.G + hh];
-                const float w = v.y > 0.0f ? v.y * ex2_approx((v.x - M) * kLog2e) : 0.0f;
-                mass[c] = w;
-                ls += w;
-            }
-            const float Ltot = block_sum_reduce(ls, red);
-            const float inv = Ltot > 0.0f ? 1.0f / Ltot : 0.0f;
-            for (int c = threadIdx.x; c < N; c += blockDim.x) {
-                const float m = c < nb ? mass[c] * inv : 0.0f;
-                key[c] = c < nb ? ((uint64_t)(~ordered(m)) << 32) | (uint32_t)c : ~0ull;
-            }
-            __syncthreads();
-            bitonic_sort(key, N);
-            // exclusive prefix sum of the masses in sorted order: thread t owns positions
-            // per*t .. per*t + per - 1
-            float run = 0.0f;
-            const int t0 = threadIdx.x * per;
-            for (int t = t0; t < t0 + per && t < N; t++)
-                if (key[t] != ~0ull) run += mass[(uint32_t)key[t]] * inv;
-            // block-wide exclusive scan of the per-thread sums
-            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-            float incl = run;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            if (lane == 31) wsum[warp] = incl;
-            __syncthreads();
-            float before = 0.0f;
-            for (int w = 0; w < warp; w++) before += wsum[w];
-            before += incl - run;
-            for (int t = t0; t < t0 + per && t < N; t++) {
-                if (key[t] == ~0ull) break;
-                const uint32_t c = (uint32_t)key[t];
-                if (before < budget) keep[c] = 1;
-                before += mass[c] * inv;
-            }
-            __syncthreads();
-        }
+        return;
     }
-    for (int c = threadIdx.x; c < a.max_blocks; c += blockDim.x)
-        a.keep_mask[row + c] = c < nb ? keep[c] : 0;
+    // Top-p, head hh: global softmax normalisation over the blocks, M = max, L = sum e^(m - M) l
+    float lm = -INFINITY;
+    for (int c = threadIdx.x; c < nb; c += blockDim.x)
+        if (ml[(row + c) * a.G + hh].y > 0.0f) lm = fmaxf(lm, ml[(row + c) * a.G + hh].x);
+    const float M = block_max_reduce(lm, red);
+    float ls = 0.0f;
+    for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+        const float2 v = ml[(row + c) * a.G + hh];
+        const float w = v.y > 0.0f ? v.y * ex2_approx((v.x - M) * kLog2e) : 0.0f;
+        mass[c] = w;
+        ls += w;
+    }
+    const float Ltot = block_sum_reduce(ls, red);
+    const float inv = Ltot > 0.0f ? 1.0f / Ltot : 0.0f;
+    for (int c = threadIdx.x; c < N; c += blockDim.x) {
+        if (c < nb) mass[c] *= inv;
+        key[c] = c < nb ? ((uint64_t)(~ordered(c < nb ? mass[c] : 0.0f)) << 32) | (uint32_t)c
+                        : ~0ull;
+    }
+    __syncthreads();
+    bitonic_sort(key, N);
+    // exclusive prefix sum of the masses in sorted order: thread t owns positions per*t .. +per-1
+    const int per = (N + kSelThreads - 1) / kSelThreads;
+    float run = 0.0f;
+    const int t0 = threadIdx.x * per;
+    for (int t = t0; t < t0 + per && t < N; t++)
+        if (key[t] != ~0ull) run += mass[(uint32_t)key[t]];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    float before = 0.0f;
+    for (int w = 0; w < warp; w++) before += wsum[w];
+    before += incl - run;
+    for (int t = t0; t < t0 + per && t < N; t++) {
+        if (key[t] == ~0ull) break;
+        const uint32_t c = (uint32_t)key[t];
+        if (before < budget) keep[c] = 1;
+        before += mass[c];
+    }
 }
 
 }  // namespace
@@ -251,7 +288,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DecodeArgs a, int s
 size_t select_smem_bytes(int max_blocks) {
     int N = 1;
     while (N < max_blocks) N <<= 1;
-    return (size_t)N * (8 + 4 + 1);
+    return (size_t)N * (8 + 4);
 }
 
 int select_max_blocks() { return kSelMaxBlocks; }
@@ -273,7 +310,8 @@ cudaError_t launch_select(const DecodeArgs &a, int selector, float budget, float
         if (e != cudaSuccess) return e;
         attr_bytes = smem;
     }
-    select_kernel<<<units, kSelThreads, smem, stream>>>(a, selector, budget, N, imp, ml);
+    const dim3 g2(units, selector == FFD_SELECT_TOPP ? a.G : 1);
+    select_kernel<<<g2, kSelThreads, smem, stream>>>(a, selector, budget, N, imp, ml);
     return cudaGetLastError();
 }
 
