@@ -60,6 +60,10 @@ def args_parse(argv=None):
     ap.add_argument("--peaked", action="store_true",
                     help="measure the peaked-attention inputs (sink shift and needles in score "
                          "units) as the primary workload")
+    ap.add_argument("--sweep", metavar="MD",
+                    help="instead of the benchmark line: time every workload (literal and peaked, "
+                         "each delta) next to the dense kernel, one JSON line per case, and "
+                         "write a markdown table to MD")
     return ap.parse_args(argv)
 
 
@@ -696,8 +700,103 @@ def run_reference(a):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_sweep(a):
+    """Every workload, literal and peaked inputs, each of its deltas: the decode step timed one
+    launch at a time with L2 flushed in between (the 32K workload's cache fits in L2), next to the
+    dense kernel on the same inputs."""
+    import torch
+
+    import ffd_synth
+    import sparse_quantized_attention_gb300 as ffd
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, _ = measured_peaks()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    sm = float(np.float32(1.0 / math.sqrt(128.0)))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, reps=30):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return float(np.median(ts))
+
+    rows = []
+    for wid, w in sorted(ffd_synth.WORKLOADS.items()):
+        dense_us = None
+        for label, scale in (("literal", 1.0), ("peaked", ffd_synth.peaked_scale())):
+            inp = ffd_synth.make_inputs(w, signal_scale=scale)
+            bf = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(  # noqa
+                torch.bfloat16).to(dev)
+            d = {"q": bf(inp.q_bits), "k": bf(inp.k_bits), "v": bf(inp.v_bits),
+                 "sl": torch.from_numpy(inp.seq_lens).to(dev),
+                 "bt": torch.from_numpy(inp.block_table).to(dev)}
+            P, Hkv = d["k"].shape[0], d["k"].shape[1]
+            qc = ffd.alloc_quantized_cache(P, Hkv, device=dev)
+            ffd.ffd_quantize_keys(d["k"], qc)
+            out = torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.float32, device=dev)
+            mask = torch.zeros((w.batch, Hkv, inp.max_blocks), dtype=torch.uint8, device=dev)
+            if dense_us is None:
+                pdn = ffd.make_params(w.batch, w.num_q_heads, Hkv, P, inp.max_blocks,
+                                      sink=w.sink, local=w.local, delta=5.0, sm_scale=sm)
+                wsd = ffd.alloc_workspace(pdn, dense=True, device=dev)
+                dense_us = timed(lambda: ffd.ffd_dense_decode(pdn, d["q"], d["k"], d["v"], d["sl"],
+                                                              d["bt"], out, wsd))
+            for delta in w.deltas:
+                p = ffd.make_params(w.batch, w.num_q_heads, Hkv, P, inp.max_blocks, sink=w.sink,
+                                    local=w.local, delta=delta, sm_scale=sm)
+                ws = ffd.alloc_workspace(p, device=dev)
+                ffd.ffd_decode_attention(p, d["q"], qc, d["v"], d["sl"], d["bt"], out, ws,
+                                         keep_mask=mask)
+                if ffd.ffd_get_error(ws) != 0:
+                    raise RuntimeError(f"device error on workload {wid}")
+                keep = mask.cpu().numpy()
+                kept = kept_tokens(inp.seq_lens, keep)
+                by = step_bytes(w, inp.seq_lens, inp.max_blocks, kept)
+                us = timed(lambda: ffd.ffd_decode_attention(p, d["q"], qc, d["v"], d["sl"],
+                                                            d["bt"], out, ws))
+                nb_total = int(sum((int(n) + 63) // 64 for n in inp.seq_lens)) * Hkv
+                gbs = by["step"] / (us * 1e-6) / 1e9
+                row = {"workload": w.name, "inputs": label, "delta": delta,
+                       "batch": w.batch, "heads": f"{w.num_q_heads}/{Hkv}",
+                       "context": int(np.max(inp.seq_lens)), "us_per_step": round(us, 2),
+                       "kv_tokens_per_s": round(float(np.sum(inp.seq_lens)) / (us * 1e-6), 1),
+                       "sparsity": round(1 - int(keep.sum()) / max(1, nb_total), 4),
+                       "needed_mb": round(by["step"] / 1e6, 1), "gbs": round(gbs, 1),
+                       "frac_of_measured": round(gbs / peaks["hbm_gbs"], 3),
+                       "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 3),
+                       "dense_us": round(dense_us, 2),
+                       "speedup_vs_dense": round(dense_us / us, 2)}
+                rows.append(row)
+                print(json.dumps(row), flush=True)
+            del d, qc
+            torch.cuda.empty_cache()
+    with open(a.sweep, "w") as f:
+        f.write("| workload | inputs | delta | context | us/step | KV tokens/s | sparsity | "
+                "needed MB | GB/s | of measured copy peak | of 8 TB/s | dense us | speedup |\n")
+        f.write("|---|---|---|---|---|---|---|---|---|---|---|---|---|\n")
+        for r in rows:
+            f.write(f"| {r['workload']} | {r['inputs']} | {r['delta']:g} | {r['context']} | "
+                    f"{r['us_per_step']} | {r['kv_tokens_per_s']:.3g} | {r['sparsity']} | "
+                    f"{r['needed_mb']} | {r['gbs']} | {r['frac_of_measured']} | "
+                    f"{r['frac_of_8tbs']} | {r['dense_us']} | {r['speedup_vs_dense']} |\n")
+    return rows
+
+
 def main(argv=None):
     a = args_parse(argv)
+    if a.sweep:
+        run_sweep(a)
+        return 0
     rank, world, local = dist_env()
     if a.impl == "reference":
         if rank != 0:

@@ -94,7 +94,7 @@ ffd_status make_decode_plan(const ffd_decode_params *p, Plan *pl) {
     pl->part_off = off;
     off = align_up(off + (size_t)(units + ctas) * kRefineGroups * G * kPartStride * sizeof(float));
     pl->cnt_off = off;
-    off = align_up(off + 3 * (size_t)units * sizeof(int));
+    off = align_up(off + 4 * (size_t)units * sizeof(int));
     pl->total = off;
     return FFD_OK;
 }
@@ -121,7 +121,7 @@ ffd_status make_dense_plan(const ffd_decode_params *p, Plan *pl) {
     pl->part_off = off;
     off = align_up(off + (size_t)(units + ctas) * kRefineGroups * G * kPartStride * sizeof(float));
     pl->cnt_off = off;
-    off = align_up(off + 3 * (size_t)units * sizeof(int));
+    off = align_up(off + 4 * (size_t)units * sizeof(int));
     pl->total = off;
     return FFD_OK;
 }
@@ -454,7 +454,7 @@ ffd_status ffd_decode_attention_static(const ffd_decode_params *params, const vo
     // the in-kernel merge must start at zero.
     const size_t units = (size_t)params->batch * params->num_kv_heads;
     if (cudaMemsetAsync(ws, 0, kAlign, s) != cudaSuccess ||
-        cudaMemsetAsync(static_cast<char *>(ws) + pl.cnt_off, 0, 3 * units * sizeof(int), s) !=
+        cudaMemsetAsync(static_cast<char *>(ws) + pl.cnt_off, 0, 4 * units * sizeof(int), s) !=
             cudaSuccess)
         return FFD_ERR_CUDA;
     DecodeArgs a = make_args(params, pl, ws);

@@ -50,7 +50,8 @@ struct DecodeArgs {
     int *err;        // device error word
     float *ws_m1;    // [B*Hkv][nf][kMaxG] stage-1 block maxima over the sink / local tokens
     float *ws_part;  // main-kernel split records: [B*Hkv + CTAs][kRefineGroups][G][kPartStride]
-    int *ws_cnt;     // [3][B*Hkv]: merge tickets, stage-1 slots, mergers done; zero between calls
+    int *ws_cnt;     // [4][B*Hkv]: merge tickets, stage-1 slots, merge reports, merger
+                     // declarations; zero between calls
     cudaEvent_t prof_start, prof_stop;  // optional: recorded around the main kernel
 };
 

@@ -9,12 +9,12 @@
 //
 // Every arithmetic step is a single IEEE fp32 operation with an explicit rounding intrinsic, so
 // the outputs are bit-defined. The per-channel code needs round-half-even of the correctly
-// rounded quotient (x - zero) / scale (and r / r_scale). Instead of one IEEE division per
-// channel the quotient is formed from a correctly rounded reciprocal, with the clamp folded into
-// a saturating multiply, and rounded with one fused multiply-add. Where that fast quotient lies
-// within a few ulps of a rounding boundary k + 1/2 (ties are frequent: keys, zeros and scales sit
-// on the bf16 / fp16 grids), the side of the boundary is decided exactly from the sign of
-// x - zero - (k + 1/2) scale (boundary_step below).
+// rounded quotient (x - zero) / scale (and r / r_scale), without an IEEE division per channel:
+// the 2-bit code counts the exact rounding boundaries (k + 1/2) scale below x - zero; the int8
+// code is formed from a correctly rounded reciprocal, with the clamp folded into a saturating
+// multiply, and rounded with one fused multiply-add, and where that fast quotient lies within a
+// few ulps of a rounding boundary (ties are frequent: keys, zeros and scales sit on the bf16 /
+// fp16 grids) the side of the boundary is decided exactly (boundary_step below).
 #pragma once
 
 #include "common.cuh"
@@ -27,11 +27,9 @@ namespace quant {
 constexpr float kMagic = 12582912.0f;
 // kMagic - 127, the base of the residual codes' sums (its low byte is 0x81 = -127 mod 256)
 constexpr float kMagicB = 12582785.0f;
-// Half-widths of the windows around k + 1/2 in which the fast quotient is not trusted. Stage A
-// evaluates a / scale as 3 sat(a * rcp(3 scale)): absolute error below 4e-7 on [0, 3]. Stage B
-// evaluates r / r_scale as 254 sat(r * rcp(254 r_scale) + 1/2) - 127: error below 1.6e-5 on
-// [-127, 127].
-constexpr float kNearA = 1.0e-5f;
+// Half-width of the window around k + 1/2 in which the fast residual quotient is not trusted: it
+// evaluates r / r_scale as 254 sat(r * rcp(254 r_scale) + 1/2) - 127, with an error below
+// 1.6e-5 on [-127, 127].
 constexpr float kNearB = 4.0e-5f;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -48,17 +46,6 @@ __device__ __forceinline__ float boundary_step(float a, float b, float c, float 
     const float e = __fmaf_rn(-__fadd_rn(c, 0.5f * dir), b, a);
     if (e == 0.0f) return c_odd ? dir : 0.0f;
     return (e > 0.0f) == (d > 0.0f) ? dir : 0.0f;
-}
-
-// 2-bit code of a = x - zero: clamp(rint(a / scale), 0, 3), from r3 = rcp(3 scale) (0 when
-// scale is 0).
-__device__ __forceinline__ float code2_of(float a, float scale, float r3) {
-    const float tp = __saturatef(__fmul_rn(a, r3));
-    float code = __fsub_rn(__fmaf_rn(tp, 3.0f, kMagic), kMagic);
-    const float d = __fmaf_rn(tp, 3.0f, -code);
-    if (fabsf(d) > 0.5f - kNearA)
-        code = __fadd_rn(code, boundary_step(a, scale, code, d, ((int)code & 1) != 0));
-    return code;
 }
 
 // int8 code of r: clamp(rint(r / r_scale), -127, 127) in the low byte (two's complement), from
@@ -120,7 +107,14 @@ __device__ __forceinline__ void quantize_group(const uint32_t (&u)[16], GroupCod
     group_params(u, o);
     const float zf = __half2float(o.zero);
     const float sf = __half2float(o.scale);
-    const float r3 = sf == 0.0f ? 0.0f : __frcp_rn(__fmul_rn(sf, 3.0f));  // 3 sf is exact
+    // 2-bit codes by comparison with the rounding boundaries (k + 1/2) scale, k = 0, 1, 2, which
+    // are exact in fp32: on these grids the IEEE quotient a / scale lies on the same side of
+    // k + 1/2 as a lies of (k + 1/2) scale, and equals k + 1/2 only when a does (see
+    // boundary_step), so the code is the number of boundaries below a, a tie at 1/2 or 5/2
+    // rounding down and a tie at 3/2 rounding up (half to even). scale 0 gives code 0.
+    const float b0 = sf == 0.0f ? INFINITY : __fmul_rn(0.5f, sf);
+    const float b1 = sf == 0.0f ? INFINITY : __fmul_rn(1.5f, sf);
+    const float b2 = sf == 0.0f ? INFINITY : __fmul_rn(2.5f, sf);
 
     // stage A: 2-bit codes and the residual r = x - x^2. The codes are summed as code * 4^c in
     // fp32 (exact: each sum stays below 2^24), 12 + 4 channels per 32-bit word.
@@ -130,7 +124,8 @@ __device__ __forceinline__ void quantize_group(const uint32_t (&u)[16], GroupCod
 #pragma unroll
     for (int c = 0; c < 32; c++) {
         const float x = (c & 1) ? bf16_hi(u[c >> 1]) : bf16_lo(u[c >> 1]);
-        const float code = code2_of(__fsub_rn(x, zf), sf, r3);
+        const float a = __fsub_rn(x, zf);
+        const float code = (a > b0 ? 1.0f : 0.0f) + (a >= b1 ? 1.0f : 0.0f) + (a > b2 ? 1.0f : 0.0f);
         const int part = (c >> 4) * 2 + ((c & 15) >= 12);
         const float weight = (float)(1u << (2 * ((c & 15) % 12)));
         acc[part] = __fmaf_rn(code, weight, acc[part]);

@@ -285,8 +285,8 @@ __device__ __forceinline__ void softmax_pv(M *m, uint8_t *px_buf, const uint8_t 
 // Split merge: out_i = sum_r e^(m_r - M) num_r / sum_r e^(m_r - M) den_r over a unit's records.
 // Records of CTAs cf..cl, one per refine group, are contiguous from
 // ws_part[(u + cf) * kRefineGroups]; a record holds (num[128], m, den) per head. Counters in
-// ws_cnt: [0, units) merge tickets, [units, 2 units) stage-1 slots, [2 units, 3 units) mergers
-// done.
+// ws_cnt: [0, units) merge tickets, [units, 2 units) stage-1 slots, [2 units, 3 units) merge
+// reports, [3 units, 4 units) merger declarations.
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ float *unit_record(const DecodeArgs &a, int u, int c, int grp) {
     return a.ws_part + ((size_t)(u + c) * kRefineGroups + grp) * a.G * kPartStride;
@@ -346,6 +346,12 @@ __device__ __forceinline__ int *done_counter(const DecodeArgs &a, int u) {
     return a.ws_cnt + 2 * a.B * a.Hkv + u;
 }
 
+// Declarations of the unit's ranked mergers: bit r (rank r has taken its ticket), bit 8 + r (and
+// its CTA has no work after this segment).
+__device__ __forceinline__ int *declare_word(const DecodeArgs &a, int u) {
+    return a.ws_cnt + 3 * a.B * a.Hkv + u;
+}
+
 // A refine group's record of softmax state R: (num[128], m, den) per head, den summed over the
 // group's warps through m->lsum, each warp writing its own channels.
 template <class M>
@@ -393,9 +399,34 @@ __device__ __forceinline__ void write_record(const DecodeArgs &a, M *m, const Re
     }
 }
 
-// After its record is written: the group's ticket for the unit of sub-chunk s. The last
-// min(G, groups of the unit) groups to take one wait for the remaining ones (groups that are
-// already finishing the unit, or earlier units, so every wait ends) and merge one head each.
+// Bounded wait until (*word & mask) == mask (bits other groups set right after their tickets).
+template <class M>
+__device__ __forceinline__ unsigned int wait_bits(const DecodeArgs &a, M *m, const int *word,
+                                                  unsigned int mask) {
+    unsigned int v = (unsigned int)ld_acquire_gpu(word);
+    const uint64_t t0 = globaltimer_ns();
+    while ((v & mask) != mask) {
+        if (aborted(m)) break;
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            raise_error(a.err, FFD_ERRBIT_TIMEOUT);
+            *reinterpret_cast<volatile uint32_t *>(&m->aborted) = 1;
+            break;
+        }
+        __nanosleep(32);
+        v = (unsigned int)ld_acquire_gpu(word);
+    }
+    return v;
+}
+
+// After its record is written: the group's ticket for the unit of sub-chunk s. The groups that
+// take the last nm = min(G, groups of the unit) tickets are ranked 0 .. nm-1 in ticket order and
+// merge the unit's heads, head i by rank i % nm. A ranked group declares right after its ticket
+// whether it is final (its CTA has no work after this segment). The last group finds every record
+// written; it waits for the other ranks' declarations (made a moment after their tickets) and
+// merges its own heads and those of every rank that is not final. A final group of lower rank
+// waits for the remaining tickets (their groups are at the ends of their ranges too) and merges
+// its heads. A group whose CTA still has work never waits for other groups' records: the other
+// parts of the unit may be walked at the very end of other CTAs' ranges.
 template <class M>
 __device__ __forceinline__ void finish_unit(const DecodeArgs &a, M *m, const Sub &s, int cta,
                                             int ncta, int64_t T, int grp, int mt, int lane) {
@@ -406,26 +437,45 @@ __device__ __forceinline__ void finish_unit(const DecodeArgs &a, M *m, const Sub
     const int64_t first = s.x0 - s.j0;  // global index of the unit's first block
     const int cf = cta_of(first, T, ncta), cl = cta_of(first + s.nblk - 1, T, ncta);
     const int target = kRefineGroups * (cl - cf + 1);
-    // the last nm groups to finish merge the unit, head i by merger i % nm
     const int nm = a.G < target ? a.G : target;
+    const bool final_seg = s.x0 + s.cnt == T * (cta + 1) / ncta;
     if (mt == 0 && lane == 0) {
-        const int old = atomicAdd(a.ws_cnt + u, 1);
-        m->merge_flag[grp] = old >= target - nm ? (uint32_t)(old - (target - nm) + 1) : 0u;
+        const int r = atomicAdd(a.ws_cnt + u, 1) - (target - nm);
+        uint32_t role = 0;  // bit 0: merges; bit 1: waits for every ticket first; bits 8..15:
+                            // ranks whose heads it merges; 4: ranked, merges nothing
+        if (r >= 0 && r < nm - 1) {
+            atomicOr(reinterpret_cast<unsigned int *>(declare_word(a, u)),
+                     (1u << r) | (final_seg ? 1u << (8 + r) : 0u));
+            role = final_seg ? 3u | ((1u << r) << 8) : 4u;
+        } else if (r == nm - 1) {
+            const unsigned int d = wait_bits(a, m, declare_word(a, u), (1u << r) - 1u);
+            uint32_t cover = 1u << r;
+            for (int q = 0; q < r; q++)
+                if (!((d >> (8 + q)) & 1u)) cover |= 1u << q;
+            role = 1u | (cover << 8);
+        }
+        m->merge_flag[grp] = role;
     }
     named_barrier_sync(bar_id, 128);
-    const int rank = (int)m->merge_flag[grp] - 1;
-    if (rank < 0) return;
-    // wait for the others (the last ones of the unit, already past their final block)
-    if (mt == 0 && lane == 0) wait_count(a, m, a.ws_cnt + u, target);
-    named_barrier_sync(bar_id, 128);
-    __threadfence();
-    for (int i = rank; i < a.G; i += nm) merge_head(a, s.b, s.h, cf, cl, i, mt, lane);
+    const uint32_t role = m->merge_flag[grp];
+    if (role == 0) return;
+    if (role & 1u) {
+        if ((role & 2u) && mt == 0 && lane == 0) wait_count(a, m, a.ws_cnt + u, target);
+        named_barrier_sync(bar_id, 128);
+        __threadfence();
+        const uint32_t cover = (role >> 8) & 0xffu;
+        for (int i = 0; i < a.G; i++)
+            if ((cover >> (i % nm)) & 1u) merge_head(a, s.b, s.h, cf, cl, i, mt, lane);
+        named_barrier_sync(bar_id, 128);
+    }
     if (mt == 0 && lane == 0) {
-        // every merger has seen the full ticket: the last one clears the counters for the next call
+        // every ranked group reports once its heads are merged (or at once when it merges none);
+        // the last report clears the unit's counters for the next call
         if (atomicAdd(done_counter(a, u), 1) == nm - 1) {
             a.ws_cnt[u] = 0;
             *slot_counter(a, u) = 0;
             *done_counter(a, u) = 0;
+            *declare_word(a, u) = 0;
         }
     }
 }

@@ -45,6 +45,7 @@ APPEND_CASES = [
                                                   random_pages=True, seed=11), [3000, 1, 1729])),
     ("page-boundary", lambda: (ffd_synth.custom(2, 8, 2, 4096, sink=64, local=256,
                                                 random_pages=True, seed=12), [65, 4096])),
+    ("batched-paged-32x", lambda: (ffd_synth.WORKLOADS[4], None)),
 ]
 
 

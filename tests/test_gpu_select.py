@@ -91,6 +91,7 @@ CASES = [
                                                   random_pages=True, seed=21),
                                  [6000, 1, 2500], ffd_synth.peaked_scale())),
     ("llama-32k-peaked", lambda: (ffd_synth.WORKLOADS[1], None, ffd_synth.peaked_scale())),
+    ("batched-paged-peaked", lambda: (ffd_synth.WORKLOADS[4], None, ffd_synth.peaked_scale())),
 ]
 
 

@@ -39,6 +39,7 @@ CASES = [
     ("ragged-paged-g7", lambda: (ffd_synth.custom(3, 14, 2, 3000, sink=16, local=200,
                                                   random_pages=True, seed=5),
                                  [3000, 1, 777], ffd_synth.peaked_scale())),
+    ("batched-paged-32x-4k-16k", lambda: (ffd_synth.WORKLOADS[4], None, 1.0)),
 ]
 
 
