@@ -213,8 +213,8 @@ __device__ __forceinline__ bool tile_passes(float4 e, bool v0, bool v1, float th
 
 // ------------------------------------------------------------------------------------------
 // Stage 1 (pseudo-max), run by the refine groups at the start of the main kernel, before any
-// block reaches them. The (unit, forced-block slot) pairs are dealt round-robin to the
-// ncta * kRefineGroups groups of the grid; in a group, warp mt takes rows 16mt .. 16mt+15 of the
+// block reaches them. The (unit, forced-block slot) pairs are cut into equal contiguous runs,
+// one per group of the grid (ncta * kRefineGroups); in a group, warp mt takes rows 16mt .. 16mt+15 of the
 // slot's block. Exact scores s = sm q . K^ (thumbnail + residual, on tensor cores) of the block's
 // sink and local tokens; their per-head maximum goes to ws_m1 (the pseudo-max m~ of a unit is the
 // maximum over its slots), then the unit's slot counter is raised. Scan warp 0 of every CTA that
@@ -229,18 +229,25 @@ __device__ __forceinline__ void pseudo_max_slots(const DecodeArgs &a, Misc *m, i
     const int workers = nctas * kRefineGroups;
     const int tid = 32 * mt + lane;
     const int g = lane >> 2, tig = lane & 3;
-    int it = 0;
-    for (int z = cta * kRefineGroups + grp; z < nz; z += workers, it++) {
+    // a worker takes a contiguous run of (unit, slot) pairs, so that with more pairs than workers
+    // (many short sequences) it keeps one unit's query operands and length across its slots
+    const int wk = cta * kRefineGroups + grp;
+    const int z0 = (int)((int64_t)nz * wk / workers), z1 = (int)((int64_t)nz * (wk + 1) / workers);
+    int it = 0, cu = -1, raw_n = 0, n = 0;
+    ThumbOps Q;
+    ResidOps QR;
+    for (int z = z0; z < z1; z++, it++) {
         const int u = z / a.nf, slot = z % a.nf;
         const int b = u / a.Hkv, h = u % a.Hkv;
-        // the query operands do not depend on the page: their loads overlap the two dependent
-        // loads (sequence length, then block table) that locate the block
-        ThumbOps Q;
-        ResidOps QR;
-        load_thumb_ops(a, b, h, lane, Q);
-        load_resid_ops(a, b, h, lane, QR);
-        const int raw_n = a.seq_lens[b];
-        const int n = len_of(a, b);
+        if (u != cu) {
+            // the query operands do not depend on the page: their loads overlap the two dependent
+            // loads (sequence length, then block table) that locate the block
+            load_thumb_ops(a, b, h, lane, Q);
+            load_resid_ops(a, b, h, lane, QR);
+            raw_n = a.seq_lens[b];
+            n = len_of(a, b);
+            cu = u;
+        }
         const int nb = (n + kPage - 1) / kPage;
         if (slot == 0) {
             if (tid == 0 && h == 0 && raw_n != n) raise_error(a.err, FFD_ERRBIT_BOUNDS);
