@@ -158,6 +158,9 @@ def barrier(device=None):
 # Clocks                                                                                       #
 # ------------------------------------------------------------------------------------------- #
 
+LEAD_CYCLES = 400_000  # device cycles of the pre-timing delay (~0.2 ms at 2 GHz)
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -180,6 +183,11 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        # nvidia-smi's start-up (driver queries, seconds on a fresh machine) must not overlap the
+        # timed region: wait for its first sample (at most 15 s)
+        t_end = time.time() + 15.0
+        while not self.samples and time.time() < t_end and self.proc.poll() is None:
+            time.sleep(0.01)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -337,6 +345,10 @@ def run_ours(a, rank, world, local):
     barrier(local)
     torch.cuda.synchronize(dev)
     clocks.mark_on()
+    # a short device-side delay (a bounded clock spin, about 0.2 ms) queued ahead of the start
+    # event, so that the first timed launch is already enqueued when the device reaches it: the
+    # events then measure device time only (the host's launch cost is in the end-to-end figure)
+    torch.cuda._sleep(LEAD_CYCLES)
     t0.record(stream)
     for i in range(a.steps):
         step()
@@ -595,9 +607,28 @@ def peaked_variant(a, w, delta, dev, ffd, torch, upload, dense_ms):
                            "sparsity": round(1 - int(smask.sum()) / nb_total, 4)}
     if ffd.ffd_get_error(ws) != 0 or ffd.ffd_get_error(sws) != 0:
         raise RuntimeError("device error in the selector comparison")
+    # run-time termination (ART) over the Top-delta mask: one CTA walks each (sequence, KV head)
+    # unit; thresholds 0 use every kept block (compare with the fused step's stage 3)
+    aws = ffd.alloc_art_workspace(params, device=dev)
+    used = torch.zeros((w.batch, w.num_kv_heads), dtype=torch.int32, device=dev)
+    aout = torch.empty_like(out)
+    ffd.ffd_decode_attention_masked(params, d["q"], qc, d["v"], d["seq_lens"], d["block_table"],
+                                    mask, out, ws)
+    art = []
+    for tau, phi, pat in ((0.0, 0.0, 1), (1e-3, 1e-4, 2), (1e-2, 1e-3, 2)):
+        def run_art():
+            ffd.ffd_art_attention(params, tau, phi, pat, d["q"], qc, d["v"], d["seq_lens"],
+                                  d["block_table"], aout, aws, keep_in=mask, blocks_used=used)
+        run_art()
+        t_art = timed(run_art, reps=5)
+        art.append({"tau": tau, "phi": phi, "patience": pat, "us": round(t_art, 2),
+                    "mean_blocks_used": round(float(used.float().mean()), 1),
+                    "max_abs_vs_all_kept": float((aout - out).abs().max())})
+    if ffd.ffd_get_error(aws) != 0:
+        raise RuntimeError("device error in the ART comparison")
     del d, qc
     return {"signal_scale": round(ffd_synth.peaked_scale(), 4), "us_per_step": round(ms * 1e3, 2),
-            "delta_sweep": sweep, "selectors": selectors,
+            "delta_sweep": sweep, "selectors": selectors, "art": art,
             "needed_bytes_per_step": by["step"], "gbs": round(by["step"] / (ms * 1e-3) / 1e9, 1),
             "sparsity": round(1 - int(keep.sum()) / nb_total, 4),
             "speedup_vs_dense": round(dense_ms / ms, 3),

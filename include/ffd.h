@@ -284,6 +284,46 @@ ffd_status ffd_decode_attention_masked(const ffd_decode_params *params, const vo
                                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * ffd_art_attention -- attention with run-time termination (ART) over the blocks of a mask:
+ * each (sequence, KV head) unit walks block 0, then the blocks of keep_in (or all blocks) from the
+ * most recent to the oldest, folding each into an online softmax, and stops early once its
+ * partial output is stable.
+ * Source: "ART: Attention Run-time Termination" (technical summary page), §2.2 (stop when the
+ * change in magnitude and the change in direction of the partial output both fall below tau and
+ * phi), §2.3 (the criterion must hold `patience` times in a row), §2.4 (any block order is exact
+ * because online softmax is permutation invariant; block 0 is always evaluated first). The FFD
+ * pages name ART as an orthogonal layer. This library's reading: after t >= 2 blocks, with
+ * P_i(t) = o_i / l_i the normalised partial output of head i,
+ *   d_scale = max_i | |P_i(t)| - |P_i(t-1)| | / |P_i(t-1)|,
+ *   d_direction = max_i (1 - cos(P_i(t), P_i(t-1))) over the group's heads,
+ * the criterion is d_scale < tau and d_direction < phi (strict), and the unit stops after the
+ * block at which it has held `patience` times in a row. Scores are the exact
+ * s_ij = sm_scale * q_i . K^_j of ffd_decode_attention.
+ *   params      as for ffd_decode_attention (delta, sink_tokens, local_tokens and num_splits are
+ *               ignored)
+ *   tau, phi    thresholds, >= 0 (0 disables termination: every listed block is used)
+ *   patience    >= 1
+ *   q_bf16, thumb, resid, v_bf16, seq_lens, block_table   as for ffd_decode_attention
+ *   keep_in     device u8 [B][Hkv][max_blocks_per_seq] or NULL (all blocks): nonzero = the block
+ *               may be visited; block 0 is visited whatever it says
+ *   out         device f32 [B][Hq][128]: o / l after the last block used (0 for n = 0)
+ *   blocks_used device i32 [B][Hkv] or NULL: blocks folded in per unit
+ *   workspace   device, >= ffd_art_workspace_size(params) bytes, 256-byte aligned; its first 4
+ *               bytes are the device error word (zero it before first use)
+ * One kernel launch, one CTA per (sequence, KV head): the traversal of a unit is sequential, so
+ * the parallelism is across units. Errors: FFD_ERR_INVALID_ARG for NULL pointers, misaligned
+ * buffers, tau or phi negative or NaN, patience < 1; otherwise as ffd_decode_attention
+ * (FFD_ERRBIT_BOUNDS for a block-table entry outside [0, P): that block contributes nothing).
+ */
+size_t ffd_art_workspace_size(const ffd_decode_params *params);
+ffd_status ffd_art_attention(const ffd_decode_params *params, float tau, float phi,
+                             int32_t patience, const void *q_bf16, const uint8_t *thumb,
+                             const uint8_t *resid, const void *v_bf16, const int32_t *seq_lens,
+                             const int32_t *block_table, const uint8_t *keep_in, float *out,
+                             int32_t *blocks_used, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/*
  * ffd_decode_attention_static -- ffd_decode_attention without a caller-supplied workspace.
  * The paper has no counterpart: this entry point exists for callers that cannot allocate device
  * memory for a workspace, such as a plain C host that links only this library and owns no device

@@ -9,7 +9,8 @@ from .ffd import (CacheDesc, DecodeParams, FFDError, QuantizedCache, alloc_quant
                   ffd_dense_decode, ffd_dense_workspace_size, ffd_get_error, ffd_quantize_keys,
                   ffd_set_profile_events, ffd_status_string, ffd_version, lib, library_path,
                   make_params, SELECT_TOPK, SELECT_TOPP, alloc_select_workspace,
-                  ffd_select_workspace_size, ffd_select_blocks, ffd_decode_attention_masked)
+                  ffd_select_workspace_size, ffd_select_blocks, ffd_decode_attention_masked,
+                  ffd_art_workspace_size, alloc_art_workspace, ffd_art_attention)
 
 __all__ = ["CacheDesc", "DecodeParams", "FFDError", "QuantizedCache", "alloc_quantized_cache",
            "alloc_workspace", "ffd_append_kv", "ffd_decode_attention", "ffd_decode_attention_static",
@@ -18,4 +19,5 @@ __all__ = ["CacheDesc", "DecodeParams", "FFDError", "QuantizedCache", "alloc_qua
            "ffd_quantize_keys", "ffd_set_profile_events", "ffd_status_string", "ffd_version",
            "lib", "library_path", "make_params", "SELECT_TOPK", "SELECT_TOPP",
            "alloc_select_workspace", "ffd_select_workspace_size", "ffd_select_blocks",
-           "ffd_decode_attention_masked"]
+           "ffd_decode_attention_masked", "ffd_art_workspace_size", "alloc_art_workspace",
+           "ffd_art_attention"]

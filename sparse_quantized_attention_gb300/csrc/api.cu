@@ -20,6 +20,8 @@ cudaError_t launch_select(const DecodeArgs &a, int selector, float budget, float
                           cudaStream_t stream);
 size_t select_smem_bytes(int max_blocks);
 int select_max_blocks();
+cudaError_t launch_art(const DecodeArgs &a, float tau, float phi, int patience, int32_t *used,
+                       cudaStream_t stream);
 }  // namespace ffd
 
 using namespace ffd;
@@ -169,7 +171,7 @@ const char *ffd_status_string(ffd_status s) {
     return "FFD_ERR_UNKNOWN";
 }
 
-int32_t ffd_version(void) { return 202; }
+int32_t ffd_version(void) { return 203; }
 
 ffd_status ffd_quantize_keys(const ffd_cache_desc *cache, const void *k_bf16, uint8_t *thumb,
                              uint8_t *resid, const int32_t *page_ids, int32_t num_page_ids,
@@ -365,6 +367,48 @@ ffd_status ffd_decode_attention_masked(const ffd_decode_params *params, const vo
     a.keep_in = keep_in;
     a.m_tilde = m_tilde;
     cudaError_t e = launch_decode(a, pl.ctas, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+}
+
+// Workspace of ffd_art_attention: the error word only (the kernel keeps its state on chip).
+size_t ffd_art_workspace_size(const ffd_decode_params *params) {
+    return check_params(params) == FFD_OK ? kAlign : 0;
+}
+
+ffd_status ffd_art_attention(const ffd_decode_params *params, float tau, float phi,
+                             int32_t patience, const void *q_bf16, const uint8_t *thumb,
+                             const uint8_t *resid, const void *v_bf16, const int32_t *seq_lens,
+                             const int32_t *block_table, const uint8_t *keep_in, float *out,
+                             int32_t *blocks_used, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+    if (!q_bf16 || !thumb || !resid || !v_bf16 || !seq_lens || !block_table || !out || !workspace)
+        return FFD_ERR_INVALID_ARG;
+    if (!aligned16(thumb) || !aligned16(resid) || !aligned16(v_bf16) || !aligned16(q_bf16) ||
+        (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+        return FFD_ERR_INVALID_ARG;
+    if (!(tau >= 0.0f) || !(phi >= 0.0f) || patience < 1) return FFD_ERR_INVALID_ARG;
+    ffd_status st = check_params(params);
+    if (st != FFD_OK) return st;
+    if (workspace_bytes < kAlign) return FFD_ERR_WORKSPACE;
+    DecodeArgs a{};
+    a.B = params->batch;
+    a.Hq = params->num_q_heads;
+    a.Hkv = params->num_kv_heads;
+    a.G = params->num_q_heads / params->num_kv_heads;
+    a.P = params->num_pages;
+    a.max_blocks = params->max_blocks_per_seq;
+    a.sm_scale = params->sm_scale;
+    a.q = static_cast<const __nv_bfloat16 *>(q_bf16);
+    a.thumb = thumb;
+    a.resid = resid;
+    a.v = static_cast<const __nv_bfloat16 *>(v_bf16);
+    a.seq_lens = seq_lens;
+    a.block_table = block_table;
+    a.keep_in = keep_in;
+    a.out = out;
+    a.err = static_cast<int *>(workspace);
+    cudaError_t e = launch_art(a, tau, phi, patience, blocks_used,
+                               static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
 }
 

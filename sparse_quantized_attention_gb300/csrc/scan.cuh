@@ -134,4 +134,108 @@ __device__ __forceinline__ float4 scan_tile(const uint8_t *base, int r0, int r1,
     return e;
 }
 
+// Query operands of the residual correction: int8 codes enter the MMA as (c8 + 128), with the
+// same scaling as the thumbnail codes; the +128 is removed with the per-group query sums.
+struct ResidOps {
+    uint32_t br0[8], br1[8];  // chunk 2gg + half, head g
+    float qs[2][4];
+};
+
+__device__ __forceinline__ void load_resid_ops(const DecodeArgs &a, int b, int h, int lane,
+                                               ResidOps &Q) {
+    const int g = lane >> 2, tig = lane & 3;
+    const bool hv = g < a.G;
+    const __nv_bfloat16 *qrow = q_row(a, b, h, g);
+    const float sr = __int_as_float((127 + kKq) << 23);  // 2^kKq
+    float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) {
+        const int base = 32 * gg + 8 * tig;
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) y[e] = hv ? __bfloat162float(qrow[base + e]) : 0.0f;
+        Q.br0[2 * gg] = pack_bf16x2(y[0] * sr, y[2] * sr);
+        Q.br1[2 * gg] = pack_bf16x2(y[1] * sr, y[3] * sr);
+        Q.br0[2 * gg + 1] = pack_bf16x2(y[4] * sr, y[6] * sr);
+        Q.br1[2 * gg + 1] = pack_bf16x2(y[5] * sr, y[7] * sr);
+        part[gg] = ((y[0] + y[1]) + (y[2] + y[3])) + ((y[4] + y[5]) + (y[6] + y[7]));
+    }
+    group_sums(part, tig, Q.qs);
+}
+
+// D[gg] = sum over group gg of q . (c8 + 128) (scaled by 2^(kKq-133)).
+// x0[gg] / x1[gg]: bytes 32gg + 8tig .. +7 of rows g / g+8.
+__device__ __forceinline__ void resid_mma(float (&D)[4][4], const uint2 (&x0)[4],
+                                          const uint2 (&x1)[4], const ResidOps &Q) {
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) D[gg][0] = D[gg][1] = D[gg][2] = D[gg][3] = 0.0f;
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) {
+#pragma unroll
+        for (int half = 0; half < 2; half++) {
+            const uint32_t v0 = half ? x0[gg].y : x0[gg].x;
+            const uint32_t v1 = half ? x1[gg].y : x1[gg].x;
+            const uint32_t a0 = (v0 & 0x00FF00FFu) ^ 0x00800080u;
+            const uint32_t a1 = (v1 & 0x00FF00FFu) ^ 0x00800080u;
+            const uint32_t a2 = ((v0 >> 8) & 0x00FF00FFu) ^ 0x00800080u;
+            const uint32_t a3 = ((v1 >> 8) & 0x00FF00FFu) ^ 0x00800080u;
+            mma_bf16(D[gg], a0, a1, a2, a3, Q.br0[2 * gg + half], Q.br1[2 * gg + half]);
+        }
+    }
+}
+
+// Residual correction sm * sum_g r_scale_g q_g . c8_g of accumulator entry e.
+__device__ __forceinline__ float corr_score(const float (&D)[4][4], int e, const float (&sr)[4],
+                                            const float (&qs)[4], float sm) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++)
+        acc = fmaf(sr[gg], fmaf(kUnscale, D[gg][e], -128.0f * qs[gg]), acc);
+    return acc * sm;
+}
+
+
+// Exact scores s = sm * q . K^ (thumbnail plus residual) of rows r0 and r1 of a block whose
+// thumbnail and residual records are at trec and rrec (global or shared memory), for heads 2tig,
+// 2tig+1: {(r0,h0), (r0,h1), (r1,h0), (r1,h1)}.
+__device__ __forceinline__ float4 exact_tile(const uint8_t *trec, const uint8_t *rrec, int r0,
+                                             int r1, int tig, const ThumbOps &Q,
+                                             const ResidOps &QR, float sm) {
+    uint32_t w0[8], w1[8];
+    {
+        const uint4 *c0 = reinterpret_cast<const uint4 *>(trec + r0 * kThumbRow);
+        const uint4 *c1 = reinterpret_cast<const uint4 *>(trec + r1 * kThumbRow);
+        const uint4 p0 = c0[0], p1 = c0[1], p2 = c1[0], p3 = c1[1];
+        w0[0] = p0.x; w0[1] = p0.y; w0[2] = p0.z; w0[3] = p0.w;
+        w0[4] = p1.x; w0[5] = p1.y; w0[6] = p1.z; w0[7] = p1.w;
+        w1[0] = p2.x; w1[1] = p2.y; w1[2] = p2.z; w1[3] = p2.w;
+        w1[4] = p3.x; w1[5] = p3.y; w1[6] = p3.z; w1[7] = p3.w;
+    }
+    uint2 x0[4], x1[4];
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) {
+        x0[gg] = *reinterpret_cast<const uint2 *>(rrec + resid_offset(r0, 32 * gg + 8 * tig));
+        x1[gg] = *reinterpret_cast<const uint2 *>(rrec + resid_offset(r1, 32 * gg + 8 * tig));
+    }
+    float sf0[4], sf1[4], zf0[4], zf1[4], sr0[4], sr1[4];
+    const uint2 *ts = reinterpret_cast<const uint2 *>(trec + kThumbScaleOff);
+    const uint2 *tz = reinterpret_cast<const uint2 *>(trec + kThumbZeroOff);
+    const uint2 *rs = reinterpret_cast<const uint2 *>(rrec + kResidScaleOff);
+    unpack4h(ts[r0], sf0);
+    unpack4h(ts[r1], sf1);
+    unpack4h(tz[r0], zf0);
+    unpack4h(tz[r1], zf1);
+    unpack4h(rs[r0], sr0);
+    unpack4h(rs[r1], sr1);
+    float D[4][4], Dr[4][4];
+    thumb_mma(D, w0, w1, 0x00030003u << (2 * tig), Q);
+    resid_mma(Dr, x0, x1, QR);
+    float4 e;
+    e.x = est_score(D, 0, sf0, zf0, Q.qs[0], sm) + corr_score(Dr, 0, sr0, Q.qs[0], sm);
+    e.y = est_score(D, 1, sf0, zf0, Q.qs[1], sm) + corr_score(Dr, 1, sr0, Q.qs[1], sm);
+    e.z = est_score(D, 2, sf1, zf1, Q.qs[0], sm) + corr_score(Dr, 2, sr1, Q.qs[0], sm);
+    e.w = est_score(D, 3, sf1, zf1, Q.qs[1], sm) + corr_score(Dr, 3, sr1, Q.qs[1], sm);
+    return e;
+}
+
 }  // namespace ffd

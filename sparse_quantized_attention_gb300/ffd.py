@@ -101,6 +101,12 @@ def lib() -> ctypes.CDLL:
             L.ffd_decode_attention_masked.argtypes = [ctypes.POINTER(DecodeParams)] + \
                 [P] * 11 + [ctypes.c_size_t, P]
             L.ffd_decode_attention_masked.restype = st
+            L.ffd_art_workspace_size.argtypes = [ctypes.POINTER(DecodeParams)]
+            L.ffd_art_workspace_size.restype = ctypes.c_size_t
+            L.ffd_art_attention.argtypes = [ctypes.POINTER(DecodeParams), ctypes.c_float,
+                                            ctypes.c_float, ctypes.c_int32] + [P] * 10 + \
+                [ctypes.c_size_t, P]
+            L.ffd_art_attention.restype = st
             L.ffd_set_profile_events.argtypes = [P, P]
             L.ffd_set_profile_events.restype = st
             L.ffd_get_error.argtypes = [P, P]
@@ -249,6 +255,29 @@ def ffd_decode_attention_masked(params: DecodeParams, q, cache: QuantizedCache, 
         _ptr(block_table), _ptr(keep_in), _ptr(out), _ptr(keep_mask), _ptr(m_tilde),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
         "ffd_decode_attention_masked")
+
+
+def ffd_art_workspace_size(params: DecodeParams) -> int:
+    return int(lib().ffd_art_workspace_size(ctypes.byref(params)))
+
+
+def alloc_art_workspace(params: DecodeParams, device="cuda") -> torch.Tensor:
+    n = ffd_art_workspace_size(params)
+    if n == 0:
+        raise FFDError(1, "ART workspace size")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def ffd_art_attention(params: DecodeParams, tau: float, phi: float, patience: int, q,
+                      cache: QuantizedCache, v, seq_lens, block_table, out, workspace, *,
+                      keep_in=None, blocks_used=None, stream=None) -> None:
+    """Attention with run-time termination (ART) over block 0 and the blocks of ``keep_in`` (all
+    blocks when None), most recent first; ``blocks_used`` [B, Hkv] int32 receives the count."""
+    _check(lib().ffd_art_attention(
+        ctypes.byref(params), tau, phi, patience, _ptr(q), *map(_ptr, cache), _ptr(v),
+        _ptr(seq_lens), _ptr(block_table), _ptr(keep_in), _ptr(out), _ptr(blocks_used),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "ffd_art_attention")
 
 
 def ffd_dense_decode(params: DecodeParams, q, k, v, seq_lens, block_table, out, workspace, *,

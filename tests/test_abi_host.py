@@ -190,3 +190,29 @@ def test_select_and_masked_reject_bad_arguments(lib):
     for key in ("q", "th", "rs", "v", "sl", "bt", "ki", "out", "ws"):
         assert masked(**{key: None}) == 1, key
     assert masked(v=FAKE + 2) == 1
+
+
+def test_art_rejects_bad_arguments(lib):
+    p = _params()
+    need = ffd.ffd_art_workspace_size(p)
+    assert need == 256
+
+    def art(tau=0.01, phi=0.001, patience=2, ws_bytes=need, **kw):
+        a = dict(q=FAKE, th=FAKE, rs=FAKE, v=FAKE, sl=FAKE, bt=FAKE, ki=None, out=FAKE, bu=None,
+                 ws=FAKE)
+        a.update(kw)
+        return lib.ffd_art_attention(
+            ctypes.byref(kw.pop("p", p)), tau, phi, patience,
+            *[a[x] for x in ("q", "th", "rs", "v", "sl", "bt", "ki", "out", "bu", "ws")],
+            ws_bytes, None)
+
+    for key in ("q", "th", "rs", "v", "sl", "bt", "out", "ws"):
+        assert art(**{key: None}) == 1, key
+    assert art(tau=-1e-3) == 1 and art(phi=-1.0) == 1
+    assert art(tau=math.nan) == 1 and art(phi=math.nan) == 1
+    assert art(patience=0) == 1 and art(patience=-3) == 1
+    assert art(th=FAKE + 4) == 1 and art(v=FAKE + 2) == 1 and art(ws=FAKE + 16) == 1
+    assert art(ws_bytes=need - 1) == 3
+    bad = _params()
+    bad.head_dim = 64
+    assert art(p=bad) == 2 and ffd.ffd_art_workspace_size(bad) == 0
