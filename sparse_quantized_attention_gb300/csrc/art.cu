@@ -143,14 +143,15 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(DecodeArgs a, float ta
         return ok;
     };
 
-    float m[kMaxG], l[kMaxG], o[kMaxG], prev[kMaxG], pn[kMaxG];
+    float m[kMaxG], l[kMaxG], o[kMaxG], prev[kMaxG], pn[kMaxG], rpn[kMaxG];
 #pragma unroll
     for (int i = 0; i < kMaxG; i++) {
         m[i] = -INFINITY;
         l[i] = 0.0f;
         o[i] = 0.0f;
         prev[i] = 0.0f;
-        pn[i] = 0.0f;  // squared norm of the previous probe
+        pn[i] = 0.0f;   // squared norm of the previous probe
+        rpn[i] = 0.0f;  // 1 / its norm
     }
     int used = 0, streak = 0;
     int hi = nb - 1;       // top block of the next chunk of the kept-block list
@@ -257,35 +258,42 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(DecodeArgs a, float ta
         for (int i = 0; i < kMaxG; i++) {
             o[i] = fmaf(alpha[i], o[i], acc[i]);
             l[i] = fmaf(alpha[i], l[i], ps[i]);
-            cur[i] = l[i] > 0.0f ? o[i] / l[i] : 0.0f;
+            cur[i] = l[i] > 0.0f ? o[i] * __frcp_rn(l[i]) : 0.0f;
             nn[i] = cur[i] * cur[i];
         }
         used++;
         // the probe and the stability criterion (every thread takes the same decision)
         cta_sum8(nn, red_n);
+        float rn[kMaxG];  // 1 / |P_i(t)|
+#pragma unroll
+        for (int i = 0; i < kMaxG; i++) rn[i] = nn[i] > 0.0f ? rsqrtf(nn[i]) : 0.0f;
         bool stop = false;
         if (used >= 2) {
             float dd[kMaxG];
 #pragma unroll
             for (int i = 0; i < kMaxG; i++) {
-                const float nc = sqrtf(nn[i]), np = sqrtf(pn[i]);
-                const float x = nc > 0.0f ? cur[i] / nc : 0.0f;
-                const float y = np > 0.0f ? prev[i] / np : 0.0f;
-                dd[i] = (x - y) * (x - y);
+                const float x = cur[i] * rn[i] - prev[i] * rpn[i];
+                dd[i] = x * x;
             }
             cta_sum8(dd, red_d);
-            float ds = 0.0f, dr = 0.0f;
+            // head lane & 7 on every lane (the same values in every warp), then the maxima
+            const int i = lane & 7;
+            float nni = 0.0f, pni = 0.0f, ddi = 0.0f;
 #pragma unroll
-            for (int i = 0; i < kMaxG; i++) {
-                if (i < G) {
-                    const float nc = sqrtf(nn[i]), np = sqrtf(pn[i]);
-                    ds = fmaxf(ds, np > 0.0f ? fabsf(nc - np) / np : nc);
-                    // 1 - cos; a zero probe on one side only counts as orthogonal
-                    const float d = (nc > 0.0f && np > 0.0f)
-                                        ? 0.5f * dd[i]
-                                        : ((nc == 0.0f && np == 0.0f) ? 0.0f : 1.0f);
-                    dr = fmaxf(dr, d);
-                }
+            for (int k = 0; k < kMaxG; k++)
+                if (k == i) nni = nn[k], pni = pn[k], ddi = dd[k];
+            float ds = 0.0f, dr = 0.0f;
+            if (i < G) {
+                const float nc = sqrtf(nni), np = sqrtf(pni);
+                ds = np > 0.0f ? fabsf(nc - np) / np : nc;
+                // 1 - cos; a zero probe on one side only counts as orthogonal
+                dr = (nc > 0.0f && np > 0.0f) ? 0.5f * ddi
+                                              : ((nc == 0.0f && np == 0.0f) ? 0.0f : 1.0f);
+            }
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) {
+                ds = fmaxf(ds, __shfl_xor_sync(0xffffffffu, ds, off));
+                dr = fmaxf(dr, __shfl_xor_sync(0xffffffffu, dr, off));
             }
             streak = (ds < tau && dr < phi) ? streak + 1 : 0;
             stop = streak >= patience;
@@ -295,6 +303,7 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(DecodeArgs a, float ta
         for (int i = 0; i < kMaxG; i++) {
             prev[i] = cur[i];
             pn[i] = nn[i];
+            rpn[i] = rn[i];
         }
         // every read of stage st is behind the barriers above: refill it with the block after cn
         const int cn2 = cn >= 0 ? advance() : -1;
