@@ -26,7 +26,8 @@ namespace ffd {
 
 namespace {
 
-constexpr int kStatBlocks = 8;     // blocks per CTA of the statistics pass
+constexpr int kStatBlocks = 32;    // blocks per CTA of the statistics pass
+constexpr int kStatWarps = 4;      // its warps; warp w takes blocks w, w + 4, ...
 constexpr int kSelThreads = 1024;  // threads of the selection CTA
 constexpr int kSelMaxBlocks = 16384;
 constexpr float kLog2e = 1.4426950408889634f;  // 1 / ln 2
@@ -42,118 +43,137 @@ __device__ __forceinline__ int stat_len(const DecodeArgs &a, int b) {
 }
 
 // Pass 1. CTA (x, u) takes blocks kStatBlocks x .. of unit u: it writes their initial keep-mask
-// bytes (1 for a sink or local block, 0 otherwise, 0 past the sequence), brings their thumbnail
-// records into shared memory with one bulk copy each (all issued at once), and then warp mt scores
-// rows 16mt .. 16mt+15 of each block for every head of the group (scan_tile). Block importance ->
-// imp[u][c]; per head (max, sum e^(s^ - max)) -> ml[u][c][G].
+// bytes (1 for a sink or local block, 0 otherwise, 0 past the sequence); then each warp takes
+// every fourth of those blocks on its own, with no CTA barrier: lane 0 brings the block's
+// thumbnail record into the warp's two shared-memory stages by one bulk copy (the next block's
+// copy is in flight while the current one is scored), and the warp scores all 64 rows for every
+// head of the group (four scan_tile m-tiles). Block importance -> imp[u][c]; per head (max,
+// sum e^(s^ - max)) -> ml[u][c][G].
 __global__ void __launch_bounds__(128) block_stats_kernel(DecodeArgs a, float *imp, float2 *ml) {
-    __shared__ __align__(128) uint8_t recs[kStatBlocks][kThumbRec];
-    __shared__ __align__(8) uint64_t full;
-    __shared__ int pages[kStatBlocks];
-    __shared__ float s_imp[4];
-    __shared__ float2 s_ml[4][kMaxG];
+    __shared__ __align__(128) uint8_t recs[kStatWarps][2][kThumbRec];
+    __shared__ __align__(8) uint64_t full[kStatWarps][2];
     const int u = blockIdx.y;
     const int b = u / a.Hkv, h = u - b * a.Hkv;
     const int n = stat_len(a, b);
     const int nb = (n + kPage - 1) / kPage;
     const int c0 = blockIdx.x * kStatBlocks;
     const size_t row = (size_t)u * a.max_blocks;
-    if (threadIdx.x < kStatBlocks && c0 + threadIdx.x < a.max_blocks) {
-        const int c = c0 + threadIdx.x;
+    {
         const ForcedBlocks fb(n, a.S, a.L);
-        a.keep_mask[row + c] = c < nb && fb.forced(c);
+        for (int k = threadIdx.x; k < kStatBlocks; k += blockDim.x) {
+            const int c = c0 + k;
+            if (c < a.max_blocks) a.keep_mask[row + c] = c < nb && fb.forced(c);
+        }
     }
-    if (c0 >= nb) return;  // CTA-uniform
-    const int cnt = nb - c0 < kStatBlocks ? nb - c0 : kStatBlocks;
+    const int cend = nb < c0 + kStatBlocks ? nb : c0 + kStatBlocks;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == 0) {
-        int page = -1;
-        if (lane < cnt) {
-            page = a.block_table[(size_t)b * a.max_blocks + c0 + lane];
-            if (page < 0 || page >= a.P) {
-                raise_error(a.err, FFD_ERRBIT_BOUNDS);
-                page = -1;
-            }
-        }
-        const uint32_t good = __ballot_sync(0xffffffffu, page >= 0);
-        if (lane < kStatBlocks) pages[lane] = page;
-        if (lane == 0) {
-            mbar_init(&full, 1);
-            fence_barrier_init();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&full, (uint32_t)__popc(good) * kThumbRec);
-        __syncwarp();
-        if (page >= 0)
-            tma_load_1d(recs[lane], a.thumb + ((size_t)page * a.Hkv + h) * kThumbRec, kThumbRec,
-                        &full);
-    }
+    if (c0 + warp >= cend) return;  // warp-uniform; no CTA barrier follows
     const int g = lane >> 2, tig = lane & 3;
-    const int r0 = 16 * warp + g, r1 = r0 + 8;
     const uint32_t m0 = 0x00030003u << (2 * tig);
     const int h0 = 2 * tig, h1 = 2 * tig + 1;
-    ThumbOps Q;
-    load_thumb_ops(a, b, h, lane, Q);  // overlaps the copies
-    __syncthreads();                   // barrier initialised, pages published
-    // bounded wait for the copies (they were issued by this CTA)
-    const uint64_t t0 = globaltimer_ns();
-    bool ok = true;
-    while (!mbar_try_wait(&full, 0)) {
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-            if (threadIdx.x == 0) raise_error(a.err, FFD_ERRBIT_TIMEOUT);
-            ok = false;
-            break;
-        }
+    const bool w0 = h0 < a.G, w1 = h1 < a.G;
+    const int32_t *bt = a.block_table + (size_t)b * a.max_blocks;
+    if (lane == 0) {
+        mbar_init(&full[warp][0], 1);
+        mbar_init(&full[warp][1], 1);
+        fence_barrier_init();
     }
-    if (!ok) return;
-    for (int k = 0; k < cnt; k++) {
-        const int c = c0 + k;
-        const bool bad = pages[k] < 0;  // block-uniform
-        float4 e = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        if (!bad) e = scan_tile(recs[k], r0, r1, m0, Q, a.sm_scale);
-        const bool v0 = c * kPage + r0 < n, v1 = c * kPage + r1 < n;
-        const bool w0 = h0 < a.G, w1 = h1 < a.G;
-        const float x00 = v0 && w0 ? e.x : -INFINITY, x01 = v0 && w1 ? e.y : -INFINITY;
-        const float x10 = v1 && w0 ? e.z : -INFINITY, x11 = v1 && w1 ? e.w : -INFINITY;
-        // importance: max over the warp's rows and every head
-        const float wm = warp_max(fmaxf(fmaxf(x00, x01), fmaxf(x10, x11)));
-        // per head: max over the warp's 16 rows (lanes with the same tig), then the sum
-        float mh0 = fmaxf(x00, x10), mh1 = fmaxf(x01, x11);
+    __syncwarp();
+    // The copy of block c into stage st (false, nothing issued, for a page outside [0, P)).
+    auto issue = [&](int c, int st) -> bool {
+        int page = 0;
+        if (lane == 0) page = bt[c];
+        page = __shfl_sync(0xffffffffu, page, 0);
+        if (page < 0 || page >= a.P) {
+            if (lane == 0) raise_error(a.err, FFD_ERRBIT_BOUNDS);
+            return false;
+        }
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&full[warp][st], kThumbRec);
+            tma_load_1d(recs[warp][st], a.thumb + ((size_t)page * a.Hkv + h) * kThumbRec,
+                        kThumbRec, &full[warp][st]);
+        }
+        return true;
+    };
+    uint32_t phases = 0u;  // bit st: parity of stage st's next completion
+    auto wait_stage = [&](int st) -> bool {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&full[warp][st], (phases >> st) & 1u)) {
+            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                phases ^= 1u << st;
+                if (lane == 0) raise_error(a.err, FFD_ERRBIT_TIMEOUT);
+                return false;
+            }
+        }
+        phases ^= 1u << st;
+        return true;
+    };
+    ThumbOps Q;
+    load_thumb_ops(a, b, h, lane, Q);  // overlaps the first copies
+    int c = c0 + warp, st = 0;
+    uint32_t have = (issue(c, 0) ? 1u : 0u);
+    if (c + kStatWarps < cend && issue(c + kStatWarps, 1)) have |= 2u;
+    bool ok = true;
+    for (; c < cend; c += kStatWarps, st ^= 1) {
+        const bool good = (have >> st) & 1u;
+        if (good) {
+            ok = __all_sync(0xffffffffu, wait_stage(st));
+            if (!ok) break;
+        }
+        const int rows = n - c * kPage < kPage ? n - c * kPage : kPage;
+        float x[4][4];
+#pragma unroll
+        for (int mt = 0; mt < 4; mt++) {
+            const int r0 = 16 * mt + g, r1 = r0 + 8;
+            float4 e = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (good) e = scan_tile(recs[warp][st], r0, r1, m0, Q, a.sm_scale);
+            const bool v0 = r0 < rows, v1 = r1 < rows;
+            x[mt][0] = v0 && w0 ? e.x : -INFINITY;
+            x[mt][1] = v0 && w1 ? e.y : -INFINITY;
+            x[mt][2] = v1 && w0 ? e.z : -INFINITY;
+            x[mt][3] = v1 && w1 ? e.w : -INFINITY;
+        }
+        __syncwarp();  // every lane has read the stage: it can be refilled
+        have &= ~(1u << st);
+        if (c + 2 * kStatWarps < cend && issue(c + 2 * kStatWarps, st)) have |= 1u << st;
+        // per head: max over the block's 64 rows (lanes with the same tig), then the sum
+        float mh0 = -INFINITY, mh1 = -INFINITY;
+#pragma unroll
+        for (int mt = 0; mt < 4; mt++) {
+            mh0 = fmaxf(mh0, fmaxf(x[mt][0], x[mt][2]));
+            mh1 = fmaxf(mh1, fmaxf(x[mt][1], x[mt][3]));
+        }
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
             mh0 = fmaxf(mh0, __shfl_xor_sync(0xffffffffu, mh0, o));
             mh1 = fmaxf(mh1, __shfl_xor_sync(0xffffffffu, mh1, o));
         }
         const float b0 = mh0 == -INFINITY ? 0.0f : mh0, b1 = mh1 == -INFINITY ? 0.0f : mh1;
-        float l0 = ex2_approx((x00 - b0) * kLog2e) + ex2_approx((x10 - b0) * kLog2e);
-        float l1 = ex2_approx((x01 - b1) * kLog2e) + ex2_approx((x11 - b1) * kLog2e);
+        float l0 = 0.0f, l1 = 0.0f;
+#pragma unroll
+        for (int mt = 0; mt < 4; mt++) {
+            l0 += ex2_approx((x[mt][0] - b0) * kLog2e) + ex2_approx((x[mt][2] - b0) * kLog2e);
+            l1 += ex2_approx((x[mt][1] - b1) * kLog2e) + ex2_approx((x[mt][3] - b1) * kLog2e);
+        }
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, o);
             l1 += __shfl_xor_sync(0xffffffffu, l1, o);
         }
-        if (lane == 0) s_imp[warp] = wm;
-        if (g == 0) {
-            s_ml[warp][h0] = make_float2(mh0, l0);
-            s_ml[warp][h1] = make_float2(mh1, l1);
-        }
-        __syncthreads();
+        // importance: max over every head (the quads' heads, then across quads)
+        float im = fmaxf(mh0, mh1);
+        im = fmaxf(im, __shfl_xor_sync(0xffffffffu, im, 1));
+        im = fmaxf(im, __shfl_xor_sync(0xffffffffu, im, 2));
         const size_t slot = row + c;
-        if (threadIdx.x == 0)
-            imp[slot] = fmaxf(fmaxf(s_imp[0], s_imp[1]), fmaxf(s_imp[2], s_imp[3]));
-        if (threadIdx.x < a.G) {
-            const int hh = threadIdx.x;
-            float M = -INFINITY;
-            for (int w = 0; w < 4; w++) M = fmaxf(M, s_ml[w][hh].x);
-            float L = 0.0f;
-            if (M != -INFINITY)
-                for (int w = 0; w < 4; w++)
-                    if (s_ml[w][hh].x != -INFINITY)
-                        L += s_ml[w][hh].y * ex2_approx((s_ml[w][hh].x - M) * kLog2e);
-            ml[slot * a.G + hh] = make_float2(M, L);
+        if (lane == 0) imp[slot] = im;
+        if (g == 0) {
+            if (w0) ml[slot * a.G + h0] = make_float2(mh0, l0);
+            if (w1) ml[slot * a.G + h1] = make_float2(mh1, l1);
         }
-        __syncthreads();
     }
+    // copies still in flight into this warp's stages are waited for (bounded) before it exits
+    for (int k = 0; k < 2; k++)
+        if ((have >> k) & 1u) __all_sync(0xffffffffu, wait_stage(k));
 }
 
 // Float -> unsigned key whose unsigned order is the float's order (NaN never occurs here).
