@@ -162,3 +162,29 @@ def test_thresholds_stop_where_the_oracle_stops(case, q, patience):
             assert at.used == used[b, h]
             _close(out[b, h * G:(h + 1) * G], at.out)
     assert exact >= 1
+
+
+def test_bad_block_table_entry_raises_and_contributes_nothing():
+    """A block-table entry outside [0, P) sets the bounds bit; that block adds nothing and still
+    counts as visited; the other blocks give the softmax over themselves."""
+    w = ffd_synth.custom(1, 8, 2, 1000, seed=57)
+    inp, dev, qc, qk = _setup(w)
+    G = w.num_q_heads // w.num_kv_heads
+    nb = (int(inp.seq_lens[0]) + 63) // 64
+    bad = 5
+    bt = dev["block_table"].clone()
+    bt[0, bad] = inp.num_pages  # one past the last page
+    p = H.params_for(inp, 5.0)
+    ws = ffd.alloc_art_workspace(p)
+    out = torch.zeros((1, w.num_q_heads, 128), device="cuda")
+    used = torch.zeros((1, w.num_kv_heads), dtype=torch.int32, device="cuda")
+    ffd.ffd_art_attention(p, 0.0, 0.0, 1, dev["q"], qc, dev["v"], dev["seq_lens"], bt, out, ws,
+                          blocks_used=used)
+    assert ffd.ffd_get_error(ws) == 5  # FFD_ERR_BOUNDS
+    got = out.cpu().numpy().astype(np.float64)
+    keep = np.ones(nb, np.uint8)
+    keep[bad] = 0
+    for h in range(w.num_kv_heads):
+        assert used[0, h] == nb
+        res, _ = _oracle(inp, qk, 0, h, keep, 0.0, 0.0, 1)
+        _close(got[0, h * G:(h + 1) * G], res.out)
