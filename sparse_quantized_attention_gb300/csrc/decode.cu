@@ -91,7 +91,7 @@ struct PageSlot {
     uint32_t bad;        // entries outside [0, P), one bit per block (row 0, never loaded)
     uint32_t forced;     // blocks holding a sink or local token (kept whatever the scan says)
     int32_t cnt;         // blocks; 0 marks the end of this CTA's schedule
-    int32_t pad;
+    int32_t tail;        // rows of block cnt - 1 when it is the sequence's partial last block, else 0
 };
 
 struct Misc {
@@ -113,6 +113,8 @@ struct Misc {
     uint64_t ring_empty[kRing];
     uint64_t unit_ready[2];
     uint64_t unit_free[2];
+    uint64_t tail_full;  // the ring warp's own copies of a partial last block
+    uint32_t tails;      // partial last blocks the ring warp has copied so far
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc region");
 
@@ -283,7 +285,8 @@ __device__ __forceinline__ void pager(const DecodeArgs &a, const Smem &S, int ct
         if (lane < s.cnt) page = a.block_table[(size_t)s.b * a.max_blocks + s.j0 + lane];
         const bool bad = lane < s.cnt && (page < 0 || page >= a.P);
         const uint32_t badmask = __ballot_sync(0xffffffffu, bad);
-        const ForcedBlocks fb(len_of(a, s.b), a.S, a.L);
+        const int n = len_of(a, s.b);
+        const ForcedBlocks fb(n, a.S, a.L);
         // with a caller-given mask (comparison selectors) the mask alone decides: the scan's
         // thresholds are +inf and the given blocks take the place of the forced ones
         const bool given = a.keep_in && lane < s.cnt &&
@@ -296,6 +299,7 @@ __device__ __forceinline__ void pager(const DecodeArgs &a, const Smem &S, int ct
             P.bad = badmask;
             P.forced = forced;
             P.cnt = s.cnt;
+            P.tail = s.j0 + s.cnt == s.nblk ? (n & (kPage - 1)) : 0;
             if (badmask) raise_error(a.err, FFD_ERRBIT_BOUNDS);
         }
         __syncwarp();
@@ -345,7 +349,10 @@ __device__ __forceinline__ void thumb_issuer(const DecodeArgs &a, const Smem &S,
 
 // Ring warp: publishes the kept blocks of sub-chunk t (scan votes, plus the forced blocks, less
 // the never-loaded ones), then issues the residual record and the V tile of each kept block into
-// the next ring slot as it frees up; lanes 0 and 1 issue the two copies side by side.
+// the next ring slot as it frees up; lanes 0 and 1 issue the two copies side by side. A sequence's
+// partial last block is copied under the warp's own barrier instead: the warp waits for it, zeroes
+// the V rows past the sequence (they hold whatever the cache holds, and a zero probability times a
+// NaN would poison P.V) and then completes the slot's fill barrier itself.
 __device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S, int lane) {
     const DecodeArgs &a = prm.a;
     Misc *m = S.misc;
@@ -367,6 +374,7 @@ __device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S
             m->vote[(t + kThumbBufs) % kDepth] = 0;
             mbar_arrive(&m->ring_seen[ds]);
         }
+        const int tail_k = P.tail ? cnt - 1 : -1;  // the partial last block, if any
         for (int k = 0; k < cnt; k++) {
             if (!(mask & (1u << k))) continue;
             const int slot = kb % kRing, round = kb / kRing;
@@ -375,10 +383,28 @@ __device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S
             const int row = P.row[k];
             uint8_t *d = S.ring + slot * kSlotBytes;
             uint64_t *bar = &m->ring_full[(kb - 1) % kRefineGroups][slot];  // kb advanced above
-            if (lane == 0) mbar_arrive_expect_tx(bar, kSlotTx);
+            const bool tail = k == tail_k;
+            uint64_t *cb = tail ? &m->tail_full : bar;
+            if (lane == 0) mbar_arrive_expect_tx(cb, kSlotTx);
             __syncwarp();
-            if (lane == 0) tma_load_1d(d, a.resid + (size_t)(row / kPage) * kResidRec, kResidRec, bar);
-            else if (lane == 1) tma_load_3d(d + kSlotV, &prm.tm_v, 0, row, 0, bar);
+            if (lane == 0) tma_load_1d(d, a.resid + (size_t)(row / kPage) * kResidRec, kResidRec, cb);
+            else if (lane == 1) tma_load_3d(d + kSlotV, &prm.tm_v, 0, row, 0, cb);
+            if (tail) {  // warp-uniform; once per sequence
+                const int rows = P.tail;
+                const uint32_t nt = *reinterpret_cast<volatile uint32_t *>(&m->tails);
+                drain_bar(a, &m->tail_full, nt & 1);  // bounded, and never left in flight
+                for (int c = lane; c < (kPage - rows) * 16; c += 32) {  // both 64 x 128 B halves
+                    const int r = rows + (c >> 4), half = (c >> 3) & 1;
+                    *reinterpret_cast<uint4 *>(d + kSlotV + half * 8192 + r * 128 + (c & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async();  // before the slot's next bulk copy
+                __syncwarp();
+                if (lane == 0) {
+                    m->tails = nt + 1;
+                    mbar_arrive(bar);
+                }
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&m->pages_empty[t % kPageSlots]);
@@ -659,6 +685,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             mbar_init(&m->unit_ready[i], 1);  // scan warp 0
             mbar_init(&m->unit_free[i], 4 * kRefineGroups);  // refine warps
         }
+        mbar_init(&m->tail_full, 1);  // the ring warp
+        m->tails = 0;
         fence_barrier_init();
     }
     __syncthreads();

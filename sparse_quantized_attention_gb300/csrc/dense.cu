@@ -30,6 +30,7 @@ struct DensePages {
     int32_t row[kSub];  // first row of each block's tile: (page * Hkv + h) * 64
     uint32_t bad;       // entries outside [0, P), one bit per block (never loaded)
     int32_t cnt;        // blocks; 0 ends this CTA's schedule
+    int32_t tail;       // rows of block cnt - 1 when it is the sequence's partial last block, else 0
 };
 
 struct DenseMisc {
@@ -44,6 +45,8 @@ struct DenseMisc {
     uint64_t pages_empty[kDPageSlots];
     uint64_t full[kRefineGroups][kDRing];    // [group of the block][slot]
     uint64_t empty[kDRing];
+    uint64_t tail_full;  // the copy warp's own copies of a partial last block
+    uint32_t tails;      // partial last blocks the copy warp has copied so far
 };
 static_assert(sizeof(DenseMisc) <= kDMiscBytes, "control block");
 
@@ -76,6 +79,7 @@ __device__ __forceinline__ void dense_pager(const DecodeArgs &a, DenseMisc *m, i
         if (lane == 0) {
             P.bad = badm;
             P.cnt = more ? s.cnt : 0;
+            P.tail = more && s.j0 + s.cnt == s.nblk ? (len_of(a, s.b) & (kPage - 1)) : 0;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&m->pages_full[ps]);
@@ -85,7 +89,10 @@ __device__ __forceinline__ void dense_pager(const DecodeArgs &a, DenseMisc *m, i
 
 // Copy warp: block kb goes to ring slot kb % kDRing as soon as the slot is free; lanes 0 and 1
 // issue the K and V copies side by side. Each refine group has its own fill barrier per slot
-// (consecutive phases = its blocks kb, kb + kDFillPeriod, ...).
+// (consecutive phases = its blocks kb, kb + kDFillPeriod, ...). A sequence's partial last block
+// is copied under the warp's own barrier: the warp waits for it, zeroes the V rows past the
+// sequence (a zero probability times a NaN there would poison P.V) and then completes the slot's
+// fill barrier itself.
 __device__ __forceinline__ void dense_ring(const DenseParams &prm, DenseMisc *m, uint8_t *ring,
                                            int lane) {
     const DecodeArgs &a = prm.a;
@@ -100,21 +107,40 @@ __device__ __forceinline__ void dense_ring(const DenseParams &prm, DenseMisc *m,
         const DensePages &P = m->ps[ps];
         const int cnt = P.cnt;
         if (cnt == 0 || aborted(m)) break;
+        const int tail_k = P.tail ? cnt - 1 : -1;  // the partial last block, if any
         for (int k = 0; k < cnt; k++, kb++) {
             const int slot = kb % kDRing, round = kb / kDRing;
             if (round > 0) wait_bar(a, m, &m->empty[slot], (round - 1) & 1);
             uint64_t *bar = &m->full[kb % kRefineGroups][slot];
             const bool bad = (P.bad >> k) & 1u;
             uint8_t *d = ring + slot * kDSlotBytes;
+            const bool tail = !bad && k == tail_k;
+            uint64_t *cb = tail ? &m->tail_full : bar;
             if (lane == 0) {
                 m->slot_bad[slot] = bad;
                 if (bad) mbar_arrive(bar);
-                else mbar_arrive_expect_tx(bar, kDSlotBytes);
+                else mbar_arrive_expect_tx(cb, kDSlotBytes);
             }
             __syncwarp();
             if (!bad) {
-                if (lane == 0) tma_load_3d(d + kDSlotK, &prm.tm_k, 0, P.row[k], 0, bar);
-                else if (lane == 1) tma_load_3d(d + kDSlotV, &prm.tm_v, 0, P.row[k], 0, bar);
+                if (lane == 0) tma_load_3d(d + kDSlotK, &prm.tm_k, 0, P.row[k], 0, cb);
+                else if (lane == 1) tma_load_3d(d + kDSlotV, &prm.tm_v, 0, P.row[k], 0, cb);
+            }
+            if (tail) {  // warp-uniform; once per sequence
+                const int rows = P.tail;
+                const uint32_t nt = *reinterpret_cast<volatile uint32_t *>(&m->tails);
+                drain_bar(a, &m->tail_full, nt & 1);  // bounded, and never left in flight
+                for (int c = lane; c < (kPage - rows) * 16; c += 32) {  // both 64 x 128 B halves
+                    const int r = rows + (c >> 4), half = (c >> 3) & 1;
+                    *reinterpret_cast<uint4 *>(d + kDSlotV + half * 8192 + r * 128 + (c & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async();  // before the slot's next bulk copy
+                __syncwarp();
+                if (lane == 0) {
+                    m->tails = nt + 1;
+                    mbar_arrive(bar);
+                }
             }
         }
         __syncwarp();
@@ -221,6 +247,8 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_kernel(const __grid_consta
             for (int g = 0; g < kRefineGroups; g++) mbar_init(&m->full[g][i], 1);
             mbar_init(&m->empty[i], 4);  // the refine group that took the block
         }
+        mbar_init(&m->tail_full, 1);  // the copy warp
+        m->tails = 0;
         fence_barrier_init();
     }
     __syncthreads();
