@@ -15,79 +15,77 @@
 //   * the order is block 0, then the kept blocks from the most recent to the oldest.
 //
 // The criterion makes one unit's traversal sequential, so the parallelism is across units, the
-// regime the page reports its gains in (large batches): one CTA of 128 threads walks one
-// (sequence, KV head) unit. Per block, warp mt computes the exact scores (thumbnail + residual, on
-// the tensor cores) of rows 16mt .. 16mt+15 for every head, thread t owns the online-softmax
-// probabilities of head t % 8 on rows t/8 + 16j, and thread t accumulates output channel t of
-// every head over the block's V rows. A block's three records (thumbnail 3 KB, residual 8.5 KB,
-// V 16 KB) are brought into shared memory by bulk copies, double-buffered: the next block's copies
-// are in flight while the current block is processed. 1 - cos is formed as |P/|P| - Q/|Q||^2 / 2,
-// which keeps its precision when the two directions are close.
+// regime the page reports its gains in (large batches): one CTA of 128 threads (one refine group
+// of the decode kernel) walks one (sequence, KV head) unit. A block's three records (thumbnail
+// 3 KB, residual 8.5 KB, V 16 KB as a swizzled tensor tile) are brought into shared memory by
+// bulk copies, double-buffered: the next block's copies are in flight while the current block is
+// processed. Per block, warp mt computes the exact scores of rows 16mt .. 16mt+15 for every head
+// (the thumbnail + residual tensor-core tile of scan.cuh), and the group's online softmax and P.V
+// on the tensor cores (softmax_pv of splitkv.cuh, P as bf16 hi + lo parts) fold the block in; warp
+// mt then holds O^T for channels 32mt .. 32mt+31. The probe needs, per head, l, then |P|^2, then
+// for the direction |P/|P| - P'/|P'||^2 = 2 (1 - cos), which keeps its precision when the two
+// directions are close: three CTA reductions per block. Every thread takes the same decision from
+// the reduced values, so no broadcast is needed.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "scan.cuh"
+#include "splitkv.cuh"
 
 namespace ffd {
 
 namespace {
 
-constexpr float kLog2eArt = 1.4426950408889634f;
 constexpr int kArtThreads = 128;
-
-// One block's records in shared memory (each part 128-byte aligned).
-struct alignas(128) ArtStage {
-    uint8_t thumb[kThumbRec];
-    uint8_t resid[kResidRec];
-    __nv_bfloat16 v[kPage * kD];
-};
+// One block's records in shared memory: the V tile first (1 KB aligned for the 128-byte swizzle).
+constexpr int kArtV = 0;
+constexpr int kArtThumb = kPage * kD * 2;
+constexpr int kArtResid = kArtThumb + kThumbRec;
+constexpr int kArtStage = 28672;  // 28 KB: a multiple of 1 KB
+static_assert(kArtResid + kResidRec <= kArtStage && kArtStage % 1024 == 0, "stage layout");
 constexpr uint32_t kArtStageTx = kThumbRec + kResidRec + kPage * kD * 2;
-static_assert(kThumbRec % 128 == 0 && (kThumbRec + kResidRec) % 128 == 0, "stage alignment");
-constexpr size_t kArtSmem = 2 * sizeof(ArtStage);
+constexpr int kArtPx = 2 * kArtStage;                // two P^T fragment buffers
+constexpr int kArtSmem = kArtPx + 2 * kPxBuf + 1024;  // + slack to align the base to 1 KB
 
-// Sums of eight per-thread values over the 32 lanes of a warp, transposed: on return lane L holds
-// the sum for value L / 4 (each value reaches four lanes). Nine shuffles instead of forty.
-__device__ __forceinline__ float warp_sum8_t(const float (&v)[kMaxG], int lane) {
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-    float w[4], x[2];
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const float send = b4 ? v[k] : v[k + 4];
-        const float keep = b4 ? v[k + 4] : v[k];
-        w[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-#pragma unroll
-    for (int k = 0; k < 2; k++) {
-        const float send = b3 ? w[k] : w[k + 2];
-        const float keep = b3 ? w[k + 2] : w[k];
-        x[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-    const float send = b2 ? x[0] : x[1];
-    float y = (b2 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
-    y += __shfl_xor_sync(0xffffffffu, y, 1);
-    y += __shfl_xor_sync(0xffffffffu, y, 2);
-    return y;
+// The shared control block softmax_pv expects (one refine group), and the probe reductions.
+struct ArtCtl {
+    uint32_t over[1][2][4];
+    float wmax[1][2][4][kMaxG];
+    float red_l[4][kMaxG];  // [warp][head]: l partial sums
+    float red_n[4][kMaxG];  // [warp][head]: |P|^2 partial sums
+    float red_d[4][kMaxG];  // [warp][head]: direction-change partial sums
+    int list[kArtThreads];    // kept blocks of the current chunk, most recent first
+    int wc[4];
+    uint64_t full[2];
+};
+
+struct ArtParams {
+    CUtensorMap tm_v;
+    DecodeArgs a;
+    float tau, phi;
+    int patience;
+    int32_t *used;
+};
+
+// Sum over the 8 lanes of a warp that share tig (one head pair).
+__device__ __forceinline__ float quad_col_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    v += __shfl_xor_sync(0xffffffffu, v, 16);
+    return v;
 }
 
-// CTA sums of eight per-thread values; red is a [4 warps][kMaxG] buffer of its own. On return
-// every thread holds all eight sums.
-__device__ __forceinline__ void cta_sum8(float (&v)[kMaxG], float (*red)[kMaxG]) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float y = warp_sum8_t(v, lane);
-    if ((lane & 3) == 0) red[warp][lane >> 2] = y;
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < kMaxG; i++) v[i] = (red[0][i] + red[1][i]) + (red[2][i] + red[3][i]);
+// d_scale and 1 - cos of one head (a zero probe on one side only counts as orthogonal).
+__device__ __forceinline__ void head_metrics(float nc, float np, float dd, float &ds, float &dr) {
+    ds = np > 0.0f ? fabsf(nc - np) / np : nc;
+    dr = (nc > 0.0f && np > 0.0f) ? 0.5f * dd : ((nc == 0.0f && np == 0.0f) ? 0.0f : 1.0f);
 }
 
-__global__ void __launch_bounds__(kArtThreads) art_kernel(DecodeArgs a, float tau, float phi,
-                                                          int patience, int32_t *used_out) {
-    __shared__ __align__(16) float sp[kPage][kMaxG];  // the block's scores, then its probabilities
-    __shared__ float red_m[4][kMaxG], red_l[4][kMaxG], red_n[4][kMaxG], red_d[4][kMaxG];
-    __shared__ int s_list[kArtThreads];  // kept blocks of the current chunk, most recent first
-    __shared__ int s_wc[4];
-    __shared__ __align__(8) uint64_t full[2];
-    extern __shared__ __align__(128) uint8_t art_dyn[];
-    ArtStage *stage = reinterpret_cast<ArtStage *>(art_dyn);
+__global__ void __launch_bounds__(kArtThreads) art_kernel(const __grid_constant__ ArtParams prm) {
+    const DecodeArgs &a = prm.a;
+    extern __shared__ uint8_t art_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(art_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    __shared__ ArtCtl ctl;
     const int u = blockIdx.x;
     const int b = u / a.Hkv, h = u - b * a.Hkv;
     const int G = a.G;
@@ -96,7 +94,8 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(DecodeArgs a, float ta
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int g = lane >> 2, tig = lane & 3;
     const int r0 = 16 * warp + g, r1 = r0 + 8;
-    const int hp = t & 7, rp = t >> 3;  // probability phase: head hp, rows rp + 16 j
+    const int h0 = 2 * tig, h1 = h0 + 1;
+    const bool w0 = h0 < G, w1 = h1 < G;
     ThumbOps Q;
     ResidOps QR;
     load_thumb_ops(a, b, h, lane, Q);
@@ -104,9 +103,10 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(DecodeArgs a, float ta
     const int32_t *bt = a.block_table + (size_t)b * a.max_blocks;
     const uint8_t *keep = a.keep_in ? a.keep_in + (size_t)u * a.max_blocks : nullptr;
     if (t == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
+        mbar_init(&ctl.full[0], 1);
+        mbar_init(&ctl.full[1], 1);
         fence_barrier_init();
+        prefetch_tensormap(&prm.tm_v);
     }
     __syncthreads();
     // Copies of block c's records into stage st; false (nothing issued) for a page outside
@@ -119,10 +119,11 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(DecodeArgs a, float ta
         }
         if (t == 0) {
             const size_t tile = (size_t)page * a.Hkv + h;
-            mbar_arrive_expect_tx(&full[st], kArtStageTx);
-            tma_load_1d(stage[st].thumb, a.thumb + tile * kThumbRec, kThumbRec, &full[st]);
-            tma_load_1d(stage[st].resid, a.resid + tile * kResidRec, kResidRec, &full[st]);
-            tma_load_1d(stage[st].v, a.v + tile * kPage * kD, kPage * kD * 2, &full[st]);
+            uint8_t *d = base + st * kArtStage;
+            mbar_arrive_expect_tx(&ctl.full[st], kArtStageTx);
+            tma_load_3d(d + kArtV, &prm.tm_v, 0, (int)(tile * kPage), 0, &ctl.full[st]);
+            tma_load_1d(d + kArtThumb, a.thumb + tile * kThumbRec, kThumbRec, &ctl.full[st]);
+            tma_load_1d(d + kArtResid, a.resid + tile * kResidRec, kResidRec, &ctl.full[st]);
         }
         return true;
     };
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(DecodeArgs a, float ta
     auto wait_stage = [&](int st) -> bool {
         const uint64_t t0 = globaltimer_ns();
         bool ok = true;
-        while (!mbar_try_wait(&full[st], (phases >> st) & 1u)) {
+        while (!mbar_try_wait(&ctl.full[st], (phases >> st) & 1u)) {
             if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
                 ok = false;
                 break;
@@ -142,18 +143,6 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(DecodeArgs a, float ta
         if (!ok && t == 0) raise_error(a.err, FFD_ERRBIT_TIMEOUT);
         return ok;
     };
-
-    float m[kMaxG], l[kMaxG], o[kMaxG], prev[kMaxG], pn[kMaxG], rpn[kMaxG];
-#pragma unroll
-    for (int i = 0; i < kMaxG; i++) {
-        m[i] = -INFINITY;
-        l[i] = 0.0f;
-        o[i] = 0.0f;
-        prev[i] = 0.0f;
-        pn[i] = 0.0f;   // squared norm of the previous probe
-        rpn[i] = 0.0f;  // 1 / its norm
-    }
-    int used = 0, streak = 0;
     int hi = nb - 1;       // top block of the next chunk of the kept-block list
     int pos = 0, cnt = 0;  // read position and length of the current chunk
     // The next block of the traversal after block 0: the kept blocks from the most recent down,
@@ -163,148 +152,140 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(DecodeArgs a, float ta
             const int idx = hi - t;
             const bool k = idx >= 1 && (keep == nullptr || keep[idx] != 0);
             const unsigned bal = __ballot_sync(0xffffffffu, k);
-            __syncthreads();  // earlier reads of s_list / s_wc are done
-            if (lane == 0) s_wc[warp] = __popc(bal);
+            __syncthreads();  // earlier reads of the list are done
+            if (lane == 0) ctl.wc[warp] = __popc(bal);
             __syncthreads();
             int off = 0;
-            for (int w = 0; w < warp; w++) off += s_wc[w];
-            if (k) s_list[off + __popc(bal & ((1u << lane) - 1u))] = idx;
-            cnt = (s_wc[0] + s_wc[1]) + (s_wc[2] + s_wc[3]);
+            for (int w = 0; w < warp; w++) off += ctl.wc[w];
+            if (k) ctl.list[off + __popc(bal & ((1u << lane) - 1u))] = idx;
+            cnt = (ctl.wc[0] + ctl.wc[1]) + (ctl.wc[2] + ctl.wc[3]);
             pos = 0;
             hi -= kArtThreads;
             __syncthreads();
         }
-        return pos < cnt ? s_list[pos++] : -1;
+        return pos < cnt ? ctl.list[pos++] : -1;
     };
+
+    RefineState R;
+    R.m0 = R.m1 = kNoReference;  // the first block raises it through the rescale path
+    R.nl0 = R.nl1 = -kNoReference * kLog2e;
+    R.l0 = R.l1 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 2; i++) R.o[i][0] = R.o[i][1] = R.o[i][2] = R.o[i][3] = 0.0f;
+    float px[2][4];                // the previous probe's direction o' / |o'|, this thread's entries
+    float pn0 = 0.0f, pn1 = 0.0f;  // the previous probe's norms |P| (heads h0, h1)
+    float L0 = 0.0f, L1 = 0.0f;    // the current l (heads h0, h1)
+#pragma unroll
+    for (int i = 0; i < 2; i++) px[i][0] = px[i][1] = px[i][2] = px[i][3] = 0.0f;
+    int used = 0, streak = 0, pb = 0;
+
     int c = nb > 0 ? 0 : -1;  // block 0 first
     int st = 0;
     bool have = c >= 0 && issue(c, 0);
     int cn = c >= 0 ? advance() : -1;
     bool have_n = cn >= 0 && issue(cn, 1);
     while (c >= 0) {
-        const bool bad = !have;
         if (have && !wait_stage(st)) break;  // timed out: the error word says so
-        const ArtStage &sg = stage[st];
-        // scores of the block's rows for every head (-inf for rows past n and heads past G)
-        float4 e = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        if (!bad) e = exact_tile(sg.thumb, sg.resid, r0, r1, tig, Q, QR, a.sm_scale);
-        const int rows = n - c * kPage < kPage ? n - c * kPage : kPage;
-        const bool v0 = r0 < rows, v1 = r1 < rows;
-        const int h0 = 2 * tig, h1 = h0 + 1;
-        sp[r0][h0] = v0 && h0 < G ? e.x : -INFINITY;
-        sp[r0][h1] = v0 && h1 < G ? e.y : -INFINITY;
-        sp[r1][h0] = v1 && h0 < G ? e.z : -INFINITY;
-        sp[r1][h1] = v1 && h1 < G ? e.w : -INFINITY;
-        __syncthreads();
-        // block maxima per head: thread t covers head hp on rows rp + 16 j
-        float s4[4];
-        float bm = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            s4[j] = sp[rp + 16 * j][hp];
-            bm = fmaxf(bm, s4[j]);
-        }
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-        if (lane < 8) red_m[warp][lane] = bm;
-        __syncthreads();
-        float alpha[kMaxG], mine = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kMaxG; i++) {
-            const float mn = fmaxf(fmaxf(m[i], fmaxf(red_m[0][i], red_m[1][i])),
-                                   fmaxf(red_m[2][i], red_m[3][i]));
-            alpha[i] = m[i] == -INFINITY ? 0.0f : exp2f((m[i] - mn) * kLog2eArt);
-            m[i] = mn;
-            if (i == hp) mine = mn;
-        }
-        // probabilities and their sums per head
-        float ps[kMaxG];
-#pragma unroll
-        for (int i = 0; i < kMaxG; i++) ps[i] = 0.0f;
-        float mysum = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const float p = s4[j] == -INFINITY ? 0.0f : exp2f((s4[j] - mine) * kLog2eArt);
-            sp[rp + 16 * j][hp] = p;
-            mysum += p;
-        }
-#pragma unroll
-        for (int i = 0; i < kMaxG; i++) ps[i] = i == hp ? mysum : 0.0f;
-        // lanes L and L ^ 8, L ^ 16, L ^ 24 share a head: the transposed sum collects them too
-        cta_sum8(ps, red_l);  // its barrier also orders the probability stores before PV
-        // output channel t of every head: o = alpha o + sum_r p[r] V[r][t]
-        float acc[kMaxG];
-#pragma unroll
-        for (int i = 0; i < kMaxG; i++) acc[i] = 0.0f;
-        if (!bad) {
-            const __nv_bfloat16 *vt = sg.v + t;
-#pragma unroll 4
-            for (int r = 0; r < rows; r++) {
-                const float vv = __bfloat162float(vt[(size_t)r * kD]);
-                const float4 p0 = *reinterpret_cast<const float4 *>(&sp[r][0]);
-                const float4 p1 = *reinterpret_cast<const float4 *>(&sp[r][4]);
-                acc[0] = fmaf(p0.x, vv, acc[0]);
-                acc[1] = fmaf(p0.y, vv, acc[1]);
-                acc[2] = fmaf(p0.z, vv, acc[2]);
-                acc[3] = fmaf(p0.w, vv, acc[3]);
-                acc[4] = fmaf(p1.x, vv, acc[4]);
-                acc[5] = fmaf(p1.y, vv, acc[5]);
-                acc[6] = fmaf(p1.z, vv, acc[6]);
-                acc[7] = fmaf(p1.w, vv, acc[7]);
+        if (have) {  // block-uniform
+            uint8_t *sg = base + st * kArtStage;
+            const int rows = n - c * kPage < kPage ? n - c * kPage : kPage;
+            const float4 e = exact_tile(sg + kArtThumb, sg + kArtResid, r0, r1, tig, Q, QR,
+                                        a.sm_scale);
+            const bool v0 = r0 < rows, v1 = r1 < rows;
+            if (rows < kPage) {  // the sequence's partial last block: V rows past it read as 0
+                for (int k = t; k < (kPage - rows) * 16; k += kArtThreads) {
+                    const int r = rows + (k >> 4), half = (k >> 3) & 1;
+                    *reinterpret_cast<uint4 *>(sg + kArtV + half * 8192 + r * 128 + (k & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async();  // before the stage's next bulk copy
+                __syncthreads();
             }
-        }
-        float cur[kMaxG], nn[kMaxG];
-#pragma unroll
-        for (int i = 0; i < kMaxG; i++) {
-            o[i] = fmaf(alpha[i], o[i], acc[i]);
-            l[i] = fmaf(alpha[i], l[i], ps[i]);
-            cur[i] = l[i] > 0.0f ? o[i] * __frcp_rn(l[i]) : 0.0f;
-            nn[i] = cur[i] * cur[i];
+            softmax_pv(&ctl, base + kArtPx + pb * kPxBuf, sg + kArtV, v0 && w0 ? e.x : -INFINITY,
+                       v0 && w1 ? e.y : -INFINITY, v1 && w0 ? e.z : -INFINITY,
+                       v1 && w1 ? e.w : -INFINITY, R, 0, warp, pb, lane);
+            pb ^= 1;
         }
         used++;
-        // the probe and the stability criterion (every thread takes the same decision)
-        cta_sum8(nn, red_n);
-        float rn[kMaxG];  // 1 / |P_i(t)|
+        // the probe, per head: l (this warp's rows, then the 4 warps), then |P|^2 of P = o / l
+        // (o is the whole numerator in every warp, |P| stays below max |V|, so nothing overflows
+        // however far the lazy softmax reference lags)
+        {
+            const float l0 = quad_col_sum(R.l0), l1 = quad_col_sum(R.l1);
+            if (g == 0) {
+                ctl.red_l[warp][h0] = l0;
+                ctl.red_l[warp][h1] = l1;
+            }
+        }
+        __syncthreads();
+        L0 = (ctl.red_l[0][h0] + ctl.red_l[1][h0]) + (ctl.red_l[2][h0] + ctl.red_l[3][h0]);
+        L1 = (ctl.red_l[0][h1] + ctl.red_l[1][h1]) + (ctl.red_l[2][h1] + ctl.red_l[3][h1]);
+        const float il0 = L0 > 0.0f ? __frcp_rn(L0) : 0.0f, il1 = L1 > 0.0f ? __frcp_rn(L1) : 0.0f;
+        float cur[2][4];
 #pragma unroll
-        for (int i = 0; i < kMaxG; i++) rn[i] = nn[i] > 0.0f ? rsqrtf(nn[i]) : 0.0f;
+        for (int i = 0; i < 2; i++) {
+            cur[i][0] = R.o[i][0] * il0;
+            cur[i][2] = R.o[i][2] * il0;
+            cur[i][1] = R.o[i][1] * il1;
+            cur[i][3] = R.o[i][3] * il1;
+        }
+        {
+            const float q0 = quad_col_sum((cur[0][0] * cur[0][0] + cur[0][2] * cur[0][2]) +
+                                          (cur[1][0] * cur[1][0] + cur[1][2] * cur[1][2]));
+            const float q1 = quad_col_sum((cur[0][1] * cur[0][1] + cur[0][3] * cur[0][3]) +
+                                          (cur[1][1] * cur[1][1] + cur[1][3] * cur[1][3]));
+            if (g == 0) {
+                ctl.red_n[warp][h0] = q0;
+                ctl.red_n[warp][h1] = q1;
+            }
+        }
+        __syncthreads();
+        const float N0 = (ctl.red_n[0][h0] + ctl.red_n[1][h0]) + (ctl.red_n[2][h0] + ctl.red_n[3][h0]);
+        const float N1 = (ctl.red_n[0][h1] + ctl.red_n[1][h1]) + (ctl.red_n[2][h1] + ctl.red_n[3][h1]);
+        const float nc0 = sqrtf(N0), nc1 = sqrtf(N1);  // |P|
+        const float rn0 = N0 > 0.0f ? rsqrtf(N0) : 0.0f, rn1 = N1 > 0.0f ? rsqrtf(N1) : 0.0f;
         bool stop = false;
         if (used >= 2) {
-            float dd[kMaxG];
+            float d0 = 0.0f, d1 = 0.0f;
 #pragma unroll
-            for (int i = 0; i < kMaxG; i++) {
-                const float x = cur[i] * rn[i] - prev[i] * rpn[i];
-                dd[i] = x * x;
+            for (int i = 0; i < 2; i++) {
+                const float a0 = cur[i][0] * rn0 - px[i][0], a2 = cur[i][2] * rn0 - px[i][2];
+                const float a1 = cur[i][1] * rn1 - px[i][1], a3 = cur[i][3] * rn1 - px[i][3];
+                d0 = fmaf(a0, a0, fmaf(a2, a2, d0));
+                d1 = fmaf(a1, a1, fmaf(a3, a3, d1));
             }
-            cta_sum8(dd, red_d);
-            // head lane & 7 on every lane (the same values in every warp), then the maxima
-            const int i = lane & 7;
-            float nni = 0.0f, pni = 0.0f, ddi = 0.0f;
-#pragma unroll
-            for (int k = 0; k < kMaxG; k++)
-                if (k == i) nni = nn[k], pni = pn[k], ddi = dd[k];
-            float ds = 0.0f, dr = 0.0f;
-            if (i < G) {
-                const float nc = sqrtf(nni), np = sqrtf(pni);
-                ds = np > 0.0f ? fabsf(nc - np) / np : nc;
-                // 1 - cos; a zero probe on one side only counts as orthogonal
-                dr = (nc > 0.0f && np > 0.0f) ? 0.5f * ddi
-                                              : ((nc == 0.0f && np == 0.0f) ? 0.0f : 1.0f);
+            d0 = quad_col_sum(d0);
+            d1 = quad_col_sum(d1);
+            if (g == 0) {
+                ctl.red_d[warp][h0] = d0;
+                ctl.red_d[warp][h1] = d1;
             }
-#pragma unroll
-            for (int off = 1; off < 8; off <<= 1) {
-                ds = fmaxf(ds, __shfl_xor_sync(0xffffffffu, ds, off));
-                dr = fmaxf(dr, __shfl_xor_sync(0xffffffffu, dr, off));
-            }
-            streak = (ds < tau && dr < phi) ? streak + 1 : 0;
-            stop = streak >= patience;
+            __syncthreads();
+            const float D0 = (ctl.red_d[0][h0] + ctl.red_d[1][h0]) +
+                             (ctl.red_d[2][h0] + ctl.red_d[3][h0]);
+            const float D1 = (ctl.red_d[0][h1] + ctl.red_d[1][h1]) +
+                             (ctl.red_d[2][h1] + ctl.red_d[3][h1]);
+            float ds0 = 0.0f, dr0 = 0.0f, ds1 = 0.0f, dr1 = 0.0f;
+            if (w0) head_metrics(nc0, pn0, D0, ds0, dr0);
+            if (w1) head_metrics(nc1, pn1, D1, ds1, dr1);
+            float ds = fmaxf(ds0, ds1), dr = fmaxf(dr0, dr1);
+            ds = fmaxf(ds, __shfl_xor_sync(0xffffffffu, ds, 1));
+            dr = fmaxf(dr, __shfl_xor_sync(0xffffffffu, dr, 1));
+            ds = fmaxf(ds, __shfl_xor_sync(0xffffffffu, ds, 2));
+            dr = fmaxf(dr, __shfl_xor_sync(0xffffffffu, dr, 2));
+            streak = (ds < prm.tau && dr < prm.phi) ? streak + 1 : 0;
+            stop = streak >= prm.patience;
         }
         if (stop) break;
 #pragma unroll
-        for (int i = 0; i < kMaxG; i++) {
-            prev[i] = cur[i];
-            pn[i] = nn[i];
-            rpn[i] = rn[i];
+        for (int i = 0; i < 2; i++) {
+            px[i][0] = cur[i][0] * rn0;
+            px[i][2] = cur[i][2] * rn0;
+            px[i][1] = cur[i][1] * rn1;
+            px[i][3] = cur[i][3] * rn1;
         }
+        pn0 = nc0;
+        pn1 = nc1;
         // every read of stage st is behind the barriers above: refill it with the block after cn
         const int cn2 = cn >= 0 ? advance() : -1;
         const bool have_n2 = cn2 >= 0 && issue(cn2, st);
@@ -317,21 +298,46 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(DecodeArgs a, float ta
     // copies still in flight into this CTA's shared memory are waited for (bounded) before it
     // exits: the next block's, after a stop or a timed-out wait
     if (c >= 0 && cn >= 0 && have_n) wait_stage(st ^ 1);
+    // out = o / l: this thread's channels 32mt + 16i + {g, g+8} of heads h0, h1
+    const float i0 = L0 > 0.0f ? 1.0f / L0 : 0.0f, i1 = L1 > 0.0f ? 1.0f / L1 : 0.0f;
+    float *ob = a.out + ((size_t)b * a.Hq + h * G) * kD;
 #pragma unroll
-    for (int i = 0; i < kMaxG; i++)
-        if (i < G)
-            a.out[((size_t)b * a.Hq + h * G + i) * kD + t] = l[i] > 0.0f ? o[i] / l[i] : 0.0f;
-    if (used_out && t == 0) used_out[u] = used;
+    for (int i = 0; i < 2; i++) {
+        const int ch = 32 * warp + 16 * i + g;
+        if (w0) {
+            ob[h0 * kD + ch] = R.o[i][0] * i0;
+            ob[h0 * kD + ch + 8] = R.o[i][2] * i0;
+        }
+        if (w1) {
+            ob[h1 * kD + ch] = R.o[i][1] * i1;
+            ob[h1 * kD + ch + 8] = R.o[i][3] * i1;
+        }
+    }
+    if (prm.used && t == 0) prm.used[u] = used;
 }
 
 }  // namespace
 
 cudaError_t launch_art(const DecodeArgs &a, float tau, float phi, int patience, int32_t *used,
                        cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(art_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kArtSmem);
-    if (e != cudaSuccess) return e;
-    art_kernel<<<a.B * a.Hkv, kArtThreads, kArtSmem, stream>>>(a, tau, phi, patience, used);
+    static bool attr_done = false;
+    if (!attr_done) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(art_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kArtSmem);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    ArtParams prm;
+    memset(&prm, 0, sizeof prm);
+    prm.a = a;
+    prm.tau = tau;
+    prm.phi = phi;
+    prm.patience = patience;
+    prm.used = used;
+    if (!make_tile_map(&prm.tm_v, const_cast<__nv_bfloat16 *>(a.v),
+                       (uint64_t)a.P * a.Hkv * kPage))
+        return cudaErrorInvalidValue;
+    art_kernel<<<a.B * a.Hkv, kArtThreads, kArtSmem, stream>>>(prm);
     return cudaGetLastError();
 }
 
