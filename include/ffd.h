@@ -185,7 +185,8 @@ size_t ffd_decode_workspace_size(const ffd_decode_params *params);
  *
  *   q_bf16      device bf16 [B][Hq][128], |q| < 2^27 (else FFD_ERRBIT_RANGE)
  *   thumb, resid, v_bf16   device cache in the layout above (records from ffd_quantize_keys),
- *               16-byte aligned
+ *               16-byte aligned. Rows of a sequence's last page at or past n are never used:
+ *               they may hold any bits (their V rows are zeroed on chip before P.V).
  *   seq_lens    device int32 [B], 0 <= seq_lens[b] <= 64 * max_blocks_per_seq
  *   block_table device int32 [B][max_blocks_per_seq]; only entries b < ceil(n/64) are read
  *   out         device fp32 [B][Hq][128]
