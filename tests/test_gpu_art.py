@@ -188,3 +188,38 @@ def test_bad_block_table_entry_raises_and_contributes_nothing():
         assert used[0, h] == nb
         res, _ = _oracle(inp, qk, 0, h, keep, 0.0, 0.0, 1)
         _close(got[0, h * G:(h + 1) * G], res.out)
+
+
+@pytest.fixture(scope="module")
+def full_size():
+    """The 128K Qwen2.5-7B-shaped workload (batch 4, 28/4 heads), peaked, with the Top-delta mask
+    of the decode step as ART's block list: the launch the benchmark's ART rows time."""
+    w = ffd_synth.WORKLOADS[2]
+    inp = ffd_synth.make_inputs(w, signal_scale=ffd_synth.peaked_scale())
+    dev = H.to_device(inp)
+    qc = H.quantize(dev)
+    mask = H.decode(inp, dev, qc, 5.0)["mask"]
+    yield inp, dev, qc, oracle.quantize(inp.k_bits), mask
+    del dev, qc
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("tau,phi,patience", [(0.0, 0.0, 1), (1e-2, 1e-3, 2)])
+def test_full_size_sampled_units(full_size, tau, phi, patience):
+    inp, dev, qc, qk, mask = full_size
+    w = inp.workload
+    G = w.num_q_heads // w.num_kv_heads
+    out, used = _run(inp, dev, qc, tau, phi, patience, mask)
+    # sampled units: the one that keeps the most blocks, and two fixed ones
+    kept = mask.reshape(w.batch * w.num_kv_heads, -1).sum(axis=1)
+    units = sorted({int(np.argmax(kept)), 0, w.batch * w.num_kv_heads - 1})
+    for u in units:
+        b, h = divmod(u, w.num_kv_heads)
+        res, kr = _oracle(inp, qk, b, h, mask[b, h], tau, phi, patience)
+        if tau == 0.0:
+            nb = (int(inp.seq_lens[b]) + 63) // 64
+            assert used[b, h] == len(ART.art_order(nb, kr)) == res.used
+        elif not _ambiguous(res, tau, phi):
+            assert used[b, h] == res.used, (b, h)
+        at, _ = _oracle(inp, qk, b, h, mask[b, h], tau, phi, patience, stop_after=int(used[b, h]))
+        _close(out[b, h * G:(h + 1) * G], at.out)
