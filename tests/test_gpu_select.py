@@ -92,6 +92,8 @@ CASES = [
                                  [6000, 1, 2500], ffd_synth.peaked_scale())),
     ("llama-32k-peaked", lambda: (ffd_synth.WORKLOADS[1], None, ffd_synth.peaked_scale())),
     ("batched-paged-peaked", lambda: (ffd_synth.WORKLOADS[4], None, ffd_synth.peaked_scale())),
+    # the workload and inputs the benchmark's selector rows time
+    ("qwen-128k-peaked", lambda: (ffd_synth.WORKLOADS[2], None, ffd_synth.peaked_scale())),
 ]
 
 
