@@ -14,9 +14,10 @@
 // Two passes, as the rules require (the whole sequence must be scored before anything is chosen):
 //   block_stats_kernel  streams every thumbnail record once and writes, per block, its importance
 //                       and, per head, the block's (max s^, sum of e^(s^ - max)) pair;
-//   select_kernel       one CTA per (sequence, KV head), and for Top-p per query head too: a
-//                       bitonic sort of the blocks in shared memory (for Top-p after the global
-//                       softmax normalisation, followed by a prefix sum), then the kept bytes.
+//   select_kernel       one CTA per (sequence, KV head), and for Top-p per query head too: for
+//                       Top-k a radix select of the k-th (importance, index) key in shared
+//                       memory; for Top-p the global softmax normalisation, a bitonic sort of the
+//                       blocks by mass and a prefix sum; then the kept bytes.
 // The chosen mask then goes to the decode kernel as a given mask (ffd_decode_attention_masked).
 #include "common.cuh"
 #include "ptx.cuh"
@@ -249,11 +250,72 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DecodeArgs a, int s
             const bool eligible = c < nb && !fb.forced(c) && v != -INFINITY;
             key[c] = eligible ? ((uint64_t)(~ordered(v)) << 32) | (uint32_t)c : ~0ull;
         }
-        __syncthreads();
-        bitonic_sort(key, N);
+        // the k smallest keys (unique: the block index is in the low bits) by a radix select of
+        // the k-th smallest, 8 bits a pass from the top, instead of a full sort
         const int k = (int)budget;
-        for (int t = threadIdx.x; t < k && t < N; t += blockDim.x)
-            if (key[t] != ~0ull) keep[(uint32_t)key[t]] = 1;
+        __shared__ unsigned int hist[256];
+        __shared__ uint64_t s_prefix;
+        __shared__ int s_elig, s_kk;
+        if (threadIdx.x == 0) {
+            s_prefix = 0;
+            s_elig = 0;
+            s_kk = k;
+        }
+        __syncthreads();
+        int mine = 0;
+        for (int c = threadIdx.x; c < N; c += blockDim.x) mine += key[c] != ~0ull;
+        mine = __reduce_add_sync(0xffffffffu, mine);
+        if ((threadIdx.x & 31) == 0 && mine) atomicAdd(&s_elig, mine);
+        __syncthreads();
+        const int elig = s_elig;
+        if (k <= 0) return;
+        uint64_t kth = ~0ull - 1;  // k >= eligible blocks: every eligible key
+        if (k < elig) {
+            for (int shift = 56; shift >= 0; shift -= 8) {
+                for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+                __syncthreads();
+                const uint64_t hi_mask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+                const uint64_t prefix = s_prefix;
+                for (int c = threadIdx.x; c < N; c += blockDim.x) {
+                    const uint64_t x = key[c];
+                    if ((x & hi_mask) == prefix) atomicAdd(&hist[(x >> shift) & 255u], 1u);
+                }
+                __syncthreads();
+                if (threadIdx.x < 32) {  // the bin holding the kk-th key: 8 bins per lane
+                    const int lane = threadIdx.x;
+                    unsigned int cnt8[8], tot = 0;
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        cnt8[j] = hist[8 * lane + j];
+                        tot += cnt8[j];
+                    }
+                    unsigned int incl = tot;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    const unsigned int kk = (unsigned int)s_kk;
+                    const unsigned int before = incl - tot;
+                    if (before < kk && kk <= incl) {  // exactly one lane
+                        unsigned int acc = before;
+                        int d = 0;
+                        for (; d < 8; d++) {
+                            if (acc + cnt8[d] >= kk) break;
+                            acc += cnt8[d];
+                        }
+                        s_prefix = prefix | ((uint64_t)(8 * lane + d) << shift);
+                        s_kk = (int)(kk - acc);
+                    }
+                }
+                __syncthreads();
+            }
+            kth = s_prefix;
+        }
+        for (int c = threadIdx.x; c < N; c += blockDim.x) {
+            const uint64_t x = key[c];
+            if (x != ~0ull && x <= kth) keep[(uint32_t)x] = 1;
+        }
         return;
     }
     // Top-p, head hh: global softmax normalisation over the blocks, M = max, L = sum e^(m - M) l
