@@ -320,13 +320,9 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(const __grid_constant_
 
 cudaError_t launch_art(const DecodeArgs &a, float tau, float phi, int patience, int32_t *used,
                        cudaStream_t stream) {
-    static bool attr_done = false;
-    if (!attr_done) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(art_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kArtSmem);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static int smem_set[kMaxDevicesTracked];
+    const cudaError_t ea = raise_smem_limit(art_kernel, kArtSmem, smem_set);
+    if (ea != cudaSuccess) return ea;
     ArtParams prm;
     memset(&prm, 0, sizeof prm);
     prm.a = a;

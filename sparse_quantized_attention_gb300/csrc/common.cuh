@@ -88,6 +88,22 @@ __host__ __device__ inline int max_forced_blocks(int S, int L, int max_blocks) {
     return c < max_blocks ? c : max_blocks;
 }
 
+// Host: raise a kernel's dynamic shared-memory limit to `bytes` on the current device. The
+// attribute is per device, so the sizes already set are remembered per device in `done`.
+constexpr int kMaxDevicesTracked = 64;
+template <class Kernel>
+inline cudaError_t raise_smem_limit(Kernel *kernel, int bytes, int (&done)[kMaxDevicesTracked]) {
+    int dev = 0;
+    const cudaError_t q = cudaGetDevice(&dev);
+    if (q != cudaSuccess) return q;
+    const bool tracked = dev >= 0 && dev < kMaxDevicesTracked;
+    if (tracked && done[dev] >= bytes) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && tracked) done[dev] = bytes;
+    return e;
+}
+
 __device__ __forceinline__ void raise_error(int *word, int bit) {
     if (word) atomicOr(word, bit);
 }

@@ -710,13 +710,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 // Host side
 // ------------------------------------------------------------------------------------------
 cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t stream) {
-    static bool attr_done = false;
-    if (!attr_done) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static int smem_set[kMaxDevicesTracked];
+    const cudaError_t ea = raise_smem_limit(main_kernel, kSmemBytes, smem_set);
+    if (ea != cudaSuccess) return ea;
     MainParams prm;
     memset(&prm, 0, sizeof prm);
     prm.a = a;

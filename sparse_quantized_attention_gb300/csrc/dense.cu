@@ -274,13 +274,9 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_kernel(const __grid_consta
 }  // namespace
 
 cudaError_t launch_dense(const DecodeArgs &a, int ctas, cudaStream_t stream) {
-    static bool attr_done = false;
-    if (!attr_done) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static int smem_set[kMaxDevicesTracked];
+    const cudaError_t ea = raise_smem_limit(dense_kernel, kDSmemBytes, smem_set);
+    if (ea != cudaSuccess) return ea;
     DenseParams prm;
     memset(&prm, 0, sizeof prm);
     prm.a = a;

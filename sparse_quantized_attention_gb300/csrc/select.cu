@@ -385,12 +385,10 @@ cudaError_t launch_select(const DecodeArgs &a, int selector, float budget, float
     int N = 1;
     while (N < a.max_blocks) N <<= 1;
     const size_t smem = select_smem_bytes(a.max_blocks);
-    static size_t attr_bytes = 0;
-    if (smem > 48 * 1024 && smem > attr_bytes) {
-        e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+    static int smem_set[kMaxDevicesTracked];
+    if (smem > 48 * 1024) {
+        e = raise_smem_limit(select_kernel, (int)smem, smem_set);
         if (e != cudaSuccess) return e;
-        attr_bytes = smem;
     }
     const dim3 g2(units, selector == FFD_SELECT_TOPP ? a.G : 1);
     select_kernel<<<g2, kSelThreads, smem, stream>>>(a, selector, budget, N, imp, ml);
