@@ -118,3 +118,25 @@ def test_criterion_is_strict_and_monotone(small):
                          scale * tau_eq, scale * phi_eq, 2)
         assert r.used <= prev_used
         prev_used = r.used
+
+
+def test_metrics_in_closed_form():
+    """Identical keys make every softmax weight equal, so the probe after t blocks is the mean of
+    the V rows seen. Block 0 holds V = 2 e1 and block 1 holds V = 3 e2: P(1) = 2 e1,
+    P(2) = e1 + 1.5 e2, hence d_scale = | |P(2)| - 2 | / 2 and d_direction = 1 - 2 / (2 |P(2)|)."""
+    G = 2
+    k = np.zeros((2, 1, 64, 128), np.float32) + 0.25
+    v = np.zeros((2, 1, 64, 128), np.float32)
+    v[0, 0, :, 0] = 2.0
+    v[1, 0, :, 1] = 3.0
+    q = np.random.default_rng(5).standard_normal((G, 128)).astype(np.float32)
+    qk = oracle.quantize(_bits(k))
+    res = ART.art_unit(_bits(q), 128, np.arange(2), qk, _bits(v), 0, np.ones(2, np.uint8), SM,
+                       0.0, 0.0, 1)
+    n2 = math.sqrt(1.0 + 1.5 ** 2)
+    assert res.used == 2 and len(res.d_scale) == 1
+    assert res.d_scale[0] == pytest.approx(abs(n2 - 2.0) / 2.0, rel=1e-12)
+    assert res.d_dir[0] == pytest.approx(1.0 - 1.0 / n2, rel=1e-12)
+    want = np.zeros(128)
+    want[0], want[1] = 1.0, 1.5
+    np.testing.assert_allclose(res.out, np.stack([want, want]), rtol=0, atol=1e-12)
