@@ -9,6 +9,8 @@
   exactly where the oracle does. Every unit's output is compared with the oracle stopped after the
   same number of blocks.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -223,3 +225,40 @@ def test_full_size_sampled_units(full_size, tau, phi, patience):
             assert used[b, h] == res.used, (b, h)
         at, _ = _oracle(inp, qk, b, h, mask[b, h], tau, phi, patience, stop_after=int(used[b, h]))
         _close(out[b, h * G:(h + 1) * G], at.out)
+
+
+def test_closed_form_metrics_decide_the_stop():
+    """Identical keys give equal weights, so the probe is the mean of the V rows seen. Order:
+    block 0 (V = 2 e1), block 2 (V = 3 e2), block 1 (V = 3 e2). After the second block P = e1 +
+    1.5 e2 with d_scale = | |P| - 2 | / 2 and d_direction = 1 - 1 / |P|; thresholds just above
+    both stop there (patience 1), just below them the unit runs to its end."""
+    def bf(x):
+        return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).cuda()
+    k = np.zeros((3, 1, 64, 128), np.float32) + 0.25
+    v = np.zeros((3, 1, 64, 128), np.float32)
+    v[0, 0, :, 0] = 2.0
+    v[1:, 0, :, 1] = 3.0
+    q = np.random.default_rng(6).standard_normal((1, 2, 128)).astype(np.float32)
+    kd, vd, qd = bf(k), bf(v), bf(q)
+    qc = ffd.alloc_quantized_cache(3, 1)
+    ffd.ffd_quantize_keys(kd, qc)
+    sl = torch.tensor([192], dtype=torch.int32, device="cuda")
+    bt = torch.tensor([[0, 1, 2]], dtype=torch.int32, device="cuda")
+    p = ffd.make_params(1, 2, 1, 3, 3, sink=16, local=64, delta=5.0, sm_scale=H.SM)
+    n2 = math.sqrt(1.0 + 1.5 ** 2)
+    ds, dd = abs(n2 - 2.0) / 2.0, 1.0 - 1.0 / n2
+    for scale, want_used in ((1.001, 2), (0.999, 3)):
+        ws = ffd.alloc_art_workspace(p)
+        out = torch.zeros((1, 2, 128), device="cuda")
+        used = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+        ffd.ffd_art_attention(p, ds * scale, dd * scale, 1, qd, qc, vd, sl, bt, out, ws,
+                              blocks_used=used)
+        assert ffd.ffd_get_error(ws) == 0
+        assert int(used[0, 0]) == want_used
+        got = out.cpu().numpy()
+        want = np.zeros(128)
+        if want_used == 2:
+            want[0], want[1] = 1.0, 1.5
+        else:
+            want[0], want[1] = 2.0 / 3.0, 2.0
+        np.testing.assert_allclose(got[0], np.stack([want, want]), rtol=0, atol=1e-5)
