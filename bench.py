@@ -796,6 +796,16 @@ def run_sweep(a):
                 us = timed(lambda: ffd.ffd_decode_attention(p, d["q"], qc, d["v"], d["sl"],
                                                             d["bt"], out, ws))
                 nb_total = int(sum((int(n) + 63) // 64 for n in inp.seq_lens)) * Hkv
+                # ART over the same mask with no termination (every kept block, one CTA per
+                # unit walking its blocks in sequence): the unit that keeps the most sets the time
+                aws = ffd.alloc_art_workspace(p, device=dev)
+                used = torch.zeros((w.batch, Hkv), dtype=torch.int32, device=dev)
+                art_us = timed(lambda: ffd.ffd_art_attention(
+                    p, 0.0, 0.0, 1, d["q"], qc, d["v"], d["sl"], d["bt"], out, aws,
+                    keep_in=mask, blocks_used=used))
+                art_max = int(used.max())
+                if ffd.ffd_get_error(aws) != 0:
+                    raise RuntimeError(f"device error in ART on workload {wid}")
                 gbs = by["step"] / (us * 1e-6) / 1e9
                 row = {"workload": w.name, "inputs": label, "delta": delta,
                        "batch": w.batch, "heads": f"{w.num_q_heads}/{Hkv}",
@@ -806,20 +816,24 @@ def run_sweep(a):
                        "frac_of_measured": round(gbs / peaks["hbm_gbs"], 3),
                        "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 3),
                        "dense_us": round(dense_us, 2),
-                       "speedup_vs_dense": round(dense_us / us, 2)}
+                       "speedup_vs_dense": round(dense_us / us, 2),
+                       "art_us": round(art_us, 1), "art_max_blocks": art_max,
+                       "art_us_per_block": round(art_us / max(1, art_max), 2)}
                 rows.append(row)
                 print(json.dumps(row), flush=True)
             del d, qc
             torch.cuda.empty_cache()
     with open(a.sweep, "w") as f:
         f.write("| workload | inputs | delta | context | us/step | KV tokens/s | sparsity | "
-                "needed MB | GB/s | of measured copy peak | of 8 TB/s | dense us | speedup |\n")
-        f.write("|---|---|---|---|---|---|---|---|---|---|---|---|---|\n")
+                "needed MB | GB/s | of measured copy peak | of 8 TB/s | dense us | speedup | "
+                "ART us (all kept) | ART blocks (max unit) | ART us/block |\n")
+        f.write("|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|\n")
         for r in rows:
             f.write(f"| {r['workload']} | {r['inputs']} | {r['delta']:g} | {r['context']} | "
                     f"{r['us_per_step']} | {r['kv_tokens_per_s']:.3g} | {r['sparsity']} | "
                     f"{r['needed_mb']} | {r['gbs']} | {r['frac_of_measured']} | "
-                    f"{r['frac_of_8tbs']} | {r['dense_us']} | {r['speedup_vs_dense']} |\n")
+                    f"{r['frac_of_8tbs']} | {r['dense_us']} | {r['speedup_vs_dense']} | "
+                    f"{r['art_us']} | {r['art_max_blocks']} | {r['art_us_per_block']} |\n")
     return rows
 
 
