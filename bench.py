@@ -50,7 +50,8 @@ def log(*a):
 def args_parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=3000,
+                    help="timed steps (the default keeps the timed region near 0.5 s)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2, help="workload id 0..4")
@@ -161,13 +162,86 @@ def barrier(device=None):
 LEAD_CYCLES = 400_000  # device cycles of the pre-timing delay (~0.2 ms at 2 GHz)
 
 
+class NvmlPoller:
+    """Reads the SM clock and the clock-event (throttle) reasons through NVML (the driver's
+    libnvidia-ml, read-only queries) every `period_s` on a thread, between start() and stop().
+    The driver's timed regions can be a few milliseconds long, far shorter than nvidia-smi's
+    sampling period; NVML answers in microseconds. Unavailable NVML leaves `ok` False."""
+    SM_CLOCK = 1
+    BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+            0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_index: int, period_s: float = 2.5e-4, pci_bus_id: str | None = None):
+        import ctypes
+        self.period = period_s
+        self.samples = []
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            # the CUDA device by its PCI address (NVML numbers every GPU of the machine, CUDA
+            # only the visible ones); by index when the address is unknown
+            found = pci_bus_id is not None and nv.nvmlDeviceGetHandleByPciBusId_v2(
+                pci_bus_id.encode(), ctypes.byref(self.h)) == 0
+            if not found and nv.nvmlDeviceGetHandleByIndex_v2(
+                    ctypes.c_uint(gpu_index), ctypes.byref(self.h)) != 0:
+                return
+            self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nv, self.ct = nv, ctypes
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if nv.nvmlDeviceGetMaxClockInfo(
+                self.h, self.SM_CLOCK, ctypes.byref(mx)) == 0 else None
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _sample(self):
+        c, r = self.ct.c_uint(), self.ct.c_ulonglong()
+        if self.nv.nvmlDeviceGetClockInfo(self.h, self.SM_CLOCK, self.ct.byref(c)) != 0:
+            return
+        if self.reasons_fn(self.h, self.ct.byref(r)) != 0:
+            return
+        self.samples.append((float(c.value), int(r.value)))
+
+    def _loop(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+
+    def stop(self):
+        if self.ok:
+            self._stop.set()
+            self.thread.join(timeout=2)
+            self._sample()  # one reading right after the region ends
+
+    def summary(self):
+        if not self.samples:
+            return None
+        reasons = sorted({name for _, r in self.samples for bit, name in self.BITS.items()
+                          if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "window": "timed",
+                "source": f"NVML every {self.period * 1e3:g} ms during the timed steps"}
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, pci_bus_id: str | None = None):
         self.gpu = gpu_index
+        self.pci = pci_bus_id
         self.samples = []
         self.proc = None
         self.t_on = self.t_off = None
@@ -176,7 +250,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "20", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                 "-lms", "20", "-i", self.pci or str(self.gpu)], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -195,11 +269,22 @@ class ClockSampler:
 
     def mark_on(self):
         self.t_on = time.time()
+        self.nvml = NvmlPoller(self.gpu, pci_bus_id=self.pci)
+        self.nvml.start()
 
     def mark_off(self):
+        self.nvml.stop()
         self.t_off = time.time()
 
     def stop(self) -> dict:
+        fast = self.nvml.summary() if getattr(self, "nvml", None) is not None else None
+        smi = self._stop_smi()
+        if fast and fast["samples"] >= 3:
+            fast["nvidia_smi"] = smi
+            return fast
+        return smi
+
+    def _stop_smi(self) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
                     "note": "nvidia-smi unavailable"}
@@ -230,7 +315,8 @@ class ClockSampler:
                           if v.lower().startswith("active")})
         return {"sm_mhz": statistics.median(r[1] for r in window),
                 "sm_max_mhz": max(r[2] for r in window), "reasons": reasons,
-                "samples": len(window), "window": which}
+                "samples": len(window), "window": which,
+                "source": "nvidia-smi every 20 ms"}
 
 
 # ------------------------------------------------------------------------------------------- #
@@ -273,6 +359,15 @@ def profile_traffic():
         return float(fields["dram_bytes_per_launch"].split()[0]), fields.get("workload", "").strip()
     except (KeyError, ValueError):
         return None, None
+
+
+def pci_bus_id(torch, index: int) -> str | None:
+    """PCI address of a CUDA device in NVML's form (domain:bus:device.function)."""
+    try:
+        p = torch.cuda.get_device_properties(index)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except (AttributeError, RuntimeError):
+        return None
 
 
 def run_ours(a, rank, world, local):
@@ -336,7 +431,7 @@ def run_ours(a, rank, world, local):
     by = step_bytes(w, inp.seq_lens, inp.max_blocks, kept)
 
     # timed region: W warm-up steps, then exactly K steps between barriers + syncs
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, pci_bus_id(torch, local))
     clocks.start()
     for _ in range(a.warmup):
         step()
@@ -348,17 +443,21 @@ def run_ours(a, rank, world, local):
     # a short device-side delay (a bounded clock spin, about 0.2 ms) queued ahead of the start
     # event, so that the first timed launch is already enqueued when the device reaches it: the
     # events then measure device time only (the host's launch cost is in the end-to-end figure)
+    # one event between consecutive launches: the per-launch durations (median, p10, p90) and
+    # their sum, the timed region
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps + 1)]
     torch.cuda._sleep(LEAD_CYCLES)
-    t0.record(stream)
+    evs[0].record(stream)
     for i in range(a.steps):
         step()
-    t1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     clocks.mark_off()
     barrier(local)
     torch.cuda.synchronize(dev)
     clock_info = clocks.stop()
-    total_ms = t0.elapsed_time(t1)
+    total_ms = evs[0].elapsed_time(evs[-1])
+    per_launch_us = np.array([evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(a.steps)])
     if ffd.ffd_get_error(ws) != 0:
         raise RuntimeError("device error during the timed steps")
 
@@ -367,6 +466,7 @@ def run_ours(a, rank, world, local):
     ms_per_step = max_ms / a.steps
     value = all_bytes / a.steps / (ms_per_step * 1e-3) / 1e9
 
+    aux_steps = max(3, min(a.steps, 200))  # the secondary rows: enough launches to average
     # e2e through the public API with pinned host buffers: q, seq_lens and the block table
     # packed in one pinned buffer (one host-to-device copy), the output read back (one
     # device-to-host copy), every step, inside the timed region
@@ -397,13 +497,13 @@ def run_ours(a, rank, world, local):
     torch.cuda.synchronize(dev)
     barrier(local)
     t0.record(stream)
-    for _ in range(a.steps):
+    for _ in range(aux_steps):
         e2e_step()
     t1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms, e2e_bytes = reduce_max_sum(t0.elapsed_time(t1), by["step"] * a.steps,
+    e2e_ms, e2e_bytes = reduce_max_sum(t0.elapsed_time(t1), by["step"] * aux_steps,
                                        backend_device=dev if world > 1 else "cpu")
-    e2e_value = e2e_bytes / a.steps / (e2e_ms / a.steps * 1e-3) / 1e9
+    e2e_value = e2e_bytes / aux_steps / (e2e_ms / aux_steps * 1e-3) / 1e9
     if not torch.equal(hout, out.cpu()):
         raise RuntimeError("end-to-end output differs from the device-resident step")
 
@@ -411,7 +511,7 @@ def run_ours(a, rank, world, local):
     wsd = ffd.alloc_workspace(params, dense=True, device=dev)
     outd = torch.empty_like(out)
     dense_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    dsteps = max(3, min(a.steps, 50))
+    dsteps = max(3, min(aux_steps, 50))
     for _ in range(3):
         ffd.ffd_dense_decode(params, d["q"], d["k"], d["v"], d["seq_lens"], d["block_table"],
                              outd, wsd)
@@ -455,11 +555,11 @@ def run_ours(a, rank, world, local):
         graph.replay()
     torch.cuda.synchronize(dev)
     app_ev[0].record(stream)
-    for _ in range(a.steps):
+    for _ in range(aux_steps):
         graph.replay()
     app_ev[1].record(stream)
     torch.cuda.synchronize(dev)
-    graph_us = app_ev[0].elapsed_time(app_ev[1]) / a.steps * 1e3
+    graph_us = app_ev[0].elapsed_time(app_ev[1]) / aux_steps * 1e3
     if ffd.ffd_get_error(ws) != 0:
         raise RuntimeError("device error during the graph-captured steps")
 
@@ -491,10 +591,16 @@ def run_ours(a, rank, world, local):
                      "traffic": traffic, "traffic_note": traffic_note,
                      "algorithmic_bytes_per_launch": by["main_kernel"],
                      "kernel_us": round(main_avg * 1e3, 2),
-                     "kernel_timing": "CUDA events on the launching stream around the K timed "
-                                      "steps, one launch each"},
+                     "kernel_timing": "CUDA events on the launching stream between the K timed "
+                                      "steps, one launch each",
+                     "per_launch_us": {
+                         "median": round(float(np.median(per_launch_us)), 2),
+                         "p10": round(float(np.percentile(per_launch_us, 10)), 2),
+                         "p90": round(float(np.percentile(per_launch_us, 90)), 2)}},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "us_per_step": round(e2e_ms / a.steps * 1e3, 2)},
+                "d2h_bytes_per_step": d2h, "us_per_step": round(e2e_ms / aux_steps * 1e3, 2),
+                "steps": aux_steps,
+                "timing": "CUDA events on the stream around copy in + decode + copy out"},
         "gpu_launches": LAUNCHES_PER_DECODE * a.steps,
         "clocks": clock_info,
         "ffd": {"needed_bytes_per_step": by["step"], "kept_blocks": kept_blocks,
@@ -549,13 +655,14 @@ def peaked_variant(a, w, delta, dev, ffd, torch, upload, dense_ms):
                                  out, ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
+    psteps = max(3, min(a.steps, 500))
     e0.record(stream)
-    for _ in range(a.steps):
+    for _ in range(psteps):
         ffd.ffd_decode_attention(params, d["q"], qc, d["v"], d["seq_lens"], d["block_table"],
                                  out, ws)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1) / a.steps
+    ms = e0.elapsed_time(e1) / psteps
     nb_total = int(sum((int(n) + 63) // 64 for n in inp.seq_lens)) * w.num_kv_heads
 
     def timed(fn, reps=20):
@@ -683,39 +790,43 @@ def run_reference(a):
     qk = oracle.quantize(inp.k_bits)
     cores = oracle.default_threads()
     units = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
-    # each step decodes a bounded sample of the step's units, sized so that the whole run stays
-    # within a few minutes
+    full_lens = inp.seq_lens.astype(np.int64)
+
+    def run(sample, lens, threads):
+        return oracle.decode(inp.q_bits, lens, inp.block_table, qk, inp.v_bits, sink=w.sink,
+                             local=w.local, delta=delta, sm_scale=sm, units=sample,
+                             threads=threads)
+
+    # Each step decodes a bounded sample of the step's (sequence, KV head) units: up to one unit
+    # per host core, over the first n' tokens of each sequence (n' = the full length unless the
+    # whole --steps K --warmup W run would exceed about 150 s). Calibrate on one unit.
     per_step_units = max(1, min(len(units), cores))
     steps_total = a.warmup + a.steps
     budget_s = 150.0
-    probe = oracle.decode(inp.q_bits, inp.seq_lens, inp.block_table, qk, inp.v_bits,
-                          sink=w.sink, local=w.local, delta=delta, sm_scale=sm,
-                          units=units[:1], threads=1)
+    n_probe = int(min(full_lens.max(), 16384))
     t = time.time()
-    oracle.decode(inp.q_bits, inp.seq_lens, inp.block_table, qk, inp.v_bits, sink=w.sink,
-                  local=w.local, delta=delta, sm_scale=sm, units=units[:per_step_units],
-                  threads=cores)
-    one = time.time() - t
-    while per_step_units > 1 and one * steps_total > budget_s:
-        per_step_units = max(1, per_step_units // 2)
-        one /= 2
-    full = oracle.decode(inp.q_bits, inp.seq_lens, inp.block_table, qk, inp.v_bits, sink=w.sink,
-                         local=w.local, delta=delta, sm_scale=sm, threads=cores)
-    del probe
+    run(units[:1], np.minimum(full_lens, n_probe).astype(np.int32), 1)
+    per_token = max(1e-9, (time.time() - t) / max(1, n_probe))
+    waves = math.ceil(per_step_units / cores)
+    n_cap = int(budget_s / steps_total / waves / per_token)
+    n_cap = max(1024, min(int(full_lens.max()), n_cap))
+    lens = np.minimum(full_lens, n_cap).astype(np.int32)
     times, nbytes_list = [], []
     for s in range(steps_total):
         sample = [units[(s * per_step_units + k) % len(units)] for k in range(per_step_units)]
         t = time.time()
-        oracle.decode(inp.q_bits, inp.seq_lens, inp.block_table, qk, inp.v_bits, sink=w.sink,
-                      local=w.local, delta=delta, sm_scale=sm, units=sample, threads=cores)
+        res = run(sample, lens, cores)
         dt = time.time() - t
         if s >= a.warmup:
             times.append(dt)
-            nbytes_list.append(unit_bytes(w, inp.seq_lens, full.mask, sample))
+            nbytes_list.append(unit_bytes(w, lens, res.mask, sample))
     total_t = sum(times)
     value = sum(nbytes_list) / total_t / 1e9
+    prefix = ("whole sequences" if n_cap >= full_lens.max() else
+              f"the first {n_cap} tokens of each sequence")
     sample_desc = (f"{per_step_units} of {len(units)} (sequence, KV head) units per step, "
-                   f"rotating; fp64 oracle on {min(cores, per_step_units)} host threads")
+                   f"rotating, {prefix}; fp64 oracle on {min(cores, per_step_units)} host "
+                   f"threads")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": round(total_t / a.steps * 1e3, 3),
@@ -733,8 +844,8 @@ def run_reference(a):
 
 def run_sweep(a):
     """Every workload, literal and peaked inputs, each of its deltas: the decode step timed one
-    launch at a time with L2 flushed in between (the 32K workload's cache fits in L2), next to the
-    dense kernel on the same inputs."""
+    launch at a time with L2 emptied in between by a read of twice its size (the 32K workload's
+    cache fits in L2), next to the dense kernel on the same inputs."""
     import torch
 
     import ffd_synth
@@ -744,7 +855,10 @@ def run_sweep(a):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     peaks, _ = measured_peaks()
-    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    # L2 is emptied between launches by READING a buffer twice its size: a written buffer would
+    # leave up to an L2's worth of dirty lines whose write-back then lands inside the next timed
+    # launch
+    flush = torch.zeros(2 * L2_BYTES // 8, dtype=torch.int64, device=dev)
     sm = float(np.float32(1.0 / math.sqrt(128.0)))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -753,7 +867,7 @@ def run_sweep(a):
             fn()
         ts = []
         for _ in range(reps):
-            flush.zero_()
+            flush.sum()
             e0.record(stream)
             fn()
             e1.record(stream)
@@ -837,11 +951,36 @@ def run_sweep(a):
     return rows
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_command(nprocs: int, argv, script: str | None = None) -> list:
+    """torchrun command that starts `nprocs` ranks of `script` (this file by default) on this
+    node, rendezvous on 127.0.0.1."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            f"--nproc-per-node={nprocs}", "--master-addr", "127.0.0.1",
+            f"--master-port={free_port()}", script or os.path.abspath(__file__), *argv]
+
+
+def self_launch(nprocs: int, argv, script: str | None = None) -> int:
+    """Run the job as `nprocs` ranks (one per GPU) when started without a launcher: the ranks'
+    output (rank 0 prints the JSON line) goes to this process's stdout and stderr."""
+    log(f"starting {nprocs} ranks with torch.distributed.run")
+    return subprocess.run(launch_command(nprocs, argv, script)).returncode
+
+
 def main(argv=None):
-    a = args_parse(argv)
+    raw = list(sys.argv[1:] if argv is None else argv)
+    a = args_parse(raw)
     if a.sweep:
         run_sweep(a)
         return 0
+    if a.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return self_launch(a.gpus, raw)
     rank, world, local = dist_env()
     if a.impl == "reference":
         if rank != 0:

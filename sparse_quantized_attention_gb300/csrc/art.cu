@@ -83,8 +83,7 @@ __device__ __forceinline__ void head_metrics(float nc, float np, float dd, float
 __global__ void __launch_bounds__(kArtThreads) art_kernel(const __grid_constant__ ArtParams prm) {
     const DecodeArgs &a = prm.a;
     extern __shared__ uint8_t art_raw[];
-    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(art_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *base = align_shared<1024>(art_raw);
     __shared__ ArtCtl ctl;
     const int u = blockIdx.x;
     const int b = u / a.Hkv, h = u - b * a.Hkv;

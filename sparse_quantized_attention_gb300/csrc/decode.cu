@@ -645,8 +645,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     main_kernel(const __grid_constant__ MainParams prm) {
     const DecodeArgs &a = prm.a;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *base = align_shared<1024>(smem_raw);
     Smem S;
     S.ring = base + kOffRing;
     S.thumb = base + kOffThumb;

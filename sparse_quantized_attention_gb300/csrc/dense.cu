@@ -227,8 +227,7 @@ __device__ __forceinline__ void dense_refiner(const DecodeArgs &a, DenseMisc *m,
 __global__ void __launch_bounds__(kDThreads, 1) dense_kernel(const __grid_constant__ DenseParams prm) {
     const DecodeArgs &a = prm.a;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *base = align_shared<1024>(smem_raw);
     uint8_t *ring = base;
     uint8_t *px = base + kDOffPx;
     DenseMisc *m = reinterpret_cast<DenseMisc *>(base + kDOffMisc);

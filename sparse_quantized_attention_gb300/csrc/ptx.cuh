@@ -11,6 +11,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// First `kAlign`-byte boundary at or after p, a pointer into shared memory, by pointer arithmetic:
+// an integer round trip (uintptr_t) would hide from the compiler that the result points into
+// shared memory, and every access through it would become a generic load or store.
+template <uint32_t kAlign>
+__device__ __forceinline__ uint8_t *align_shared(uint8_t *p) {
+    return p + ((kAlign - (smem_u32(p) & (kAlign - 1))) & (kAlign - 1));
+}
+
 // ---- mbarrier --------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));

@@ -53,3 +53,28 @@ def test_single_process_reduce_is_identity():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.reduce_max_sum(3.5, 42.0) == (3.5, 42.0)
+
+
+def test_self_launch_starts_n_ranks(capfd):
+    """`bench.py --gpus N` without WORLD_SIZE re-executes itself under torch.distributed.run with
+    N ranks; the same launcher started on a CPU stand-in rank joins N gloo ranks."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    env_world = os.environ.pop("WORLD_SIZE", None)
+    try:
+        cmd = bench.launch_command(2, ["--gpus", "2", "--steps", "3"],
+                                   script=os.path.join(ROOT, "tests", "rank_probe.py"))
+        assert cmd[1:3] == ["-m", "torch.distributed.run"]
+        assert "--nproc-per-node=2" in cmd and "127.0.0.1" in cmd
+        rc = bench.self_launch(2, ["--gpus", "2", "--steps", "3"],
+                               script=os.path.join(ROOT, "tests", "rank_probe.py"))
+    finally:
+        if env_world is not None:
+            os.environ["WORLD_SIZE"] = env_world
+    assert rc == 0
+    lines = [ln for ln in capfd.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    got = json.loads(lines[0])
+    assert got["n_gpus"] == 2 and got["max_ms"] == 15.0 and got["bytes"] == 3000.0
+    assert got["args"] == ["--gpus", "2", "--steps", "3"]

@@ -54,7 +54,7 @@ def test_decode_parity_full_size(cid, delta, peaked):
           f"max-abs {st['max_abs']:.2e}, rel-L2 {st['rel_l2']:.2e}")
 
 
-@pytest.mark.parametrize("cid", [0, 1, 3, 4])
+@pytest.mark.parametrize("cid", [0, 1, 2, 3, 4])
 def test_dense_parity(cid):
     inp, dev, qc, ref = _workload(cid)
     w = inp.workload
@@ -106,6 +106,24 @@ def test_decode_edge_cases(shape, delta, peaked):
     for splits in (0, 1, 3):
         gpu = H.decode(inp, dev, qc, delta, num_splits=splits)
         H.check_decode(inp, ref, gpu, delta, what=f"{w.name} splits={splits}")
+
+
+@pytest.mark.parametrize("shape", EDGE, ids=[f"edge{i}" for i in range(len(EDGE))])
+def test_dense_edge_cases(shape):
+    """The dense comparison kernel at every GQA group size 1 ... 8 (odd ones included), ragged and
+    empty sequences, random block tables, and split counts 0 (one per SM), 1 and 3."""
+    shape = dict(shape)
+    lens = shape.pop("seq_lens")
+    w = ffd_synth.custom(shape.pop("batch"), shape.pop("hq"), shape.pop("hkv"), max(lens),
+                         random_pages=True, needles=3, seed=len(lens) * 211 + max(lens),
+                         **shape)
+    inp = ffd_synth.make_inputs(w, seq_lens=list(lens))
+    dev = H.to_device(inp)
+    want = oracle.dense(inp.q_bits, inp.seq_lens, inp.block_table, inp.k_bits, inp.v_bits,
+                        sm_scale=H.SM)
+    for splits in (0, 1, 3):
+        got = H.dense(inp, dev, num_splits=splits)
+        H.compare_outputs(got, want, f"dense {w.name} splits={splits}")
 
 
 def test_split_count_invariance_and_determinism():
