@@ -456,8 +456,8 @@ __device__ __forceinline__ void fill_unit(const DecodeArgs &a, Misc *m, UnitOps 
 // Scan warp mt, every sub-chunk: provisional scores of rows 16mt .. 16mt+15 of each block into
 // the score buffer, and a vote for every block where one of those rows passes m~ - delta (an OR
 // into the sub-chunk's vote word, then one arrival on its decision barrier). Blocks k and k+3 are
-// scanned side by side (two independent dependency chains); a second tile past the sub-chunk's
-// end is computed from stale buffer contents (reads stay inside the buffer) and ignored.
+// scanned side by side (two independent dependency chains); tiles past the sub-chunk's end are
+// computed from stale buffer contents (reads stay inside the buffer) and ignored.
 __device__ __forceinline__ void scanner(const DecodeArgs &a, const Smem &S, int cta, int ncta,
                                         int mt, int lane) {
     Misc *m = S.misc;
@@ -495,18 +495,32 @@ __device__ __forceinline__ void scanner(const DecodeArgs &a, const Smem &S, int 
         const uint8_t *tbuf = S.thumb + tb * kThumbBuf;
         float4 *shat = reinterpret_cast<float4 *>(S.shat + sb * kShatBuf);
         uint32_t votes = 0;
+        // Every tile pair is computed and used unconditionally (a partial sub-chunk scores stale
+        // buffer contents past its end, masked out below): a pair whose second tile is consumed
+        // only under a condition gets that tile's computation moved under the condition, and the
+        // two tiles then no longer overlap.
 #pragma unroll 1
-        for (int kA = 0; kA < kSub / 2 && kA < s.cnt; kA++) {
+        for (int kA = 0; kA < kSub / 2; kA++) {
             const int kB = kA + kSub / 2;
             const float4 eA = scan_tile(tbuf + kA * kThumbBlock, r0, r1, m0, Q, sm);
             const float4 eB = scan_tile(tbuf + kB * kThumbBlock, r0, r1, m0, Q, sm);
-            const int tA = (s.j0 + kA) * kPage, tB = (s.j0 + kB) * kPage;
-            const bool pA = tile_passes(eA, tA + r0 < n, tA + r1 < n, thr0, thr1);
-            const bool pB = kB < s.cnt && tile_passes(eB, tB + r0 < n, tB + r1 < n, thr0, thr1);
+            const bool pA = tile_passes(eA, true, true, thr0, thr1);
+            const bool pB = tile_passes(eB, true, true, thr0, thr1);
             if (__any_sync(0xffffffffu, pA)) votes |= 1u << kA;
             if (__any_sync(0xffffffffu, pB)) votes |= 1u << kB;
             shat[(kA * 4 + mt) * 32 + lane] = eA;
-            if (kB < s.cnt) shat[(kB * 4 + mt) * 32 + lane] = eB;
+            shat[(kB * 4 + mt) * 32 + lane] = eB;
+        }
+        votes &= (1u << s.cnt) - 1u;
+        // a sequence's partial last block: rows past the sequence hold arbitrary bits and must not
+        // vote, so its vote is taken again over the rows inside the sequence (warp-uniform, once
+        // per sequence and KV head)
+        const int tail_rows = n & (kPage - 1);
+        if (s.j0 + s.cnt == s.nblk && tail_rows) {
+            const int k = s.cnt - 1;
+            const float4 e = shat[(k * 4 + mt) * 32 + lane];
+            const bool p = tile_passes(e, r0 < tail_rows, r1 < tail_rows, thr0, thr1);
+            votes = (votes & ~(1u << k)) | (__any_sync(0xffffffffu, p) ? 1u << k : 0u);
         }
         __syncwarp();
         if (lane == 0) {
