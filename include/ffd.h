@@ -58,7 +58,8 @@ typedef enum {
     FFD_ERR_BOUNDS = 5,      /* device: a block_table / page_ids entry outside [0, num_pages) */
     FFD_ERR_RANGE = 6,       /* device: a key outside the fp16 range (|k| >= 65504 or NaN), or a
                                 query with |q| >= 2^27 */
-    FFD_ERR_TIMEOUT = 7,     /* device: a pipeline wait exceeded its 2 s bound (results invalid) */
+    FFD_ERR_TIMEOUT = 7,     /* device: a pipeline wait exceeded its bound (params wait_limit_us,
+                                2 s by default); the call's results are invalid */
 } ffd_status;
 
 #define FFD_THUMB_RECORD_BYTES 3072
@@ -94,12 +95,18 @@ typedef struct {
                                    partitions, i.e. the CTAs of the persistent kernel of
                                    ffd_decode_attention or ffd_dense_decode, at most one per SM:
                                    larger values are clamped to the SM count */
+    int32_t wait_limit_us;      /* >= 0. Bound, in microseconds, of every wait inside a kernel of
+                                   this call (a CTA waiting for a copy, for another warp or for
+                                   another CTA); 0 takes the default of 2 s. A wait that runs out
+                                   sets FFD_ERRBIT_TIMEOUT, the CTA stops waiting and drains its
+                                   own copies, and the kernel ends (results invalid). */
 } ffd_decode_params;
 
 /* Human-readable name of a status. Never NULL. */
 const char *ffd_status_string(ffd_status status);
 
-/* Library version, major * 10000 + minor * 100 + patch. */
+/* Library version, major * 10000 + minor * 100 + patch (3.00: ffd_decode_params gained
+ * wait_limit_us). */
 int32_t ffd_version(void);
 
 /*

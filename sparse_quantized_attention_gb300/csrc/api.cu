@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace ffd {
 cudaError_t launch_quantize(int P, int Hkv, const int32_t *page_ids, int num_pages_listed,
@@ -34,6 +35,11 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Bound of every device wait of a call: the caller's, or the default.
+uint64_t wait_bound_ns(const ffd_decode_params *p) {
+    return p->wait_limit_us > 0 ? (uint64_t)p->wait_limit_us * 1000ull : kWaitTimeoutNs;
+}
+
 int current_sm_count() {
     static int cache[128];
     int dev = 0;
@@ -49,7 +55,7 @@ ffd_status check_params(const ffd_decode_params *p) {
     if (!p) return FFD_ERR_INVALID_ARG;
     if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->num_pages < 1 ||
         p->max_blocks_per_seq < 1 || p->sink_tokens < 0 || p->local_tokens < 0 ||
-        p->num_splits < 0)
+        p->num_splits < 0 || p->wait_limit_us < 0)
         return FFD_ERR_INVALID_ARG;
     if (p->num_q_heads % p->num_kv_heads != 0) return FFD_ERR_INVALID_ARG;
     if (isnan(p->delta) || p->delta == -INFINITY) return FFD_ERR_INVALID_ARG;
@@ -145,6 +151,7 @@ DecodeArgs make_args(const ffd_decode_params *p, const Plan &pl, void *ws) {
     a.nf = pl.nf;
     a.delta = p->delta;
     a.sm_scale = p->sm_scale;
+    a.wait_ns = wait_bound_ns(p);
     char *base = static_cast<char *>(ws);
     a.err = reinterpret_cast<int *>(base);
     a.ws_m1 = reinterpret_cast<float *>(base + pl.m1_off);
@@ -171,7 +178,7 @@ const char *ffd_status_string(ffd_status s) {
     return "FFD_ERR_UNKNOWN";
 }
 
-int32_t ffd_version(void) { return 203; }
+int32_t ffd_version(void) { return 300; }
 
 ffd_status ffd_quantize_keys(const ffd_cache_desc *cache, const void *k_bf16, uint8_t *thumb,
                              uint8_t *resid, const int32_t *page_ids, int32_t num_page_ids,
@@ -326,6 +333,7 @@ ffd_status ffd_select_blocks(const ffd_decode_params *params, int32_t selector, 
     a.S = params->sink_tokens;
     a.L = params->local_tokens;
     a.sm_scale = params->sm_scale;
+    a.wait_ns = wait_bound_ns(params);
     a.q = static_cast<const __nv_bfloat16 *>(q_bf16);
     a.thumb = thumb;
     a.seq_lens = seq_lens;
@@ -398,6 +406,7 @@ ffd_status ffd_art_attention(const ffd_decode_params *params, float tau, float p
     a.P = params->num_pages;
     a.max_blocks = params->max_blocks_per_seq;
     a.sm_scale = params->sm_scale;
+    a.wait_ns = wait_bound_ns(params);
     a.q = static_cast<const __nv_bfloat16 *>(q_bf16);
     a.thumb = thumb;
     a.resid = resid;

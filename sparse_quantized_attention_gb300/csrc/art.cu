@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(const __grid_constant_
         const uint64_t t0 = globaltimer_ns();
         bool ok = true;
         while (!mbar_try_wait(&ctl.full[st], (phases >> st) & 1u)) {
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            if (globaltimer_ns() - t0 > a.wait_ns) {
                 ok = false;
                 break;
             }

@@ -53,6 +53,7 @@ struct DecodeArgs {
     int *ws_cnt;     // [4][B*Hkv]: merge tickets, stage-1 slots, merge reports, merger
                      // declarations; zero between calls
     cudaEvent_t prof_start, prof_stop;  // optional: recorded around the main kernel
+    uint64_t wait_ns;  // bound of every device wait (mbarrier, counter) before FFD_ERRBIT_TIMEOUT
 };
 
 // Sink / local block bookkeeping of one sequence (Methodology §2: the pseudo-max uses the sink

@@ -364,6 +364,7 @@ __device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S
         if (cnt == 0 || aborted(m)) break;
         const int ds = t % kDepth;
         wait_bar(a, m, &m->decision[ds], (t / kDepth) & 1);
+        if (aborted(m)) break;  // a wait ran out: nothing more is issued
         const uint32_t mask = (*reinterpret_cast<volatile uint32_t *>(&m->vote[ds]) | P.forced) &
                               ~P.bad & ((1u << cnt) - 1u);
         __syncwarp();
@@ -380,6 +381,10 @@ __device__ __forceinline__ void ring_issuer(const MainParams &prm, const Smem &S
             const int slot = kb % kRing, round = kb / kRing;
             kb++;
             if (round > 0) wait_bar(a, m, &m->ring_empty[slot], (round - 1) & 1);
+            if (aborted(m)) {  // the slot may still be filling: arm nothing more
+                kb--;
+                break;
+            }
             const int row = P.row[k];
             uint8_t *d = S.ring + slot * kSlotBytes;
             uint64_t *bar = &m->ring_full[(kb - 1) % kRefineGroups][slot];  // kb advanced above
@@ -624,6 +629,9 @@ __device__ __forceinline__ void refiner(const DecodeArgs &a, const Smem &S, int 
         }
         const int ds = t % kDepth;
         wait_bar(a, m, &m->ring_seen[ds], (t / kDepth) & 1);
+        // the kept blocks decide the group's barriers, so the group leaves together when a wait
+        // has run out in this CTA (the mask may then never have been published)
+        if (named_barrier_or(2 + grp, 128, aborted(m))) break;
         const uint32_t mask = *reinterpret_cast<volatile uint32_t *>(&m->final_mask[ds]);
         if (grp == 0 && mt == 0 && a.keep_mask && lane < s.cnt)
             a.keep_mask[((size_t)s.b * a.Hkv + s.h) * a.max_blocks + s.j0 + lane] =

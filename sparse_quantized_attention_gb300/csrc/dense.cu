@@ -111,6 +111,7 @@ __device__ __forceinline__ void dense_ring(const DenseParams &prm, DenseMisc *m,
         for (int k = 0; k < cnt; k++, kb++) {
             const int slot = kb % kDRing, round = kb / kDRing;
             if (round > 0) wait_bar(a, m, &m->empty[slot], (round - 1) & 1);
+            if (aborted(m)) break;  // a wait ran out: the slot may still be filling, arm nothing
             uint64_t *bar = &m->full[kb % kRefineGroups][slot];
             const bool bad = (P.bad >> k) & 1u;
             uint8_t *d = ring + slot * kDSlotBytes;
@@ -191,6 +192,9 @@ __device__ __forceinline__ void dense_refiner(const DecodeArgs &a, DenseMisc *m,
             if (kb % kRefineGroups != grp) continue;
             const int slot = kb % kDRing;
             wait_bar(a, m, &m->full[grp][slot], (kb / kDFillPeriod) & 1);
+            // the slot's state decides the group's barriers, so the group leaves together when a
+            // wait has run out in this CTA
+            if (named_barrier_or(2 + grp, 128, aborted(m))) return;
             const uint8_t *d = ring + slot * kDSlotBytes;
             if (!*reinterpret_cast<volatile uint32_t *>(&m->slot_bad[slot])) {  // group-uniform
                 const uint32_t kbase = smem_u32(d + kDSlotK);

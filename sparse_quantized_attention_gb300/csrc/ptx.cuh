@@ -71,7 +71,8 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// Upper bound of any single mbarrier wait before a kernel declares a timeout.
+// Default bound of any single device wait before a kernel declares a timeout (the caller may set
+// another one per call).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
 // ---- TMA ------------------------------------------------------------------------------------
@@ -163,6 +164,19 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads
 
 // Per-warpgroup register reallocation (every thread of the warpgroup executes it). The shares
 // of all warpgroups must fit in the registers the CTA was launched with.
+// Named barrier that also returns whether pred held in any of the `threads` threads: the group
+// takes one decision from it.
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
 template <int kRegs>
 __device__ __forceinline__ void regs_increase() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));

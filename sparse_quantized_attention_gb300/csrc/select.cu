@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(128) block_stats_kernel(DecodeArgs a, float *i
     auto wait_stage = [&](int st) -> bool {
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(&full[warp][st], (phases >> st) & 1u)) {
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            if (globaltimer_ns() - t0 > a.wait_ns) {
                 phases ^= 1u << st;
                 if (lane == 0) raise_error(a.err, FFD_ERRBIT_TIMEOUT);
                 return false;

@@ -115,7 +115,7 @@ __device__ __forceinline__ int cta_of(int64_t x, int64_t T, int ncta) {
 // ------------------------------------------------------------------------------------------
 // Bounded waits.
 // ------------------------------------------------------------------------------------------
-// Bounded wait: after kWaitTimeoutNs the CTA records FFD_ERRBIT_TIMEOUT, marks itself aborted and
+// Bounded wait: after a.wait_ns the CTA records FFD_ERRBIT_TIMEOUT, marks itself aborted and
 // stops waiting (its results are then garbage, but every loop still ends).
 template <class M>
 __device__ __forceinline__ void wait_bar(const DecodeArgs &a, M *m, uint64_t *bar, uint32_t parity) {
@@ -123,7 +123,7 @@ __device__ __forceinline__ void wait_bar(const DecodeArgs &a, M *m, uint64_t *ba
     if (mbar_try_wait(bar, parity)) return;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        if (globaltimer_ns() - t0 > a.wait_ns) {
             raise_error(a.err, FFD_ERRBIT_TIMEOUT);
             *reinterpret_cast<volatile uint32_t *>(&m->aborted) = 1;
             return;
@@ -136,7 +136,7 @@ __device__ __forceinline__ void wait_bar(const DecodeArgs &a, M *m, uint64_t *ba
 __device__ __forceinline__ void drain_bar(const DecodeArgs &a, uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        if (globaltimer_ns() - t0 > a.wait_ns) {
             raise_error(a.err, FFD_ERRBIT_TIMEOUT);
             return;
         }
@@ -156,7 +156,7 @@ __device__ __forceinline__ void wait_count(const DecodeArgs &a, M *m, const int 
     const uint64_t t0 = globaltimer_ns();
     while (ld_acquire_gpu(c) < target) {
         if (aborted(m)) return;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        if (globaltimer_ns() - t0 > a.wait_ns) {
             raise_error(a.err, FFD_ERRBIT_TIMEOUT);
             *reinterpret_cast<volatile uint32_t *>(&m->aborted) = 1;
             return;
@@ -407,7 +407,7 @@ __device__ __forceinline__ unsigned int wait_bits(const DecodeArgs &a, M *m, con
     const uint64_t t0 = globaltimer_ns();
     while ((v & mask) != mask) {
         if (aborted(m)) break;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        if (globaltimer_ns() - t0 > a.wait_ns) {
             raise_error(a.err, FFD_ERRBIT_TIMEOUT);
             *reinterpret_cast<volatile uint32_t *>(&m->aborted) = 1;
             break;

@@ -44,15 +44,18 @@ class DecodeParams(ctypes.Structure):
                 ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
                 ("max_blocks_per_seq", ctypes.c_int32), ("sink_tokens", ctypes.c_int32),
                 ("local_tokens", ctypes.c_int32), ("delta", ctypes.c_float),
-                ("sm_scale", ctypes.c_float), ("num_splits", ctypes.c_int32)]
+                ("sm_scale", ctypes.c_float), ("num_splits", ctypes.c_int32),
+                ("wait_limit_us", ctypes.c_int32)]
 
 
 def make_params(batch, num_q_heads, num_kv_heads, num_pages, max_blocks_per_seq, *, sink=64,
-                local=1024, delta=5.0, sm_scale=None, num_splits=0) -> DecodeParams:
+                local=1024, delta=5.0, sm_scale=None, num_splits=0,
+                wait_limit_us=0) -> DecodeParams:
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(HEAD_DIM)
     return DecodeParams(batch, num_q_heads, num_kv_heads, HEAD_DIM, PAGE, num_pages,
-                        max_blocks_per_seq, sink, local, delta, sm_scale, num_splits)
+                        max_blocks_per_seq, sink, local, delta, sm_scale, num_splits,
+                        wait_limit_us)
 
 
 def library_path() -> str:
