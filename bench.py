@@ -43,6 +43,9 @@ LAUNCHES_PER_DECODE = 1  # one cooperative kernel: stage 1, stages 2/3, split me
 PROFILE = os.path.join(ROOT, "profiles", "ffd_main_kernel_qwen2.5-7b_128k.txt")
 
 
+SCHEDULES = {"fused": 0, "scan-refine": 1}  # FFD_SCHEDULE_FUSED, FFD_SCHEDULE_SCAN_REFINE
+
+
 def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
@@ -58,6 +61,8 @@ def args_parse(argv=None):
     ap.add_argument("--delta", type=float, default=None)
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the peaked-attention variant and the CPU baseline")
+    ap.add_argument("--schedule", choices=["fused", "scan-refine"], default="fused",
+                    help="order of the decode step's work (FFD_SCHEDULE_*; same results)")
     ap.add_argument("--peaked", action="store_true",
                     help="measure the peaked-attention inputs (sink shift and needles in score "
                          "units) as the primary workload")
@@ -412,7 +417,8 @@ def run_ours(a, rank, world, local):
     quant_bytes = P * Hkv * 64 * (256 + 32 + 8 + 8 + 128 + 8)
 
     params = ffd.make_params(w.batch, w.num_q_heads, w.num_kv_heads, P, inp.max_blocks,
-                             sink=w.sink, local=w.local, delta=delta, sm_scale=sm)
+                             sink=w.sink, local=w.local, delta=delta, sm_scale=sm,
+                             schedule=SCHEDULES[a.schedule])
     ws = ffd.alloc_workspace(params, device=dev)
     out = torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.float32, device=dev)
     mask = torch.zeros((w.batch, w.num_kv_heads, inp.max_blocks), dtype=torch.uint8, device=dev)

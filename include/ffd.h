@@ -100,13 +100,33 @@ typedef struct {
                                    another CTA); 0 takes the default of 2 s. A wait that runs out
                                    sets FFD_ERRBIT_TIMEOUT, the CTA stops waiting and drains its
                                    own copies, and the kernel ends (results invalid). */
+    int32_t schedule;           /* the order of the work of ffd_decode_attention(_static), with
+                                   the same results: FFD_SCHEDULE_FUSED (0) or
+                                   FFD_SCHEDULE_SCAN_REFINE (1), below; ignored by the masked,
+                                   dense, selector and ART calls */
 } ffd_decode_params;
+
+/* Schedules of the decode step (ffd_decode_params.schedule). Both compute the same step.
+ *   FFD_SCHEDULE_FUSED: one pipeline per CTA over an equal share of all blocks; the scan of a
+ *     block's thumbnail and the refinement of the kept blocks before it overlap. Suits steps that
+ *     keep most blocks (the refinement's bytes dominate).
+ *   FFD_SCHEDULE_SCAN_REFINE: every CTA first scans an equal share of all thumbnails with all its
+ *     compute warps, then, after a grid-wide barrier, the kept blocks of all CTAs are shared out
+ *     equally for the refinement. Suits steps that drop most blocks (the scan dominates, and the
+ *     kept blocks may crowd into a few sequences). A caller can pick it from the kept fraction of
+ *     the previous step (keep_mask). */
+#define FFD_SCHEDULE_FUSED 0
+#define FFD_SCHEDULE_SCAN_REFINE 1
 
 /* Human-readable name of a status. Never NULL. */
 const char *ffd_status_string(ffd_status status);
 
+/* The cudaError_t behind the latest FFD_ERR_CUDA returned on the calling thread (0 if none
+ * yet); kept per thread until the next such failure. */
+int32_t ffd_last_cuda_error(void);
+
 /* Library version, major * 10000 + minor * 100 + patch (3.00: ffd_decode_params gained
- * wait_limit_us). */
+ * wait_limit_us and schedule). */
 int32_t ffd_version(void);
 
 /*

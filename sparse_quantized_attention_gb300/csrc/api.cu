@@ -16,6 +16,7 @@ cudaError_t launch_append(int B, int Hkv, int P, int max_blocks, const int32_t *
                           uint8_t *thumb, uint8_t *resid, void *v_cache, void *k_cache, int *err,
                           cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, int main_ctas, cudaStream_t stream);
+cudaError_t launch_sparse(const DecodeArgs &a, int ctas, cudaStream_t stream);
 cudaError_t launch_dense(const DecodeArgs &a, int ctas, cudaStream_t stream);
 cudaError_t launch_select(const DecodeArgs &a, int selector, float budget, float *imp, float2 *ml,
                           cudaStream_t stream);
@@ -28,6 +29,14 @@ cudaError_t launch_art(const DecodeArgs &a, float tau, float phi, int patience, 
 using namespace ffd;
 
 namespace {
+
+thread_local int g_last_cuda = 0;  // the cudaError_t behind this thread's latest FFD_ERR_CUDA
+
+ffd_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return FFD_OK;
+    g_last_cuda = static_cast<int>(e);
+    return FFD_ERR_CUDA;
+}
 
 constexpr size_t kAlign = 256;
 
@@ -43,10 +52,12 @@ uint64_t wait_bound_ns(const ffd_decode_params *p) {
 int current_sm_count() {
     static int cache[128];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e), -1;
     if (dev >= 0 && dev < 128 && cache[dev] > 0) return cache[dev];
     int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_status(e), -1;
     if (dev >= 0 && dev < 128) cache[dev] = v;
     return v;
 }
@@ -56,6 +67,8 @@ ffd_status check_params(const ffd_decode_params *p) {
     if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->num_pages < 1 ||
         p->max_blocks_per_seq < 1 || p->sink_tokens < 0 || p->local_tokens < 0 ||
         p->num_splits < 0 || p->wait_limit_us < 0)
+        return FFD_ERR_INVALID_ARG;
+    if (p->schedule != FFD_SCHEDULE_FUSED && p->schedule != FFD_SCHEDULE_SCAN_REFINE)
         return FFD_ERR_INVALID_ARG;
     if (p->num_q_heads % p->num_kv_heads != 0) return FFD_ERR_INVALID_ARG;
     if (isnan(p->delta) || p->delta == -INFINITY) return FFD_ERR_INVALID_ARG;
@@ -71,13 +84,20 @@ ffd_status check_params(const ffd_decode_params *p) {
 struct Plan {
     int nf;    // stage-1 slots per unit (FFD step)
     int ctas;  // CTAs of the persistent kernel
-    size_t m1_off, part_off, cnt_off, total;
+    size_t m1_off, mt_off, part_off, kept_off, keptn_off, cnt_off, total;
 };
 
-// Workspace of ffd_decode_attention: [error word | stage-1 maxima | split records | merge
-// tickets, stage-1 slot counters]. Split records: one per (unit, CTA) pair that shares work and
-// refine group, indexed (unit + cta) * groups + group. Stage 1 has one slot per forced block (at
-// least one).
+// Split records per (unit, CTA): one per refine group, and the scan-then-refine kernel has three.
+constexpr int kRecordGroups = 3;
+// Per-unit counters: merge tickets, stage-1 slots, merge reports, merger declarations, and two
+// buffers of kept-block counts (scan-then-refine); then the grid-barrier counter.
+size_t counter_ints(size_t units) { return 6 * units + 1; }
+
+// Workspace of ffd_decode_attention: [error word | stage-1 maxima | per-unit m~ | split records |
+// kept-block lists | kept counts per CTA | counters]. Split records: one per (unit, CTA) pair that
+// shares work and refine group, indexed (unit + cta) * groups + group. Stage 1 has one slot per
+// forced block (at least one). The kept lists (one (unit, block) entry per block at most) and the
+// per-CTA counts serve the scan-then-refine schedule.
 ffd_status make_decode_plan(const ffd_decode_params *p, Plan *pl) {
     ffd_status st = check_params(p);
     if (st != FFD_OK) return st;
@@ -99,10 +119,16 @@ ffd_status make_decode_plan(const ffd_decode_params *p, Plan *pl) {
     size_t off = kAlign;
     pl->m1_off = off;
     off = align_up(off + (size_t)units * pl->nf * kMaxG * sizeof(float));
+    pl->mt_off = off;
+    off = align_up(off + (size_t)units * kMaxG * sizeof(float));
     pl->part_off = off;
-    off = align_up(off + (size_t)(units + ctas) * kRefineGroups * G * kPartStride * sizeof(float));
+    off = align_up(off + (size_t)(units + ctas) * kRecordGroups * G * kPartStride * sizeof(float));
+    pl->kept_off = off;
+    off = align_up(off + (size_t)units * p->max_blocks_per_seq * sizeof(int2));
+    pl->keptn_off = off;
+    off = align_up(off + (size_t)ctas * sizeof(int));
     pl->cnt_off = off;
-    off = align_up(off + 4 * (size_t)units * sizeof(int));
+    off = align_up(off + counter_ints(units) * sizeof(int));
     pl->total = off;
     return FFD_OK;
 }
@@ -125,7 +151,7 @@ ffd_status make_dense_plan(const ffd_decode_params *p, Plan *pl) {
     pl->ctas = ctas;
     pl->nf = 0;
     size_t off = kAlign;
-    pl->m1_off = off;
+    pl->m1_off = pl->mt_off = pl->kept_off = pl->keptn_off = off;
     pl->part_off = off;
     off = align_up(off + (size_t)(units + ctas) * kRefineGroups * G * kPartStride * sizeof(float));
     pl->cnt_off = off;
@@ -155,14 +181,22 @@ DecodeArgs make_args(const ffd_decode_params *p, const Plan &pl, void *ws) {
     char *base = static_cast<char *>(ws);
     a.err = reinterpret_cast<int *>(base);
     a.ws_m1 = reinterpret_cast<float *>(base + pl.m1_off);
+    a.ws_mt = reinterpret_cast<float *>(base + pl.mt_off);
     a.ws_part = reinterpret_cast<float *>(base + pl.part_off);
+    a.ws_kept = reinterpret_cast<int2 *>(base + pl.kept_off);
+    a.ws_keptn = reinterpret_cast<int *>(base + pl.keptn_off);
     a.ws_cnt = reinterpret_cast<int *>(base + pl.cnt_off);
+    const size_t units = (size_t)p->batch * p->num_kv_heads;
+    a.ws_ukept = a.ws_cnt + 4 * units;
+    a.ws_grid = reinterpret_cast<unsigned int *>(a.ws_cnt + 6 * units);
     return a;
 }
 
 }  // namespace
 
 extern "C" {
+
+int32_t ffd_last_cuda_error(void) { return g_last_cuda; }
 
 const char *ffd_status_string(ffd_status s) {
     switch (s) {
@@ -192,7 +226,7 @@ ffd_status ffd_quantize_keys(const ffd_cache_desc *cache, const void *k_bf16, ui
     if ((int64_t)listed * cache->num_kv_heads * kPage * 32 > INT32_MAX) return FFD_ERR_UNSUPPORTED;
     cudaError_t e = launch_quantize(cache->num_pages, cache->num_kv_heads, page_ids, listed, k_bf16,
                                     thumb, resid, error_word, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+    return cuda_status(e);
 }
 
 ffd_status ffd_append_kv(const ffd_cache_desc *cache, int32_t batch, int32_t max_blocks_per_seq,
@@ -214,7 +248,7 @@ ffd_status ffd_append_kv(const ffd_cache_desc *cache, int32_t batch, int32_t max
     cudaError_t e = launch_append(batch, cache->num_kv_heads, cache->num_pages, max_blocks_per_seq,
                                   positions, block_table, k_new_bf16, v_new_bf16, thumb, resid,
                                   v_bf16, k_bf16, error_word, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+    return cuda_status(e);
 }
 
 size_t ffd_decode_workspace_size(const ffd_decode_params *params) {
@@ -251,8 +285,10 @@ ffd_status ffd_decode_attention(const ffd_decode_params *params, const void *q_b
     a.out = out;
     a.keep_mask = keep_mask;
     a.m_tilde = m_tilde;
-    cudaError_t e = launch_decode(a, pl.ctas, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+    cudaError_t e = params->schedule == FFD_SCHEDULE_SCAN_REFINE
+                        ? launch_sparse(a, pl.ctas, static_cast<cudaStream_t>(stream))
+                        : launch_decode(a, pl.ctas, static_cast<cudaStream_t>(stream));
+    return cuda_status(e);
 }
 
 ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
@@ -276,7 +312,7 @@ ffd_status ffd_dense_decode(const ffd_decode_params *params, const void *q_bf16,
     a.block_table = block_table;
     a.out = out;
     cudaError_t e = launch_dense(a, pl.ctas, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+    return cuda_status(e);
 }
 
 // Workspace of ffd_select_blocks: [error word | importance [units][max_blocks] f32 |
@@ -344,7 +380,7 @@ ffd_status ffd_select_blocks(const ffd_decode_params *params, int32_t selector, 
     cudaError_t e = launch_select(a, selector, budget, reinterpret_cast<float *>(base + pl.imp_off),
                                   reinterpret_cast<float2 *>(base + pl.ml_off),
                                   static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+    return cuda_status(e);
 }
 
 ffd_status ffd_decode_attention_masked(const ffd_decode_params *params, const void *q_bf16,
@@ -375,7 +411,7 @@ ffd_status ffd_decode_attention_masked(const ffd_decode_params *params, const vo
     a.keep_in = keep_in;
     a.m_tilde = m_tilde;
     cudaError_t e = launch_decode(a, pl.ctas, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+    return cuda_status(e);
 }
 
 // Workspace of ffd_art_attention: the error word only (the kernel keeps its state on chip).
@@ -418,7 +454,7 @@ ffd_status ffd_art_attention(const ffd_decode_params *params, float tau, float p
     a.err = static_cast<int *>(workspace);
     cudaError_t e = launch_art(a, tau, phi, patience, blocks_used,
                                static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+    return cuda_status(e);
 }
 
 ffd_status ffd_set_profile_events(void *start, void *stop) {
@@ -432,12 +468,14 @@ ffd_status ffd_get_error(void *error_word, void *stream) {
     if (!error_word) return FFD_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int32_t h = 0;
-    if (cudaMemcpyAsync(&h, error_word, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return FFD_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return FFD_ERR_CUDA;
+    if (const cudaError_t e = cudaMemcpyAsync(&h, error_word, sizeof h, cudaMemcpyDeviceToHost, s);
+        e != cudaSuccess)
+        return cuda_status(e);
+    if (const cudaError_t e = cudaStreamSynchronize(s); e != cudaSuccess) return cuda_status(e);
     if (h != 0) {
-        if (cudaMemsetAsync(error_word, 0, sizeof h, s) != cudaSuccess) return FFD_ERR_CUDA;
-        if (cudaStreamSynchronize(s) != cudaSuccess) return FFD_ERR_CUDA;
+        cudaError_t e = cudaMemsetAsync(error_word, 0, sizeof h, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_status(e);
     }
     if (h & FFD_ERRBIT_BOUNDS) return FFD_ERR_BOUNDS;
     if (h & FFD_ERRBIT_RANGE) return FFD_ERR_RANGE;
@@ -470,11 +508,14 @@ void *g_static_ptr[kMaxDevices];
 // name as an address). Looked up once per device, with that device current.
 ffd_status static_scratch(void **out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FFD_ERR_CUDA;
+    if (const cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= kMaxDevices) return FFD_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_static_mu);
     if (!g_static_ptr[dev]) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return FFD_ERR_CUDA;
+        if (const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch); e != cudaSuccess)
+            return cuda_status(e);
+        if (!p) return FFD_ERR_CUDA;
         g_static_ptr[dev] = p;
     }
     *out = g_static_ptr[dev];
@@ -506,10 +547,11 @@ ffd_status ffd_decode_attention_static(const ffd_decode_params *params, const vo
     // The array keeps the previous call's contents: the error word and the per-unit tickets of
     // the in-kernel merge must start at zero.
     const size_t units = (size_t)params->batch * params->num_kv_heads;
-    if (cudaMemsetAsync(ws, 0, kAlign, s) != cudaSuccess ||
-        cudaMemsetAsync(static_cast<char *>(ws) + pl.cnt_off, 0, 4 * units * sizeof(int), s) !=
-            cudaSuccess)
-        return FFD_ERR_CUDA;
+    cudaError_t e = cudaMemsetAsync(ws, 0, kAlign, s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(static_cast<char *>(ws) + pl.cnt_off, 0,
+                            counter_ints(units) * sizeof(int), s);
+    if (e != cudaSuccess) return cuda_status(e);
     DecodeArgs a = make_args(params, pl, ws);
     if (error_word) a.err = reinterpret_cast<int *>(error_word);
     a.q = static_cast<const __nv_bfloat16 *>(q_bf16);
@@ -521,8 +563,9 @@ ffd_status ffd_decode_attention_static(const ffd_decode_params *params, const vo
     a.out = out;
     a.keep_mask = keep_mask;
     a.m_tilde = m_tilde;
-    cudaError_t e = launch_decode(a, pl.ctas, s);
-    return e == cudaSuccess ? FFD_OK : FFD_ERR_CUDA;
+    e = params->schedule == FFD_SCHEDULE_SCAN_REFINE ? launch_sparse(a, pl.ctas, s)
+                                                     : launch_decode(a, pl.ctas, s);
+    return cuda_status(e);
 }
 
 }  // extern "C"

@@ -28,6 +28,7 @@
 #include "ptx.cuh"
 #include "scan.cuh"
 #include "splitkv.cuh"
+#include "stage1.cuh"
 
 namespace ffd {
 
@@ -154,107 +155,6 @@ __device__ __forceinline__ bool tile_passes(float4 e, bool v0, bool v1, float th
     return (v0 && (e.x >= thr0 || e.y >= thr1)) || (v1 && (e.z >= thr0 || e.w >= thr1));
 }
 
-
-// ------------------------------------------------------------------------------------------
-// Stage 1 (pseudo-max), run by the refine groups at the start of the main kernel, before any
-// block reaches them. The (unit, forced-block slot) pairs are cut into equal contiguous runs,
-// one per group of the grid (ncta * kRefineGroups); in a group, warp mt takes rows 16mt .. 16mt+15 of the
-// slot's block. Exact scores s = sm q . K^ (thumbnail + residual, on tensor cores) of the block's
-// sink and local tokens; their per-head maximum goes to ws_m1 (the pseudo-max m~ of a unit is the
-// maximum over its slots), then the unit's slot counter is raised. Scan warp 0 of every CTA that
-// walks the unit waits for all of its slots before it sets the thresholds. Slot 0 of every unit
-// also clears the keep-mask tail past the sequence and, for an empty sequence (which no CTA
-// walks, so its counter stays at zero), writes the zero output and m~ = -inf.
-// ------------------------------------------------------------------------------------------
-__device__ __forceinline__ void pseudo_max_slots(const DecodeArgs &a, Misc *m, int cta, int nctas,
-                                                 int grp, int mt, int lane) {
-    const int units = a.B * a.Hkv;
-    const int nz = units * a.nf;
-    const int workers = nctas * kRefineGroups;
-    const int tid = 32 * mt + lane;
-    const int g = lane >> 2, tig = lane & 3;
-    // a worker takes a contiguous run of (unit, slot) pairs, so that with more pairs than workers
-    // (many short sequences) it keeps one unit's query operands and length across its slots
-    const int wk = cta * kRefineGroups + grp;
-    const int z0 = (int)((int64_t)nz * wk / workers), z1 = (int)((int64_t)nz * (wk + 1) / workers);
-    int it = 0, cu = -1, raw_n = 0, n = 0;
-    ThumbOps Q;
-    ResidOps QR;
-    for (int z = z0; z < z1; z++, it++) {
-        const int u = z / a.nf, slot = z % a.nf;
-        const int b = u / a.Hkv, h = u % a.Hkv;
-        if (u != cu) {
-            // the query operands do not depend on the page: their loads overlap the two dependent
-            // loads (sequence length, then block table) that locate the block
-            load_thumb_ops(a, b, h, lane, Q);
-            load_resid_ops(a, b, h, lane, QR);
-            raw_n = a.seq_lens[b];
-            n = len_of(a, b);
-            cu = u;
-        }
-        const int nb = (n + kPage - 1) / kPage;
-        if (slot == 0) {
-            if (tid == 0 && h == 0 && raw_n != n) raise_error(a.err, FFD_ERRBIT_BOUNDS);
-            if (a.keep_mask)
-                for (int blk = nb + tid; blk < a.max_blocks; blk += 128)
-                    a.keep_mask[(size_t)u * a.max_blocks + blk] = 0;
-            if (n == 0) {
-                for (int idx = tid; idx < a.G * kD; idx += 128)
-                    a.out[((size_t)b * a.Hq + h * a.G) * kD + idx] = 0.0f;
-                if (a.m_tilde && tid < a.G)
-                    a.m_tilde[(size_t)b * a.Hq + h * a.G + tid] = -INFINITY;
-            }
-        }
-        if (n == 0) continue;  // uniform across the group; nobody waits for this unit
-        const ForcedBlocks fb(n, a.S, a.L);
-        float *mdst = a.ws_m1 + ((size_t)u * a.nf + slot) * kMaxG;
-        int page = -1;
-        const int blk = slot < fb.count ? fb.block(slot) : 0;
-        if (slot < fb.count) {
-            page = a.block_table[(size_t)b * a.max_blocks + blk];
-            if (page < 0 || page >= a.P) page = -1;  // flagged by the page warp
-        }
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-        if (page >= 0) {  // uniform across the group
-            const size_t tile = (size_t)page * a.Hkv + h;
-            const uint8_t *trec = a.thumb + tile * kThumbRec;
-            const uint8_t *rrec = a.resid + tile * kResidRec;
-            const int r0 = 16 * mt + g, r1 = r0 + 8;
-            const float4 e = exact_tile(trec, rrec, r0, r1, tig, Q, QR, a.sm_scale);
-            const int t0 = blk * kPage + r0, t1 = blk * kPage + r1;
-            // pseudo-max candidates: sink and local tokens inside the sequence
-            const bool v0 = t0 < n && (t0 < a.S || t0 >= n - a.L);
-            const bool v1 = t1 < n && (t1 < a.S || t1 >= n - a.L);
-            const float s00 = v0 ? e.x : -INFINITY;
-            const float s01 = v0 ? e.y : -INFINITY;
-            const float s10 = v1 ? e.z : -INFINITY;
-            const float s11 = v1 ? e.w : -INFINITY;
-            mx0 = fmaxf(s00, s10);
-            mx1 = fmaxf(s01, s11);
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-            }
-        }
-        float (&red)[4][kMaxG] = m->wmax[grp][it & 1];
-        if (g == 0) {
-            red[mt][2 * tig] = mx0;
-            red[mt][2 * tig + 1] = mx1;
-        }
-        named_barrier_sync(2 + grp, 128);
-        if (tid < kMaxG) {
-            mdst[tid] = tid < a.G ? fmaxf(fmaxf(red[0][tid], red[1][tid]),
-                                          fmaxf(red[2][tid], red[3][tid]))
-                                  : -INFINITY;
-            __threadfence();
-        }
-        named_barrier_sync(2 + grp, 128);
-        if (tid == 0) atomicAdd(slot_counter(a, u), 1);
-    }
-    // the reduction buffers are the refine warps' block-maxima buffers
-    named_barrier_sync(2 + grp, 128);
-}
 
 // ------------------------------------------------------------------------------------------
 // Main kernel: waits and the copy warps.
@@ -722,7 +622,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (walker) scanner(a, S, cta, ncta, warp - 4, lane);
     } else {
         regs_increase<kRefineRegs>();
-        pseudo_max_slots(a, S.misc, cta, gridDim.x, (warp - 8) >> 2, warp & 3, lane);
+        pseudo_max_slots<kRefineGroups>(a, S.misc, cta, gridDim.x, (warp - 8) >> 2, warp & 3, lane);
         if (walker) refiner(a, S, cta, ncta, (warp - 8) >> 2, warp & 3, lane);
     }
 }

@@ -283,25 +283,27 @@ __device__ __forceinline__ void softmax_pv(M *m, uint8_t *px_buf, const uint8_t 
 
 // ------------------------------------------------------------------------------------------
 // Split merge: out_i = sum_r e^(m_r - M) num_r / sum_r e^(m_r - M) den_r over a unit's records.
-// Records of CTAs cf..cl, one per refine group, are contiguous from
-// ws_part[(u + cf) * kRefineGroups]; a record holds (num[128], m, den) per head. Counters in
+// Records of CTAs cf..cl, one per refine group (NG per CTA: kRefineGroups in the fused kernel),
+// are contiguous from ws_part[(u + cf) * NG]; a record holds (num[128], m, den) per head. Counters in
 // ws_cnt: [0, units) merge tickets, [units, 2 units) stage-1 slots, [2 units, 3 units) merge
 // reports, [3 units, 4 units) merger declarations.
 // ------------------------------------------------------------------------------------------
+template <int NG = kRefineGroups>
 __device__ __forceinline__ float *unit_record(const DecodeArgs &a, int u, int c, int grp) {
-    return a.ws_part + ((size_t)(u + c) * kRefineGroups + grp) * a.G * kPartStride;
+    return a.ws_part + ((size_t)(u + c) * NG + grp) * a.G * kPartStride;
 }
 
 // Merge of head i of a unit by one refine group (128 threads, thread = output channel), after
 // every record of the unit is written. Records are loaded in independent batches: the maxima
 // (lane r loads record r), then 16 records at a time whose weights, denominators and channel
 // values are loaded together.
+template <int NG = kRefineGroups>
 __device__ __forceinline__ void merge_head(const DecodeArgs &a, int b, int h, int cf, int cl, int i,
                                            int mt, int lane) {
     const int u = b * a.Hkv + h;
-    const int nr = kRefineGroups * (cl - cf + 1);
+    const int nr = NG * (cl - cf + 1);
     const size_t rstride = (size_t)a.G * kPartStride;
-    const float *hb = unit_record(a, u, cf, 0) + (size_t)i * kPartStride;
+    const float *hb = unit_record<NG>(a, u, cf, 0) + (size_t)i * kPartStride;
     const int ch = 32 * mt + lane;
     float M = -INFINITY;
     for (int r = lane; r < nr; r += 32) M = fmaxf(M, __ldcg(hb + r * rstride + kD));
@@ -427,7 +429,7 @@ __device__ __forceinline__ unsigned int wait_bits(const DecodeArgs &a, M *m, con
 // waits for the remaining tickets (their groups are at the ends of their ranges too) and merges
 // its heads. A group whose CTA still has work never waits for other groups' records: the other
 // parts of the unit may be walked at the very end of other CTAs' ranges.
-template <class M>
+template <class M, int NG = kRefineGroups>
 __device__ __forceinline__ void finish_unit(const DecodeArgs &a, M *m, const Sub &s, int cta,
                                             int ncta, int64_t T, int grp, int mt, int lane) {
     const uint32_t bar_id = 2 + grp;
@@ -436,7 +438,7 @@ __device__ __forceinline__ void finish_unit(const DecodeArgs &a, M *m, const Sub
     named_barrier_sync(bar_id, 128);
     const int64_t first = s.x0 - s.j0;  // global index of the unit's first block
     const int cf = cta_of(first, T, ncta), cl = cta_of(first + s.nblk - 1, T, ncta);
-    const int target = kRefineGroups * (cl - cf + 1);
+    const int target = NG * (cl - cf + 1);
     const int nm = a.G < target ? a.G : target;
     const bool final_seg = s.x0 + s.cnt == T * (cta + 1) / ncta;
     if (mt == 0 && lane == 0) {
@@ -465,7 +467,7 @@ __device__ __forceinline__ void finish_unit(const DecodeArgs &a, M *m, const Sub
         __threadfence();
         const uint32_t cover = (role >> 8) & 0xffu;
         for (int i = 0; i < a.G; i++)
-            if ((cover >> (i % nm)) & 1u) merge_head(a, s.b, s.h, cf, cl, i, mt, lane);
+            if ((cover >> (i % nm)) & 1u) merge_head<NG>(a, s.b, s.h, cf, cl, i, mt, lane);
         named_barrier_sync(bar_id, 128);
     }
     if (mt == 0 && lane == 0) {

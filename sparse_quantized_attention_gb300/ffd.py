@@ -20,17 +20,22 @@ _lock = threading.Lock()
 _lib = None
 
 FFD_OK = 0
+FFD_ERR_CUDA = 4
 STATUS_NAMES = {0: "FFD_OK", 1: "FFD_ERR_INVALID_ARG", 2: "FFD_ERR_UNSUPPORTED",
                 3: "FFD_ERR_WORKSPACE", 4: "FFD_ERR_CUDA", 5: "FFD_ERR_BOUNDS",
                 6: "FFD_ERR_RANGE", 7: "FFD_ERR_TIMEOUT"}
 HEAD_DIM = 128
 PAGE = 64
+SCHEDULE_FUSED = 0        # FFD_SCHEDULE_FUSED
+SCHEDULE_SCAN_REFINE = 1  # FFD_SCHEDULE_SCAN_REFINE
 
 
 class FFDError(RuntimeError):
-    def __init__(self, status: int, where: str):
+    def __init__(self, status: int, where: str, cuda_error: int = 0):
         self.status = status
-        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+        self.cuda_error = cuda_error
+        extra = f" (cudaError_t {cuda_error})" if cuda_error else ""
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}{extra}")
 
 
 class CacheDesc(ctypes.Structure):
@@ -45,17 +50,17 @@ class DecodeParams(ctypes.Structure):
                 ("max_blocks_per_seq", ctypes.c_int32), ("sink_tokens", ctypes.c_int32),
                 ("local_tokens", ctypes.c_int32), ("delta", ctypes.c_float),
                 ("sm_scale", ctypes.c_float), ("num_splits", ctypes.c_int32),
-                ("wait_limit_us", ctypes.c_int32)]
+                ("wait_limit_us", ctypes.c_int32), ("schedule", ctypes.c_int32)]
 
 
 def make_params(batch, num_q_heads, num_kv_heads, num_pages, max_blocks_per_seq, *, sink=64,
                 local=1024, delta=5.0, sm_scale=None, num_splits=0,
-                wait_limit_us=0) -> DecodeParams:
+                wait_limit_us=0, schedule=0) -> DecodeParams:
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(HEAD_DIM)
     return DecodeParams(batch, num_q_heads, num_kv_heads, HEAD_DIM, PAGE, num_pages,
                         max_blocks_per_seq, sink, local, delta, sm_scale, num_splits,
-                        wait_limit_us)
+                        wait_limit_us, schedule)
 
 
 def library_path() -> str:
@@ -77,6 +82,8 @@ def lib() -> ctypes.CDLL:
             L.ffd_status_string.restype = ctypes.c_char_p
             L.ffd_version.argtypes = []
             L.ffd_version.restype = ctypes.c_int32
+            L.ffd_last_cuda_error.argtypes = []
+            L.ffd_last_cuda_error.restype = ctypes.c_int32
             L.ffd_quantize_keys.argtypes = [ctypes.POINTER(CacheDesc), P, P, P, P,
                                             ctypes.c_int32, P, P]
             L.ffd_quantize_keys.restype = st
@@ -136,7 +143,8 @@ def _stream(stream):
 
 def _check(status: int, where: str):
     if status != FFD_OK:
-        raise FFDError(status, where)
+        raise FFDError(status, where,
+                       ffd_last_cuda_error() if status == FFD_ERR_CUDA else 0)
 
 
 THUMB_RECORD_BYTES = 3072
@@ -164,6 +172,11 @@ def ffd_status_string(status: int) -> str:
 
 def ffd_version() -> int:
     return int(lib().ffd_version())
+
+
+def ffd_last_cuda_error() -> int:
+    """The cudaError_t behind this thread's latest FFD_ERR_CUDA (0 if none)."""
+    return int(lib().ffd_last_cuda_error())
 
 
 def ffd_quantize_keys(k: torch.Tensor, cache: QuantizedCache, *, page_ids=None,

@@ -74,16 +74,16 @@ def assert_cache_equal(gpu: oracle.QuantizedKeys, ref: oracle.QuantizedKeys):
                                  f"gpu {a[tuple(bad[0])]} oracle {b[tuple(bad[0])]}")
 
 
-def params_for(inp, delta, num_splits=0):
+def params_for(inp, delta, num_splits=0, schedule=0):
     w = inp.workload
     return ffd.make_params(w.batch, w.num_q_heads, w.num_kv_heads, inp.num_pages,
                            inp.max_blocks, sink=w.sink, local=w.local, delta=delta,
-                           sm_scale=SM, num_splits=num_splits)
+                           sm_scale=SM, num_splits=num_splits, schedule=schedule)
 
 
-def decode(inp, dev, qc, delta, num_splits=0) -> dict:
+def decode(inp, dev, qc, delta, num_splits=0, schedule=0) -> dict:
     w = inp.workload
-    p = params_for(inp, delta, num_splits)
+    p = params_for(inp, delta, num_splits, schedule)
     d = dev["q"].device
     out = torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.float32, device=d)
     mask = torch.full((w.batch, w.num_kv_heads, inp.max_blocks), 7, dtype=torch.uint8, device=d)
