@@ -90,7 +90,7 @@ typedef struct {
     int32_t sink_tokens;        /* S >= 0: tokens 0 .. S-1 are sink tokens */
     int32_t local_tokens;       /* L >= 0: tokens n-L .. n-1 are local tokens */
     float delta;                /* delta of the Top-delta rule; +INFINITY keeps every block */
-    float sm_scale;             /* score scale, normally 1/sqrt(head_dim) */
+    float sm_scale;             /* score scale, finite and > 0; normally 1/sqrt(head_dim) */
     int32_t num_splits;         /* 0: library's choice (one per SM); else the number of KV
                                    partitions, i.e. the CTAs of the persistent kernel of
                                    ffd_decode_attention or ffd_dense_decode, at most one per SM:
@@ -114,7 +114,8 @@ typedef struct {
  *     compute warps, then, after a grid-wide barrier, the kept blocks of all CTAs are shared out
  *     equally for the refinement. Suits steps that drop most blocks (the scan dominates, and the
  *     kept blocks may crowd into a few sequences). A caller can pick it from the kept fraction of
- *     the previous step (keep_mask). */
+ *     the previous step (keep_mask). It needs batch * num_kv_heads * max_blocks_per_seq <=
+ *     INT32_MAX (else FFD_ERR_UNSUPPORTED). */
 #define FFD_SCHEDULE_FUSED 0
 #define FFD_SCHEDULE_SCAN_REFINE 1
 

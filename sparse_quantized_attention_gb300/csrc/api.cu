@@ -72,12 +72,16 @@ ffd_status check_params(const ffd_decode_params *p) {
         return FFD_ERR_INVALID_ARG;
     if (p->num_q_heads % p->num_kv_heads != 0) return FFD_ERR_INVALID_ARG;
     if (isnan(p->delta) || p->delta == -INFINITY) return FFD_ERR_INVALID_ARG;
-    if (!isfinite(p->sm_scale)) return FFD_ERR_INVALID_ARG;
+    if (!isfinite(p->sm_scale) || !(p->sm_scale > 0.0f)) return FFD_ERR_INVALID_ARG;
     if (p->head_dim != kD || p->page_size != kPage) return FFD_ERR_UNSUPPORTED;
     const int G = p->num_q_heads / p->num_kv_heads;
     if (G < 1 || G > kMaxG) return FFD_ERR_UNSUPPORTED;
     // grid.y = B * Hkv, grid.x = splits / forced slots
     if ((int64_t)p->batch * p->num_kv_heads > 65535) return FFD_ERR_UNSUPPORTED;
+    // the scan-then-refine kernel names a block by u * max_blocks_per_seq + block in an int32
+    if (p->schedule == FFD_SCHEDULE_SCAN_REFINE &&
+        (int64_t)p->batch * p->num_kv_heads * p->max_blocks_per_seq > INT32_MAX)
+        return FFD_ERR_UNSUPPORTED;
     return FFD_OK;
 }
 

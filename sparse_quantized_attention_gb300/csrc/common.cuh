@@ -50,7 +50,8 @@ struct DecodeArgs {
     int *err;        // device error word
     float *ws_m1;    // [B*Hkv][nf][kMaxG] stage-1 block maxima over the sink / local tokens
     float *ws_mt;    // [B*Hkv][kMaxG] m~ per unit and head (scan-then-refine schedule)
-    int2 *ws_kept;   // [blocks of all units] (unit, block) of the kept blocks, per CTA range
+    int2 *ws_kept;   // [blocks of all units] (u * max_blocks + block, page) of the kept blocks,
+                     // per CTA range
     int *ws_keptn;   // [CTAs] kept blocks per CTA range
     int *ws_ukept;   // [2][B*Hkv] kept blocks per unit (two buffers, alternate calls)
     unsigned int *ws_grid;  // grid-barrier arrivals (grows by the CTA count each call)

@@ -134,6 +134,43 @@ __device__ __forceinline__ float4 scan_tile(const uint8_t *base, int r0, int r1,
     return e;
 }
 
+// scan_tile's scores divided by sm * 2^(133 - kKq), for a caller that needs only their maximum
+// over rows: the query sums enter divided by 2^(133 - kKq) (qsr, a power-of-two scaling, exact
+// for normal values), so every partial sum is the scan_tile one times 2^(kKq - 133) and no
+// per-score multiply is left; the caller multiplies the maximum by sm * 2^(133 - kKq) > 0, which
+// gives the maximum of scan_tile's scores bit for bit (rounding is monotonic).
+__device__ __forceinline__ float raw_score(const float (&D)[4][4], int e, const float (&sf)[4],
+                                           const float (&zf)[4], const float (&qsr)[4]) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int gg = 0; gg < 4; gg++) acc = fmaf(sf[gg], D[gg][e], fmaf(zf[gg], qsr[gg], acc));
+    return acc;
+}
+
+__device__ __forceinline__ float4 scan_tile_raw(const uint8_t *base, int r0, int r1, uint32_t m0,
+                                                const ThumbOps &Q, const float (&qsr)[2][4]) {
+    const uint4 *c0 = reinterpret_cast<const uint4 *>(base + r0 * kThumbRow);
+    const uint4 *c1 = reinterpret_cast<const uint4 *>(base + r1 * kThumbRow);
+    const uint4 p0 = c0[0], p1 = c0[1], p2 = c1[0], p3 = c1[1];
+    const uint32_t w0[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    const uint32_t w1[8] = {p2.x, p2.y, p2.z, p2.w, p3.x, p3.y, p3.z, p3.w};
+    float D[4][4];
+    thumb_mma(D, w0, w1, m0, Q);
+    float sf0[4], sf1[4], zf0[4], zf1[4];
+    const uint2 *ts = reinterpret_cast<const uint2 *>(base + kThumbScaleOff);
+    const uint2 *tz = reinterpret_cast<const uint2 *>(base + kThumbZeroOff);
+    unpack4h(ts[r0], sf0);
+    unpack4h(ts[r1], sf1);
+    unpack4h(tz[r0], zf0);
+    unpack4h(tz[r1], zf1);
+    float4 e;
+    e.x = raw_score(D, 0, sf0, zf0, qsr[0]);
+    e.y = raw_score(D, 1, sf0, zf0, qsr[1]);
+    e.z = raw_score(D, 2, sf1, zf1, qsr[0]);
+    e.w = raw_score(D, 3, sf1, zf1, qsr[1]);
+    return e;
+}
+
 // Query operands of the residual correction: int8 codes enter the MMA as (c8 + 128), with the
 // same scaling as the thumbnail codes; the +128 is removed with the per-group query sums.
 struct ResidOps {

@@ -37,23 +37,30 @@ namespace {
 
 constexpr int kSpGroups = 3;                // compute groups of 4 warps (warps 4 .. 15)
 constexpr int kSpWarps = 4 * kSpGroups;     // compute warps
-constexpr int kSpThreads = 128 + 32 * kSpWarps;  // a producer warpgroup (warp 0 works) + compute
+constexpr int kSpThreads = 128 + 32 * kSpWarps;  // a producer warpgroup + the compute warps
 constexpr int kSpActive = 32 + 32 * kSpWarps;    // warp 0 and the compute warps
-// Registers: the launch gives 128 a thread (512 threads fill the 64K file); the producer
-// warpgroup drops to 56 and the compute warpgroups rise to 152: 128 * 56 + 384 * 152 = 65536, and
-// each SM sub-partition holds one warp of each warpgroup (56 + 3 * 152 = 512 registers a lane).
-constexpr int kSpProducerRegs = 56;
-constexpr int kSpComputeRegs = 152;
+// Registers: the launch gives 128 a thread (512 threads fill the 64K file), kept through phase A
+// (warp 0 stages thumbnails, warps 1-3 run stage 1, the compute warps scan). Phase B: the
+// producer warpgroup drops to 56 (warps 1-3 leave) and the compute warpgroups (the refinement)
+// rise to 152, which again fills the file; each SM sub-partition holds one warp of each
+// warpgroup (56 + 3 * 152 = 512 registers a lane).
+constexpr int kSpProducerRegs = 56, kSpComputeRegs = 152;
 static_assert(128 * kSpProducerRegs + 32 * kSpWarps * kSpComputeRegs == 65536, "register split");
 // named barriers: 1 the producer and compute warps, 2 + g refine group g, kSpComputeBar the compute
-// warps
+// warps, kSpScanBar every warp that scans (warps 1 .. 15: the stage-1 warps join the scan)
 constexpr int kSpActiveBar = 1;
 constexpr int kSpComputeBar = 2 + kSpGroups;
+constexpr int kSpScanBar = 3 + kSpGroups;
+constexpr int kSpScanners = 32 * (3 + kSpWarps);
 
-// Phase A: thumbnail stages, two per compute warp (warp w scores range blocks w, w + 12, ... and
-// block li uses stage li % kSpStages), and the per-block head maxima of one chunk of the range.
-constexpr int kSpStages = 2 * kSpWarps;
-constexpr int kSpChunk = 1024;              // range blocks whose maxima are held at once
+// Phase A: thumbnail stages (block li of the range uses stage li % kSpStages; the scanning warps
+// take blocks in order from a shared counter), and the per-block head maxima of one chunk of the
+// range. 48 stages keep 96 to 144 KB of thumbnails in flight per SM, which covers the copy latency
+// at the HBM rate.
+constexpr int kSpStages = 48;
+constexpr int kSpIssue = 16;                // stages armed at a time by the producer warp
+static_assert(kSpStages % kSpIssue == 0 && 32 % kSpIssue == 0, "issue batches");
+constexpr int kSpChunk = 512;               // range blocks whose maxima are held at once
 constexpr int kSpOffStages = 0;
 constexpr int kSpOffBmax = kSpOffStages + kSpStages * kThumbRec;    // float [kSpChunk][kMaxG]
 constexpr int kSpOffBunit = kSpOffBmax + kSpChunk * kMaxG * 4;       // int2 [kSpChunk]: (u, blk)
@@ -73,14 +80,16 @@ constexpr int kSpPhaseB = ((kSpRing * kSpSlotBytes + 1023) / 1024) * 1024;
 
 constexpr int kSpOffShared = kSpPhaseA > kSpPhaseB ? kSpPhaseA : kSpPhaseB;
 constexpr int kSpOffPx = ((kSpOffShared + 1023) / 1024) * 1024;      // [group][2][kPxBuf]
-constexpr int kSpOffMisc = kSpOffPx + kSpGroups * 2 * kPxBuf;
+// the refine groups' records of a unit's segment, combined into the CTA's one record
+constexpr int kSpOffComb = kSpOffPx + kSpGroups * 2 * kPxBuf;        // float [group][kMaxG][stride]
+constexpr int kSpOffMisc = kSpOffComb + kSpGroups * kMaxG * kPartStride * 4;
 constexpr int kSpMaxCtas = 256;
-constexpr int kSpMiscBytes = 4096;
+constexpr int kSpMiscBytes = 5120;
 constexpr int kSpSmemBytes = kSpOffMisc + kSpMiscBytes + 1024;       // + slack to align to 1 KB
 static_assert(kSpSmemBytes <= 232448, "shared memory per CTA");
 
-struct SpDesc {       // a phase-A stage: the block it holds
-    int32_t u, blk, rows, bad;
+struct SpDesc {       // a phase-A stage: the block it holds (page -1: not loaded)
+    int32_t u, blk, rows, page;
 };
 
 struct SpMisc {
@@ -92,7 +101,10 @@ struct SpMisc {
     int32_t ured[kSpGroups][4];           // per-group sums (a unit's first kept index)
     int32_t pref[kSpMaxCtas + 1];         // phase B: prefix of the CTAs' kept counts
     int32_t kept;                         // phase A: kept blocks of this CTA so far
+    int32_t scan_next;                    // phase A: next block of the chunk to score
     SpDesc desc[kSpStages];
+    int32_t armed_a[kSpStages];           // uses armed per phase-A stage
+    int32_t armed_b[kSpRing];             // uses armed per phase-B ring slot
     uint64_t a_full[kSpStages], a_empty[kSpStages];
     uint64_t b_full[kSpRing], b_empty[kSpRing];
 };
@@ -136,71 +148,127 @@ __device__ __forceinline__ int2 sp_locate(const DecodeArgs &a, int x) {
 // ------------------------------------------------------------------------------------------
 // Phase A
 // ------------------------------------------------------------------------------------------
+// Where range block x lies: its unit, block, rows and page (-1 for a block-table entry outside
+// [0, P)).
+struct SpLook {
+    int u, blk, rows, page;
+};
+__device__ __forceinline__ SpLook sp_lookup(const DecodeArgs &a, int x) {
+    const int2 ub = sp_locate(a, x);
+    const int b = ub.x / a.Hkv;
+    SpLook l;
+    l.u = ub.x;
+    l.blk = ub.y;
+    l.page = a.block_table[(size_t)b * a.max_blocks + ub.y];
+    if (l.page < 0 || l.page >= a.P) l.page = -1;
+    const int n = len_of(a, b);
+    l.rows = n - ub.y * kPage < kPage ? n - ub.y * kPage : kPage;
+    return l;
+}
+
 // Producer warp: range block li (global x + li) goes to stage li % kSpStages once the stage's
-// previous block has been scored; 24 blocks at a time, lane k taking block li0 + k. A block whose
-// block-table entry lies outside [0, P) is flagged (FFD_ERRBIT_BOUNDS) and not loaded.
+// previous block has been scored. The lanes look up 32 blocks at once, those after the ones being
+// armed, so that the lookups overlap the waits; the blocks are armed kSpIssue at a time (lane k of
+// a batch arms its own block), so a batch waits for blocks kSpStages earlier while the other
+// stages stay in flight. A block whose block-table entry lies outside [0, P) is flagged
+// (FFD_ERRBIT_BOUNDS) and not loaded.
 __device__ __forceinline__ void sp_stage_issuer(const DecodeArgs &a, SpMisc *m, uint8_t *base,
                                                 const SpRange &r, int lane) {
     const int len = r.x1 - r.x;
-    int last = -1;  // this lane's (stage's) last armed use
-    for (int li0 = 0; li0 < len; li0 += kSpStages) {
-        const int li = li0 + lane;
-        if (lane < kSpStages && li < len) {
-            const int2 ub = sp_locate(a, r.x + li);
-            const int b = ub.x / a.Hkv, h = ub.x - b * a.Hkv;
-            const int st = li % kSpStages, use = li / kSpStages;
-            if (use > 0) wait_bar(a, m, &m->a_empty[st], (use - 1) & 1);
-            const int page = a.block_table[(size_t)b * a.max_blocks + ub.y];
-            const bool bad = page < 0 || page >= a.P;
-            const int n = len_of(a, b);
-            const int rows = n - ub.y * kPage < kPage ? n - ub.y * kPage : kPage;
-            m->desc[st] = SpDesc{ub.x, ub.y, rows, bad ? 1 : 0};
-            if (bad) {
-                raise_error(a.err, FFD_ERRBIT_BOUNDS);
-                mbar_arrive(&m->a_full[st]);
-            } else if (!aborted(m)) {  // a wait ran out: the stage may still be filling
-                mbar_arrive_expect_tx(&m->a_full[st], kThumbRec);
-                tma_load_1d(base + kSpOffStages + st * kThumbRec,
-                            a.thumb + ((size_t)page * a.Hkv + h) * kThumbRec, kThumbRec,
-                            &m->a_full[st]);
-                last = li;
-            } else {
-                mbar_arrive(&m->a_full[st]);
+    SpLook cur = lane < len ? sp_lookup(a, r.x + lane) : SpLook{0, 0, 0, -1};
+    for (int li0 = 0; li0 < len; li0 += 32) {
+        const SpLook nxt =
+            li0 + 32 + lane < len ? sp_lookup(a, r.x + li0 + 32 + lane) : SpLook{0, 0, 0, -1};
+#pragma unroll 1
+        for (int half = 0; half < 32 / kSpIssue; half++) {
+            const int li = li0 + lane;
+            if (lane / kSpIssue == half && li < len) {
+                const int b = cur.u / a.Hkv, h = cur.u - b * a.Hkv;
+                const int st = li % kSpStages, use = li / kSpStages;
+                if (use > 0) wait_bar(a, m, &m->a_empty[st], (use - 1) & 1);
+                // after an abort nothing more is armed: the stage may still be filling
+                if (!aborted(m)) {
+                    m->desc[st] = SpDesc{cur.u, cur.blk, cur.rows, cur.page};
+                    if (cur.page < 0) {
+                        raise_error(a.err, FFD_ERRBIT_BOUNDS);
+                        mbar_arrive(&m->a_full[st]);
+                    } else {
+                        mbar_arrive_expect_tx(&m->a_full[st], kThumbRec);
+                        tma_load_1d(base + kSpOffStages + st * kThumbRec,
+                                    a.thumb + ((size_t)cur.page * a.Hkv + h) * kThumbRec,
+                                    kThumbRec, &m->a_full[st]);
+                    }
+                    m->armed_a[st] = use + 1;
+                }
             }
+            __syncwarp();
         }
-        __syncwarp();
+        cur = nxt;
     }
-    // leave no copy in flight: the last copy into this lane's stage
-    if (last >= 0) drain_bar(a, &m->a_full[lane], (last / kSpStages) & 1);
+    // leave no copy in flight: the last armed use of every stage
+    __syncwarp();
+    for (int st = lane; st < kSpStages; st += 32)
+        if (m->armed_a[st] > 0) drain_bar(a, &m->a_full[st], (m->armed_a[st] - 1) & 1);
 }
 
-// Compute warp cw scores range blocks li = cw, cw + 12, ... of chunk [c0, c1): for each head of
-// the group the maximum provisional score over the block's tokens (-inf for a block not loaded,
-// and for heads past G), into bmax[li - c0]; (unit, block) into bunit.
+// Bounded wait until the producer has armed use `target - 1` of stage st (the stage's previous
+// block has then been scored, so the parity wait that follows is unambiguous).
+__device__ __forceinline__ void wait_armed(const DecodeArgs &a, SpMisc *m, int st, int target) {
+    const volatile int32_t *armed = &m->armed_a[st];
+    if (*armed >= target) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (*armed < target) {
+        if (aborted(m)) return;
+        if (globaltimer_ns() - t0 > a.wait_ns) {
+            raise_error(a.err, FFD_ERRBIT_TIMEOUT);
+            *reinterpret_cast<volatile uint32_t *>(&m->aborted) = 1;
+            return;
+        }
+    }
+}
+
+// A scanning warp takes blocks li of chunk [c0, c1) in order from m->scan_next and scores each:
+// for each head of the group the maximum provisional score over the block's tokens (-inf for a
+// block not loaded, and for heads past G), into bmax[li - c0]; (u * max_blocks + block, page) into
+// bunit (-1 for a block not loaded). The maximum is taken over scan_tile_raw's scores and scaled
+// once.
 __device__ __forceinline__ void sp_scan_chunk(const DecodeArgs &a, SpMisc *m, uint8_t *base,
-                                              int c0, int c1, int cw, int lane, ThumbOps &Q,
-                                              int &qu) {
+                                              int c0, int c1, int lane, ThumbOps &Q,
+                                              float (&qsr)[2][4], int &qu) {
     const int g = lane >> 2, tig = lane & 3;
     const uint32_t m0 = 0x00030003u << (2 * tig);
     float *bmax = reinterpret_cast<float *>(base + kSpOffBmax);
     int2 *bunit = reinterpret_cast<int2 *>(base + kSpOffBunit);
-    for (int li = c0 + cw; li < c1; li += kSpWarps) {
+    const float post = a.sm_scale * kUnscale;  // exact: kUnscale is a power of two
+    // the next block is taken while the current one is scored (a warp holds at most two blocks,
+    // fewer than the stages, so the producer never waits on a block nobody can score)
+    int li_next = 0;
+    if (lane == 0) li_next = c0 + atomicAdd(&m->scan_next, 1);
+    for (;;) {
+        const int li = __shfl_sync(0xffffffffu, li_next, 0);
+        if (li >= c1) break;
         const int st = li % kSpStages, use = li / kSpStages;
+        wait_armed(a, m, st, use + 1);
         wait_bar(a, m, &m->a_full[st], use & 1);
+        if (lane == 0) li_next = c0 + atomicAdd(&m->scan_next, 1);
         SpDesc d = m->desc[st];
-        if (d.u < 0 || d.u >= a.B * a.Hkv) d.bad = 1;  // only after a wait ran out
+        if (d.u < 0 || d.u >= a.B * a.Hkv) d.page = -1;  // only after a wait ran out
         float mh0 = -INFINITY, mh1 = -INFINITY;
-        if (!d.bad) {  // warp-uniform
+        if (d.page >= 0) {  // warp-uniform
             if (d.u != qu) {  // the unit's query operands (thumbnail B fragments, query sums)
                 const int b = d.u / a.Hkv;
                 load_thumb_ops(a, b, d.u - b * a.Hkv, lane, Q);
+#pragma unroll
+                for (int i = 0; i < 2; i++)
+#pragma unroll
+                    for (int gg = 0; gg < 4; gg++) qsr[i][gg] = Q.qs[i][gg] * (1.0f / kUnscale);
                 qu = d.u;
             }
             const uint8_t *rec = base + kSpOffStages + st * kThumbRec;
             float4 e[4];
 #pragma unroll
-            for (int mt = 0; mt < 4; mt++) e[mt] = scan_tile(rec, 16 * mt + g, 16 * mt + g + 8, m0,
-                                                           Q, a.sm_scale);
+            for (int mt = 0; mt < 4; mt++)
+                e[mt] = scan_tile_raw(rec, 16 * mt + g, 16 * mt + g + 8, m0, Q, qsr);
 #pragma unroll
             for (int mt = 0; mt < 4; mt++) {
                 const bool v0 = 16 * mt + g < d.rows, v1 = 16 * mt + g + 8 < d.rows;
@@ -212,6 +280,8 @@ __device__ __forceinline__ void sp_scan_chunk(const DecodeArgs &a, SpMisc *m, ui
                 mh0 = fmaxf(mh0, __shfl_xor_sync(0xffffffffu, mh0, o));
                 mh1 = fmaxf(mh1, __shfl_xor_sync(0xffffffffu, mh1, o));
             }
+            mh0 *= post;
+            mh1 *= post;
         }
         __syncwarp();  // every lane has read the stage
         if (lane == 0) mbar_arrive(&m->a_empty[st]);
@@ -219,7 +289,8 @@ __device__ __forceinline__ void sp_scan_chunk(const DecodeArgs &a, SpMisc *m, ui
             bmax[(li - c0) * kMaxG + 2 * tig] = 2 * tig < a.G ? mh0 : -INFINITY;
             bmax[(li - c0) * kMaxG + 2 * tig + 1] = 2 * tig + 1 < a.G ? mh1 : -INFINITY;
         }
-        if (lane == 0) bunit[li - c0] = d.bad ? make_int2(-1, d.blk) : make_int2(d.u, d.blk);
+        if (lane == 0)
+            bunit[li - c0] = d.page < 0 ? make_int2(-1, 0) : make_int2(d.u * a.max_blocks + d.blk, d.page);
     }
 }
 
@@ -246,19 +317,23 @@ __device__ __forceinline__ void sp_vote_chunk(const DecodeArgs &a, SpMisc *m, ui
         if (li < c1) {
             const int2 ub = bunit[li - c0];
             if (ub.x >= 0) {
-                const int b = ub.x / a.Hkv;
-                const int n = len_of(a, b);
+                const int u = ub.x / a.max_blocks, blk = ub.x - u * a.max_blocks;
+                const int n = len_of(a, u / a.Hkv);
                 const ForcedBlocks fb(n, a.S, a.L);
-                keep = fb.forced(ub.y);
+                keep = fb.forced(blk);
                 if (!keep) {
-                    wait_count(a, m, slot_counter(a, ub.x), a.nf + 1);
-                    const float *mt = a.ws_mt + (size_t)ub.x * kMaxG;
-                    for (int i = 0; i < a.G && !keep; i++)
-                        keep = bmax[(li - c0) * kMaxG + i] >= __ldcg(mt + i) - a.delta;
+                    wait_count(a, m, slot_counter(a, u), a.nf + 1);
+                    // the unit's eight thresholds at once (heads past G are not compared)
+                    const float4 *mt = reinterpret_cast<const float4 *>(a.ws_mt + (size_t)u * kMaxG);
+                    const float4 t0 = __ldcg(mt), t1 = __ldcg(mt + 1);
+                    const float th[kMaxG] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+#pragma unroll
+                    for (int i = 0; i < kMaxG; i++)
+                        keep |= i < a.G && bmax[(li - c0) * kMaxG + i] >= th[i] - a.delta;
                 }
             }
             if (a.keep_mask && ub.x >= 0)
-                a.keep_mask[(size_t)ub.x * a.max_blocks + ub.y] = keep ? 1 : 0;
+                a.keep_mask[ub.x] = keep ? 1 : 0;  // u * max_blocks + block
             else if (a.keep_mask) {  // a block not loaded: its unit is located again
                 const int2 u2 = sp_locate(a, x + li);
                 a.keep_mask[(size_t)u2.x * a.max_blocks + u2.y] = 0;
@@ -282,7 +357,10 @@ __device__ __forceinline__ void sp_vote_chunk(const DecodeArgs &a, SpMisc *m, ui
             if (w0 + lane < nwin) wcnt[w0 + lane] = run + inc - c;
             run += __shfl_sync(0xffffffffu, inc, 31);
         }
-        if (lane == 0) m->kept = run;
+        if (lane == 0) {
+            m->kept = run;
+            m->scan_next = 0;  // every scanner has left the chunk's loop
+        }
     }
     named_barrier_sync(kSpComputeBar, 32 * kSpWarps);
 #pragma unroll
@@ -294,17 +372,17 @@ __device__ __forceinline__ void sp_vote_chunk(const DecodeArgs &a, SpMisc *m, ui
             const int li = c0 + 32 * w + lane;
             const int2 ub = bunit[li - c0];
             a.ws_kept[x + wcnt[w] + __popc(bits & ((1u << lane) - 1u))] = ub;
-            atomicAdd(a.ws_ukept + (size_t)ubuf * a.B * a.Hkv + ub.x, 1);
+            atomicAdd(a.ws_ukept + (size_t)ubuf * a.B * a.Hkv + ub.x / a.max_blocks, 1);
         }
     }
-    named_barrier_sync(kSpComputeBar, 32 * kSpWarps);  // the chunk's buffers may be refilled
+    named_barrier_sync(kSpScanBar, kSpScanners);  // the chunk's buffers may be refilled
 }
 
 // ------------------------------------------------------------------------------------------
 // Phase B
 // ------------------------------------------------------------------------------------------
-// Kept block k of all CTAs' lists (k < K): its (unit, block). pref[c] = kept blocks of the CTAs
-// before c; CTA c's list starts at its range start.
+// Kept block k of all CTAs' lists (k < K): its (u * max_blocks + block, page). pref[c] = kept
+// blocks of the CTAs before c; CTA c's list starts at its range start.
 __device__ __forceinline__ int2 sp_kept(const DecodeArgs &a, const SpMisc *m, const SpRange &r,
                                         int k) {
     int lo = 0, hi = r.ncta - 1;  // the last CTA c with pref[c] <= k
@@ -316,43 +394,56 @@ __device__ __forceinline__ int2 sp_kept(const DecodeArgs &a, const SpMisc *m, co
     const int xs = (int)((int64_t)r.T * lo / r.ncta);
     const int2 e = a.ws_kept[xs + (k - m->pref[lo])];
     // every entry was written this call unless a wait ran out somewhere: checked all the same
-    return e.x >= 0 && e.x < a.B * a.Hkv && e.y >= 0 && e.y < a.max_blocks ? e : make_int2(0, 0);
+    return e.x >= 0 && e.x < a.B * a.Hkv * a.max_blocks && e.y >= 0 && e.y < a.P ? e
+                                                                               : make_int2(0, 0);
 }
 
 // Producer warp: kept block j of the share [s0, s1) goes to slot j % kSpRing once it is free
-// (its previous block refined); lane k of a batch takes block j0 + k.
+// (its previous block refined). The lanes look up 32 kept blocks at once (entry and page), the
+// next 32 while the current ones are armed; lane k of a batch of kSpRing arms block j0 + k.
+__device__ __forceinline__ int2 sp_ring_lookup(const DecodeArgs &a, const SpMisc *m,
+                                               const SpRange &r, int k) {
+    const int2 e = sp_kept(a, m, r, k);
+    return make_int2((e.x / a.max_blocks) % a.Hkv, e.y);  // (KV head, page)
+}
+
 __device__ __forceinline__ void sp_ring_issuer(const SpParams &prm, SpMisc *m, uint8_t *base,
                                                const SpRange &r, int s0, int s1, int lane) {
     const DecodeArgs &a = prm.a;
     const int len = s1 - s0;
-    int last = -1;  // this lane's (slot's) last armed use
-    for (int j0 = 0; j0 < len; j0 += kSpRing) {
-        const int j = j0 + lane;
-        if (lane < kSpRing && j < len && !aborted(m)) {
-            const int slot = j % kSpRing, use = j / kSpRing;
-            const int2 ub = sp_kept(a, m, r, s0 + j);
-            const int b = ub.x / a.Hkv, h = ub.x - b * a.Hkv;
-            int page = a.block_table[(size_t)b * a.max_blocks + ub.y];  // in range: kept
-            if (page < 0 || page >= a.P) {  // only after a wait ran out
-                raise_error(a.err, FFD_ERRBIT_BOUNDS);
-                page = 0;
+    int2 cur = lane < len ? sp_ring_lookup(a, m, r, s0 + lane) : make_int2(0, 0);
+    for (int jb = 0; jb < len; jb += 32) {
+        const int2 nxt = jb + 32 + lane < len ? sp_ring_lookup(a, m, r, s0 + jb + 32 + lane)
+                                              : make_int2(0, 0);
+        const int je = len < jb + 32 ? len : jb + 32;
+        for (int j0 = jb; j0 < je; j0 += kSpRing) {
+            const int j = j0 + lane;
+            const int src = (j - jb) & 31;
+            const int h = __shfl_sync(0xffffffffu, cur.x, src);
+            const int page = __shfl_sync(0xffffffffu, cur.y, src);
+            if (lane < kSpRing && j < je) {
+                const int slot = j % kSpRing, use = j / kSpRing;
+                if (use > 0) wait_bar(a, m, &m->b_empty[slot], (use - 1) & 1);
+                if (!aborted(m)) {  // after an abort nothing more is armed
+                    const size_t tile = (size_t)page * a.Hkv + h;
+                    uint8_t *d = base + slot * kSpSlotBytes;
+                    mbar_arrive_expect_tx(&m->b_full[slot], kSpSlotTx);
+                    tma_load_1d(d, a.resid + tile * kResidRec, kResidRec, &m->b_full[slot]);
+                    tma_load_3d(d + kSpSlotV, &prm.tm_v, 0, (int)(tile * kPage), 0,
+                                &m->b_full[slot]);
+                    tma_load_1d(d + kSpSlotThumb, a.thumb + tile * kThumbRec, kThumbRec,
+                                &m->b_full[slot]);
+                    m->armed_b[slot] = use + 1;
+                }
             }
-            if (use > 0) wait_bar(a, m, &m->b_empty[slot], (use - 1) & 1);
-            if (!aborted(m)) {
-                const size_t tile = (size_t)page * a.Hkv + h;
-                uint8_t *d = base + slot * kSpSlotBytes;
-                mbar_arrive_expect_tx(&m->b_full[slot], kSpSlotTx);
-                tma_load_1d(d, a.resid + tile * kResidRec, kResidRec, &m->b_full[slot]);
-                tma_load_3d(d + kSpSlotV, &prm.tm_v, 0, (int)(tile * kPage), 0, &m->b_full[slot]);
-                tma_load_1d(d + kSpSlotThumb, a.thumb + tile * kThumbRec, kThumbRec,
-                            &m->b_full[slot]);
-                last = j;
-            }
+            __syncwarp();
         }
-        __syncwarp();
+        cur = nxt;
     }
-    // leave no copy in flight: the last copy into this lane's slot
-    if (last >= 0) drain_bar(a, &m->b_full[lane], (last / kSpRing) & 1);
+    // leave no copy in flight: the last armed use of every slot
+    __syncwarp();
+    for (int slot = lane; slot < kSpRing; slot += 32)
+        if (m->armed_b[slot] > 0) drain_bar(a, &m->b_full[slot], (m->armed_b[slot] - 1) & 1);
 }
 
 // Kept blocks before unit u in the kept order (the units' counts, summed by refine group grp).
@@ -370,41 +461,73 @@ __device__ __forceinline__ int sp_unit_first(const DecodeArgs &a, SpMisc *m, con
 }
 
 // Refine group grp: walks the share's kept blocks in order (every group sees every unit change,
-// so each writes a record for each unit of the share) and refines blocks j % kSpGroups == grp.
+// and every CTA-wide barrier below) and refines blocks j = grp (mod kSpGroups) from ring slot
+// j % kSpRing. At the end of a unit's segment the three groups' softmax states go to shared memory
+// and group 0 combines them into the CTA's one record of the unit (records, tickets and merge
+// reads are a third of one record per group), then takes the unit's ticket and merges when last.
+// After an abort a group stops computing but keeps walking, so that the barriers still match.
+__device__ __forceinline__ void sp_combine(const DecodeArgs &a, const float *rec, float *dst,
+                                           int tid) {
+    for (int i = 0; i < a.G; i++) {
+        const float *r0 = rec + (size_t)i * kPartStride;
+        const float *r1 = r0 + kMaxG * kPartStride, *r2 = r1 + kMaxG * kPartStride;
+        const float m0 = r0[kD], m1 = r1[kD], m2 = r2[kD];
+        const float M = fmaxf(m0, fmaxf(m1, m2));  // finite: references never go to -inf
+        const float f0 = exp2f((m0 - M) * kLog2e), f1 = exp2f((m1 - M) * kLog2e);
+        const float f2 = exp2f((m2 - M) * kLog2e);
+        float *d = dst + (size_t)i * kPartStride;
+        d[tid] = fmaf(f2, r2[tid], fmaf(f1, r1[tid], f0 * r0[tid]));
+        if (tid == 0) {
+            d[kD] = M;
+            d[kD + 1] = fmaf(f2, r2[kD + 1], fmaf(f1, r1[kD + 1], f0 * r0[kD + 1]));
+        }
+    }
+}
+
 __device__ __forceinline__ void sp_refiner(const DecodeArgs &a, SpMisc *m, uint8_t *base,
                                            const SpRange &r, int K, int nctab, int s0, int s1,
                                            const int *ukept, int grp, int mt, int lane) {
     const int g = lane >> 2, tig = lane & 3;
     const int r0 = 16 * mt + g, r1 = r0 + 8;
     const int cta = blockIdx.x;
+    float *comb = reinterpret_cast<float *>(base + kSpOffComb);
     ThumbOps Q;
     ResidOps QR;
     RefineState R;
     int cu = -1, seg0 = 0, n = 0, pb = 0;
+    bool dead = false;  // group-uniform: stopped computing after an abort
     auto end_segment = [&](int k_end) {
-        const int b = cu / a.Hkv;
-        write_record(a, m, R, unit_record<kSpGroups>(a, cu, cta, grp), grp, mt, lane);
-        Sub s;
-        s.b = b;
-        s.h = cu - b * a.Hkv;
-        s.cnt = k_end - seg0;
-        s.x0 = seg0;
-        const int first = sp_unit_first(a, m, ukept, cu, grp, mt, lane);
-        s.j0 = seg0 - first;
-        s.nblk = __ldcg(ukept + cu);
-        s.first = s.last = true;
-        finish_unit<SpMisc, kSpGroups>(a, m, s, cta, nctab, K, grp, mt, lane);
+        if (!dead) write_record(a, m, R, comb + grp * kMaxG * kPartStride, grp, mt, lane);
+        // every group's record is in; one decision for the whole CTA
+        const bool live = !named_barrier_or(kSpComputeBar, 32 * kSpWarps, aborted(m));
+        if (grp == 0 && live)
+            sp_combine(a, comb, unit_record<1>(a, cu, cta, 0), 32 * mt + lane);
+        named_barrier_sync(kSpComputeBar, 32 * kSpWarps);  // the shared records are free again
+        if (grp == 0 && live) {
+            const int b = cu / a.Hkv;
+            Sub s;
+            s.b = b;
+            s.h = cu - b * a.Hkv;
+            s.cnt = k_end - seg0;
+            s.x0 = seg0;
+            const int first = sp_unit_first(a, m, ukept, cu, grp, mt, lane);
+            s.j0 = seg0 - first;
+            s.nblk = __ldcg(ukept + cu);
+            s.first = s.last = true;
+            finish_unit<SpMisc, 1>(a, m, s, cta, nctab, K, grp, mt, lane);
+        }
     };
     for (int j0 = 0; j0 < s1 - s0; j0 += 32) {
         // the (unit, block) of 32 consecutive kept blocks, one per lane
         const int jl = j0 + lane < s1 - s0 ? j0 + lane : s1 - s0 - 1;
         const int2 mine = sp_kept(a, m, r, s0 + jl);
+        const int mu = mine.x / a.max_blocks, mblk = mine.x - mu * a.max_blocks;
         const int cnt = s1 - s0 - j0 < 32 ? s1 - s0 - j0 : 32;
         for (int i = 0; i < cnt; i++) {
             const int j = j0 + i;
-            const int u = __shfl_sync(0xffffffffu, mine.x, i);
-            const int blk = __shfl_sync(0xffffffffu, mine.y, i);
-            if (u != cu) {  // group-uniform
+            const int u = __shfl_sync(0xffffffffu, mu, i);
+            const int blk = __shfl_sync(0xffffffffu, mblk, i);
+            if (u != cu) {  // CTA-uniform
                 if (cu >= 0) end_segment(s0 + j);
                 cu = u;
                 seg0 = s0 + j;
@@ -422,11 +545,12 @@ __device__ __forceinline__ void sp_refiner(const DecodeArgs &a, SpMisc *m, uint8
 #pragma unroll
                 for (int q = 0; q < 2; q++) R.o[q][0] = R.o[q][1] = R.o[q][2] = R.o[q][3] = 0.0f;
             }
-            if (j % kSpGroups != grp) continue;
+            if (j % kSpGroups != grp || dead) continue;
             const int slot = j % kSpRing;
             wait_bar(a, m, &m->b_full[slot], (j / kSpRing) & 1);
             // a slot that never filled (a wait ran out) must not split the group's barriers
-            if (named_barrier_or(2 + grp, 128, aborted(m))) return;
+            dead = named_barrier_or(2 + grp, 128, aborted(m));
+            if (dead) continue;
             uint8_t *d = base + slot * kSpSlotBytes;
             const int rows = n - blk * kPage < kPage ? n - blk * kPage : kPage;
             if (rows < kPage) {  // the sequence's partial last block: V rows past it are zeroed
@@ -516,14 +640,17 @@ __global__ void __launch_bounds__(kSpThreads, 1) sparse_kernel(const __grid_cons
     if (threadIdx.x == 0) {
         m->aborted = 0;
         m->kept = 0;
+        m->scan_next = 0;
         for (int i = 0; i < kSpStages; i++) {
             mbar_init(&m->a_full[i], 1);
             mbar_init(&m->a_empty[i], 1);  // the compute warp that scored the block
-            m->desc[i] = SpDesc{-1, 0, 0, 1};  // read as "not loaded" if a wait runs out first
+            m->desc[i] = SpDesc{-1, 0, 0, -1};  // read as "not loaded" if a wait runs out first
+            m->armed_a[i] = 0;
         }
         for (int i = 0; i < kSpRing; i++) {
             mbar_init(&m->b_full[i], 1);
             mbar_init(&m->b_empty[i], 4);  // the refine group that took the block
+            m->armed_b[i] = 0;
         }
         fence_barrier_init();
     }
@@ -536,10 +663,25 @@ __global__ void __launch_bounds__(kSpThreads, 1) sparse_kernel(const __grid_cons
     const SpRange r = sp_range(a);
 
     if (warp < 4) {
-        regs_decrease<kSpProducerRegs>();
+        // ---- phase A: stage the range's thumbnails (warp 0); stage 1 (warps 1-3)
+        if (warp == 0) {
+            if (lane == 0) prefetch_tensormap(&prm.tm_v);
+            if (blockIdx.x < r.ncta) sp_stage_issuer(a, m, base, r, lane);
+        } else {
+            pseudo_max_warp(a, blockIdx.x * 3 + warp - 1, gridDim.x * 3, lane);
+            // then scan with the compute warps (the vote is theirs)
+            ThumbOps Q;
+            float qsr[2][4];
+            int qu = -1;
+            for (int c0 = 0; c0 < r.x1 - r.x; c0 += kSpChunk) {
+                const int c1 = r.x1 - r.x < c0 + kSpChunk ? r.x1 - r.x : c0 + kSpChunk;
+                sp_scan_chunk(a, m, base, c0, c1, lane, Q, qsr, qu);
+                named_barrier_sync(kSpScanBar, kSpScanners);  // the chunk's maxima are in
+                named_barrier_sync(kSpScanBar, kSpScanners);  // the chunk's votes are in
+            }
+        }
+        regs_decrease<kSpProducerRegs>();  // the whole warpgroup
         if (warp != 0) return;
-        // ---- phase A: stage the range's thumbnails
-        if (blockIdx.x < r.ncta) sp_stage_issuer(a, m, base, r, lane);
         named_barrier_sync(kSpActiveBar, kSpActive);
         if (lane == 0) sp_grid_barrier(a, m);
         __syncwarp();
@@ -554,32 +696,36 @@ __global__ void __launch_bounds__(kSpThreads, 1) sparse_kernel(const __grid_cons
             a.ws_ukept[(size_t)(ubuf ^ 1) * units + u] = 0;
         sp_empty_units(a, ukept, lane);
     } else {
-        regs_increase<kSpComputeRegs>();
         const int cw = warp - 4, grp = cw >> 2, mt = cw & 3;
-        // ---- phase A: stage 1, then score and vote the range chunk by chunk
-        pseudo_max_slots<kSpGroups, SpMisc, true>(a, m, blockIdx.x, gridDim.x, grp, mt, lane);
+        // ---- phase A: score and vote the range chunk by chunk
         ThumbOps Q;
+        float qsr[2][4];
         int qu = -1;
         for (int c0 = 0; c0 < r.x1 - r.x; c0 += kSpChunk) {
             const int c1 = r.x1 - r.x < c0 + kSpChunk ? r.x1 - r.x : c0 + kSpChunk;
-            sp_scan_chunk(a, m, base, c0, c1, cw, lane, Q, qu);
-            named_barrier_sync(kSpComputeBar, 32 * kSpWarps);  // the chunk's maxima are in
+            sp_scan_chunk(a, m, base, c0, c1, lane, Q, qsr, qu);
+            named_barrier_sync(kSpScanBar, kSpScanners);  // the chunk's maxima are in
             sp_vote_chunk(a, m, base, r.x, c0, c1, cw, lane, ubuf);
         }
         if (cw == 0 && lane == 0 && blockIdx.x < r.ncta) a.ws_keptn[blockIdx.x] = m->kept;
         named_barrier_sync(kSpActiveBar, kSpActive);
+        regs_increase<kSpComputeRegs>();  // once the producer warpgroup has released its share
         named_barrier_sync(kSpActiveBar, kSpActive);  // the grid barrier is passed
-        if (cw == 0) {  // prefix of the CTAs' kept counts
+        if (cw == 0) {  // prefix of the CTAs' kept counts (all loads first)
+            int v[kSpMaxCtas / 32];
+#pragma unroll
+            for (int k = 0; k < kSpMaxCtas / 32; k++)
+                v[k] = 32 * k + lane < r.ncta ? __ldcg(a.ws_keptn + 32 * k + lane) : 0;
             int run = 0;
-            for (int c0 = 0; c0 < r.ncta; c0 += 32) {
-                const int v = c0 + lane < r.ncta ? __ldcg(a.ws_keptn + c0 + lane) : 0;
-                int inc = v;
+#pragma unroll
+            for (int k = 0; k < kSpMaxCtas / 32; k++) {
+                int inc = v[k];
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const int y = __shfl_up_sync(0xffffffffu, inc, o);
                     if (lane >= o) inc += y;
                 }
-                if (c0 + lane < r.ncta) m->pref[c0 + lane] = run + inc - v;
+                if (32 * k + lane < r.ncta) m->pref[32 * k + lane] = run + inc - v[k];
                 run += __shfl_sync(0xffffffffu, inc, 31);
             }
             if (lane == 0) m->pref[r.ncta] = run;

@@ -83,6 +83,8 @@ def test_workspace_sizes(lib):
     (dict(sink=-1), 1),
     (dict(num_splits=-2), 1),
     (dict(sm_scale=math.inf), 1),
+    (dict(sm_scale=0.0), 1),
+    (dict(sm_scale=-0.088), 1),
     (dict(wait_limit_us=-1), 1),                    # a negative wait bound
 ])
 def test_decode_rejects_bad_params(lib, kw, status):
