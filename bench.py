@@ -40,10 +40,21 @@ THUMB_B = 48          # bytes per token and KV head: 32 code bytes + 4 fp16 scal
 REFINE_B = 136 + 256  # int8 residual + 4 fp16 residual scales + bf16 V
 DENSE_B = 512         # bf16 K + V
 LAUNCHES_PER_DECODE = 1  # one cooperative kernel: stage 1, stages 2/3, split merge
-PROFILE = os.path.join(ROOT, "profiles", "ffd_main_kernel_qwen2.5-7b_128k.txt")
+# the committed ncu summary of each schedule's kernel, and the sources its hash covers
+PROFILES = {0: os.path.join(ROOT, "profiles", "ffd_main_kernel_qwen2.5-7b_128k.txt"),
+            1: os.path.join(ROOT, "profiles", "ffd_sparse_kernel_qwen2.5-7b_128k_peaked.txt")}
 
 
 SCHEDULES = {"fused": 0, "scan-refine": 1}  # FFD_SCHEDULE_FUSED, FFD_SCHEDULE_SCAN_REFINE
+SCHEDULE_NAMES = {v: k for k, v in SCHEDULES.items()}
+
+
+def pick_schedule(a, ffd, total_blocks: int, kept_blocks: int) -> int:
+    """--schedule auto: the library's suggestion from the kept blocks of a first (untimed) step,
+    as a serving loop would take it from the previous step; else the named schedule."""
+    if a.schedule == "auto":
+        return ffd.ffd_suggest_schedule(total_blocks, kept_blocks)
+    return SCHEDULES[a.schedule]
 
 
 def log(*a):
@@ -61,8 +72,9 @@ def args_parse(argv=None):
     ap.add_argument("--delta", type=float, default=None)
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the peaked-attention variant and the CPU baseline")
-    ap.add_argument("--schedule", choices=["fused", "scan-refine"], default="fused",
-                    help="order of the decode step's work (FFD_SCHEDULE_*; same results)")
+    ap.add_argument("--schedule", choices=["auto", "fused", "scan-refine"], default="auto",
+                    help="order of the decode step's work (FFD_SCHEDULE_*; same results); auto: "
+                         "ffd_suggest_schedule from a first untimed step's keep mask")
     ap.add_argument("--peaked", action="store_true",
                     help="measure the peaked-attention inputs (sink shift and needles in score "
                          "units) as the primary workload")
@@ -336,28 +348,35 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0}, "fallback"
 
 
-MAIN_KERNEL_SOURCES = ("decode.cu", "scan.cuh", "splitkv.cuh", "common.cuh", "ptx.cuh")
+MAIN_KERNEL_SOURCES = {
+    0: ("decode.cu", "stage1.cuh", "scan.cuh", "splitkv.cuh", "common.cuh", "ptx.cuh"),
+    1: ("sparse.cu", "stage1.cuh", "scan.cuh", "splitkv.cuh", "common.cuh", "ptx.cuh")}
 
 
-def main_kernel_sha256():
-    """SHA-256 over the sources the main kernel is compiled from, in a fixed order."""
+def main_kernel_sha256(schedule: int = 0):
+    """SHA-256 over the sources a schedule's kernel is compiled from, in a fixed order."""
     h = hashlib.sha256()
-    for name in MAIN_KERNEL_SOURCES:
+    for name in MAIN_KERNEL_SOURCES[schedule]:
         with open(os.path.join(ROOT, "sparse_quantized_attention_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def profile_traffic():
-    """DRAM bytes per launch of the main kernel from the committed ncu summary, if the kernel
-    source has not changed since the counters were taken (else None)."""
+def profile_traffic(schedule: int = 0, workload: str | None = None):
+    # workload: words that the summary's workload line must contain (name and input kind)
+    """DRAM bytes per launch of the schedule's kernel from the committed ncu summary, if the
+    kernel source has not changed since the counters were taken and the summary is of this
+    workload (else None)."""
     try:
-        text = open(PROFILE).read()
+        text = open(PROFILES[schedule]).read()
     except OSError:
         return None, None
     fields = dict(line.split(":", 1) for line in text.splitlines() if ":" in line)
+    have_wl = fields.get("workload", "")
+    if workload is not None and not all(part in have_wl for part in workload.split()):
+        return None, "the committed capture is of another workload"
     want = fields.get("source_sha256", "").strip()
-    have = main_kernel_sha256()
+    have = main_kernel_sha256(schedule)
     if want != have:
         return None, "kernel changed since the ncu capture"
     try:
@@ -417,8 +436,7 @@ def run_ours(a, rank, world, local):
     quant_bytes = P * Hkv * 64 * (256 + 32 + 8 + 8 + 128 + 8)
 
     params = ffd.make_params(w.batch, w.num_q_heads, w.num_kv_heads, P, inp.max_blocks,
-                             sink=w.sink, local=w.local, delta=delta, sm_scale=sm,
-                             schedule=SCHEDULES[a.schedule])
+                             sink=w.sink, local=w.local, delta=delta, sm_scale=sm)
     ws = ffd.alloc_workspace(params, device=dev)
     out = torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.float32, device=dev)
     mask = torch.zeros((w.batch, w.num_kv_heads, inp.max_blocks), dtype=torch.uint8, device=dev)
@@ -435,6 +453,7 @@ def run_ours(a, rank, world, local):
     nb_total = int(sum((int(n) + 63) // 64 for n in inp.seq_lens)) * w.num_kv_heads
     kept_blocks = int(keep.sum())
     by = step_bytes(w, inp.seq_lens, inp.max_blocks, kept)
+    params.schedule = pick_schedule(a, ffd, nb_total, kept_blocks)
 
     # timed region: W warm-up steps, then exactly K steps between barriers + syncs
     clocks = ClockSampler(local, pci_bus_id(torch, local))
@@ -574,7 +593,8 @@ def run_ours(a, rank, world, local):
     # give the kernel's average launch duration (the launch gaps included)
     main_avg = total_ms / a.steps
     achieved = by["main_kernel"] / (main_avg * 1e-3) / 1e9
-    traffic, traffic_note = profile_traffic()
+    traffic, traffic_note = profile_traffic(params.schedule,
+                                            w.name + (" peaked" if a.peaked else " literal"))
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -584,11 +604,14 @@ def run_ours(a, rank, world, local):
                    "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "context": w.seq_len, "sink": w.sink,
                    "local": w.local, "delta": delta, "page": 64, "head_dim": 128,
+                   "schedule": SCHEDULE_NAMES[params.schedule],
                    "l2": f"inputs larger than L2 ({by['step'] / 1e6:.0f} MB read per step vs "
                          f"{L2_BYTES / 1e6:.0f} MB L2), no flush",
                    "parallelism": "single GPU" if world == 1 else
                    f"replicas x{world} (own sequences per rank)"},
-        "roofline": {"bound": "hbm", "kernel": "ffd main (stages 1-3, merge)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "ffd " + {0: "fused", 1: "scan-then-refine"}[params.schedule] +
+                               " (stages 1-3, merge)",
                      "achieved": round(achieved, 1), "peak": peaks.get("hbm_gbs"),
                      "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
@@ -655,21 +678,27 @@ def peaked_variant(a, w, delta, dev, ffd, torch, upload, dense_ms):
     keep = mask.cpu().numpy()
     kept = kept_tokens(inp.seq_lens, keep)
     by = step_bytes(w, inp.seq_lens, inp.max_blocks, kept)
-    stream = torch.cuda.current_stream(dev)
-    for _ in range(a.warmup):
-        ffd.ffd_decode_attention(params, d["q"], qc, d["v"], d["seq_lens"], d["block_table"],
-                                 out, ws)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-    psteps = max(3, min(a.steps, 500))
-    e0.record(stream)
-    for _ in range(psteps):
-        ffd.ffd_decode_attention(params, d["q"], qc, d["v"], d["seq_lens"], d["block_table"],
-                                 out, ws)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1) / psteps
     nb_total = int(sum((int(n) + 63) // 64 for n in inp.seq_lens)) * w.num_kv_heads
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    psteps = max(3, min(a.steps, 500))
+    by_schedule = {}
+    for sched in (0, 1):  # both schedules, then the chosen one is the variant's figure
+        params.schedule = sched
+        for _ in range(a.warmup):
+            ffd.ffd_decode_attention(params, d["q"], qc, d["v"], d["seq_lens"], d["block_table"],
+                                     out, ws)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(psteps):
+            ffd.ffd_decode_attention(params, d["q"], qc, d["v"], d["seq_lens"], d["block_table"],
+                                     out, ws)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        by_schedule[SCHEDULE_NAMES[sched]] = e0.elapsed_time(e1) / psteps
+    chosen = pick_schedule(a, ffd, nb_total, int(keep.sum()))
+    params.schedule = chosen
+    ms = by_schedule[SCHEDULE_NAMES[chosen]]
 
     def timed(fn, reps=20):
         for _ in range(3):
@@ -690,9 +719,11 @@ def peaked_variant(a, w, delta, dev, ffd, torch, upload, dense_ms):
         mk = torch.zeros_like(mask)
         ffd.ffd_decode_attention(pd, d["q"], qc, d["v"], d["seq_lens"], d["block_table"], out,
                                  ws, keep_mask=mk)
+        pd.schedule = pick_schedule(a, ffd, nb_total, int(mk.sum()))
         us = timed(lambda: ffd.ffd_decode_attention(pd, d["q"], qc, d["v"], d["seq_lens"],
                                                     d["block_table"], out, ws))
         sweep.append({"delta": dl if math.isfinite(dl) else "inf", "us": round(us, 2),
+                      "schedule": SCHEDULE_NAMES[pd.schedule],
                       "sparsity": round(1 - int(mk.sum()) / nb_total, 4)})
     # the comparison selectors on the same thumbnails: Top-k at the budget Top-delta used (its
     # mean kept non-forced blocks per unit), Top-p at p = 0.9 and 0.99; select + attention
@@ -741,6 +772,8 @@ def peaked_variant(a, w, delta, dev, ffd, torch, upload, dense_ms):
         raise RuntimeError("device error in the ART comparison")
     del d, qc
     return {"signal_scale": round(ffd_synth.peaked_scale(), 4), "us_per_step": round(ms * 1e3, 2),
+            "schedule": SCHEDULE_NAMES[chosen],
+            "us_per_step_by_schedule": {k: round(v * 1e3, 2) for k, v in by_schedule.items()},
             "delta_sweep": sweep, "selectors": selectors, "art": art,
             "needed_bytes_per_step": by["step"], "gbs": round(by["step"] / (ms * 1e-3) / 1e9, 1),
             "sparsity": round(1 - int(keep.sum()) / nb_total, 4),
@@ -913,9 +946,15 @@ def run_sweep(a):
                 keep = mask.cpu().numpy()
                 kept = kept_tokens(inp.seq_lens, keep)
                 by = step_bytes(w, inp.seq_lens, inp.max_blocks, kept)
-                us = timed(lambda: ffd.ffd_decode_attention(p, d["q"], qc, d["v"], d["sl"],
-                                                            d["bt"], out, ws))
                 nb_total = int(sum((int(n) + 63) // 64 for n in inp.seq_lens)) * Hkv
+                us_by = {}
+                for sched in (0, 1):
+                    p.schedule = sched
+                    us_by[SCHEDULE_NAMES[sched]] = timed(
+                        lambda: ffd.ffd_decode_attention(p, d["q"], qc, d["v"], d["sl"], d["bt"],
+                                                         out, ws))
+                p.schedule = pick_schedule(a, ffd, nb_total, int(keep.sum()))
+                us = us_by[SCHEDULE_NAMES[p.schedule]]
                 # ART over the same mask with no termination (every kept block, one CTA per
                 # unit walking its blocks in sequence): the unit that keeps the most sets the time
                 aws = ffd.alloc_art_workspace(p, device=dev)
@@ -930,6 +969,9 @@ def run_sweep(a):
                 row = {"workload": w.name, "inputs": label, "delta": delta,
                        "batch": w.batch, "heads": f"{w.num_q_heads}/{Hkv}",
                        "context": int(np.max(inp.seq_lens)), "us_per_step": round(us, 2),
+                       "schedule": SCHEDULE_NAMES[p.schedule],
+                       "us_fused": round(us_by["fused"], 2),
+                       "us_scan_refine": round(us_by["scan-refine"], 2),
                        "kv_tokens_per_s": round(float(np.sum(inp.seq_lens)) / (us * 1e-6), 1),
                        "sparsity": round(1 - int(keep.sum()) / max(1, nb_total), 4),
                        "needed_mb": round(by["step"] / 1e6, 1), "gbs": round(gbs, 1),
@@ -944,13 +986,15 @@ def run_sweep(a):
             del d, qc
             torch.cuda.empty_cache()
     with open(a.sweep, "w") as f:
-        f.write("| workload | inputs | delta | context | us/step | KV tokens/s | sparsity | "
+        f.write("| workload | inputs | delta | context | us/step | schedule | fused us | "
+                "scan-refine us | KV tokens/s | sparsity | "
                 "needed MB | GB/s | of measured copy peak | of 8 TB/s | dense us | speedup | "
                 "ART us (all kept) | ART blocks (max unit) | ART us/block |\n")
-        f.write("|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|\n")
+        f.write("|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|---|\n")
         for r in rows:
             f.write(f"| {r['workload']} | {r['inputs']} | {r['delta']:g} | {r['context']} | "
-                    f"{r['us_per_step']} | {r['kv_tokens_per_s']:.3g} | {r['sparsity']} | "
+                    f"{r['us_per_step']} | {r['schedule']} | {r['us_fused']} | "
+                    f"{r['us_scan_refine']} | {r['kv_tokens_per_s']:.3g} | {r['sparsity']} | "
                     f"{r['needed_mb']} | {r['gbs']} | {r['frac_of_measured']} | "
                     f"{r['frac_of_8tbs']} | {r['dense_us']} | {r['speedup_vs_dense']} | "
                     f"{r['art_us']} | {r['art_max_blocks']} | {r['art_us_per_block']} |\n")

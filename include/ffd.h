@@ -119,6 +119,13 @@ typedef struct {
 #define FFD_SCHEDULE_FUSED 0
 #define FFD_SCHEDULE_SCAN_REFINE 1
 
+/* The schedule this library suggests for a step over total_blocks blocks (sum over sequences and
+ * KV heads of ceil(n / 64)) when the previous step kept kept_blocks of them (the count of ones in
+ * its keep_mask): FFD_SCHEDULE_SCAN_REFINE when fewer than half the blocks were kept and there are
+ * at least 64 blocks per SM of the current device, else FFD_SCHEDULE_FUSED (also for arguments
+ * out of range). Host only; reads the device's SM count once. */
+int32_t ffd_suggest_schedule(int64_t total_blocks, int64_t kept_blocks);
+
 /* Human-readable name of a status. Never NULL. */
 const char *ffd_status_string(ffd_status status);
 

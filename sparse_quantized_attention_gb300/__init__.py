@@ -10,7 +10,9 @@ from .ffd import (CacheDesc, DecodeParams, FFDError, QuantizedCache, alloc_quant
                   ffd_set_profile_events, ffd_status_string, ffd_version, lib, library_path,
                   make_params, SELECT_TOPK, SELECT_TOPP, alloc_select_workspace,
                   ffd_select_workspace_size, ffd_select_blocks, ffd_decode_attention_masked,
-                  ffd_art_workspace_size, alloc_art_workspace, ffd_art_attention)
+                  ffd_art_workspace_size, alloc_art_workspace, ffd_art_attention,
+                  ffd_suggest_schedule, ffd_last_cuda_error, SCHEDULE_FUSED,
+                  SCHEDULE_SCAN_REFINE)
 
 __all__ = ["CacheDesc", "DecodeParams", "FFDError", "QuantizedCache", "alloc_quantized_cache",
            "alloc_workspace", "ffd_append_kv", "ffd_decode_attention", "ffd_decode_attention_static",
@@ -20,4 +22,5 @@ __all__ = ["CacheDesc", "DecodeParams", "FFDError", "QuantizedCache", "alloc_qua
            "lib", "library_path", "make_params", "SELECT_TOPK", "SELECT_TOPP",
            "alloc_select_workspace", "ffd_select_workspace_size", "ffd_select_blocks",
            "ffd_decode_attention_masked", "ffd_art_workspace_size", "alloc_art_workspace",
-           "ffd_art_attention"]
+           "ffd_art_attention", "ffd_suggest_schedule", "ffd_last_cuda_error", "SCHEDULE_FUSED",
+           "SCHEDULE_SCAN_REFINE"]

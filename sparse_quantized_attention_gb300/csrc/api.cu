@@ -202,6 +202,18 @@ extern "C" {
 
 int32_t ffd_last_cuda_error(void) { return g_last_cuda; }
 
+int32_t ffd_suggest_schedule(int64_t total_blocks, int64_t kept_blocks) {
+    if (total_blocks <= 0 || kept_blocks < 0 || kept_blocks > total_blocks)
+        return FFD_SCHEDULE_FUSED;
+    const int sms = current_sm_count();
+    if (sms <= 0) return FFD_SCHEDULE_FUSED;
+    // the scan-then-refine kernel reads the thumbnails once more than the fused one and gains by
+    // scanning with every warp and balancing the refinement: that pays once the kept blocks are a
+    // minority and every SM has a long enough scan
+    return 2 * kept_blocks < total_blocks && total_blocks >= 64LL * sms ? FFD_SCHEDULE_SCAN_REFINE
+                                                                      : FFD_SCHEDULE_FUSED;
+}
+
 const char *ffd_status_string(ffd_status s) {
     switch (s) {
         case FFD_OK: return "FFD_OK";

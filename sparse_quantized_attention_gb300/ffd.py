@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
             L.ffd_version.restype = ctypes.c_int32
             L.ffd_last_cuda_error.argtypes = []
             L.ffd_last_cuda_error.restype = ctypes.c_int32
+            L.ffd_suggest_schedule.argtypes = [ctypes.c_int64, ctypes.c_int64]
+            L.ffd_suggest_schedule.restype = ctypes.c_int32
             L.ffd_quantize_keys.argtypes = [ctypes.POINTER(CacheDesc), P, P, P, P,
                                             ctypes.c_int32, P, P]
             L.ffd_quantize_keys.restype = st
@@ -172,6 +174,11 @@ def ffd_status_string(status: int) -> str:
 
 def ffd_version() -> int:
     return int(lib().ffd_version())
+
+
+def ffd_suggest_schedule(total_blocks: int, kept_blocks: int) -> int:
+    """SCHEDULE_FUSED or SCHEDULE_SCAN_REFINE for a step like the previous one (host only)."""
+    return int(lib().ffd_suggest_schedule(int(total_blocks), int(kept_blocks)))
 
 
 def ffd_last_cuda_error() -> int:

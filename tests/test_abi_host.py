@@ -219,3 +219,9 @@ def test_art_rejects_bad_arguments(lib):
     bad = _params()
     bad.head_dim = 64
     assert art(p=bad) == 2 and ffd.ffd_art_workspace_size(bad) == 0
+
+
+def test_suggest_schedule_rejects_bad_counts(lib):
+    import sparse_quantized_attention_gb300 as ffd
+    for total, kept in ((0, 0), (-5, 1), (100, -1), (100, 101)):
+        assert ffd.ffd_suggest_schedule(total, kept) == ffd.SCHEDULE_FUSED

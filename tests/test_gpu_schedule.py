@@ -96,3 +96,15 @@ def test_scan_refine_reports_bad_block_table_entry():
     again = H.decode(inp, dev, qc, 5.0, schedule=SCAN_REFINE)
     np.testing.assert_array_equal(got["out"][0], again["out"][0])
     H.check_decode(inp, oracle.quantize(inp.k_bits), again, 5.0, what="clean rerun")
+
+
+@pytest.mark.gpu
+def test_suggest_schedule_on_this_device():
+    import torch
+    import sparse_quantized_attention_gb300 as ffd
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    total = 64 * sms
+    assert ffd.ffd_suggest_schedule(total, total // 2 - 1) == ffd.SCHEDULE_SCAN_REFINE
+    assert ffd.ffd_suggest_schedule(total, total // 2) == ffd.SCHEDULE_FUSED
+    assert ffd.ffd_suggest_schedule(total - 1, 0) == ffd.SCHEDULE_FUSED  # too few blocks per SM
+    assert ffd.ffd_suggest_schedule(1 << 40, 1 << 20) == ffd.SCHEDULE_SCAN_REFINE
