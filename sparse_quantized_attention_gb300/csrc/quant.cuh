@@ -1,7 +1,7 @@
-// quant.cuh -- the per-group quantiser shared by the whole-cache quantiser, the append kernel and
-// the decode kernel's fused append: one thread turns the 32 bf16 keys of one channel group of one
-// token into the group's 2-bit thumbnail codes, fp16 scale and zero, int8 residual codes and fp16
-// residual scale, and stores them into the (page, KV head) records.
+// quant.cuh -- the per-group quantiser shared by the whole-cache quantiser and the append kernel:
+// one thread turns the 32 bf16 keys of one channel group of one token into the group's 2-bit
+// thumbnail codes, fp16 scale and zero, int8 residual codes and fp16 residual scale, and stores
+// them into the (page, KV head) records.
 //
 // Source: "Faster Than Flash", Methodology §1 (2-bit thumbnails for score estimation, 8-bit
 // residuals that rebuild the keys close to fp16 precision); the format is the one include/ffd.h
@@ -14,7 +14,9 @@
 // code is formed from a correctly rounded reciprocal, with the clamp folded into a saturating
 // multiply, and rounded with one fused multiply-add, and where that fast quotient lies within a
 // few ulps of a rounding boundary (ties are frequent: keys, zeros and scales sit on the bf16 /
-// fp16 grids) the side of the boundary is decided exactly (boundary_step below).
+// fp16 grids) the side of the boundary is decided exactly (boundary_step below). The adds and
+// fused multiply-adds run two channels at a time on the packed fp32 pipe (f32x2: IEEE
+// round-to-nearest in each lane, so every lane's result is the scalar operation's).
 #pragma once
 
 #include "common.cuh"
@@ -46,19 +48,6 @@ __device__ __forceinline__ float boundary_step(float a, float b, float c, float 
     const float e = __fmaf_rn(-__fadd_rn(c, 0.5f * dir), b, a);
     if (e == 0.0f) return c_odd ? dir : 0.0f;
     return (e > 0.0f) == (d > 0.0f) ? dir : 0.0f;
-}
-
-// int8 code of r: clamp(rint(r / r_scale), -127, 127) in the low byte (two's complement), from
-// r254 = rcp(254 r_scale) (0 when r_scale is 0).
-__device__ __forceinline__ uint32_t code8_of(float r, float rscale, float r254) {
-    const float tp = __saturatef(__fmaf_rn(r, r254, 0.5f));
-    float cm = __fmaf_rn(tp, 254.0f, kMagicB);  // kMagicB + (code + 127)
-    const float d = __fmaf_rn(tp, 254.0f, -__fsub_rn(cm, kMagicB));
-    if (fabsf(d) > 0.5f - kNearB) {
-        const float code = __fsub_rn(cm, kMagic);  // exact
-        cm = __fadd_rn(cm, boundary_step(r, rscale, code, d, (__float_as_uint(cm) & 1u) != 0));
-    }
-    return __float_as_uint(cm);
 }
 
 // The quantised form of one group of 32 channels of one token.
@@ -102,38 +91,78 @@ __device__ __forceinline__ void group_params(const uint32_t (&u)[16], GroupCodes
     o.scale = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
 }
 
+// 2-bit code of a = x - zero: the number of rounding boundaries (k + 1/2) scale below a (b0, b1,
+// b2), exact in fp32. On these grids the IEEE quotient a / scale lies on the same side of k + 1/2
+// as a lies of (k + 1/2) scale, and equals k + 1/2 only when a does (see boundary_step), so a tie
+// at 1/2 or 5/2 rounds down and a tie at 3/2 rounds up (half to even). scale 0 gives code 0.
+__device__ __forceinline__ float code2_of(float a, float b0, float b1, float b2) {
+    return (a > b0 ? 1.0f : 0.0f) + (a >= b1 ? 1.0f : 0.0f) + (a > b2 ? 1.0f : 0.0f);
+}
+
+// The int8 codes clamp(rint(r / r_scale), -127, 127) of two residuals r, in the low byte of each
+// result (two's complement), from r254 = rcp(254 r_scale) (0 when r_scale is 0): the clamp is the
+// saturation of tp = r r254 + 1/2, and tp * 254 + kMagicB rounds to kMagicB + code + 127. The
+// distance to the nearest rounding boundary is formed negated (e = -d, exactly, as rounding is
+// symmetric), and the exact side test runs only for a lane within kNearB of a boundary.
+__device__ __forceinline__ void code8_pair(float2 r, float rscale, float r254, uint32_t &b0,
+                                           uint32_t &b1) {
+    const float2 tp = make_float2(__saturatef(__fmaf_rn(r.x, r254, 0.5f)),
+                                  __saturatef(__fmaf_rn(r.y, r254, 0.5f)));
+    float2 cm = __ffma2_rn(tp, make_float2(254.0f, 254.0f), make_float2(kMagicB, kMagicB));
+    const float2 q = __fadd2_rn(cm, make_float2(-kMagicB, -kMagicB));  // code + 127, exact
+    const float2 e = __ffma2_rn(tp, make_float2(-254.0f, -254.0f), q);
+    const bool near_x = fabsf(e.x) > 0.5f - kNearB, near_y = fabsf(e.y) > 0.5f - kNearB;
+    if (near_x | near_y) {  // one branch for the pair; rarely taken
+        if (near_x) {
+            const float code = __fsub_rn(cm.x, kMagic);  // exact
+            cm.x = __fadd_rn(cm.x, boundary_step(r.x, rscale, code, -e.x,
+                                                  (__float_as_uint(cm.x) & 1u) != 0));
+        }
+        if (near_y) {
+            const float code = __fsub_rn(cm.y, kMagic);
+            cm.y = __fadd_rn(cm.y, boundary_step(r.y, rscale, code, -e.y,
+                                                  (__float_as_uint(cm.y) & 1u) != 0));
+        }
+    }
+    b0 = __float_as_uint(cm.x);
+    b1 = __float_as_uint(cm.y);
+}
+
 // Quantise the group held in u (word m: channels 2m in the low half, 2m+1 in the high half).
 __device__ __forceinline__ void quantize_group(const uint32_t (&u)[16], GroupCodes &o) {
     group_params(u, o);
     const float zf = __half2float(o.zero);
     const float sf = __half2float(o.scale);
-    // 2-bit codes by comparison with the rounding boundaries (k + 1/2) scale, k = 0, 1, 2, which
-    // are exact in fp32: on these grids the IEEE quotient a / scale lies on the same side of
-    // k + 1/2 as a lies of (k + 1/2) scale, and equals k + 1/2 only when a does (see
-    // boundary_step), so the code is the number of boundaries below a, a tie at 1/2 or 5/2
-    // rounding down and a tie at 3/2 rounding up (half to even). scale 0 gives code 0.
     const float b0 = sf == 0.0f ? INFINITY : __fmul_rn(0.5f, sf);
     const float b1 = sf == 0.0f ? INFINITY : __fmul_rn(1.5f, sf);
     const float b2 = sf == 0.0f ? INFINITY : __fmul_rn(2.5f, sf);
 
-    // stage A: 2-bit codes and the residual r = x - x^2. The codes are summed as code * 4^c in
-    // fp32 (exact: each sum stays below 2^24), 12 + 4 channels per 32-bit word.
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    float r[32];
+    // stage A: 2-bit codes and the residual r = x - x^2, two channels (one word) at a time. The
+    // codes are summed as code * 4^c in fp32 (exact: each sum stays below 2^24; even and odd
+    // channels in separate lanes, added at the end), 12 + 4 channels per 32-bit word; both
+    // channels of a word fall in the same part.
+    float2 acc[4];
+#pragma unroll
+    for (int p = 0; p < 4; p++) acc[p] = make_float2(0.0f, 0.0f);
+    float2 r[16];
     float amax = 0.0f;
 #pragma unroll
-    for (int c = 0; c < 32; c++) {
-        const float x = (c & 1) ? bf16_hi(u[c >> 1]) : bf16_lo(u[c >> 1]);
-        const float a = __fsub_rn(x, zf);
-        const float code = (a > b0 ? 1.0f : 0.0f) + (a >= b1 ? 1.0f : 0.0f) + (a > b2 ? 1.0f : 0.0f);
+    for (int m = 0; m < 16; m++) {
+        const int c = 2 * m;
+        const float2 x = make_float2(bf16_lo(u[m]), bf16_hi(u[m]));
+        const float2 a = __fadd2_rn(x, make_float2(-zf, -zf));  // x - zero
+        const float2 code = make_float2(code2_of(a.x, b0, b1, b2), code2_of(a.y, b0, b1, b2));
         const int part = (c >> 4) * 2 + ((c & 15) >= 12);
-        const float weight = (float)(1u << (2 * ((c & 15) % 12)));
-        acc[part] = __fmaf_rn(code, weight, acc[part]);
-        r[c] = __fsub_rn(x, __fmaf_rn(code, sf, zf));
-        amax = fmaxf(amax, fabsf(r[c]));
+        const float w0 = (float)(1u << (2 * ((c & 15) % 12)));
+        acc[part] = __ffma2_rn(code, make_float2(w0, 4.0f * w0), acc[part]);
+        // r = x - (code * scale + zero); the negated product-sum is exact negation
+        r[m] = __fadd2_rn(x, __ffma2_rn(code, make_float2(-sf, -sf), make_float2(-zf, -zf)));
+        amax = fmaxf(amax, fmaxf(fabsf(r[m].x), fabsf(r[m].y)));
     }
-    o.codes[0] = __float2uint_rn(acc[0]) | (__float2uint_rn(acc[1]) << 24);
-    o.codes[1] = __float2uint_rn(acc[2]) | (__float2uint_rn(acc[3]) << 24);
+    o.codes[0] = __float2uint_rn(__fadd_rn(acc[0].x, acc[0].y)) |
+                 (__float2uint_rn(__fadd_rn(acc[1].x, acc[1].y)) << 24);
+    o.codes[1] = __float2uint_rn(__fadd_rn(acc[2].x, acc[2].y)) |
+                 (__float2uint_rn(__fadd_rn(acc[3].x, acc[3].y)) << 24);
 
     o.rscale = __float2half_rn(__fdiv_rn(amax, 127.0f));
     const float sr = __half2float(o.rscale);
@@ -143,8 +172,8 @@ __device__ __forceinline__ void quantize_group(const uint32_t (&u)[16], GroupCod
 #pragma unroll
     for (int w = 0; w < 8; w++) {
         uint32_t b[4];
-#pragma unroll
-        for (int e = 0; e < 4; e++) b[e] = code8_of(r[4 * w + e], sr, r254);
+        code8_pair(r[2 * w], sr, r254, b[0], b[1]);
+        code8_pair(r[2 * w + 1], sr, r254, b[2], b[3]);
         o.packed[w] = __byte_perm(__byte_perm(b[0], b[1], 0x0040),
                                   __byte_perm(b[2], b[3], 0x0040), 0x5410);
     }
