@@ -18,8 +18,9 @@
 // regime the page reports its gains in (large batches): one CTA of 128 threads (one refine group
 // of the decode kernel) walks one (sequence, KV head) unit. A block's three records (thumbnail
 // 3 KB, residual 8.5 KB, V 16 KB as a swizzled tensor tile) are brought into shared memory by
-// bulk copies, double-buffered: the next block's copies are in flight while the current block is
-// processed. Per block, warp mt computes the exact scores of rows 16mt .. 16mt+15 for every head
+// bulk copies into a ring of kArtStages stages: the next kArtStages - 1 blocks' copies are in
+// flight while the current block is processed, so the walk runs at the rate of the arithmetic
+// rather than of the copy latency. Per block, warp mt computes the exact scores of rows 16mt .. 16mt+15 for every head
 // (the thumbnail + residual tensor-core tile of scan.cuh), and the group's online softmax and P.V
 // on the tensor cores (softmax_pv of splitkv.cuh, P as bf16 hi + lo parts) fold the block in; warp
 // mt then holds O^T for channels 32mt .. 32mt+31. The probe needs, per head, l, then |P|^2, then
@@ -43,7 +44,8 @@ constexpr int kArtResid = kArtThumb + kThumbRec;
 constexpr int kArtStage = 28672;  // 28 KB: a multiple of 1 KB
 static_assert(kArtResid + kResidRec <= kArtStage && kArtStage % 1024 == 0, "stage layout");
 constexpr uint32_t kArtStageTx = kThumbRec + kResidRec + kPage * kD * 2;
-constexpr int kArtPx = 2 * kArtStage;                // two P^T fragment buffers
+constexpr int kArtStages = 5;
+constexpr int kArtPx = kArtStages * kArtStage;       // two P^T fragment buffers
 constexpr int kArtSmem = kArtPx + 2 * kPxBuf + 1024;  // + slack to align the base to 1 KB
 
 // The shared control block softmax_pv expects (one refine group), and the probe reductions.
@@ -51,11 +53,11 @@ struct ArtCtl {
     uint32_t over[1][2][4];
     float wmax[1][2][4][kMaxG];
     float red_l[4][kMaxG];  // [warp][head]: l partial sums
-    float red_n[4][kMaxG];  // [warp][head]: |P|^2 partial sums
+    float red_n[4][kMaxG];  // [warp][head]: |o|^2 partial sums
     float red_d[4][kMaxG];  // [warp][head]: direction-change partial sums
     int list[kArtThreads];    // kept blocks of the current chunk, most recent first
     int wc[4];
-    uint64_t full[2];
+    uint64_t full[kArtStages];
 };
 
 struct ArtParams {
@@ -102,8 +104,7 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(const __grid_constant_
     const int32_t *bt = a.block_table + (size_t)b * a.max_blocks;
     const uint8_t *keep = a.keep_in ? a.keep_in + (size_t)u * a.max_blocks : nullptr;
     if (t == 0) {
-        mbar_init(&ctl.full[0], 1);
-        mbar_init(&ctl.full[1], 1);
+        for (int i = 0; i < kArtStages; i++) mbar_init(&ctl.full[i], 1);
         fence_barrier_init();
         prefetch_tensormap(&prm.tm_v);
     }
@@ -178,13 +179,23 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(const __grid_constant_
     for (int i = 0; i < 2; i++) px[i][0] = px[i][1] = px[i][2] = px[i][3] = 0.0f;
     int used = 0, streak = 0, pb = 0;
 
-    int c = nb > 0 ? 0 : -1;  // block 0 first
+    // the ring: stage k holds the k-th next block of the traversal (blk[k] < 0: none), issued
+    // (bit k of inflight) unless its page was out of range
+    int blk[kArtStages];
+    uint32_t inflight = 0u;
+#pragma unroll
+    for (int k = 0; k < kArtStages; k++) {
+        blk[k] = k == 0 ? (nb > 0 ? 0 : -1) : (blk[k - 1] >= 0 ? advance() : -1);  // block 0 first
+        if (blk[k] >= 0 && issue(blk[k], k)) inflight |= 1u << k;
+    }
     int st = 0;
-    bool have = c >= 0 && issue(c, 0);
-    int cn = c >= 0 ? advance() : -1;
-    bool have_n = cn >= 0 && issue(cn, 1);
-    while (c >= 0) {
-        if (have && !wait_stage(st)) break;  // timed out: the error word says so
+    while (blk[st] >= 0) {
+        const int c = blk[st];
+        const bool have = (inflight >> st) & 1u;
+        if (have) {
+            inflight &= ~(1u << st);
+            if (!wait_stage(st)) break;  // timed out: the error word says so
+        }
         if (have) {  // block-uniform
             uint8_t *sg = base + st * kArtStage;
             const int rows = n - c * kPage < kPage ? n - c * kPage : kPage;
@@ -285,18 +296,17 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(const __grid_constant_
         }
         pn0 = nc0;
         pn1 = nc1;
-        // every read of stage st is behind the barriers above: refill it with the block after cn
-        const int cn2 = cn >= 0 ? advance() : -1;
-        const bool have_n2 = cn2 >= 0 && issue(cn2, st);
-        c = cn;
-        have = have_n;
-        cn = cn2;
-        have_n = have_n2;
-        st ^= 1;
+        // every read of stage st is behind the barriers above: refill it with the block
+        // kArtStages - 1 after the next (the last block in the ring decides whether there is one)
+        const int last = blk[(st + kArtStages - 1) % kArtStages];
+        blk[st] = last >= 0 ? advance() : -1;
+        if (blk[st] >= 0 && issue(blk[st], st)) inflight |= 1u << st;
+        st = st + 1 == kArtStages ? 0 : st + 1;
     }
     // copies still in flight into this CTA's shared memory are waited for (bounded) before it
-    // exits: the next block's, after a stop or a timed-out wait
-    if (c >= 0 && cn >= 0 && have_n) wait_stage(st ^ 1);
+    // exits: the ring's blocks after a stop or a timed-out wait
+    for (int k = 0; k < kArtStages; k++)
+        if ((inflight >> k) & 1u) wait_stage(k);
     // out = o / l: this thread's channels 32mt + 16i + {g, g+8} of heads h0, h1
     const float i0 = L0 > 0.0f ? 1.0f / L0 : 0.0f, i1 = L1 > 0.0f ? 1.0f / L1 : 0.0f;
     float *ob = a.out + ((size_t)b * a.Hq + h * G) * kD;

@@ -224,6 +224,7 @@ __device__ __forceinline__ void wait_armed(const DecodeArgs &a, SpMisc *m, int s
             *reinterpret_cast<volatile uint32_t *>(&m->aborted) = 1;
             return;
         }
+        __nanosleep(32);  // leave the issue slots to the warps that are scoring
     }
 }
 
@@ -265,15 +266,12 @@ __device__ __forceinline__ void sp_scan_chunk(const DecodeArgs &a, SpMisc *m, ui
                 qu = d.u;
             }
             const uint8_t *rec = base + kSpOffStages + st * kThumbRec;
-            float4 e[4];
-#pragma unroll
-            for (int mt = 0; mt < 4; mt++)
-                e[mt] = scan_tile_raw(rec, 16 * mt + g, 16 * mt + g + 8, m0, Q, qsr);
 #pragma unroll
             for (int mt = 0; mt < 4; mt++) {
+                const float4 e = scan_tile_raw(rec, 16 * mt + g, 16 * mt + g + 8, m0, Q, qsr);
                 const bool v0 = 16 * mt + g < d.rows, v1 = 16 * mt + g + 8 < d.rows;
-                mh0 = fmaxf(mh0, fmaxf(v0 ? e[mt].x : -INFINITY, v1 ? e[mt].z : -INFINITY));
-                mh1 = fmaxf(mh1, fmaxf(v0 ? e[mt].y : -INFINITY, v1 ? e[mt].w : -INFINITY));
+                mh0 = fmaxf(mh0, fmaxf(v0 ? e.x : -INFINITY, v1 ? e.z : -INFINITY));
+                mh1 = fmaxf(mh1, fmaxf(v0 ? e.y : -INFINITY, v1 ? e.w : -INFINITY));
             }
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) {
