@@ -745,7 +745,13 @@ def peaked_variant(a, w, delta, dev, ffd, torch, upload, dense_ms):
         select()
         t_sel = timed(select)
         t_att = timed(attend)
+        # the selector's own roofline: it streams every thumbnail record once (the per-block
+        # statistics it writes and the mask are small beside them)
+        sel_gbs = nb_total * 3072 / (t_sel * 1e-6) / 1e9
         selectors[name] = {"budget": budget, "select_us": round(t_sel, 2),
+                           "select_thumbnail_gbs": round(sel_gbs, 1),
+                           "select_frac_of_measured_copy_peak": round(
+                               sel_gbs / measured_peaks()[0]["hbm_gbs"], 3),
                            "attention_us": round(t_att, 2),
                            "step_us": round(t_sel + t_att, 2),
                            "sparsity": round(1 - int(smask.sum()) / nb_total, 4)}

@@ -16,8 +16,9 @@
 //                       and, per head, the block's (max s^, sum of e^(s^ - max)) pair;
 //   select_kernel       one CTA per (sequence, KV head), and for Top-p per query head too: for
 //                       Top-k a radix select of the k-th (importance, index) key in shared
-//                       memory; for Top-p the global softmax normalisation, a bitonic sort of the
-//                       blocks by mass and a prefix sum; then the kept bytes.
+//                       memory; for Top-p the global softmax normalisation and a mass-weighted
+//                       radix select of the cut (no sort: four passes over 8-bit digits of the
+//                       blocks' mass keys, each a count and mass histogram); then the kept bytes.
 // The chosen mask then goes to the decode kernel as a given mask (ffd_decode_attention_masked).
 #include "common.cuh"
 #include "ptx.cuh"
@@ -111,6 +112,13 @@ __global__ void __launch_bounds__(128) block_stats_kernel(DecodeArgs a, float *i
     };
     ThumbOps Q;
     load_thumb_ops(a, b, h, lane, Q);  // overlaps the first copies
+    // scores as scan_tile_raw's times sm * 2^(133 - kKq): bit for bit scan_tile's
+    float qsr[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; i++)
+#pragma unroll
+        for (int gg = 0; gg < 4; gg++) qsr[i][gg] = Q.qs[i][gg] * (1.0f / kUnscale);
+    const float post = a.sm_scale * kUnscale;
     int c = c0 + warp, st = 0;
     uint32_t have = (issue(c, 0) ? 1u : 0u);
     if (c + kStatWarps < cend && issue(c + kStatWarps, 1)) have |= 2u;
@@ -127,7 +135,13 @@ __global__ void __launch_bounds__(128) block_stats_kernel(DecodeArgs a, float *i
         for (int mt = 0; mt < 4; mt++) {
             const int r0 = 16 * mt + g, r1 = r0 + 8;
             float4 e = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            if (good) e = scan_tile(recs[warp][st], r0, r1, m0, Q, a.sm_scale);
+            if (good) {
+                e = scan_tile_raw(recs[warp][st], r0, r1, m0, Q, qsr);
+                e.x *= post;
+                e.y *= post;
+                e.z *= post;
+                e.w *= post;
+            }
             const bool v0 = r0 < rows, v1 = r1 < rows;
             x[mt][0] = v0 && w0 ? e.x : -INFINITY;
             x[mt][1] = v0 && w1 ? e.y : -INFINITY;
@@ -183,23 +197,9 @@ __device__ __forceinline__ uint32_t ordered(float f) {
     return (x & 0x80000000u) ? ~x : (x | 0x80000000u);
 }
 
-// Ascending bitonic sort of key[0 .. N), N a power of two, by the whole CTA.
-__device__ void bitonic_sort(uint64_t *key, int N) {
-    for (int k = 2; k <= N; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = threadIdx.x; i < N; i += blockDim.x) {
-                const int ixj = i ^ j;
-                if (ixj > i) {
-                    const uint64_t x = key[i], y = key[ixj];
-                    if ((x > y) == ((i & k) == 0)) {
-                        key[i] = y;
-                        key[ixj] = x;
-                    }
-                }
-            }
-            __syncthreads();
-        }
-    }
+// Float -> float of an ordered key (the inverse of ordered).
+__device__ __forceinline__ float unordered(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 __device__ __forceinline__ float block_max_reduce(float v, float *red) {
@@ -233,7 +233,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DecodeArgs a, int s
     uint64_t *key = reinterpret_cast<uint64_t *>(smem);
     float *mass = reinterpret_cast<float *>(key + N);
     __shared__ float red[kSelThreads / 32];
-    __shared__ float wsum[kSelThreads / 32];
     const int u = blockIdx.x, hh = blockIdx.y;
     const int b = u / a.Hkv;
     int n = a.seq_lens[b];
@@ -332,36 +331,122 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(DecodeArgs a, int s
     }
     const float Ltot = block_sum_reduce(ls, red);
     const float inv = Ltot > 0.0f ? 1.0f / Ltot : 0.0f;
-    for (int c = threadIdx.x; c < N; c += blockDim.x) {
-        if (c < nb) mass[c] *= inv;
-        key[c] = c < nb ? ((uint64_t)(~ordered(c < nb ? mass[c] : 0.0f)) << 32) | (uint32_t)c
-                        : ~0ull;
-    }
+    for (int c = threadIdx.x; c < nb; c += blockDim.x) mass[c] *= inv;
     __syncthreads();
-    bitonic_sort(key, N);
-    // exclusive prefix sum of the masses in sorted order: thread t owns positions per*t .. +per-1
-    const int per = (N + kSelThreads - 1) / kSelThreads;
-    float run = 0.0f;
-    const int t0 = threadIdx.x * per;
-    for (int t = t0; t < t0 + per && t < N; t++)
-        if (key[t] != ~0ull) run += mass[(uint32_t)key[t]];
+    if (!(budget > 0.0f)) return;  // only the forced blocks (pass 1 kept them)
+    // The cut: blocks ranked by (mass descending, index ascending) are kept while the mass ranked
+    // before them is below p. With keys k = ordered(mass), the boundary key K* is found 8 bits at
+    // a time from the top: among the blocks whose key matches the digits found so far, a count and
+    // a mass histogram of the next digit; every block in a digit bucket above the boundary bucket
+    // B is kept (all of them lie before the cut), every block below it is dropped, and the search
+    // continues inside B with `before` raised by the mass of the buckets above it. B is the lowest
+    // non-empty bucket whose higher buckets leave the running mass below p. The masses are summed
+    // in 2^-31 fixed point (exact and order-independent; the cut moves by at most nb 2^-32), and
+    // the lanes of a warp that hit the same bucket add once (match + reduce) before the atomics.
+    __shared__ unsigned int hcnt[256];
+    __shared__ unsigned int hmass[256];
+    __shared__ unsigned long long s_before;
+    __shared__ int s_bucket;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float incl = run;
+    const float kFx = 2147483648.0f;  // 2^31
+    const unsigned long long p_fx = (unsigned long long)((double)budget * 2147483648.0);
+    uint32_t prefix = 0u, known = 0u;
+    unsigned long long before = 0ull;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+            hcnt[i] = 0u;
+            hmass[i] = 0u;
+        }
+        __syncthreads();
+        for (int cb = warp * 32; cb < nb; cb += blockDim.x) {  // warp-converged
+            const int c = cb + lane;
+            const float mc = c < nb ? mass[c] : 0.0f;
+            const uint32_t k = ordered(mc);
+            const bool valid = c < nb && (k & known) == prefix;
+            const unsigned int active = __ballot_sync(0xffffffffu, valid);
+            if (valid) {
+                const uint32_t d = (k >> shift) & 255u;
+                const unsigned int peers = __match_any_sync(active, d);
+                const unsigned int sum = __reduce_add_sync(peers, __float2uint_rn(mc * kFx));
+                if (lane == __ffs(peers) - 1) {
+                    atomicAdd(&hcnt[d], (unsigned int)__popc(peers));
+                    atomicAdd(&hmass[d], sum);
+                }
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {  // lane L holds digits 8L .. 8L+7
+            unsigned long long mz[8];
+            unsigned int cz[8];
+            unsigned long long tot = 0ull;
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                mz[j] = hmass[8 * lane + j];
+                cz[j] = hcnt[8 * lane + j];
+                tot += mz[j];
+            }
+            // mass of the digits above this lane's: suffix over the higher lanes
+            unsigned long long above = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_down_sync(0xffffffffu, above, o);
+                if (lane + o < 32) above += y;
+            }
+            above -= tot;
+            int best = 256;  // the lowest qualifying non-empty digit of this lane
+            unsigned long long best_before = 0ull;
+            unsigned long long run = above;  // mass of the digits above digit 8L + j
+#pragma unroll
+            for (int j = 7; j >= 0; j--) {
+                if (cz[j] > 0u && before + run < p_fx) {
+                    best = 8 * lane + j;
+                    best_before = before + run;
+                }
+                run += mz[j];
+            }
+            int lo = best;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            if (best == lo && lo < 256) {  // exactly one lane
+                s_bucket = lo;
+                s_before = best_before;
+            }
+            if (lane == 0 && lo == 256) s_bucket = 256;  // no block in range: nothing more to keep
+        }
+        __syncthreads();
+        const int B = s_bucket;
+        if (B == 256) return;  // the blocks matching the prefix are all past the cut
+        before = s_before;
+        prefix |= (uint32_t)B << shift;
+        known |= 255u << shift;
+        __syncthreads();  // the histograms are cleared again only after every thread read B
+    }
+    // keys above K* = prefix are kept; among the blocks of key K* (equal masses w), in index order,
+    // the j-th is kept while before + j w < p: a CTA-wide count of the ties before each block
+    const unsigned long long w_fx = __float2uint_rn(unordered(prefix) * kFx);
+    const int per = (nb + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int c0 = threadIdx.x * per, c1 = c0 + per < nb ? c0 + per : nb;
+    int ties = 0;
+    for (int c = c0; c < c1; c++) ties += ordered(mass[c]) == prefix;
+    int incl = ties;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
     }
-    if (lane == 31) wsum[warp] = incl;
+    __shared__ int wties[kSelThreads / 32];
+    if (lane == 31) wties[warp] = incl;
     __syncthreads();
-    float before = 0.0f;
-    for (int w = 0; w < warp; w++) before += wsum[w];
-    before += incl - run;
-    for (int t = t0; t < t0 + per && t < N; t++) {
-        if (key[t] == ~0ull) break;
-        const uint32_t c = (uint32_t)key[t];
-        if (before < budget) keep[c] = 1;
-        before += mass[c];
+    int rank = incl - ties;
+    for (int v = 0; v < warp; v++) rank += wties[v];
+    for (int c = c0; c < c1; c++) {
+        const uint32_t k = ordered(mass[c]);
+        if (k > prefix) {
+            keep[c] = 1;
+        } else if (k == prefix) {
+            if (before + (unsigned long long)rank * w_fx < p_fx) keep[c] = 1;
+            rank++;
+        }
     }
 }
 
