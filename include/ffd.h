@@ -11,6 +11,8 @@
  * Conventions for every function:
  *   - Pointers marked "device" are device memory owned by the caller; the library allocates no
  *     memory and keeps no state between calls other than what the caller's workspace holds.
+ *     One exception: ffd_decode_attention_static keeps its scratch in a static device array of
+ *     the library (and that array's address per device); see its own comment.
  *   - Calls are asynchronous on the given stream (a cudaStream_t passed as void*; NULL is the
  *     legacy default stream), except ffd_get_error, which synchronises that stream.
  *   - Argument errors are detected on the host before anything is enqueued and returned as a
@@ -373,8 +375,10 @@ ffd_status ffd_art_attention(const ffd_decode_params *params, float tau, float p
  *   - Limit: parameters whose ffd_decode_workspace_size() exceeds 4 MiB are rejected with
  *     FFD_ERR_WORKSPACE before anything is enqueued (use ffd_decode_attention for those).
  *   - Set-up: the first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call before any stream
- *     capture. A failed look-up returns FFD_ERR_CUDA.
+ *     (cudaGetSymbolAddress) with that device current, and looks it up again whenever the
+ *     thread's current CUDA context is not the one of the last look-up (a cudaDeviceReset
+ *     replaces the primary context and the array's address with it); make the first call after
+ *     such a change before any stream capture. A failed look-up returns FFD_ERR_CUDA.
  *   - Sharing: every call on a device uses the same array and it keeps the previous call's
  *     contents; each call clears the parts that must start at zero (error word, merge tickets,
  *     slot counters)

@@ -7,6 +7,8 @@
 #include "common.cuh"
 #include "ptx.cuh"
 
+#include <cudaTypedefs.h>
+
 namespace ffd {
 cudaError_t launch_quantize(int P, int Hkv, const int32_t *page_ids, int num_pages_listed,
                             const void *k, uint8_t *thumb, uint8_t *resid, int *err,
@@ -519,20 +521,42 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 std::mutex g_static_mu;
 void *g_static_ptr[kMaxDevices];
+void *g_static_ctx[kMaxDevices];  // the context g_static_ptr[dev] was looked up in
+
+// The CUDA context current on this thread (null before the runtime has made one). A
+// cudaDeviceReset replaces the device's primary context, and the module's symbol addresses go
+// with it.
+void *current_context() {
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    }
+    CUcontext c = nullptr;
+    if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+    return c;
+}
 
 // Device address of g_static_scratch on the current device (host code must not use the array's
-// name as an address). Looked up once per device, with that device current.
+// name as an address). Looked up with that device current, again whenever the current context is
+// not the one of the last look-up (after a cudaDeviceReset, say).
 ffd_status static_scratch(void **out) {
     int dev = 0;
     if (const cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_status(e);
     if (dev < 0 || dev >= kMaxDevices) return FFD_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_static_mu);
-    if (!g_static_ptr[dev]) {
-        void *p = nullptr;
+    void *ctx = current_context();
+    if (!g_static_ptr[dev] || !ctx || ctx != g_static_ctx[dev]) {
+        void *p = nullptr;  // the look-up makes the primary context if there is none yet
         if (const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch); e != cudaSuccess)
             return cuda_status(e);
         if (!p) return FFD_ERR_CUDA;
         g_static_ptr[dev] = p;
+        g_static_ctx[dev] = current_context();
     }
     *out = g_static_ptr[dev];
     return FFD_OK;

@@ -74,3 +74,42 @@ def test_static_scratch_rejects_oversized_problem():
         ffd.ffd_decode_attention_static(big, dev["q"], qc, dev["v"], dev["seq_lens"],
                                         dev["block_table"], out)
     assert e.value.status == 3  # FFD_ERR_WORKSPACE
+
+
+def test_static_scratch_without_error_word_matches_workspace_path():
+    """error_word NULL: device errors go to the scratch's own word (cleared every call) and are not
+    reported; the results equal the workspace path's, in both schedules."""
+    w = ffd_synth.custom(3, 14, 2, 3000, sink=16, local=200, random_pages=True, seed=9)
+    inp = ffd_synth.make_inputs(w, seq_lens=[3000, 1, 777], signal_scale=ffd_synth.peaked_scale())
+    dev = H.to_device(inp)
+    qc = H.quantize(dev)
+    for schedule in (0, 1):
+        ref = H.decode(inp, dev, qc, 5.0, schedule=schedule)
+        p = H.params_for(inp, 5.0, schedule=schedule)
+        out = torch.full((w.batch, w.num_q_heads, 128), float("nan"), dtype=torch.float32,
+                         device="cuda")
+        mask = torch.full((w.batch, w.num_kv_heads, inp.max_blocks), 7, dtype=torch.uint8,
+                          device="cuda")
+        ffd.ffd_decode_attention_static(p, dev["q"], qc, dev["v"], dev["seq_lens"],
+                                        dev["block_table"], out, keep_mask=mask)
+        torch.cuda.synchronize()
+        assert np.array_equal(mask.cpu().numpy(), ref["mask"])
+        H.compare_outputs(out.cpu().numpy(), ref["out"].astype(np.float64),
+                          f"static, no error word, schedule {schedule}")
+
+
+def test_static_scratch_reports_bad_block_table_entry():
+    """An out-of-range block-table entry through the static entry point: FFD_ERR_BOUNDS from the
+    caller's error word, the entry's block dropped, and a clean call afterwards is correct."""
+    w = ffd_synth.custom(2, 4, 2, 700, sink=16, local=64, seed=3)
+    inp = ffd_synth.make_inputs(w, seq_lens=[700, 500])
+    dev = H.to_device(inp)
+    qc = H.quantize(dev)
+    bt = dev["block_table"].clone()
+    bt[1, 3] = inp.num_pages + 5
+    got = _static_decode(inp, dict(dev, block_table=bt), qc, 5.0)
+    assert got["err"] == 5  # FFD_ERR_BOUNDS
+    assert got["mask"][1, 0, 3] == 0
+    again = _static_decode(inp, dev, qc, 5.0)
+    assert again["err"] == 0
+    H.check_decode(inp, oracle.quantize(inp.k_bits), again, 5.0, what="static clean rerun")
