@@ -24,8 +24,9 @@ cudaError_t launch_select(const DecodeArgs &a, int selector, float budget, float
                           cudaStream_t stream);
 size_t select_smem_bytes(int max_blocks);
 int select_max_blocks();
+size_t art_list_bytes(int units, int max_blocks);
 cudaError_t launch_art(const DecodeArgs &a, float tau, float phi, int patience, int32_t *used,
-                       cudaStream_t stream);
+                       int32_t *list, cudaStream_t stream);
 }  // namespace ffd
 
 using namespace ffd;
@@ -43,6 +44,11 @@ ffd_status cuda_status(cudaError_t e) {
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// ART's workspace: the error word, then the units' traversal lists.
+size_t art_workspace_bytes(const ffd_decode_params *p) {
+    return kAlign + align_up(art_list_bytes(p->batch * p->num_kv_heads, p->max_blocks_per_seq));
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -434,7 +440,7 @@ ffd_status ffd_decode_attention_masked(const ffd_decode_params *params, const vo
 
 // Workspace of ffd_art_attention: the error word only (the kernel keeps its state on chip).
 size_t ffd_art_workspace_size(const ffd_decode_params *params) {
-    return check_params(params) == FFD_OK ? kAlign : 0;
+    return check_params(params) == FFD_OK ? art_workspace_bytes(params) : 0;
 }
 
 ffd_status ffd_art_attention(const ffd_decode_params *params, float tau, float phi,
@@ -451,7 +457,7 @@ ffd_status ffd_art_attention(const ffd_decode_params *params, float tau, float p
     if (!(tau >= 0.0f) || !(phi >= 0.0f) || patience < 1) return FFD_ERR_INVALID_ARG;
     ffd_status st = check_params(params);
     if (st != FFD_OK) return st;
-    if (workspace_bytes < kAlign) return FFD_ERR_WORKSPACE;
+    if (workspace_bytes < art_workspace_bytes(params)) return FFD_ERR_WORKSPACE;
     DecodeArgs a{};
     a.B = params->batch;
     a.Hq = params->num_q_heads;
@@ -471,6 +477,7 @@ ffd_status ffd_art_attention(const ffd_decode_params *params, float tau, float p
     a.out = out;
     a.err = static_cast<int *>(workspace);
     cudaError_t e = launch_art(a, tau, phi, patience, blocks_used,
+                               reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + kAlign),
                                static_cast<cudaStream_t>(stream));
     return cuda_status(e);
 }

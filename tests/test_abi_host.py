@@ -198,7 +198,9 @@ def test_select_and_masked_reject_bad_arguments(lib):
 def test_art_rejects_bad_arguments(lib):
     p = _params()
     need = ffd.ffd_art_workspace_size(p)
-    assert need == 256
+    # the error word, then one traversal list per (sequence, KV head) unit
+    units = p.batch * p.num_kv_heads
+    assert need == 256 + (units * p.max_blocks_per_seq * 4 + 255) // 256 * 256
 
     def art(tau=0.01, phi=0.001, patience=2, ws_bytes=need, **kw):
         a = dict(q=FAKE, th=FAKE, rs=FAKE, v=FAKE, sl=FAKE, bt=FAKE, ki=None, out=FAKE, bu=None,
