@@ -347,9 +347,11 @@ ffd_status ffd_decode_attention_masked(const ffd_decode_params *params, const vo
  *   out         device f32 [B][Hq][128]: o / l after the last block used (0 for n = 0)
  *   blocks_used device i32 [B][Hkv] or NULL: blocks folded in per unit
  *   workspace   device, >= ffd_art_workspace_size(params) bytes, 256-byte aligned; its first 4
- *               bytes are the device error word (zero it before first use)
- * One kernel launch, one CTA per (sequence, KV head): the traversal of a unit is sequential, so
- * the parallelism is across units. Errors: FFD_ERR_INVALID_ARG for NULL pointers, misaligned
+ *               bytes are the device error word (zero it before first use), then one traversal
+ *               list of max_blocks_per_seq int32 per (sequence, KV head), rewritten every call
+ * One kernel launch, one CTA per (sequence, KV head): the traversal of a unit is sequential
+ * through the probe, so three groups of the CTA score the next blocks into per-block states while
+ * one warp merges them in order and takes the probe; the parallelism beyond that is across units. Errors: FFD_ERR_INVALID_ARG for NULL pointers, misaligned
  * buffers, tau or phi negative or NaN, patience < 1; otherwise as ffd_decode_attention
  * (FFD_ERRBIT_BOUNDS for a block-table entry outside [0, P): that block contributes nothing).
  */
