@@ -351,7 +351,8 @@ ffd_status ffd_decode_attention_masked(const ffd_decode_params *params, const vo
  *               list of max_blocks_per_seq int32 per (sequence, KV head), rewritten every call
  * One kernel launch, one CTA per (sequence, KV head): the traversal of a unit is sequential
  * through the probe, so three groups of the CTA score the next blocks into per-block states while
- * one warp merges them in order and takes the probe; the parallelism beyond that is across units. Errors: FFD_ERR_INVALID_ARG for NULL pointers, misaligned
+ * four warps merge them in order, two blocks at a time, and take the probes; the parallelism
+ * beyond that is across units. Errors: FFD_ERR_INVALID_ARG for NULL pointers, misaligned
  * buffers, tau or phi negative or NaN, patience < 1; otherwise as ffd_decode_attention
  * (FFD_ERRBIT_BOUNDS for a block-table entry outside [0, P): that block contributes nothing).
  */

@@ -22,12 +22,16 @@
 // in the group's two stages by bulk and tensor copies, its exact scores come from the thumbnail +
 // residual tensor-core tile (`exact_tile`, scan.cuh) and `softmax_pv` (splitkv.cuh) forms the
 // block's state from a fresh reference, which the group writes to one of its two state slots.
-// One more warp, the sequencer, merges the states in traversal order into the running state it
-// holds in registers (four lanes per head, 32 channels each), takes the probe and its two metrics
-// with warp shuffles alone, and stops the walk. The sequential path per block is a merge
-// and a few warp reductions; the scoring, softmax and P.V of the next blocks run beside it. The
-// direction change is formed as |P/|P| - P'/|P'||^2 = 2 (1 - cos), which keeps its precision when
-// the two directions are close. The traversal list is built once at the start, in the workspace.
+// Four more warps, the sequencer, merge the states in traversal order into the running state
+// they hold in registers (two heads a warp, sixteen lanes a head, eight channels a lane), take
+// the probe and its two metrics, and stop the walk. They take the blocks two at a time: the
+// states after the first and after the second block are merged in order and the two probes are
+// formed side by side, so the sequential path is one merge pair, a few warp reductions and one
+// named barrier per two blocks; the scoring, softmax and P.V of the next blocks run beside it.
+// The direction change is formed as |P/|P| - P'/|P'||^2 = 2 (1 - cos), which keeps its precision
+// when the two directions are close; |P| = |o| / l and P/|P| = o / |o|, so l enters the scale
+// change only. The traversal list is built once at the start, in the workspace; each group reads
+// its list entries and block-table pages an iteration ahead of their use.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "scan.cuh"
@@ -38,8 +42,11 @@ namespace ffd {
 namespace {
 
 constexpr int kArtGroups = 3;                        // refine groups (4 warps each)
-constexpr int kArtSeqWarp = 4 * kArtGroups;          // the sequencer warp
-constexpr int kArtThreads = 32 * (kArtSeqWarp + 1);
+constexpr int kArtSeqWarp = 4 * kArtGroups;          // the first sequencer warp
+constexpr int kArtSeqWarps = 4;                      // sequencer warps: two heads each
+constexpr int kArtWarps = kArtSeqWarp + kArtSeqWarps;
+constexpr int kArtThreads = 32 * kArtWarps;
+constexpr int kArtSeqBar = 1;                        // named barrier of the sequencer warps
 // One block's records in shared memory: the V tile first (1 KB aligned for the 128-byte swizzle).
 constexpr int kArtV = 0;
 constexpr int kArtThumb = kPage * kD * 2;
@@ -61,7 +68,8 @@ struct ArtCtl {
     float lsum[kArtGroups][4][kMaxG];
     uint32_t aborted;
     int32_t stop_at;  // traversal positions >= stop_at are not needed (the sequencer stopped)
-    int32_t wc[kArtSeqWarp + 1];
+    int32_t wc[kArtWarps];
+    float seq_met[2][kArtSeqWarps][4];  // the sequencer warps' metrics of a pair of blocks
     uint64_t full[kArtStages];
     uint64_t state_full[kArtSlots], state_empty[kArtSlots];
 };
@@ -144,7 +152,7 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(const __grid_constant_
             int off = nl;
             for (int w = 0; w < warp; w++) off += ctl.wc[w];
             if (k) list[off + __popc(bal & ((1u << lane) - 1u))] = idx;
-            for (int w = 0; w <= kArtSeqWarp; w++) nl += ctl.wc[w];
+            for (int w = 0; w < kArtWarps; w++) nl += ctl.wc[w];
             __syncthreads();  // wc is rewritten by the next chunk
         }
     }
@@ -161,11 +169,11 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(const __grid_constant_
         ResidOps QR;
         load_thumb_ops(a, b, h, lane, Q);
         load_resid_ops(a, b, h, lane, QR);
-        // Copies of traversal position p into the group's stage s; false (nothing issued) for a
-        // page outside [0, P). Group-uniform; one thread of the group issues.
+        // Copies of a traversal position's block, on `page`, into the group's stage s; false
+        // (nothing issued) for a page outside [0, P). Group-uniform; one thread of the group
+        // issues.
         int issued = 0;  // bit s: a copy into the group's stage s is in flight
-        auto issue = [&](int p, int s) -> bool {
-            const int page = bt[list[p]];
+        auto issue = [&](int page, int s) -> bool {
             if (page < 0 || page >= a.P) {
                 if (mt == 0 && lane == 0) raise_error(a.err, FFD_ERRBIT_BOUNDS);
                 return false;
@@ -182,13 +190,21 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(const __grid_constant_
             issued |= 1 << s;
             return true;
         };
+        // The list and block-table reads run ahead of their use, so that neither waits in the
+        // loop: cs0 / cs1 is the block in stage 0 / 1, nx_c the block of the next position to
+        // copy.
+        int cs0 = g < nl ? list[g] : 0, cs1 = g + kArtGroups < nl ? list[g + kArtGroups] : 0;
+        int nx_c = g + 2 * kArtGroups < nl ? list[g + 2 * kArtGroups] : 0;
         uint32_t have = 0u;  // bit s: stage s holds (or will hold) a loaded block
-        if (g < nl && issue(g, 0)) have |= 1u;
-        if (g + kArtGroups < nl && issue(g + kArtGroups, 1)) have |= 2u;
+        if (g < nl && issue(bt[cs0], 0)) have |= 1u;
+        if (g + kArtGroups < nl && issue(bt[cs1], 1)) have |= 2u;
         int pb = 0;
         uint32_t fph = 0u;  // bit s: parity of the group's stage s's next completion
         for (int p = g, j = 0; p < nl; p += kArtGroups, j++) {
             const int s = j & 1;
+            const int pn = p + 2 * kArtGroups;  // the position this iteration copies into stage s
+            const int pn_page = pn < nl ? bt[nx_c] : -1;
+            const int nn_c = pn + kArtGroups < nl ? list[pn + kArtGroups] : 0;
             const bool good = (have >> s) & 1u;
             // the block's copies, unless the sequencer has stopped before it (the flag is only
             // ever lowered; a group that sees it late computes one block more, harmlessly); one
@@ -210,7 +226,7 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(const __grid_constant_
             for (int i = 0; i < 2; i++) R.o[i][0] = R.o[i][1] = R.o[i][2] = R.o[i][3] = 0.0f;
             if (good) {
                 uint8_t *sg = base + (g * 2 + s) * kArtStage;
-                const int c = list[p];
+                const int c = s ? cs1 : cs0;
                 const int rows = n - c * kPage < kPage ? n - c * kPage : kPage;
                 const float4 e = exact_tile(sg + kArtThumb, sg + kArtResid, r0, r1, tig, Q, QR,
                                             a.sm_scale);
@@ -239,8 +255,10 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(const __grid_constant_
                 j < 2 || art_wait(a, ctl, &ctl.state_empty[slot], ((j >> 1) - 1) & 1, p);
             if (named_barrier_or(bar_id, 128, !ok)) break;
             have &= ~(1u << s);
-            const int pn = p + 2 * kArtGroups;
-            if (pn < nl && issue(pn, s)) have |= 1u << s;  // unneeded after a stop: drained
+            if (pn < nl && issue(pn_page, s)) have |= 1u << s;  // unneeded after a stop: drained
+            if (s) cs1 = nx_c;
+            else cs0 = nx_c;
+            nx_c = nn_c;
             write_record(a, &ctl, R, reinterpret_cast<float *>(base + kArtState) +
                                          slot * kMaxG * kPartStride,
                          g, mt, lane);
@@ -261,89 +279,157 @@ __global__ void __launch_bounds__(kArtThreads) art_kernel(const __grid_constant_
         return;
     }
 
-    // ---- the sequencer: the running state, lane L holding head L / 4, channels 32 (L % 4) .. +31
-    const int hh = lane >> 2, cq = 32 * (lane & 3);
+    // ---- the sequencer: warp sw holds the running state of heads 2 sw and 2 sw + 1, lane L head
+    // 2 sw + L / 16 and channels 8 (L % 16) .. +7. The warps take the blocks two at a time: the
+    // state after the first (a) and after the second (b) are merged in order, as one block at a
+    // time would, and the two probes' metrics are formed side by side; the four warps exchange
+    // their heads' maxima through shared memory at one named barrier (which also tells that every
+    // warp has read the slots), and the stop decisions, at a and then at b, are the same in all.
+    const int sw = warp - kArtSeqWarp;
+    const int hh = 2 * sw + (lane >> 4), cq = 8 * (lane & 15);
     const bool hv = hh < G;
-    float o[32], px[32];
+    float o[8], px[8];
     float M = -INFINITY, Ls = 0.0f, pn = 0.0f;
 #pragma unroll
-    for (int k = 0; k < 32; k++) o[k] = px[k] = 0.0f;
+    for (int k = 0; k < 8; k++) o[k] = px[k] = 0.0f;
     int used = 0, streak = 0;
-    for (int p = 0; p < nl; p++) {
-        const int g = p % kArtGroups, j = p / kArtGroups, slot = g * 2 + (j & 1);
-        if (!__all_sync(0xffffffffu, art_wait(a, ctl, &ctl.state_full[slot], (j >> 1) & 1, -1)))
-            break;  // warp-uniform
-        const float *rec = reinterpret_cast<const float *>(base + kArtState) +
-                           (slot * kMaxG + (hv ? hh : 0)) * kPartStride;
-        // merge the block's state: M' = max(M, m), o = e^(M - M') o + e^(m - M') o_b, same for l
+    // merge one block's state (rec) into (Mx, Lx, ox): M' = max(M, m), o = e^(M - M') o +
+    // e^(m - M') o_b, same for l; while the running maximum holds the state is not rescaled
+    auto merge = [&](const float *rec, float &Mx, float &Lx, float (&ox)[8]) {
         const float mb = rec[kD];
-        if (hv && mb != -INFINITY) {  // a block not loaded adds nothing
-            const float lb = rec[kD + 1];
-            const float Mn = fmaxf(M, mb);
-            const float fa = M == -INFINITY ? 0.0f : exp2f((M - Mn) * kLog2e);
-            const float fb = exp2f((mb - Mn) * kLog2e);
+        if (!hv || mb == -INFINITY) return;  // a block not loaded adds nothing
+        const float lb = rec[kD + 1];
+        if (mb > Mx) {
+            const float fa = Mx == -INFINITY ? 0.0f : exp2f((Mx - mb) * kLog2e);
 #pragma unroll
-            for (int k = 0; k < 32; k += 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(rec + cq + k);
-                o[k] = fmaf(fb, v.x, fa * o[k]);
-                o[k + 1] = fmaf(fb, v.y, fa * o[k + 1]);
-                o[k + 2] = fmaf(fb, v.z, fa * o[k + 2]);
-                o[k + 3] = fmaf(fb, v.w, fa * o[k + 3]);
-            }
-            Ls = fmaf(fb, lb, fa * Ls);
-            M = Mn;
+            for (int k = 0; k < 8; k++) ox[k] = fa * ox[k];
+            Lx = fa * Lx;
+            Mx = mb;
         }
-        __syncwarp();  // every lane has read the slot
-        if (lane == 0) mbar_arrive(&ctl.state_empty[slot]);
-        used++;
-        // the probe P = o / l of this lane's head: |P| over the head's four lanes, then the
-        // direction change against the last probe
-        const float il = Ls > 0.0f ? __frcp_rn(Ls) : 0.0f;
-        float q = 0.0f;
+        const float fb = exp2f((mb - Mx) * kLog2e);
 #pragma unroll
-        for (int k = 0; k < 32; k++) {
-            const float c = o[k] * il;
-            q = fmaf(c, c, q);
+        for (int k = 0; k < 8; k += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(rec + cq + k);
+            ox[k] = fmaf(fb, v.x, ox[k]);
+            ox[k + 1] = fmaf(fb, v.y, ox[k + 1]);
+            ox[k + 2] = fmaf(fb, v.z, ox[k + 2]);
+            ox[k + 3] = fmaf(fb, v.w, ox[k + 3]);
         }
-        q += __shfl_xor_sync(0xffffffffu, q, 1);
-        q += __shfl_xor_sync(0xffffffffu, q, 2);
-        const float nc = sqrtf(q);
-        const float rn = q > 0.0f ? rsqrtf(q) : 0.0f;
-        if (used >= 2) {
-            float d = 0.0f;
+        Lx = fmaf(fb, lb, Lx);
+    };
+    const float *states = reinterpret_cast<const float *>(base + kArtState);
+    for (int p = 0; p < nl; p += 2) {
+        const bool two = p + 1 < nl;
+        const int ja = p / kArtGroups, sa = (p % kArtGroups) * 2 + (ja & 1);
+        const int jb = (p + 1) / kArtGroups, sb = ((p + 1) % kArtGroups) * 2 + (jb & 1);
+        bool ok = art_wait(a, ctl, &ctl.state_full[sa], (ja >> 1) & 1, -1);
+        if (two && ok) ok = art_wait(a, ctl, &ctl.state_full[sb], (jb >> 1) & 1, -1);
+        ok = __all_sync(0xffffffffu, ok);
+        float Ma = M, La = Ls, oa[8];
 #pragma unroll
-            for (int k = 0; k < 32; k++) {
-                const float e = o[k] * il * rn - px[k];
-                d = fmaf(e, e, d);
-            }
-            d += __shfl_xor_sync(0xffffffffu, d, 1);
-            d += __shfl_xor_sync(0xffffffffu, d, 2);
-            float ds = 0.0f, dr = 0.0f;
-            if (hv) head_metrics(nc, pn, d, ds, dr);
+        for (int k = 0; k < 8; k++) oa[k] = o[k];
+        if (ok) merge(states + (sa * kMaxG + (hv ? hh : 0)) * kPartStride, Ma, La, oa);
+        float Mb = Ma, Lb = La, ob[8];
 #pragma unroll
-            for (int o2 = 4; o2 < 32; o2 <<= 1) {
-                ds = fmaxf(ds, __shfl_xor_sync(0xffffffffu, ds, o2));
-                dr = fmaxf(dr, __shfl_xor_sync(0xffffffffu, dr, o2));
-            }
-            streak = (ds < prm.tau && dr < prm.phi) ? streak + 1 : 0;
+        for (int k = 0; k < 8; k++) ob[k] = oa[k];
+        if (ok && two) merge(states + (sb * kMaxG + (hv ? hh : 0)) * kPartStride, Mb, Lb, ob);
+        // the probes P = o / l of this lane's head: |P| = |o| / l and the direction o / |o|
+        // (l cancels), |o|^2 over the head's sixteen lanes; then the direction changes, a against
+        // the last probe, b against a
+        float qa = 0.0f, qb = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            qa = fmaf(oa[k], oa[k], qa);
+            qb = fmaf(ob[k], ob[k], qb);
         }
-        pn = nc;
 #pragma unroll
-        for (int k = 0; k < 32; k++) px[k] = o[k] * il * rn;
-        if (used >= 2 && streak >= prm.patience) break;
+        for (int o2 = 1; o2 < 16; o2 <<= 1) {
+            qa += __shfl_xor_sync(0xffffffffu, qa, o2);
+            qb += __shfl_xor_sync(0xffffffffu, qb, o2);
+        }
+        const float nca = sqrtf(qa) * (La > 0.0f ? __frcp_rn(La) : 0.0f);
+        const float ncb = sqrtf(qb) * (Lb > 0.0f ? __frcp_rn(Lb) : 0.0f);
+        const float rna = qa > 0.0f ? rsqrtf(qa) : 0.0f, rnb = qb > 0.0f ? rsqrtf(qb) : 0.0f;
+        float da = 0.0f, db = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const float ca = oa[k] * rna, cb = ob[k] * rnb;
+            const float ea = ca - px[k], eb = cb - ca;
+            da = fmaf(ea, ea, da);
+            db = fmaf(eb, eb, db);
+            px[k] = two ? cb : ca;  // the direction of the last probe taken
+        }
+#pragma unroll
+        for (int o2 = 1; o2 < 16; o2 <<= 1) {
+            da += __shfl_xor_sync(0xffffffffu, da, o2);
+            db += __shfl_xor_sync(0xffffffffu, db, o2);
+        }
+        float dsa = 0.0f, dra = 0.0f, dsb = 0.0f, drb = 0.0f;
+        if (hv) {
+            head_metrics(nca, pn, da, dsa, dra);
+            head_metrics(ncb, nca, db, dsb, drb);
+        }
+        dsa = fmaxf(dsa, __shfl_xor_sync(0xffffffffu, dsa, 16));
+        dra = fmaxf(dra, __shfl_xor_sync(0xffffffffu, dra, 16));
+        dsb = fmaxf(dsb, __shfl_xor_sync(0xffffffffu, dsb, 16));
+        drb = fmaxf(drb, __shfl_xor_sync(0xffffffffu, drb, 16));
+        float *met = ctl.seq_met[(p >> 1) & 1][sw];
+        if (lane == 0) {
+            met[0] = dsa;
+            met[1] = dra;
+            met[2] = dsb;
+            met[3] = drb;
+        }
+        // every sequencer warp has read the slots and written its maxima (one decision for all)
+        if (named_barrier_or(kArtSeqBar, 32 * kArtSeqWarps, !ok)) break;
+        if (sw == 0 && lane == 0) {
+            mbar_arrive(&ctl.state_empty[sa]);
+            if (two) mbar_arrive(&ctl.state_empty[sb]);
+        }
+        float m4[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            m4[i] = ctl.seq_met[(p >> 1) & 1][0][i];
+#pragma unroll
+            for (int w = 1; w < kArtSeqWarps; w++) m4[i] = fmaxf(m4[i], ctl.seq_met[(p >> 1) & 1][w][i]);
+        }
+        // block a: the criterion is first checked after the second block
+        bool stop = false;
+        if (used + 1 >= 2) {
+            streak = (m4[0] < prm.tau && m4[1] < prm.phi) ? streak + 1 : 0;
+            stop = streak >= prm.patience;
+        }
+        if (stop || !two) {  // the state after a is the last one
+            M = Ma;
+            Ls = La;
+#pragma unroll
+            for (int k = 0; k < 8; k++) o[k] = oa[k];
+            pn = nca;
+            used += 1;
+            if (stop) break;
+            continue;
+        }
+        streak = (m4[2] < prm.tau && m4[3] < prm.phi) ? streak + 1 : 0;
+        M = Mb;
+        Ls = Lb;
+#pragma unroll
+        for (int k = 0; k < 8; k++) o[k] = ob[k];
+        pn = ncb;
+        used += 2;
+        if (streak >= prm.patience) break;
     }
     // the groups stop fetching and scoring past the stop (also after an abort)
-    if (lane == 0) *reinterpret_cast<volatile int32_t *>(&ctl.stop_at) = used;
-    // out = o / l: this lane's 32 channels of its head
+    if (sw == 0 && lane == 0) *reinterpret_cast<volatile int32_t *>(&ctl.stop_at) = used;
+    // out = o / l: this lane's 8 channels of its head
     if (hv) {
         float *ob = a.out + ((size_t)b * a.Hq + h * G + hh) * kD + cq;
         const float iv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
 #pragma unroll
-        for (int k = 0; k < 32; k += 4)
+        for (int k = 0; k < 8; k += 4)
             *reinterpret_cast<float4 *>(ob + k) =
                 make_float4(o[k] * iv, o[k + 1] * iv, o[k + 2] * iv, o[k + 3] * iv);
     }
-    if (prm.used && lane == 0) prm.used[u] = used;
+    if (prm.used && sw == 0 && lane == 0) prm.used[u] = used;
 }
 
 }  // namespace

@@ -50,11 +50,11 @@ __device__ __forceinline__ const __nv_bfloat16 *q_row(const DecodeArgs &a, int b
     return a.q + ((size_t)b * a.Hq + h * a.G + (g < a.G ? g : 0)) * kD;
 }
 
-__device__ __forceinline__ void load_thumb_ops(const DecodeArgs &a, int b, int h, int lane,
-                                               ThumbOps &Q) {
-    const int g = lane >> 2, tig = lane & 3;
-    const bool hv = g < a.G;
-    const __nv_bfloat16 *qrow = q_row(a, b, h, g);
+// The operands from qrow, the query row of head g (global or shared memory; hv: g < G, else the
+// head is padding and its operands are zero).
+__device__ __forceinline__ void thumb_ops_from_row(const __nv_bfloat16 *qrow, bool hv, int lane,
+                                                   int *err, ThumbOps &Q) {
+    const int tig = lane & 3;
     float big = 0.0f;
     auto ld = [&](int c) {
         const float v = hv ? __bfloat162float(qrow[c]) : 0.0f;
@@ -72,7 +72,24 @@ __device__ __forceinline__ void load_thumb_ops(const DecodeArgs &a, int b, int h
         part[kc >> 1] += (x0 + x1) + (x2 + x3);
     }
     group_sums(part, tig, Q.qs);
-    if (!(big < kQMax)) raise_error(a.err, FFD_ERRBIT_RANGE);
+    if (!(big < kQMax)) raise_error(err, FFD_ERRBIT_RANGE);
+}
+
+__device__ __forceinline__ void load_thumb_ops(const DecodeArgs &a, int b, int h, int lane,
+                                               ThumbOps &Q) {
+    const int g = lane >> 2;
+    thumb_ops_from_row(q_row(a, b, h, g), g < a.G, lane, a.err, Q);
+}
+
+// The query rows of unit (b, h) -- G rows of kD bf16, contiguous in q -- copied to shared memory
+// at sq (16-byte vectors; q is 16-byte aligned and a unit's rows start at a multiple of 256
+// bytes) by threads tid = 0 .. nthr-1. One round trip, in place of every warp's scattered reads
+// of the same rows; the caller synchronises before reading sq.
+__device__ __forceinline__ void stage_query(const DecodeArgs &a, int b, int h, __nv_bfloat16 *sq,
+                                            int tid, int nthr) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((size_t)b * a.Hq + h * a.G) * kD);
+    uint4 *dst = reinterpret_cast<uint4 *>(sq);
+    for (int i = tid; i < a.G * kD / 8; i += nthr) dst[i] = src[i];
 }
 
 // D[gg] = sum over group gg of q . code (scaled by 2^(kKq-133)) for rows (g, g+8) x heads.
@@ -178,11 +195,9 @@ struct ResidOps {
     float qs[2][4];
 };
 
-__device__ __forceinline__ void load_resid_ops(const DecodeArgs &a, int b, int h, int lane,
-                                               ResidOps &Q) {
-    const int g = lane >> 2, tig = lane & 3;
-    const bool hv = g < a.G;
-    const __nv_bfloat16 *qrow = q_row(a, b, h, g);
+__device__ __forceinline__ void resid_ops_from_row(const __nv_bfloat16 *qrow, bool hv, int lane,
+                                                   ResidOps &Q) {
+    const int tig = lane & 3;
     const float sr = __int_as_float((127 + kKq) << 23);  // 2^kKq
     float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
@@ -198,6 +213,12 @@ __device__ __forceinline__ void load_resid_ops(const DecodeArgs &a, int b, int h
         part[gg] = ((y[0] + y[1]) + (y[2] + y[3])) + ((y[4] + y[5]) + (y[6] + y[7]));
     }
     group_sums(part, tig, Q.qs);
+}
+
+__device__ __forceinline__ void load_resid_ops(const DecodeArgs &a, int b, int h, int lane,
+                                               ResidOps &Q) {
+    const int g = lane >> 2;
+    resid_ops_from_row(q_row(a, b, h, g), g < a.G, lane, Q);
 }
 
 // D[gg] = sum over group gg of q . (c8 + 128) (scaled by 2^(kKq-133)).

@@ -82,7 +82,9 @@ constexpr int kSpOffShared = kSpPhaseA > kSpPhaseB ? kSpPhaseA : kSpPhaseB;
 constexpr int kSpOffPx = ((kSpOffShared + 1023) / 1024) * 1024;      // [group][2][kPxBuf]
 // the refine groups' records of a unit's segment, combined into the CTA's one record
 constexpr int kSpOffComb = kSpOffPx + kSpGroups * 2 * kPxBuf;        // float [group][kMaxG][stride]
-constexpr int kSpOffMisc = kSpOffComb + kSpGroups * kMaxG * kPartStride * 4;
+// each refine group's copy of the current unit's query rows (bf16 [kMaxG][kD])
+constexpr int kSpOffQ = kSpOffComb + kSpGroups * kMaxG * kPartStride * 4;
+constexpr int kSpOffMisc = kSpOffQ + kSpGroups * kMaxG * kD * 2;
 constexpr int kSpMaxCtas = 256;
 constexpr int kSpMiscBytes = 5120;
 constexpr int kSpSmemBytes = kSpOffMisc + kSpMiscBytes + 1024;       // + slack to align to 1 KB
@@ -530,8 +532,13 @@ __device__ __forceinline__ void sp_refiner(const DecodeArgs &a, SpMisc *m, uint8
                 cu = u;
                 seg0 = s0 + j;
                 const int b = u / a.Hkv, h = u - b * a.Hkv;
-                load_thumb_ops(a, b, h, lane, Q);
-                load_resid_ops(a, b, h, lane, QR);
+                // the group's query rows, staged once (the previous unit's readers have all passed
+                // end_segment's barriers)
+                __nv_bfloat16 *sq = reinterpret_cast<__nv_bfloat16 *>(base + kSpOffQ) + grp * kMaxG * kD;
+                stage_query(a, b, h, sq, 32 * mt + lane, 128);
+                named_barrier_sync(2 + grp, 128);
+                thumb_ops_from_row(sq + (g < a.G ? g : 0) * kD, g < a.G, lane, a.err, Q);
+                resid_ops_from_row(sq + (g < a.G ? g : 0) * kD, g < a.G, lane, QR);
                 n = len_of(a, b);
                 const float mt0 = __ldcg(a.ws_mt + (size_t)u * kMaxG + 2 * tig);
                 const float mt1 = __ldcg(a.ws_mt + (size_t)u * kMaxG + 2 * tig + 1);
