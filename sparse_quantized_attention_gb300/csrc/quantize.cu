@@ -19,7 +19,9 @@ namespace ffd {
 
 using namespace quant;
 
-__global__ void __launch_bounds__(256, 4) quantize_keys_kernel(
+// Five CTAs per SM (48 registers a thread, a few bytes of spill): the kernel is issue-bound, and
+// the fifth CTA's warps fill the issue slots that the loads' latency leaves empty with four.
+__global__ void __launch_bounds__(256, 5) quantize_keys_kernel(
     int P, int Hkv, const int32_t *__restrict__ page_ids, const __nv_bfloat16 *__restrict__ k,
     uint8_t *__restrict__ thumb, uint8_t *__restrict__ resid, int *err) {
     int page = blockIdx.x / Hkv;
