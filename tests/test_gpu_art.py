@@ -104,8 +104,10 @@ def test_without_termination_uses_every_listed_block(case, masked):
             _close(out[b, h * G:(h + 1) * G], res.out)
 
 
-@pytest.mark.parametrize("patience", [1, 3])
+@pytest.mark.parametrize("patience", [1, 2, 3])
 def test_huge_thresholds_stop_after_patience(case, patience):
+    """Stops after 1 + patience blocks: the second block of a pair the sequencer takes together
+    (patience 1, 3) and the first one (patience 2)."""
     inp, dev, qc, qk, _ = case
     w = inp.workload
     G = w.num_q_heads // w.num_kv_heads
