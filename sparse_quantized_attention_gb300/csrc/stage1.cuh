@@ -37,6 +37,10 @@ __device__ __forceinline__ void pseudo_max_slots(const DecodeArgs &a, M *m, int 
     const int wk = cta * NG + grp;
     const int z0 = (int)((int64_t)nz * wk / workers), z1 = (int)((int64_t)nz * (wk + 1) / workers);
     int it = 0, cu = -1, raw_n = 0, n = 0;
+    // block-table entries of 32 consecutive slots of the current unit, one per lane (slot
+    // pg_base + lane), read together instead of one dependent read per pair
+    int pg_base = -1, pg_mine = -1;
+    int pending = 0;  // slots of unit cu written since its counter was last raised
     ThumbOps Q;
     ResidOps QR;
     for (int z = z0; z < z1; z++, it++) {
@@ -50,6 +54,7 @@ __device__ __forceinline__ void pseudo_max_slots(const DecodeArgs &a, M *m, int 
             raw_n = a.seq_lens[b];
             n = len_of(a, b);
             cu = u;
+            pg_base = -1;
         }
         const int nb = (n + kPage - 1) / kPage;
         if (slot == 0) {
@@ -70,7 +75,12 @@ __device__ __forceinline__ void pseudo_max_slots(const DecodeArgs &a, M *m, int 
         int page = -1;
         const int blk = slot < fb.count ? fb.block(slot) : 0;
         if (slot < fb.count) {
-            page = a.block_table[(size_t)b * a.max_blocks + blk];
+            if (pg_base < 0 || slot >= pg_base + 32) {  // warp-uniform
+                pg_base = slot;
+                const int sl = slot + lane;
+                pg_mine = sl < fb.count ? a.block_table[(size_t)b * a.max_blocks + fb.block(sl)] : -1;
+            }
+            page = __shfl_sync(0xffffffffu, pg_mine, slot - pg_base);
             if (page < 0 || page >= a.P) page = -1;  // flagged by the page warp
         }
         float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -96,20 +106,27 @@ __device__ __forceinline__ void pseudo_max_slots(const DecodeArgs &a, M *m, int 
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
             }
         }
+        // the reduction buffers alternate between pairs: a buffer is written again two pairs
+        // later, after the next pair's barrier, which every reader of this pair has passed
         float (&red)[4][kMaxG] = m->wmax[grp][it & 1];
         if (g == 0) {
             red[mt][2 * tig] = mx0;
             red[mt][2 * tig + 1] = mx1;
         }
         named_barrier_sync(2 + grp, 128);
-        if (tid < kMaxG) {
+        if (tid < kMaxG)
             mdst[tid] = tid < a.G ? fmaxf(fmaxf(red[0][tid], red[1][tid]),
                                           fmaxf(red[2][tid], red[3][tid]))
                                   : -INFINITY;
-            __threadfence();
+        pending++;
+        // the unit's counter is raised once per run of its slots: the writers' fence, then one
+        // add of the slots written
+        if (z + 1 == z1 || (z + 1) / a.nf != u) {
+            if (tid < kMaxG) __threadfence();
+            named_barrier_sync(2 + grp, 128);
+            if (tid == 0) atomicAdd(slot_counter(a, u), pending);
+            pending = 0;
         }
-        named_barrier_sync(2 + grp, 128);
-        if (tid == 0) atomicAdd(slot_counter(a, u), 1);
     }
     // the reduction buffers are the refine warps' block-maxima buffers
     named_barrier_sync(2 + grp, 128);
