@@ -93,10 +93,12 @@ typedef struct {
     int32_t local_tokens;       /* L >= 0: tokens n-L .. n-1 are local tokens */
     float delta;                /* delta of the Top-delta rule; +INFINITY keeps every block */
     float sm_scale;             /* score scale, finite and > 0; normally 1/sqrt(head_dim) */
-    int32_t num_splits;         /* 0: library's choice (one per SM); else the number of KV
-                                   partitions, i.e. the CTAs of the persistent kernel of
-                                   ffd_decode_attention or ffd_dense_decode, at most one per SM:
-                                   larger values are clamped to the SM count */
+    int32_t num_splits;         /* 0: library's choice (one per SM, or one per 4 blocks of
+                                   batch * num_kv_heads * max_blocks_per_seq when that is
+                                   fewer); else the number of KV partitions, i.e. the CTAs of
+                                   the persistent kernel of ffd_decode_attention or
+                                   ffd_dense_decode, at most one per SM: larger values are
+                                   clamped to the SM count */
     int32_t wait_limit_us;      /* >= 0. Bound, in microseconds, of every wait inside a kernel of
                                    this call (a CTA waiting for a copy, for another warp or for
                                    another CTA); 0 takes the default of 2 s. A wait that runs out

@@ -93,6 +93,17 @@ ffd_status check_params(const ffd_decode_params *p) {
     return FFD_OK;
 }
 
+// The library's CTA count (num_splits 0): one per SM, or fewer when the cache holds fewer than
+// kMinBlocksPerCta blocks a CTA (B * Hkv * max_blocks_per_seq bounds the blocks from above, as the
+// lengths are on the device): a tiny cache split over every SM pays the start-up of every CTA and
+// the merge of as many records for a block or less each.
+constexpr int64_t kMinBlocksPerCta = 4;
+int default_ctas(const ffd_decode_params *p, int sms) {
+    const int64_t blocks = (int64_t)p->batch * p->num_kv_heads * p->max_blocks_per_seq;
+    const int64_t want = (blocks + kMinBlocksPerCta - 1) / kMinBlocksPerCta;
+    return want < sms ? (want > 0 ? (int)want : 1) : sms;
+}
+
 struct Plan {
     int nf;    // stage-1 slots per unit (FFD step)
     int ctas;  // CTAs of the persistent kernel
@@ -121,7 +132,7 @@ ffd_status make_decode_plan(const ffd_decode_params *p, Plan *pl) {
     int ctas = p->num_splits;
     if (ctas == 0) {
         if (sms <= 0) return FFD_ERR_CUDA;
-        ctas = sms;
+        ctas = default_ctas(p, sms);
     } else if (sms > 0 && ctas > sms) {
         ctas = sms;
     }
@@ -156,7 +167,7 @@ ffd_status make_dense_plan(const ffd_decode_params *p, Plan *pl) {
     int ctas = p->num_splits;
     if (ctas == 0) {
         if (sms <= 0) return FFD_ERR_CUDA;
-        ctas = sms;
+        ctas = default_ctas(p, sms);
     } else if (sms > 0 && ctas > sms) {
         ctas = sms;
     }

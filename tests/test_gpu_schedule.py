@@ -94,7 +94,10 @@ def test_scan_refine_reports_bad_block_table_entry():
     assert got["err"] == 5
     assert got["mask"][1, 0, 3] == 0
     again = H.decode(inp, dev, qc, 5.0, schedule=SCAN_REFINE)
-    np.testing.assert_array_equal(got["out"][0], again["out"][0])
+    # the other sequence is untouched up to rounding: the kept blocks of all units are shared out
+    # to the CTAs in equal runs, so the dropped block moves the runs' boundaries and with them the
+    # order in which sequence 0's blocks are summed
+    np.testing.assert_allclose(got["out"][0], again["out"][0], rtol=0, atol=2e-6)
     H.check_decode(inp, oracle.quantize(inp.k_bits), again, 5.0, what="clean rerun")
 
 
