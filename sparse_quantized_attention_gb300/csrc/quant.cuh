@@ -37,6 +37,21 @@ constexpr float kNearB = 4.0e-5f;
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// x / b rounded to nearest, for x >= 0 and a divisor b with c = RN(1/b), without an IEEE division
+// in the common case: q0 = RN(x c) lies within an ulp of x / b, the remainder x - q0 b is exact in
+// one fused multiply-add, and one more fused multiply-add rounds the quotient correctly
+// (Markstein's correction step with a precomputed reciprocal). For b = 3 and b = 127 the result
+// equals the IEEE quotient for every finite non-negative fp32 x (tests/test_gpu_quant_division.py
+// checks all of them); a non-finite x takes the IEEE division.
+constexpr float kThird = 1.0f / 3.0f;    // RN(1/3)
+constexpr float kInv127 = 1.0f / 127.0f; // RN(1/127)
+__device__ __forceinline__ float div_const(float x, float b, float c) {
+    if (!(x <= 3.4028234663852886e38f)) return __fdiv_rn(x, b);  // +inf or NaN
+    const float q0 = __fmul_rn(x, c);
+    const float r = __fmaf_rn(-q0, b, x);
+    return __fmaf_rn(r, c, q0);
+}
+
 // Exact rounding near a boundary. With t the fast quotient of a / b and c = rint(t), the only
 // rounding boundary within reach is k = c + 1/2 sign(t - c); k * b is exact in fp32 (k has at
 // most 9 significant bits, b is an fp16 value), so e = a - k b, formed by one fused multiply-add,
@@ -88,7 +103,7 @@ __device__ __forceinline__ void group_params(const uint32_t (&u)[16], GroupCodes
     if (mn == 0.0f) mn = 0.0f;  // a signed-zero extreme counts as +0
     if (mx == 0.0f) mx = 0.0f;
     o.zero = __float2half_rn(mn);
-    o.scale = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+    o.scale = __float2half_rn(div_const(__fsub_rn(mx, mn), 3.0f, kThird));
 }
 
 // 2-bit code of a = x - zero: the number of rounding boundaries (k + 1/2) scale below a (b0, b1,
@@ -164,7 +179,7 @@ __device__ __forceinline__ void quantize_group(const uint32_t (&u)[16], GroupCod
     o.codes[1] = __float2uint_rn(__fadd_rn(acc[2].x, acc[2].y)) |
                  (__float2uint_rn(__fadd_rn(acc[3].x, acc[3].y)) << 24);
 
-    o.rscale = __float2half_rn(__fdiv_rn(amax, 127.0f));
+    o.rscale = __float2half_rn(div_const(amax, 127.0f, kInv127));
     const float sr = __half2float(o.rscale);
     const float r254 = sr == 0.0f ? 0.0f : __frcp_rn(__fmul_rn(sr, 254.0f));  // exact product
 
